@@ -1,0 +1,148 @@
+"""CPU oracle for the XOR-swizzle data-movement path -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or calls it, and it imports nothing
+from the product package: the two share no code.
+
+The arithmetic lives in ``swz_oracle.c`` (plain C, one element per loop
+iteration); this module only compiles it with gcc and marshals numpy arrays
+through ctypes.  The parity status of every function is stated in the C
+file's header: everything is pinned except the bank model's pass split for
+8- and 16-byte accesses ("parity unpinned" for w = 8, 16).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swz_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+ORC_OK = 0
+ORC_BAD_ARG = 1
+ORC_NOT_CLOSED = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, no CUDA)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
+                           "-o", tmp, _SRC])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = build()
+        L = ctypes.CDLL(path)
+        u64, i64, i32, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.orc_swizzle.argtypes = [u64, i32, i32, i32]
+        L.orc_swizzle.restype = u64
+        L.orc_relayout.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, i32]
+        L.orc_relayout.restype = i32
+        L.orc_relayout_positions.argtypes = [vp, i64, i64, i32, i32, i32, vp]
+        L.orc_relayout_positions.restype = i32
+        L.orc_transpose.argtypes = [vp, vp, i64, i64, i32]
+        L.orc_transpose.restype = i32
+        L.orc_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp]
+        L.orc_bank_profile.restype = i32
+        L.orc_slice_collision.argtypes = [u64, i32, i32, i32]
+        L.orc_slice_collision.restype = u64
+        L.orc_slice_is_layout.argtypes = [u64, i32, i32, i32]
+        L.orc_slice_is_layout.restype = i32
+        L.orc_dump_layout.argtypes = [ctypes.c_char_p, i64, i64, i64, i32, i32, i32, i32]
+        L.orc_dump_layout.restype = i64
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# The oracle follows the pages' own argument order: swizzle<base, bits, shift>,
+# i.e. (M, B, S).  The wrappers below take keyword arguments B, M, S so that a
+# caller cannot mix the orders up.
+
+def swizzle(offset: int, *, B: int, M: int, S: int) -> int:
+    return int(lib().orc_swizzle(offset, M, B, S))
+
+
+def relayout(src: np.ndarray, *, tile_elems: int, B: int, M: int, S: int,
+             direction: int) -> np.ndarray:
+    """src: contiguous array whose size is a multiple of tile_elems elements."""
+    src = np.ascontiguousarray(src)
+    dst = np.empty_like(src)
+    esize = src.dtype.itemsize
+    n_tiles = src.size // tile_elems if tile_elems else 0
+    assert n_tiles * tile_elems == src.size
+    rc = lib().orc_relayout(_ptr(dst), _ptr(src), n_tiles, tile_elems, esize, M, B, S, direction)
+    if rc != ORC_OK:
+        raise ValueError(f"orc_relayout failed with {rc}")
+    return dst
+
+
+def relayout_positions(idx: np.ndarray, *, tile_elems: int, B: int, M: int, S: int) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty_like(idx)
+    rc = lib().orc_relayout_positions(_ptr(idx), idx.size, tile_elems, M, B, S, _ptr(out))
+    if rc != ORC_OK:
+        raise ValueError(f"orc_relayout_positions failed with {rc}")
+    return out
+
+
+def transpose(src: np.ndarray) -> np.ndarray:
+    """src: 2-D contiguous array; returns its transpose as a new contiguous array."""
+    src = np.ascontiguousarray(src)
+    rows, cols = src.shape
+    dst = np.empty((cols, rows), dtype=src.dtype)
+    rc = lib().orc_transpose(_ptr(dst), _ptr(src), rows, cols, src.dtype.itemsize)
+    if rc != ORC_OK:
+        raise ValueError(f"orc_transpose failed with {rc}")
+    return dst
+
+
+def bank_profile(addrs: np.ndarray, width: int, active: np.ndarray | None = None):
+    """addrs: (n, 32) uint32 byte addresses. Returns (ways, wavefronts) int32 arrays."""
+    addrs = np.ascontiguousarray(addrs, dtype=np.uint32).reshape(-1, 32)
+    n = addrs.shape[0]
+    ways = np.empty(n, dtype=np.int32)
+    wf = np.empty(n, dtype=np.int32)
+    act_ptr = None
+    if active is not None:
+        active = np.ascontiguousarray(active, dtype=np.uint32)
+        assert active.shape == (n,)
+        act_ptr = _ptr(active)
+    rc = lib().orc_bank_profile(_ptr(addrs), act_ptr, n, width, _ptr(ways), _ptr(wf))
+    if rc != ORC_OK:
+        raise ValueError(f"orc_bank_profile failed with {rc}")
+    return ways, wf
+
+
+def slice_collision(A: int, *, B: int, M: int, S: int) -> int:
+    return int(lib().orc_slice_collision(A, M, B, S))
+
+
+def slice_is_layout(A: int, *, B: int, M: int, S: int) -> bool:
+    return bool(lib().orc_slice_is_layout(A, M, B, S))
+
+
+def dump_layout(rows: int, cols: int, esize: int, *, B: int, M: int, S: int) -> str:
+    n = lib().orc_dump_layout(None, 0, rows, cols, esize, M, B, S)
+    buf = ctypes.create_string_buffer(int(n) + 1)
+    lib().orc_dump_layout(buf, n + 1, rows, cols, esize, M, B, S)
+    return buf.value.decode()

@@ -1,0 +1,274 @@
+/*
+ * swz_oracle.c -- plain, slow CPU oracle for the XOR-swizzle data-movement path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or
+ * helper with the CUDA library; it is written from the pages' definitions
+ * with one element per loop iteration and no blocking or reordering.
+ *
+ * Sources (page title, section):
+ *   [P1] "NVIDIA CuTe Swizzle" -- the bit diagram, sub-word broadcast,
+ *        "minimum steps are not a conflict".
+ *   [P2] "CuTe Swizzle 学习手册" -- bank structure, conflict rules,
+ *        "Swizzle 数学公式".
+ *   [P3] "cutlass 入门" -- "swizzle 融入 layout 优化" (slice collision).
+ *   [P4] "CUDA 013 - Swizzle 的工作原理" -- "计算公式" (the base/bits/shift
+ *        function), "更通用的映射规则" (offset-based rule, worked example),
+ *        "什么是 Bank Conflict".
+ *
+ * Parity status per function (what pins it is listed in the test suite):
+ *   orc_swizzle            pinned (worked example, 2-D closed forms, bit diagrams)
+ *   orc_relayout           pinned (reduces to orc_swizzle + byte copies)
+ *   orc_transpose          pinned (textbook transpose, explicit small cases)
+ *   orc_bank_profile       pinned for access widths 1,2,4; the phase split
+ *                          used for 8- and 16-byte accesses is a reading the
+ *                          pages do not fix: "parity unpinned" for w = 8, 16.
+ *   orc_slice_collision    pinned (truth tables, brute-force additivity)
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <stdio.h>
+
+/* Status codes of this oracle (independent of the library's codes). */
+#define ORC_OK 0
+#define ORC_BAD_ARG 1
+#define ORC_NOT_CLOSED 2
+
+/*
+ * [P4] "计算公式": the function is parameterised by base (low bits kept as
+ * they are), bits (width of the two fields) and shift (distance between the
+ * fields).  The zz field starts at bit `base`, the yy field at bit
+ * `base + shift`; aa = zz ^ yy replaces zz, every other bit is kept.
+ * Written in the clear-then-set form of that section.
+ */
+uint64_t orc_swizzle(uint64_t offset, int base, int bits, int shift)
+{
+    uint64_t bits_mask, zz, yy, aa;
+    if (bits <= 0)
+        return offset;
+    bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << bits) - 1);
+    zz = (offset >> base) & bits_mask;
+    yy = (offset >> (base + shift)) & bits_mask;
+    aa = zz ^ yy;
+    offset = offset & ~(bits_mask << base); /* clear the zz field */
+    offset = offset | (aa << base);         /* set the aa field */
+    return offset;
+}
+
+/*
+ * Batched relayout.  [P4] "使用示例" example 1: the element at logical offset
+ * `o` of a tile is accessed at the swizzled offset swizzle(o).  Forward
+ * (direction 0) stores logical element i at physical position swizzle(i);
+ * inverse (direction 1) reads the physical position swizzle(i) back into
+ * logical position i.  Offsets are local to each tile of tile_elems elements.
+ */
+int orc_relayout(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems,
+                 int esize, int base, int bits, int shift, int direction)
+{
+    unsigned char *d = (unsigned char *)dst;
+    const unsigned char *s = (const unsigned char *)src;
+    int64_t t, i;
+    if (!dst || !src || n_tiles < 0 || tile_elems < 0 || esize <= 0)
+        return ORC_BAD_ARG;
+    if (direction != 0 && direction != 1)
+        return ORC_BAD_ARG;
+    for (t = 0; t < n_tiles; ++t) {
+        int64_t tile0 = t * tile_elems;
+        for (i = 0; i < tile_elems; ++i) {
+            uint64_t j = orc_swizzle((uint64_t)i, base, bits, shift);
+            if (j >= (uint64_t)tile_elems)
+                return ORC_NOT_CLOSED;
+            if (direction == 0)
+                memcpy(d + (size_t)(tile0 + (int64_t)j) * esize,
+                       s + (size_t)(tile0 + i) * esize, (size_t)esize);
+            else
+                memcpy(d + (size_t)(tile0 + i) * esize,
+                       s + (size_t)(tile0 + (int64_t)j) * esize, (size_t)esize);
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Relayout of selected logical offsets only: for each global logical index
+ * idx[k] (tile * tile_elems + local), out_pos[k] receives the global physical
+ * index that element lands on (direction 0), or the global physical index it
+ * is read from (direction 1).  Used to check samples of very large buffers.
+ */
+int orc_relayout_positions(const int64_t *idx, int64_t n, int64_t tile_elems,
+                           int base, int bits, int shift, int64_t *out_pos)
+{
+    int64_t k;
+    if (!idx || !out_pos || tile_elems <= 0)
+        return ORC_BAD_ARG;
+    for (k = 0; k < n; ++k) {
+        int64_t tile = idx[k] / tile_elems;
+        int64_t local = idx[k] % tile_elems;
+        uint64_t j = orc_swizzle((uint64_t)local, base, bits, shift);
+        if (j >= (uint64_t)tile_elems)
+            return ORC_NOT_CLOSED;
+        out_pos[k] = tile * tile_elems + (int64_t)j;
+    }
+    return ORC_OK;
+}
+
+/* Matrix transpose, the textbook definition: out[c][r] = in[r][c]. */
+int orc_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int esize)
+{
+    unsigned char *d = (unsigned char *)dst;
+    const unsigned char *s = (const unsigned char *)src;
+    int64_t r, c;
+    if (!dst || !src || rows < 0 || cols < 0 || esize <= 0)
+        return ORC_BAD_ARG;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            memcpy(d + (size_t)(c * rows + r) * esize,
+                   s + (size_t)(r * cols + c) * esize, (size_t)esize);
+    return ORC_OK;
+}
+
+/*
+ * Bank model for one warp-wide shared-memory access.
+ *
+ * [P2] "Shared Memory 的 Bank 结构": 32 banks of 4 bytes, bank =
+ *   (byte_addr / 4) % 32.
+ * [P2] "什么情况下产生冲突" / [P4] "什么是 Bank Conflict": threads that touch
+ *   different addresses in the same bank are served one after the other;
+ *   N distinct addresses in one bank make an N-way conflict.  Threads that
+ *   touch the same address are served together (broadcast).
+ * [P1]: two 16-bit values in one 32-bit word are broadcast together, so the
+ *   unit of "same address" is the 4-byte word.
+ * [P1]: an operation that moves more data than one pass can carry needs
+ *   several passes; that minimum is not a conflict.  Conflicts are counted
+ *   within each pass.
+ *
+ * Reading where the pages are silent (parity unpinned for w = 8, 16): a warp
+ * access of w <= 4 bytes per lane is one pass over all 32 lanes; w = 8 is two
+ * passes (lanes 0-15, 16-31); w = 16 is four passes of 8 lanes.  In each pass
+ * every active lane touches the words floor(a/4) .. floor((a+w-1)/4); the
+ * pass costs the largest number of distinct words that fall in one bank.
+ * ways = largest pass cost, wavefronts = sum of pass costs.
+ *
+ * addrs: n patterns of 32 byte addresses; active: n lane masks or NULL (all
+ * lanes active).  Outputs ways[n], wavefronts[n].
+ */
+int orc_bank_profile(const uint32_t *addrs, const uint32_t *active, int64_t n,
+                     int width, int32_t *ways, int32_t *wavefronts)
+{
+    int64_t p;
+    int passes, lanes_per_pass;
+    if (!addrs || !ways || !wavefronts || n < 0)
+        return ORC_BAD_ARG;
+    if (width != 1 && width != 2 && width != 4 && width != 8 && width != 16)
+        return ORC_BAD_ARG;
+    passes = (width <= 4) ? 1 : width / 4;
+    lanes_per_pass = 32 / passes;
+    for (p = 0; p < n; ++p) {
+        uint32_t mask = active ? active[p] : 0xffffffffu;
+        int32_t worst = 0, total = 0;
+        int pass;
+        for (pass = 0; pass < passes; ++pass) {
+            /* distinct words touched in this pass; at most 8 lanes x 5 words
+               or 32 lanes x 2 words */
+            uint64_t words[64];
+            int n_words = 0, lane, k, bank, cost = 0;
+            for (lane = pass * lanes_per_pass; lane < (pass + 1) * lanes_per_pass; ++lane) {
+                uint64_t a, first, last, wd;
+                if (!((mask >> lane) & 1u))
+                    continue;
+                a = addrs[p * 32 + lane];
+                first = a / 4;
+                last = (a + (uint64_t)width - 1) / 4;
+                for (wd = first; wd <= last; ++wd) {
+                    int seen = 0;
+                    for (k = 0; k < n_words; ++k)
+                        if (words[k] == wd)
+                            seen = 1;
+                    if (!seen)
+                        words[n_words++] = wd;
+                }
+            }
+            for (bank = 0; bank < 32; ++bank) {
+                int count = 0;
+                for (k = 0; k < n_words; ++k)
+                    if ((int)(words[k] % 32) == bank)
+                        ++count;
+                if (count > cost)
+                    cost = count;
+            }
+            if (cost > worst)
+                worst = cost;
+            total += cost;
+        }
+        ways[p] = worst;
+        wavefronts[p] = total;
+    }
+    return ORC_OK;
+}
+
+/*
+ * [P3] "swizzle 融入 layout 优化": A is the slice's largest index (its bits
+ * are the bits that can change).  collision = A & ~swizzle(A); a set bit
+ * marks a pair of fields whose y bit and z bit are both active, in which case
+ * the swizzle cannot be folded into a plain layout.
+ */
+uint64_t orc_slice_collision(uint64_t A, int base, int bits, int shift)
+{
+    return A & ~orc_swizzle(A, base, bits, shift);
+}
+
+/*
+ * Brute-force check of the property the collision rule predicts: the
+ * swizzle, restricted to every x whose bits are a subset of A, equals a plain
+ * layout sum_i x_i * swizzle(2^i) (integer sum of per-bit strides).
+ * Returns 1 when it does, 0 when some subset breaks it.
+ */
+int orc_slice_is_layout(uint64_t A, int base, int bits, int shift)
+{
+    uint64_t x = 0;
+    for (;;) {
+        uint64_t sum = 0;
+        int i;
+        for (i = 0; i < 64; ++i)
+            if ((x >> i) & 1u)
+                sum += orc_swizzle((uint64_t)1 << i, base, bits, shift);
+        if (sum != orc_swizzle(x, base, bits, shift))
+            return 0;
+        if (x == A)
+            break;
+        x = (x - A) & A; /* next subset of A in increasing order */
+    }
+    return 1;
+}
+
+/*
+ * Text dump of a swizzled rows x cols tile ([P2] "如何验证 Swizzle 是否正确消除
+ * 冲突": print the mapping and the bank of each element).  One line per row:
+ * for every column "physical_offset/bank".  Returns the number of characters
+ * needed (excluding the terminator); writes at most cap bytes.
+ */
+int64_t orc_dump_layout(char *buf, int64_t cap, int64_t rows, int64_t cols, int esize,
+                        int base, int bits, int shift)
+{
+    int64_t r, c, used = 0;
+    char tmp[64];
+    for (r = 0; r < rows; ++r) {
+        for (c = 0; c < cols; ++c) {
+            uint64_t phys = orc_swizzle((uint64_t)(r * cols + c), base, bits, shift);
+            uint64_t bank = (phys * (uint64_t)esize / 4) % 32;
+            int len = snprintf(tmp, sizeof tmp, "%s%llu/%llu", c ? " " : "",
+                               (unsigned long long)phys, (unsigned long long)bank);
+            if (buf && used + len < cap)
+                memcpy(buf + used, tmp, (size_t)len);
+            used += len;
+        }
+        if (buf && used + 1 < cap)
+            buf[used] = '\n';
+        used += 1;
+    }
+    if (buf && cap > 0)
+        buf[used < cap ? used : cap - 1] = '\0';
+    return used;
+}

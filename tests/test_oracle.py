@@ -1,0 +1,364 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a value the
+pages print (fixtures under tests/golden/, each citing its page and section),
+a coordinate-level restatement of a 2-D mapping the pages describe, the bit
+diagrams read position by position, closed forms and invariants, and brute
+force on tiny inputs.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+from conftest import read_golden
+
+SWEEP = [(B, M, S) for B in range(1, 6) for M in range(0, 5) for S in range(B, 8)]
+CONFIG_SWIZZLES = [(3, 3, 3), (3, 4, 3), (5, 2, 5), (5, 0, 5), (4, 0, 4)]
+
+
+# ---------------------------------------------------------------- swizzle ---
+
+def test_worked_example_673(orc):
+    g = {row[0]: row[1] for row in read_golden("worked_example_673.txt")}
+    rows, cols = int(g["rows"]), int(g["cols"])
+    base, bits, shift = int(g["base"]), int(g["bits"]), int(g["shift"])
+    r, c = int(g["logical_row"]), int(g["logical_col"])
+    off = r * cols + c
+    assert off == int(g["offset"]) == int(g["offset_binary"], 2)
+    sw = orc.swizzle(off, B=bits, M=base, S=shift)
+    assert sw == int(g["swizzled"]) == int(g["swizzled_binary"], 2)
+    assert divmod(sw, cols) == (int(g["physical_row"]), int(g["physical_col"]))
+    # the same fact through the relayout: the element with logical value 673
+    # of an int[32][64] array lands at physical position 683
+    iota = np.arange(rows * cols, dtype=np.int32)
+    phys = orc.relayout(iota, tile_elems=rows * cols, B=bits, M=base, S=shift, direction=0)
+    assert phys.reshape(rows, cols)[int(g["physical_row"]), int(g["physical_col"])] == off
+
+
+def _mapping_32x32(y, x):
+    # 32 x 32 words: the column index is XOR-ed with the row index
+    return y, x ^ y
+
+
+def _mapping_64x32(y, x):
+    # 64 rows: the two 32-row halves are swizzled the same way (row taken mod 32)
+    return y, x ^ (y & 31)
+
+
+def _mapping_32x64(y, x):
+    # 64 columns: each 32-column half is swizzled on its own
+    half, within = divmod(x, 32)
+    return y, half * 32 + (within ^ y)
+
+
+def _mapping_half_pairs(y, x):
+    # 16-bit data, two neighbours kept together: swizzle the pair index
+    pair, lane = divmod(x, 2)
+    return y, (pair ^ y) * 2 + lane
+
+
+@pytest.mark.parametrize("rows,cols,mapping,params", [
+    (32, 32, _mapping_32x32, (5, 0, 5)),
+    (64, 32, _mapping_64x32, (5, 0, 5)),
+    (32, 64, _mapping_32x64, (5, 0, 6)),
+    (32, 64, _mapping_half_pairs, (5, 1, 5)),
+])
+def test_two_d_mappings(orc, rows, cols, mapping, params):
+    """"CUDA 013 - Swizzle 的工作原理", section "swizzle 映射案例": the four 2-D
+    mappings equal the offset rule of section "计算公式" with these parameters."""
+    B, M, S = params
+    for y in range(rows):
+        for x in range(cols):
+            py, px = mapping(y, x)
+            assert orc.swizzle(y * cols + x, B=B, M=M, S=S) == py * cols + px
+
+
+def _diagram_positions(pattern_or_tokens):
+    """Return (z_positions, y_positions), least significant first."""
+    if isinstance(pattern_or_tokens, str):
+        tokens = list(pattern_or_tokens)
+    else:
+        tokens = pattern_or_tokens
+    assert len(tokens) == 32
+    z, y = {}, {}
+    for i, t in enumerate(tokens):
+        bit = 31 - i
+        if t.startswith("Z"):
+            z[bit] = t
+        elif t.startswith("Y"):
+            y[bit] = t
+    zs, ys = sorted(z), sorted(y)
+    return zs, ys
+
+
+def test_bit_diagrams(orc):
+    """"NVIDIA CuTe Swizzle" (diagram and example) and "cutlass 入门"
+    (section "具体过程"): read the field positions off each diagram and check the
+    oracle bit by bit: each Z bit becomes Z xor the Y bit in the same place of
+    its field, every other bit is kept."""
+    rows = {r[0]: r[1:] for r in read_golden("bit_diagrams.txt")}
+    expected_params = {}
+    rng = np.random.default_rng(12345)
+    for name, fields in rows.items():
+        pattern = fields[0] if len(fields) == 1 else fields
+        zs, ys = _diagram_positions(pattern)
+        assert len(zs) == len(ys) > 0
+        assert zs == list(range(zs[0], zs[0] + len(zs)))
+        assert ys == list(range(ys[0], ys[0] + len(ys)))
+        B, M, S = len(zs), zs[0], ys[0] - zs[0]
+        expected_params[name] = (B, M, S)
+        for x in itertools.chain(rng.integers(0, 2**32, 2000, dtype=np.uint64).tolist(),
+                                 [0, 2**32 - 1]):
+            want = 0
+            for bit in range(32):
+                v = (x >> bit) & 1
+                if bit in zs:
+                    v ^= (x >> ys[zs.index(bit)]) & 1
+                want |= v << bit
+            assert orc.swizzle(int(x), B=B, M=M, S=S) == want
+    # counting the characters gives these parameters
+    assert expected_params == {"p1_diagram": (3, 4, 10), "p1_example": (2, 3, 11),
+                               "p3_tokens": (4, 4, 11)}
+
+
+@pytest.mark.parametrize("B,M,S", SWEEP + CONFIG_SWIZZLES)
+def test_swizzle_invariants(orc, B, M, S):
+    """Consequences of the definition, exhaustively over offsets 0..65535."""
+    x = np.arange(1 << 16, dtype=np.uint64)
+    sw = np.array([orc.swizzle(int(v), B=B, M=M, S=S) for v in x], dtype=np.uint64)
+    # a bijection of 0..65535 onto itself
+    assert np.array_equal(np.sort(sw), x)
+    # self-inverse when the two fields do not overlap (S >= B)
+    if S >= B:
+        back = np.array([orc.swizzle(int(v), B=B, M=M, S=S) for v in sw], dtype=np.uint64)
+        assert np.array_equal(back, x)
+    # the low M bits are kept: groups of 2^M elements stay contiguous and in order
+    low = (1 << M) - 1
+    assert np.array_equal(sw & np.uint64(low), x & np.uint64(low))
+    # bits at and above M+B are only read, never written
+    assert np.array_equal(sw >> np.uint64(M + B), x >> np.uint64(M + B))
+
+
+def test_swizzle_degenerate(orc):
+    x = list(range(4096))
+    # B = 0: the identity
+    assert [orc.swizzle(v, B=0, M=3, S=3) for v in x] == x
+    # S = 0: the field is XOR-ed with itself, so it is cleared; not a bijection
+    vals = {orc.swizzle(v, B=3, M=2, S=0) for v in x}
+    assert len(vals) < len(x)
+    assert all(((orc.swizzle(v, B=3, M=2, S=0) >> 2) & 7) == 0 for v in x)
+    # 1 <= S < B: still a bijection, but not always an involution
+    sw = [orc.swizzle(v, B=3, M=0, S=1) for v in x]
+    assert sorted(sw) == x
+    assert any(orc.swizzle(s, B=3, M=0, S=1) != v for v, s in zip(x, sw))
+
+
+# --------------------------------------------------------------- relayout ---
+
+def test_relayout_roundtrip_and_closed(orc):
+    rng = np.random.default_rng(0)
+    for (B, M, S), esize in itertools.product([(3, 3, 3), (3, 0, 1), (2, 1, 1), (5, 2, 5)],
+                                              [1, 2, 4, 8, 16]):
+        tile = 1 << (B + M + S)
+        dt = np.dtype(f"V{esize}")
+        src = rng.integers(0, 256, 3 * tile * esize, dtype=np.uint8).view(dt)
+        fwd = orc.relayout(src, tile_elems=tile, B=B, M=M, S=S, direction=0)
+        inv = orc.relayout(fwd, tile_elems=tile, B=B, M=M, S=S, direction=1)
+        assert inv.tobytes() == src.tobytes()
+        if S >= B:
+            inv2 = orc.relayout(fwd, tile_elems=tile, B=B, M=M, S=S, direction=0)
+            assert inv2.tobytes() == src.tobytes()
+
+
+def test_relayout_tile_local(orc):
+    # two tiles relayout independently: the second tile equals a relayout of
+    # its own data
+    B, M, S = 2, 1, 3
+    tile = 64
+    src = np.arange(2 * tile, dtype=np.int32)
+    out = orc.relayout(src, tile_elems=tile, B=B, M=M, S=S, direction=0)
+    second = orc.relayout(src[tile:] - tile, tile_elems=tile, B=B, M=M, S=S, direction=0)
+    assert np.array_equal(out[tile:] - tile, second)
+
+
+def test_relayout_not_closed(orc):
+    # a tile of 6 elements is not closed under Swizzle<2,0,1>: offset 4 maps to 6
+    assert orc.swizzle(4, B=2, M=0, S=1) == 6
+    with pytest.raises(ValueError):
+        orc.relayout(np.arange(6, dtype=np.int32), tile_elems=6, B=2, M=0, S=1, direction=0)
+
+
+def test_relayout_usage_loop(orc):
+    """"CUDA 013 - Swizzle 的工作原理", section "使用示例", example 1: the element
+    at logical (y, x) of int num[32][128] is accessed at the coordinate given by
+    the swizzled offset split into row and column."""
+    rows, cols, B, M, S = 32, 128, 5, 0, 7
+    logical = np.arange(rows * cols, dtype=np.int32).reshape(rows, cols)
+    phys = orc.relayout(logical.ravel(), tile_elems=rows * cols, B=B, M=M, S=S, direction=0)
+    phys = phys.reshape(rows, cols)
+    for y in range(rows):
+        for x in range(cols):
+            # 32 x 32 blocks: column bits 0..4 XOR row bits 0..4
+            new_y, new_x = y, (x & ~31) | ((x & 31) ^ (y & 31))
+            assert phys[new_y, new_x] == logical[y, x]
+
+
+def test_relayout_positions(orc):
+    idx = np.array([0, 673, 2047, 2048 + 673], dtype=np.int64)
+    pos = orc.relayout_positions(idx, tile_elems=2048, B=5, M=0, S=6)
+    assert pos.tolist() == [0, 683, orc.swizzle(2047, B=5, M=0, S=6), 2048 + 683]
+
+
+# -------------------------------------------------------------- transpose ---
+
+def test_transpose_small(orc):
+    a = np.array([[1, 2, 3], [4, 5, 6]], dtype=np.int32)
+    assert orc.transpose(a).tolist() == [[1, 4], [2, 5], [3, 6]]
+
+
+@pytest.mark.parametrize("dtype", [np.uint8, np.uint16, np.float32, np.float64])
+def test_transpose_matches_library(orc, dtype):
+    rng = np.random.default_rng(7)
+    a = rng.integers(0, 255, size=(37, 53)).astype(dtype)
+    t = orc.transpose(a)
+    assert np.array_equal(t, a.T)
+    assert np.array_equal(orc.transpose(t), a)
+
+
+# ------------------------------------------------------------- bank model ---
+
+def _ways(orc, addrs, width, active=None):
+    a = np.zeros(32, dtype=np.uint32)
+    a[:len(addrs)] = addrs
+    act = None
+    if active is None and len(addrs) < 32:
+        active = (1 << len(addrs)) - 1
+    if active is not None:
+        act = np.array([active], dtype=np.uint32)
+    w, wf = orc.bank_profile(a.reshape(1, 32), width, act)
+    return int(w[0]), int(wf[0])
+
+
+def test_bank_column_fp32(orc):
+    """"CuTe Swizzle 学习手册", section "冲突的典型场景": an 8 x 32 fp32 array read
+    down column 0 puts every lane on bank 0; a row read is conflict-free."""
+    col = [4 * (r * 32 + 0) for r in range(8)]
+    assert _ways(orc, col, 4) == (8, 8)
+    col32 = [4 * (r * 32 + 5) for r in range(32)]
+    assert _ways(orc, col32, 4) == (32, 32)
+    row = [4 * (0 * 32 + c) for c in range(32)]
+    assert _ways(orc, row, 4) == (1, 1)
+
+
+def test_bank_padding_and_xor(orc):
+    """"CUDA 013 - Swizzle 的工作原理": a [32][33] array and the (y, x ^ y)
+    mapping both make a column read conflict-free."""
+    padded = [4 * (r * 33 + 7) for r in range(32)]
+    assert _ways(orc, padded, 4) == (1, 1)
+    xor = [4 * (r * 32 + (7 ^ r)) for r in range(32)]
+    assert _ways(orc, xor, 4) == (1, 1)
+    for x in range(32):
+        sw = [4 * orc.swizzle(r * 32 + x, B=5, M=0, S=5) for r in range(32)]
+        assert _ways(orc, sw, 4) == (1, 1)
+
+
+def test_bank_fp16_64_columns(orc):
+    """"CuTe Swizzle 学习手册": an 8 x 64 fp16 array (128-byte rows) read down a
+    column.  Unswizzled: 8-way.  Swizzle<3,3,3> in element units: conflict
+    free, both as 2-byte scalars and as 16-byte row vectors.  Element-unit
+    Swizzle<3,4,3> on the same rows is 2-way (the "matrix too narrow" case of
+    the pitfalls table)."""
+    for col in range(64):
+        plain = [2 * (r * 64 + col) for r in range(8)]
+        assert _ways(orc, plain, 2)[0] == 8
+        s333 = [2 * orc.swizzle(r * 64 + col, B=3, M=3, S=3) for r in range(8)]
+        assert _ways(orc, s333, 2) == (1, 1)
+    for chunk in range(8):
+        vec333 = [2 * orc.swizzle(r * 64 + 8 * chunk, B=3, M=3, S=3) for r in range(8)]
+        assert _ways(orc, vec333, 16) == (1, 1)
+        vec_plain = [2 * (r * 64 + 8 * chunk) for r in range(8)]
+        assert _ways(orc, vec_plain, 16) == (8, 8)
+        s343 = [2 * orc.swizzle(r * 64 + 8 * chunk, B=3, M=4, S=3) for r in range(8)]
+        assert _ways(orc, s343, 2)[0] == 2
+
+
+def test_bank_usage_examples(orc):
+    """"CUDA 013 - Swizzle 的工作原理", section "使用示例": with each example's
+    parameters, reading one column of basic elements down the rows is
+    conflict-free within every pass."""
+    for name, esize, rows, cols, base, bits, shift in read_golden("usage_examples.txt"):
+        esize, rows, cols = int(esize), int(rows), int(cols)
+        base, bits, shift = int(base), int(bits), int(shift)
+        unit = esize << base                      # bytes kept together
+        lanes = 32 if unit <= 4 else 32 // (unit // 4)
+        per_row = cols >> base                    # basic elements per row
+        for col_unit in range(per_row):
+            addrs = []
+            for r in range(min(rows, lanes)):
+                off = r * cols + (col_unit << base)
+                addrs.append(esize * orc.swizzle(off, B=bits, M=base, S=shift))
+            w, _ = _ways(orc, addrs, unit)
+            assert w == 1, (name, col_unit)
+
+
+def test_bank_broadcast(orc):
+    """Same word: broadcast ("CuTe Swizzle 学习手册"); two 16-bit halves of one
+    word are served together ("NVIDIA CuTe Swizzle")."""
+    assert _ways(orc, [128] * 32, 4) == (1, 1)
+    assert _ways(orc, [0, 2] * 16, 2) == (1, 1)
+    assert _ways(orc, [0, 1, 2, 3] * 8, 1) == (1, 1)
+
+
+def test_bank_minimum_passes(orc):
+    """"NVIDIA CuTe Swizzle": a 16 x 16 fp16 tile (256 elements, 512 bytes) read
+    by one warp takes four passes; that is the minimum, not a conflict."""
+    addrs = [16 * l for l in range(32)]
+    ways, wavefronts = _ways(orc, addrs, 16)
+    assert ways == 1 and wavefronts == 4
+
+
+def test_bank_inactive_and_unaligned(orc):
+    # inactive lanes do not count
+    col = [4 * (r * 32) for r in range(32)]
+    assert _ways(orc, col, 4, active=0x1)[0] == 1
+    assert _ways(orc, col, 4, active=0)[0] == 0
+    # a 4-byte access at byte 2 straddles words 0 and 1
+    assert _ways(orc, [2, 130], 4) == (2, 2)
+
+
+# -------------------------------------------------------- slice collision ---
+
+def test_collision_truth_table(orc):
+    """"cutlass 入门", section "swizzle 融入 layout 优化": for one (Z_i, Y_i)
+    pair, C at Z_i is set exactly when both bits are active."""
+    table = [tuple(int(v) for v in row) for row in read_golden("collision_truth_table.txt")]
+    assert len(table) == 4
+    B, M, S = 3, 2, 4
+    for i in range(B):
+        z, y = M + i, M + S + i
+        for a_z, a_y, sw_z, c_z in table:
+            A = (a_z << z) | (a_y << y)
+            assert (orc.swizzle(A, B=B, M=M, S=S) >> z) & 1 == sw_z
+            C = orc.slice_collision(A, B=B, M=M, S=S)
+            assert (C >> z) & 1 == c_z
+            assert C & ~(1 << z) == 0
+
+
+@pytest.mark.parametrize("B,M,S", [(1, 0, 1), (2, 0, 2), (2, 1, 2), (2, 0, 3), (3, 0, 3),
+                                   (2, 0, 1), (3, 0, 1), (3, 1, 2)])
+def test_collision_predicts_layout(orc, B, M, S):
+    """Brute force: C == 0 exactly when the swizzle restricted to the slice is a
+    plain layout (a sum of per-bit strides), on every mask A of the low bits."""
+    nbits = B + M + S + 1
+    for A in range(1 << nbits):
+        C = orc.slice_collision(A, B=B, M=M, S=S)
+        assert (C == 0) == orc.slice_is_layout(A, B=B, M=M, S=S), (A, C)
+
+
+def test_dump_layout(orc):
+    text = orc.dump_layout(32, 64, 4, B=5, M=0, S=6)
+    lines = text.splitlines()
+    assert len(lines) == 32
+    entry = lines[10].split()[33]
+    assert entry == f"683/{683 % 32}"
