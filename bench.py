@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""Benchmark of the XOR-swizzle data-movement path on GB300.
+
+One step = the headline workload: Swizzle<3,4,3> relayout of 4096 bf16 tiles
+of 128 x 64 (64 MiB, N(0,1) values from seed 1), forward (logical ->
+swizzled) then inverse (swizzled -> logical), through the C ABI.  The metric
+is algorithmic bytes moved (read + write, 2 x 64 MiB per launch) per second.
+
+Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
+barrier and a device synchronisation.  L2 is flushed before every step
+(write 512 MiB, then read another 512 MiB so that no dirty line is left for
+the timed kernels to write back); each step is timed on its launch stream
+with CUDA events and the flushes are outside those intervals.  SM clocks and
+throttle reasons are sampled with nvidia-smi during the timed steps.
+
+The JSON line also carries:
+  roofline      the relayout kernel's achieved GB/s against the measured HBM
+                copy bandwidth (MEASURED_PEAKS.json), with the DRAM traffic per
+                launch from the committed ncu summary when it matches the
+                current kernel source;
+  e2e           the same metric through the C ABI from pinned host buffers,
+                host->device and device->host copies inside the timed region;
+  cpu_baseline  the CPU oracle (single thread) on the same workload;
+  rows          every other row of the path measured in the same run: the
+                small relayout, the 1 GiB int8 and uint16-sweep relayouts, the
+                fp32 / fp16 / fp64 transposes with each staging, the bank
+                profiler (skip with --no-rows).
+
+--impl reference times the CPU oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak
+scaling, no collective on the data path); value = all ranks' bytes / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+MiB = 1 << 20
+GB = 1e9
+METRIC = "relayout/transpose GB/s (read+write) & % of GB300 HBM peak; smem bank conflicts"
+TILES, ROWS, COLS, ESIZE = 4096, 128, 64, 2
+B, M, S = 3, 4, 3
+WORKLOAD = ("Swizzle<3,4,3> relayout forward then inverse of 4096 bf16 tiles of 128x64 "
+            "(64 MiB, N(0,1) from seed 1)")
+STEP_BYTES = 2 * 2 * TILES * ROWS * COLS * ESIZE     # two launches, each reads and writes 64 MiB
+LAUNCH_BYTES = 2 * TILES * ROWS * COLS * ESIZE
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return p.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "xor_swizzle_movement_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("source_hash") == src_hash:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.rows = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5:
+            time.sleep(0.02)
+        self.rows.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = list(self.rows)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)}
+
+
+# ----------------------------------------------------------------------------
+
+
+def make_flush(torch, dev):
+    w = torch.empty(512 * MiB, dtype=torch.uint8, device=dev)
+    r = torch.ones(512 * MiB // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        w.fill_(1)
+        r.sum()
+    return flush
+
+
+def timed_launches(torch, fn, reps, flush, warm=3):
+    """fn() launches kernels on the current stream; returns per-rep ms (events),
+    L2 flushed before each rep."""
+    st = torch.cuda.current_stream()
+    for _ in range(warm):
+        flush()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush()
+        a.record(st)
+        fn()
+        b.record(st)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_rows(torch, swz, dev, flush, peak):
+    """Each remaining row of the path at its full size (inputs drawn on the GPU
+    from the row's seed)."""
+    out = {}
+    gen = torch.Generator(device=dev)
+
+    def rand_bytes(n, seed):
+        gen.manual_seed(seed)
+        return torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=gen)
+
+    def summary(ms_list, nbytes):
+        ms = statistics.median(ms_list)
+        gbs = nbytes / (ms * 1e-3) / GB
+        return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3)}
+
+    # small relayout: 256 fp16 tiles 64x64, Swizzle<3,3,3>, forward then inverse (4 MiB moved per launch)
+    src = rand_bytes(256 * 64 * 64 * 2, 0)
+    a, b = torch.empty_like(src), torch.empty_like(src)
+    cold = timed_launches(torch, lambda: (swz.swz_relayout(a, src, 256, 64, 64, 2, 3, 3, 3, 0),
+                                          swz.swz_relayout(b, a, 256, 64, 64, 2, 3, 3, 3, 1)), 50, flush)
+    warm_ms = timed_launches(torch, lambda: (swz.swz_relayout(a, src, 256, 64, 64, 2, 3, 3, 3, 0),
+                                             swz.swz_relayout(b, a, 256, 64, 64, 2, 3, 3, 3, 1)), 50,
+                             lambda: None)
+    out["relayout_fp16_64x64_sw333_2MiB"] = {"cold_l2": summary(cold, 4 * src.numel()),
+                                             "warm_l2": summary(warm_ms, 4 * src.numel()),
+                                             "note": "4 MiB per launch: launch-latency bound, % of HBM not meaningful"}
+    del src, a, b
+
+    # int8 tiles 64x128, Swizzle<5,2,5>, 1 GiB, forward and inverse
+    src = rand_bytes(1 << 30, 4)
+    dst = torch.empty_like(src)
+    n_tiles = (1 << 30) // (64 * 128)
+    fwd = timed_launches(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0), 10, flush)
+    inv = timed_launches(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 1), 10, flush)
+    out["relayout_int8_64x128_sw525_1GiB"] = {"forward": summary(fwd, 2 << 30), "inverse": summary(inv, 2 << 30)}
+
+    # one 1 GiB uint16 buffer, every (B, M, S) with B 1..5, M 0..4, S B..7, forward
+    n = 1 << 29
+    res = []
+    for Bq in range(1, 6):
+        for Mq in range(0, 5):
+            for Sq in range(Bq, 8):
+                ms = timed_launches(torch, lambda: swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0), 3,
+                                    flush, warm=1)
+                res.append(((2 << 30) / (statistics.median(ms) * 1e-3) / GB, (Bq, Mq, Sq)))
+    res.sort()
+    vals = [r[0] for r in res]
+    out["relayout_uint16_1GiB_sweep125"] = {
+        "min": {"GB/s": round(vals[0], 1), "BMS": res[0][1]},
+        "median_GB/s": round(statistics.median(vals), 1),
+        "max": {"GB/s": round(vals[-1], 1), "BMS": res[-1][1]},
+        "min_frac_of_hbm": round(vals[0] / peak, 3)}
+    del src, dst
+
+    # transposes
+    def transpose_rows(name, n, esize, variants, seed):
+        s_ = rand_bytes(n * n * esize, seed)
+        d_ = torch.empty_like(s_)
+        r = {}
+        for v, vname in variants:
+            ms = timed_launches(torch, lambda: swz.swz_transpose(d_, s_, n, n, esize, v), 10, flush)
+            r[vname] = summary(ms, 2 * n * n * esize)
+        out[name] = r
+
+    transpose_rows("transpose_fp32_8192", 8192, 4, [(0, "swizzled_sw505"), (1, "unswizzled"), (2, "padded_33")], 2)
+    transpose_rows("transpose_fp16_16384", 16384, 2,
+                   [(0, "swizzled_sw343_ldmatrix"), (3, "tma_swizzle128b"), (1, "unswizzled"), (2, "padded")], 3)
+    transpose_rows("transpose_fp64_8192", 8192, 8, [(0, "swizzled_sw404"), (1, "unswizzled"), (2, "padded_17")], 4)
+
+    # bank profiler: 2^22 random aligned 4-byte patterns
+    npat = 1 << 22
+    gen.manual_seed(5)
+    pats = (torch.randint(0, 228 * 1024 // 4, (npat, 32), dtype=torch.int32, device=dev, generator=gen) * 4)
+    ways = torch.empty(npat, dtype=torch.int32, device=dev)
+    wf = torch.empty(npat, dtype=torch.int32, device=dev)
+    ms = timed_launches(torch, lambda: swz.swz_bank_profile(pats, None, npat, 4, ways, wf), 10, flush)
+    med = statistics.median(ms)
+    out["bank_profile_4M_patterns_w4"] = {"ms": round(med, 4), "Gpatterns/s": round(npat / (med * 1e-3) / 1e9, 3),
+                                          "GB/s": round(npat * 136 / (med * 1e-3) / GB, 1)}
+    return out
+
+
+def cpu_baseline(host_src, seconds=10.0):
+    """The CPU oracle (single thread, as it stands) on the whole workload,
+    forward then inverse, repeated for about `seconds`."""
+    import oracle
+    t_end = time.perf_counter() + seconds
+    times = []
+    while True:
+        t0 = time.perf_counter()
+        fwd = oracle.relayout(host_src, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
+        oracle.relayout(fwd, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end:
+            break
+    mean = sum(times) / len(times)
+    return {"value": round(STEP_BYTES / mean / GB, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"whole workload (forward + inverse of {TILES} tiles), {len(times)} repetitions, "
+                      f"{mean * 1e3:.1f} ms each, single thread"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    from xor_swizzle_movement_gb300 import inputs
+    import oracle
+    host = inputs.bf16_normal(TILES * ROWS * COLS, seed=1)
+    # one step = forward + inverse of a bounded sample (512 of the 4096 tiles)
+    sample_tiles = 512
+    part = host[: sample_tiles * ROWS * COLS]
+    step_bytes = STEP_BYTES * sample_tiles // TILES
+    for _ in range(args.warmup):
+        oracle.relayout(part, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        f = oracle.relayout(part, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
+        oracle.relayout(f, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / GB
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tiles": sample_tiles},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{sample_tiles} of {TILES} tiles per step, forward + inverse, single thread"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, world, local = dist_info()
+    import numpy as np
+    import torch
+    import xor_swizzle_movement_gb300 as swz
+    from xor_swizzle_movement_gb300 import inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    swz.lib()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+
+    peak, peak_kind = peaks()
+    n_el = TILES * ROWS * COLS
+    host = inputs.bf16_normal(n_el, seed=1)
+    host_t = torch.from_numpy(host.view(np.int16)).pin_memory()
+    src = host_t.to(dev)
+    phys = torch.empty_like(src)
+    back = torch.empty_like(src)
+    flush = make_flush(torch, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        swz.swz_relayout(phys, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
+        swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
+
+    for _ in range(max(args.warmup, 3)):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    assert torch.equal(back, src), "relayout round trip failed"
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        if gpu_id and not gpu_id.startswith("GPU-"):
+            gpu_id = "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for e0, e1, e2 in ev:
+        flush()
+        e0.record(stream)
+        swz.swz_relayout(phys, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
+        e1.record(stream)
+        swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    launch_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev] + [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * STEP_BYTES * args.steps / (total_ms * 1e-3) / GB
+
+    # roofline of the relayout kernel (both launches of a step are that kernel)
+    avg_launch_s = statistics.mean(launch_ms) * 1e-3
+    achieved = LAUNCH_BYTES / avg_launch_s / GB
+    src_hash = source_hash("swz_relayout.cu", "swz_common.cuh")
+    traffic = committed_traffic("relayout_vec_kernel<2,0,false> 4096x128x64 bf16 Sw<3,4,3>", src_hash)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 3), "traffic": traffic,
+                "peak_kind": f"{peak_kind} HBM copy bandwidth", "kernel": "relayout_vec_kernel",
+                "forward_ms": round(statistics.mean(launch_ms[: args.steps]), 4),
+                "inverse_ms": round(statistics.mean(launch_ms[args.steps:]), 4)}
+
+    # end to end through the C ABI from pinned host buffers
+    out_host = torch.empty_like(host_t).pin_memory()
+    e2e_steps = max(10, min(200, args.steps // 10))
+    for _ in range(3):
+        d = host_t.to(dev, non_blocking=True)
+        swz.swz_relayout(phys, d, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
+        swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
+        out_host.copy_(back, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        d = host_t.to(dev, non_blocking=True)
+        swz.swz_relayout(phys, d, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
+        swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
+        out_host.copy_(back, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    assert torch.equal(out_host, host_t), "end-to-end round trip failed"
+    e2e = {"value": round(STEP_BYTES / e2e_s / GB, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": n_el * ESIZE, "d2h_bytes_per_step": n_el * ESIZE,
+           "ms_per_step": round(e2e_s * 1e3, 4)}
+
+    rows = None
+    if not args.no_rows and rank == 0:
+        rows = measure_rows(torch, swz, dev, flush, peak)
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tiles": TILES, "rows": ROWS, "cols": COLS, "elem_bytes": ESIZE,
+                       "swizzle_BMS": [B, M, S], "step": "forward launch + inverse launch",
+                       "bytes_per_step": STEP_BYTES,
+                       "l2": "flushed before every step (512 MiB write + 512 MiB read, untimed)",
+                       "parallelism": f"replicas x{world}"},
+            "frac_of_hbm_peak": round(value / world / peak, 3),
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,
+            "clocks": clk, "wall_s_timed_loop": round(wall, 3)}
+    if rows is not None:
+        line["rows"] = rows
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(host)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

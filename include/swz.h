@@ -1,0 +1,207 @@
+/*
+ * swz.h -- C ABI of the XOR-swizzle data-movement library for GB300 (sm_103a).
+ *
+ * The swizzle is CuTe's Swizzle<B, M, S> acting on an element offset x:
+ *
+ *     sw(x) = x ^ (((x >> (M + S)) & ((1 << B) - 1)) << M)
+ *
+ * ("CuTe Swizzle 学习手册", section "Swizzle 数学公式"; the same function with
+ * base = M, bits = B, shift = S in "CUDA 013 - Swizzle 的工作原理", section
+ * "计算公式").  The B bits that start at bit M + S are XOR-ed into the B bits
+ * that start at bit M; the low M bits (a group of 2^M elements that stays
+ * contiguous) and every other bit are kept.  All B, M, S arguments below are
+ * in ELEMENT-offset units.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named dst/src/out are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or retains them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  GPU work is enqueued on it and the call returns without
+ *     waiting; the caller synchronises.
+ *   - The return value reports argument validation and launch errors only.
+ *     On any error nothing is launched and no output byte is written.  A
+ *     fault during execution surfaces, as in any CUDA call, at the next
+ *     synchronising call on that stream.
+ *   - No exception or C++ type crosses this boundary.
+ */
+#ifndef SWZ_H
+#define SWZ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum swz_status {
+    SWZ_OK = 0,
+    SWZ_ERR_NULL = 1,        /* a required pointer is NULL */
+    SWZ_ERR_PARAM = 2,       /* B, M, S, element size, direction or variant out of range */
+    SWZ_ERR_SHAPE = 3,       /* negative or overflowing sizes, tile not closed under sw */
+    SWZ_ERR_ALIGN = 4,       /* a pointer is not aligned to the element size */
+    SWZ_ERR_ALIAS = 5,       /* dst and src overlap (in-place is not supported) */
+    SWZ_ERR_CUDA = 6,        /* the CUDA runtime reported an error at launch */
+    SWZ_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (see swz_transpose) */
+    SWZ_ERR_UNSUPPORTED = 8  /* a valid request this build has no kernel for */
+} swz_status;
+
+/* Transpose staging variants (see swz_transpose). */
+enum {
+    SWZ_T_SWIZZLED = 0,   /* shared-memory tile under the per-size swizzle */
+    SWZ_T_UNSWIZZLED = 1, /* plain [T][T] tile: column access is bank-conflicted */
+    SWZ_T_PADDED = 2,     /* [T][T + pad] tile: conflict-free, wastes shared memory */
+    SWZ_T_TMA = 3         /* 16-bit data only: tile loaded by a TMA tensor copy
+                             with the hardware 128-byte swizzle */
+};
+
+/*
+ * Batched tile relayout.
+ *
+ * Source: "CUDA 013 - Swizzle 的工作原理", sections "更通用的映射规则" and
+ * "使用示例" (an element whose logical offset is o lives at the swizzled
+ * offset sw(o)); "NVIDIA CuTe Swizzle" and "cutlass 入门" for the parameters.
+ *
+ * dst, src : device buffers of n_tiles * rows * cols elements of esize bytes,
+ *            each tile stored contiguously, row-major (offset o = r * cols + c).
+ * esize    : 1, 2, 4, 8 or 16 bytes.  Elements are copied as raw bits.
+ * B, M, S  : swizzle parameters in element units; 0 <= B <= 16,
+ *            0 <= M <= 32, and when B > 0: 1 <= S <= 32, B + M + S <= 48.
+ *            S = 0 is rejected (it is not a bijection); 1 <= S < B is
+ *            accepted (a bijection, but not its own inverse).
+ * direction: 0 = forward, logical row-major to swizzled physical order:
+ *                dst[t][sw(i)] = src[t][i];
+ *            1 = inverse, swizzled physical to logical:
+ *                dst[t][i] = src[t][sw(i)].
+ *            Offsets i are local to each tile.
+ *
+ * Errors: SWZ_ERR_NULL (dst or src NULL with a non-empty request),
+ * SWZ_ERR_PARAM, SWZ_ERR_SHAPE (negative sizes, byte size overflowing
+ * int64, or rows * cols not a multiple of 2^(M + B), so that a tile would not
+ * be closed under sw), SWZ_ERR_ALIGN (dst or src not aligned to esize),
+ * SWZ_ERR_ALIAS (the two byte ranges overlap), SWZ_ERR_CUDA.
+ * An empty request (no element) returns SWZ_OK and launches nothing.
+ */
+swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t rows,
+                        int64_t cols, int esize, int B, int M, int S, int direction,
+                        void *stream);
+
+/*
+ * Matrix transpose HBM -> shared memory -> HBM.
+ *
+ * out[c][r] = in[r][c] for a rows x cols row-major matrix of esize-byte
+ * elements (raw bits).  The tile is staged in shared memory; the variant
+ * selects its layout.  The swizzled layouts are chosen per element size so
+ * that both the row-wise fill and the column-wise drain are free of bank
+ * conflicts ("CuTe Swizzle 学习手册", sections "冲突的典型场景" and
+ * "不同矩阵配置的选择指南"; "CUDA 013 - Swizzle 的工作原理", sections
+ * "如何避免 Bank Conflict", "swizzle 映射案例" and "行列位数"):
+ *   esize 4 : 32 x 32 units, element Swizzle<5,0,5> (column XOR row);
+ *   esize 8 : 16 x 16 units, element Swizzle<4,0,4>;
+ *   esize 2 : 128-byte rows (64 elements) under the byte-address Swizzle<3,4,3>
+ *             (16-byte chunk index XOR row mod 8; element Swizzle<3,3,3>),
+ *             drained by 8 x 8 transposing matrix loads;
+ *   esize 1, 16 : 32 x 32 units, element Swizzle<5,0,5>.
+ * SWZ_T_UNSWIZZLED uses the plain layout, SWZ_T_PADDED pads each row by one
+ * element (by 16 bytes for esize 2).  SWZ_T_TMA is accepted for esize 2 only.
+ *
+ * dst: cols x rows elements; src: rows x cols elements; both device buffers.
+ * rows, cols >= 0 (any value: edge tiles are handled element by element).
+ *
+ * Errors: SWZ_ERR_NULL, SWZ_ERR_PARAM (esize not in {1,2,4,8,16}, unknown
+ * variant, SWZ_T_TMA with esize != 2), SWZ_ERR_SHAPE, SWZ_ERR_ALIGN,
+ * SWZ_ERR_ALIAS, SWZ_ERR_CUDA.
+ */
+swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int esize,
+                         int variant, void *stream);
+
+/*
+ * Shared-memory bank-conflict profiler for warp access patterns.
+ *
+ * Model: 32 banks of 4 bytes, bank = (byte_addr / 4) % 32 ("CuTe Swizzle
+ * 学习手册", section "Shared Memory 的 Bank 结构"); lanes touching different
+ * 4-byte words of one bank are served one after another (N-way), lanes
+ * touching the same word are served together, including two 16-bit halves
+ * of one word ("CuTe Swizzle 学习手册", section "什么情况下产生冲突";
+ * "CUDA 013 - Swizzle 的工作原理", section "什么是 Bank Conflict"; "NVIDIA CuTe
+ * Swizzle").  An access wider than one pass can carry takes several passes
+ * and that minimum is not a conflict ("NVIDIA CuTe Swizzle").  The split
+ * into passes is not fixed by those sources; this library reads it as: up to
+ * 4 bytes per lane, one pass of 32 lanes; 8 bytes, two passes (lanes 0-15,
+ * 16-31); 16 bytes, four passes of 8 lanes.  In a pass each active lane
+ * touches the words floor(a/4) .. floor((a + w - 1)/4); the pass costs the
+ * largest number of distinct words in one bank.
+ *
+ * byte_addrs  : device, n x 32 uint32 byte addresses (pattern p, lane l at
+ *               p * 32 + l).
+ * active      : device, n uint32 lane masks, or NULL for all lanes active.
+ * access_bytes: 1, 2, 4, 8 or 16.
+ * ways        : device, n int32: the worst pass cost (1 = conflict-free,
+ *               0 = no active lane).
+ * wavefronts  : device, n int32: the sum of the pass costs.
+ *
+ * Errors: SWZ_ERR_NULL, SWZ_ERR_PARAM, SWZ_ERR_SHAPE (n < 0), SWZ_ERR_CUDA.
+ */
+swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, int64_t n,
+                            int access_bytes, int32_t *ways, int32_t *wavefronts,
+                            void *stream);
+
+/*
+ * Slice collision ("cutlass 入门", section "swizzle 融入 layout 优化").
+ *
+ * A is the largest index of a slice, so its set bits are the bits that can
+ * change.  C = A & ~sw(A).  C == 0 means no (Y_i, Z_i) pair of the swizzle has
+ * both bits active, so on this slice the swizzle equals a plain layout and
+ * can be folded into it; each set bit of C names a colliding Z bit.
+ *
+ * Host function, synchronous, no GPU involved.  C_out: host pointer.
+ * Errors: SWZ_ERR_NULL (C_out NULL), SWZ_ERR_PARAM (B, M, S out of the range
+ * of swz_relayout, or B + M + S > 64).
+ */
+swz_status swz_slice_collision(uint64_t A, int B, int M, int S, uint64_t *C_out);
+
+/*
+ * Batched slice collision on the GPU: C[k] = A[k] & ~sw(A[k]) for n masks.
+ * A, C: device arrays of n uint64.  Same parameter rules as
+ * swz_slice_collision; SWZ_ERR_SHAPE for n < 0.
+ */
+swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M, int S,
+                                     uint64_t *C, void *stream);
+
+/*
+ * Device status of bounded waits.
+ *
+ * The SWZ_T_TMA transpose waits on shared-memory barriers that its tensor
+ * copies complete; every such wait gives up after a time limit (2 s), records
+ * the expiry in a per-device status word and returns, leaving the context
+ * usable.  This call synchronises `stream`, then reads and clears the status
+ * word of the current device: SWZ_ERR_TIMEOUT if a wait gave up since the
+ * last call, SWZ_OK otherwise, SWZ_ERR_CUDA if the synchronisation or the
+ * read failed.  The status word is one 4-byte device allocation per device,
+ * made by the first SWZ_T_TMA call on that device and kept until exit.
+ */
+swz_status swz_device_status(void *stream);
+
+/*
+ * Self-test of the bounded wait: launches the SWZ_T_TMA transpose kernel
+ * with no tensor copy issued, so each of its waits expires after wait_ns
+ * nanoseconds; the kernel records SWZ_ERR_TIMEOUT and returns without
+ * writing dst.  Read the outcome with swz_device_status().  rows, cols > 0,
+ * cols a multiple of 8, src 16-byte aligned (SWZ_ERR_SHAPE, SWZ_ERR_ALIGN).
+ */
+swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, int64_t cols,
+                                    uint64_t wait_ns, void *stream);
+
+/* sw(x) on the host (the same function the kernels apply). */
+uint64_t swz_apply(uint64_t x, int B, int M, int S);
+
+/* A static, human-readable name of a status code. */
+const char *swz_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int swz_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWZ_H */

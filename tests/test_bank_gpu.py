@@ -1,0 +1,103 @@
+"""GPU bank profiler and batched slice collision against the CPU oracle
+(exact integer results)."""
+import numpy as np
+import pytest
+
+from gpu_util import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def swz():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import xor_swizzle_movement_gb300 as m
+    m.lib()
+    return m
+
+
+def gpu_profile(swz, pats, width, active=None):
+    n = pats.shape[0]
+    dp = torch.from_numpy(np.ascontiguousarray(pats, dtype=np.uint32).view(np.int32)).cuda()
+    da = None if active is None else torch.from_numpy(active.view(np.int32)).cuda()
+    w = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    f = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    swz.swz_bank_profile(dp, da, n, width, w, f)
+    torch.cuda.synchronize()
+    return w.cpu().numpy(), f.cpu().numpy()
+
+
+def structured_patterns():
+    """Column/row/broadcast/swizzled patterns of the oracle pins, as rows of 32 addresses."""
+    pats = []
+    for col in range(32):
+        pats.append([4 * (r * 32 + col) for r in range(32)])            # fp32 column
+        pats.append([4 * (r * 33 + col) for r in range(32)])            # padded
+        pats.append([4 * (r * 32 + (col ^ r)) for r in range(32)])      # XOR swizzle
+    pats.append([4 * c for c in range(32)])                             # row
+    pats.append([128] * 32)                                             # broadcast
+    pats.append([(l % 2) * 2 for l in range(32)])                       # halves of one word
+    pats.append([16 * l for l in range(32)])                            # 512 contiguous bytes
+    return np.array(pats, dtype=np.uint32)
+
+
+@pytest.mark.parametrize("width", [1, 2, 4, 8, 16])
+def test_structured(swz, orc, width):
+    pats = structured_patterns()
+    pats = (pats // width) * width  # aligned to the access width
+    gw, gf = gpu_profile(swz, pats, width)
+    ow, of = orc.bank_profile(pats, width)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
+@pytest.mark.parametrize("width", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("masked", [False, True])
+def test_random(swz, orc, width, aligned, masked):
+    from xor_swizzle_movement_gb300 import inputs
+    n = 8192
+    pats = inputs.bank_patterns(n, width, seed=5, aligned=aligned)
+    # narrow address ranges force collisions and shared words
+    pats[: n // 2] %= 512
+    act = inputs.active_masks(n, seed=6) if masked else None
+    if masked:
+        act[:16] = 0
+    gw, gf = gpu_profile(swz, pats, width, act)
+    ow, of = orc.bank_profile(pats, width, act)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
+@pytest.mark.slow
+def test_bench_size(swz, orc):
+    """2^22 aligned random 4-byte patterns: the benchmark's profiler batch."""
+    from xor_swizzle_movement_gb300 import inputs
+    n = 1 << 22
+    pats = inputs.bank_patterns(n, 4, seed=5)
+    gw, gf = gpu_profile(swz, pats, 4)
+    ow, of = orc.bank_profile(pats, 4)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
+def test_errors(swz):
+    w = torch.zeros(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(swz.SwzError) as e:
+        swz.swz_bank_profile(w, None, 1, 3, w, w)
+    assert e.value.status == swz.SWZ_ERR_PARAM
+    with pytest.raises(swz.SwzError) as e:
+        swz.swz_bank_profile(None, None, 1, 4, w, w)
+    assert e.value.status == swz.SWZ_ERR_NULL
+    swz.swz_bank_profile(None, None, 0, 4, None, None)  # empty
+
+
+@pytest.mark.parametrize("B,M,S", [(3, 2, 4), (3, 3, 3), (2, 0, 1), (5, 0, 5), (4, 4, 11)])
+def test_slice_collision_batch(swz, orc, B, M, S):
+    masks = np.concatenate([np.arange(1 << 16, dtype=np.uint64),
+                            np.random.default_rng(3).integers(0, 2**63, 4096, dtype=np.uint64)])
+    dA = torch.from_numpy(masks.view(np.int64)).cuda()
+    dC = torch.empty_like(dA)
+    swz.swz_slice_collision_batch(dA, masks.size, B, M, S, dC)
+    torch.cuda.synchronize()
+    got = dC.cpu().numpy().view(np.uint64)
+    for i in range(0, masks.size, 13):
+        assert int(got[i]) == orc.slice_collision(int(masks[i]), B=B, M=M, S=S)

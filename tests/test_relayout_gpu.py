@@ -1,0 +1,181 @@
+"""GPU relayout (swz_relayout through the C ABI) against the CPU oracle.
+
+Bit-exact comparisons: relayout is a permutation of raw element bits.
+Inputs are the seeded generators of xor_swizzle_movement_gb300.inputs."""
+import itertools
+
+import numpy as np
+import pytest
+
+from gpu_util import empty_device, guards_intact, to_device, to_host, torch, void_dtype
+
+pytestmark = pytest.mark.gpu
+
+SWEEP = [(B, M, S) for B in range(1, 6) for M in range(0, 5) for S in range(B, 8)]
+
+
+@pytest.fixture(scope="module")
+def swz():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import xor_swizzle_movement_gb300 as m
+    m.lib()
+    return m
+
+
+def run_relayout(swz, host, n_tiles, rows, cols, esize, B, M, S, direction, src_off=0, dst_off=0):
+    nbytes = host.nbytes
+    _, src = to_device(host, src_off)
+    full, dst = empty_device(nbytes, dst_off)
+    swz.swz_relayout(dst, src, n_tiles, rows, cols, esize, B, M, S, direction)
+    torch.cuda.synchronize()
+    assert guards_intact(full, dst_off, nbytes)
+    return to_host(dst, host.dtype)
+
+
+def test_small_fp16_tiles_sw333(swz, orc):
+    """256 tiles of 64 x 64 16-bit elements, Swizzle<3,3,3>, forward then inverse."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.uint16_bits(256 * 64 * 64, seed=0)
+    fwd = run_relayout(swz, host, 256, 64, 64, 2, 3, 3, 3, 0)
+    assert np.array_equal(fwd, orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=0))
+    inv = run_relayout(swz, host, 256, 64, 64, 2, 3, 3, 3, 1)
+    assert np.array_equal(inv, orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=1))
+    back = run_relayout(swz, fwd, 256, 64, 64, 2, 3, 3, 3, 1)
+    assert np.array_equal(back, host)
+
+
+@pytest.mark.slow
+def test_bf16_tiles_sw343_full(swz, orc):
+    """4096 bf16 tiles of 128 x 64 (64 MiB), Swizzle<3,4,3>, both directions."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.bf16_normal(4096 * 128 * 64, seed=1)
+    for direction in (0, 1):
+        got = run_relayout(swz, host, 4096, 128, 64, 2, 3, 4, 3, direction)
+        want = orc.relayout(host, tile_elems=128 * 64, B=3, M=4, S=3, direction=direction)
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("B,M,S", SWEEP)
+def test_uint16_sweep(swz, orc, B, M, S):
+    """Every (B, M, S) of the sweep on one 2^20-element uint16 buffer."""
+    from xor_swizzle_movement_gb300 import inputs
+    n = 1 << 20
+    host = inputs.random_bytes(2 * n, seed=4).view(np.uint16)
+    for direction in (0, 1):
+        got = run_relayout(swz, host, 1, 1, n, 2, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=n, B=B, M=M, S=S, direction=direction)
+        assert np.array_equal(got, want), direction
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B,M,S", [(1, 0, 1), (3, 3, 3), (5, 4, 7)])
+def test_uint16_sweep_1gib_sampled(swz, orc, B, M, S):
+    """A 1 GiB uint16 buffer as one tile: checked on a sample of 2^20
+    positions against the oracle's position map, plus forward then inverse
+    round trip on the whole buffer."""
+    n = 1 << 29
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    src = torch.randint(0, 256, (2 * n,), dtype=torch.uint8, device="cuda", generator=g)
+    fwd = torch.empty_like(src)
+    back = torch.empty_like(src)
+    swz.swz_relayout(fwd, src, 1, 1, n, 2, B, M, S, 0)
+    swz.swz_relayout(back, fwd, 1, 1, n, 2, B, M, S, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    rng = np.random.default_rng(1)
+    idx = np.sort(rng.choice(n, 1 << 20, replace=False)).astype(np.int64)
+    pos = orc.relayout_positions(idx, tile_elems=n, B=B, M=M, S=S)
+    s16 = src.view(torch.int16)
+    f16 = fwd.view(torch.int16)
+    ti = torch.from_numpy(idx).cuda()
+    tp = torch.from_numpy(pos).cuda()
+    # forward: logical element idx lands at physical pos
+    assert torch.equal(f16[tp], s16[ti])
+
+
+@pytest.mark.slow
+def test_int8_tiles_sw525_full(swz, orc):
+    """int8 tiles of 64 x 128 (1 GiB), Swizzle<5,2,5> (4-byte groups)."""
+    from xor_swizzle_movement_gb300 import inputs
+    n_tiles = (1 << 30) // (64 * 128)
+    host = inputs.random_bytes(1 << 30, seed=4)
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, 64, 128, 1, 5, 2, 5, direction)
+        want = orc.relayout(host, tile_elems=64 * 128, B=5, M=2, S=5, direction=direction)
+        assert np.array_equal(got, want), direction
+
+
+GRID_BMS = [(3, 0, 1), (3, 1, 2), (2, 0, 1), (4, 1, 1), (5, 0, 2), (3, 3, 3), (2, 5, 3), (1, 0, 1),
+            (4, 0, 4), (0, 2, 3), (5, 2, 5), (2, 2, 6)]
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("B,M,S", GRID_BMS)
+def test_esize_grid(swz, orc, esize, B, M, S):
+    """All element sizes, including S < B (not self-inverse), several tiles."""
+    from xor_swizzle_movement_gb300 import inputs
+    tile = 1 << (B + M + S)
+    rows, cols = (tile // 8, 8) if tile >= 8 else (1, tile)
+    n_tiles = 3
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=4).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, rows, cols, esize, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), direction
+
+
+@pytest.mark.parametrize("esize,rows,cols,B,M,S,n_tiles", [
+    (2, 3, 4, 2, 0, 1, 5),      # 24-byte tiles: element-by-element path
+    (4, 5, 16, 2, 1, 2, 7),     # 320-byte tiles, period 32 does not divide 80
+    (2, 24, 64, 3, 3, 3, 9),    # period 512 does not divide 1536: tile-local offsets
+    (1, 3, 64, 3, 2, 3, 11),    # tile-local offsets, 192-byte tiles
+    (8, 6, 8, 2, 1, 3, 5),      # 384-byte tiles, period 64 does not divide 48
+    (16, 3, 4, 2, 0, 2, 3),     # 16-byte elements, tile-local
+])
+def test_ragged_tiles(swz, orc, esize, rows, cols, B, M, S, n_tiles):
+    from xor_swizzle_movement_gb300 import inputs
+    tile = rows * cols
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=7).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, rows, cols, esize, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes()
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8])
+def test_misaligned_pointers(swz, orc, esize):
+    """Pointers aligned to the element size but not to 16 bytes."""
+    from xor_swizzle_movement_gb300 import inputs
+    B, M, S, rows, cols, n_tiles = 3, 1, 3, 16, 8, 6
+    host = inputs.random_bytes(n_tiles * rows * cols * esize, seed=8).view(void_dtype(esize))
+    got = run_relayout(swz, host, n_tiles, rows, cols, esize, B, M, S, 0, src_off=esize, dst_off=3 * esize)
+    want = orc.relayout(host, tile_elems=rows * cols, B=B, M=M, S=S, direction=0)
+    assert got.tobytes() == want.tobytes()
+
+
+def test_empty_and_errors(swz):
+    _, a = empty_device(4096)
+    _, b = empty_device(4096)
+    # empty requests launch nothing and succeed
+    swz.swz_relayout(b, a, 0, 64, 64, 2, 3, 3, 3, 0)
+    swz.swz_relayout(b, a, 5, 0, 64, 2, 3, 3, 3, 0)
+    cases = [
+        (dict(n_tiles=1, rows=3, cols=4, esize=2, B=2, M=2, S=2), swz.SWZ_ERR_SHAPE),  # 12 % 16 != 0
+        (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=0), swz.SWZ_ERR_PARAM),  # S = 0
+        (dict(n_tiles=1, rows=8, cols=8, esize=3, B=3, M=0, S=3), swz.SWZ_ERR_PARAM),  # esize
+        (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=-1), swz.SWZ_ERR_PARAM),
+        (dict(n_tiles=-1, rows=8, cols=8, esize=2, B=3, M=0, S=3), swz.SWZ_ERR_SHAPE),
+    ]
+    for kw, status in cases:
+        with pytest.raises(swz.SwzError) as e:
+            swz.swz_relayout(b, a, kw["n_tiles"], kw["rows"], kw["cols"], kw["esize"], kw["B"], kw["M"],
+                             kw["S"], 0)
+        assert e.value.status == status, kw
+    with pytest.raises(swz.SwzError) as e:
+        swz.swz_relayout(a, a, 1, 8, 8, 2, 3, 0, 3, 0)
+    assert e.value.status == swz.SWZ_ERR_ALIAS
+    with pytest.raises(swz.SwzError) as e:
+        swz.swz_relayout(a[1:], b, 1, 8, 8, 2, 3, 0, 3, 0)
+    assert e.value.status == swz.SWZ_ERR_ALIGN

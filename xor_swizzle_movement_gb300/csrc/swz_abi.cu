@@ -1,0 +1,142 @@
+// swz_abi.cu -- the C ABI declared in include/swz.h: argument validation,
+// dispatch to the kernels, status codes.  Nothing here allocates memory.
+#include "swz_common.cuh"
+
+namespace swz {
+
+swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize,
+                           int B, int M, int S, int direction, cudaStream_t st);
+swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
+                            cudaStream_t st);
+swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, int64_t n, int width,
+                               int32_t *ways, int32_t *wavefronts, cudaStream_t st);
+swz_status slice_collision_launch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
+                                  cudaStream_t st);
+
+swz_status launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SWZ_OK : SWZ_ERR_CUDA;
+}
+
+bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+namespace {
+
+bool valid_esize(int e) { return e == 1 || e == 2 || e == 4 || e == 8 || e == 16; }
+
+// B, M, S in element units.  S = 0 makes the map non-injective; negative S
+// (the YYY field moved below ZZZ) has no formula on the pages.
+bool valid_bms(int B, int M, int S, int max_total) {
+    if (B < 0 || B > 16 || M < 0 || M > 32) return false;
+    if (B == 0) return S >= 0 && S <= 32;
+    return S >= 1 && S <= 32 && B + M + S <= max_total;
+}
+
+// a * b without int64 overflow (a, b >= 0)
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+bool aligned_to(const void *p, int64_t n) { return (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(n)) == 0; }
+
+}  // namespace
+}  // namespace swz
+
+extern "C" {
+
+swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t rows, int64_t cols,
+                        int esize, int B, int M, int S, int direction, void *stream) {
+    using namespace swz;
+    if (!valid_esize(esize) || !valid_bms(B, M, S, 48) || (direction != 0 && direction != 1))
+        return SWZ_ERR_PARAM;
+    if (n_tiles < 0 || rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
+    int64_t tile_elems, n_elems, n_bytes;
+    if (!mul_ok(rows, cols, &tile_elems) || !mul_ok(n_tiles, tile_elems, &n_elems) ||
+        !mul_ok(n_elems, esize, &n_bytes))
+        return SWZ_ERR_SHAPE;
+    if (n_elems == 0) return SWZ_OK;
+    if (tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
+    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+    return relayout_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction,
+                           static_cast<cudaStream_t>(stream));
+}
+
+swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int esize, int variant,
+                         void *stream) {
+    using namespace swz;
+    if (!valid_esize(esize) || variant < SWZ_T_SWIZZLED || variant > SWZ_T_TMA) return SWZ_ERR_PARAM;
+    if (variant == SWZ_T_TMA && esize != 2) return SWZ_ERR_PARAM;
+    if (rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
+    int64_t n_elems, n_bytes;
+    if (!mul_ok(rows, cols, &n_elems) || !mul_ok(n_elems, esize, &n_bytes)) return SWZ_ERR_SHAPE;
+    if (n_elems == 0) return SWZ_OK;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
+    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+    return transpose_launch(dst, src, rows, cols, esize, variant, static_cast<cudaStream_t>(stream));
+}
+
+swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, int64_t n,
+                            int access_bytes, int32_t *ways, int32_t *wavefronts, void *stream) {
+    using namespace swz;
+    if (!valid_esize(access_bytes)) return SWZ_ERR_PARAM;
+    if (n < 0 || n > INT64_MAX / 128) return SWZ_ERR_SHAPE;
+    if (n == 0) return SWZ_OK;
+    if (!byte_addrs || !ways || !wavefronts) return SWZ_ERR_NULL;
+    if (!aligned_to(byte_addrs, 4) || !aligned_to(ways, 4) || !aligned_to(wavefronts, 4) ||
+        (active && !aligned_to(active, 4)))
+        return SWZ_ERR_ALIGN;
+    return bank_profile_launch(byte_addrs, active, n, access_bytes, ways, wavefronts,
+                               static_cast<cudaStream_t>(stream));
+}
+
+swz_status swz_slice_collision(uint64_t A, int B, int M, int S, uint64_t *C_out) {
+    using namespace swz;
+    if (!valid_bms(B, M, S, 64)) return SWZ_ERR_PARAM;
+    if (!C_out) return SWZ_ERR_NULL;
+    *C_out = A & ~sw_fwd(A, B, M, S);
+    return SWZ_OK;
+}
+
+swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
+                                     void *stream) {
+    using namespace swz;
+    if (!valid_bms(B, M, S, 64)) return SWZ_ERR_PARAM;
+    if (n < 0) return SWZ_ERR_SHAPE;
+    if (n == 0) return SWZ_OK;
+    if (!A || !C) return SWZ_ERR_NULL;
+    if (!aligned_to(A, 8) || !aligned_to(C, 8)) return SWZ_ERR_ALIGN;
+    if (ranges_overlap(A, n * 8, C, n * 8) && A != C) return SWZ_ERR_ALIAS;
+    return slice_collision_launch(A, n, B, M, S, C, static_cast<cudaStream_t>(stream));
+}
+
+uint64_t swz_apply(uint64_t x, int B, int M, int S) {
+    if (!swz::valid_bms(B, M, S, 64)) return x;
+    return swz::sw_fwd(x, B, M, S);
+}
+
+const char *swz_status_string(int status) {
+    switch (status) {
+        case SWZ_OK: return "SWZ_OK";
+        case SWZ_ERR_NULL: return "SWZ_ERR_NULL: a required pointer is NULL";
+        case SWZ_ERR_PARAM: return "SWZ_ERR_PARAM: swizzle parameter, element size, direction or variant out of range";
+        case SWZ_ERR_SHAPE: return "SWZ_ERR_SHAPE: bad sizes or a tile not closed under the swizzle";
+        case SWZ_ERR_ALIGN: return "SWZ_ERR_ALIGN: pointer not aligned to the element size";
+        case SWZ_ERR_ALIAS: return "SWZ_ERR_ALIAS: dst and src overlap";
+        case SWZ_ERR_CUDA: return "SWZ_ERR_CUDA: CUDA launch error";
+        case SWZ_ERR_TIMEOUT: return "SWZ_ERR_TIMEOUT: a bounded device wait gave up";
+        case SWZ_ERR_UNSUPPORTED: return "SWZ_ERR_UNSUPPORTED: no kernel for this request";
+        default: return "unknown swz_status";
+    }
+}
+
+int swz_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,276 @@
+// swz_relayout.cu -- batched tile relayout between logical row-major order and
+// Swizzle<B,M,S> physical order (sm_103a).
+//
+// Both directions are written as a gather over DESTINATION elements, so every
+// thread stores to consecutive 16-byte vectors:
+//   inverse  dst[i] = src[sw(i)]            -> source of y is sw(y)
+//   forward  dst[sw(i)] = src[i]            -> source of y is sw^-1(y)
+// (sw^-1 == sw when S >= B; otherwise the unitriangular inverse, see sw_inv.)
+//
+// Why a 16-byte vector always maps to ONE source vector: bit p of sw(x) (and
+// of sw^-1(x)) depends only on bits p and above of x, because the field that
+// is read (starting at M + S, S >= 1) sits above the field that is written.
+// So the bits of the source offset at and above log2(16 / esize) depend only
+// on the same bits of the destination offset: all lanes of a destination
+// vector come from one source vector, permuted inside it.  The kernel is one
+// 16-byte load, an in-register lane permutation, one 16-byte store.  A warp's
+// 32 source vectors are a permutation of one aligned 512-byte block (the bits
+// above the warp's span are again only read), so loads stay coalesced.
+//
+// The in-register lane permutation has three forms, chosen on the host:
+//   kLanesFixed   M >= log2 V: groups of 2^M elements cover whole vectors,
+//                 the lanes are not moved at all;
+//   kLanesXor     M + S >= log2 V: the XOR constant is the same for every lane
+//                 of the vector, the permutation is lane -> lane ^ L;
+//   kLanesGeneral otherwise: per-lane source computed from the swizzle.
+#include "swz_common.cuh"
+
+namespace swz {
+namespace {
+
+enum LaneMode { kLanesFixed = 0, kLanesXor = 1, kLanesGeneral = 2 };
+
+struct RelayoutArgs {
+    uint4 *dst;
+    const uint4 *src;
+    int64_t nvec;       // 16-byte vectors in the whole buffer
+    int64_t tile_vecs;  // 16-byte vectors per tile
+    int B, M, S;
+    int steps;          // 1: source = sw(y); >1: source = sw^-1(y) by `steps` iterations
+    int per_thread;     // vectors per thread, 1..4
+};
+
+template <int E>
+struct VecTraits {
+    static constexpr int V = 16 / E;  // lanes (elements) per vector
+    static constexpr int LV = (E == 1) ? 4 : (E == 2) ? 3 : (E == 4) ? 2 : (E == 8) ? 1 : 0;
+};
+
+__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t i) {
+    const uint32_t lo = (i & 1u) ? a1 : a0;
+    const uint32_t hi = (i & 1u) ? a3 : a2;
+    return (i & 2u) ? hi : lo;
+}
+
+// out lane l = in lane l ^ L
+template <int E>
+__device__ __forceinline__ uint4 lanes_xor(uint4 v, uint32_t L) {
+    if constexpr (E == 16) {
+        return v;
+    } else {
+        uint32_t wx;
+        if constexpr (E == 8) wx = L << 1;
+        else if constexpr (E == 4) wx = L;
+        else if constexpr (E == 2) wx = L >> 1;
+        else wx = L >> 2;
+        uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w, t;
+        if (wx & 1u) { t = w0; w0 = w1; w1 = t; t = w2; w2 = w3; w3 = t; }
+        if (wx & 2u) { t = w0; w0 = w2; w2 = t; t = w1; w1 = w3; w3 = t; }
+        if constexpr (E == 2) {
+            if (L & 1u) {
+                w0 = __byte_perm(w0, 0, 0x1032); w1 = __byte_perm(w1, 0, 0x1032);
+                w2 = __byte_perm(w2, 0, 0x1032); w3 = __byte_perm(w3, 0, 0x1032);
+            }
+        }
+        if constexpr (E == 1) {
+            const uint32_t sel = 0x3210u ^ (0x1111u * (L & 3u));
+            w0 = __byte_perm(w0, 0, sel); w1 = __byte_perm(w1, 0, sel);
+            w2 = __byte_perm(w2, 0, sel); w3 = __byte_perm(w3, 0, sel);
+        }
+        return make_uint4(w0, w1, w2, w3);
+    }
+}
+
+// out lane l = in lane (g(y + l) mod V), g = the gather function
+template <int E>
+__device__ __forceinline__ uint4 lanes_general(uint4 v, uint64_t y, const RelayoutArgs &a) {
+    constexpr int V = VecTraits<E>::V;
+    if constexpr (E == 16) {
+        return v;
+    } else {
+        uint32_t p[V];
+#pragma unroll
+        for (int l = 0; l < V; ++l)
+            p[l] = static_cast<uint32_t>(sw_inv(y + l, a.B, a.M, a.S, a.steps)) & (V - 1);
+        const uint32_t i0 = v.x, i1 = v.y, i2 = v.z, i3 = v.w;
+        uint32_t o[4];
+        if constexpr (E == 8) {
+#pragma unroll
+            for (int l = 0; l < 2; ++l) {
+                o[2 * l] = p[l] ? i2 : i0;
+                o[2 * l + 1] = p[l] ? i3 : i1;
+            }
+        } else if constexpr (E == 4) {
+#pragma unroll
+            for (int l = 0; l < 4; ++l) o[l] = pick4(i0, i1, i2, i3, p[l]);
+        } else if constexpr (E == 2) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t pa = p[2 * k], pb = p[2 * k + 1];
+                const uint32_t wa = pick4(i0, i1, i2, i3, pa >> 1);
+                const uint32_t wb = pick4(i0, i1, i2, i3, pb >> 1);
+                const uint32_t ha = (pa & 1u) * 2u, hb = 4u + (pb & 1u) * 2u;
+                const uint32_t sel = ha | ((ha + 1u) << 4) | (hb << 8) | ((hb + 1u) << 12);
+                o[k] = __byte_perm(wa, wb, sel);
+            }
+        } else {  // E == 1
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t p0 = p[4 * k], p1 = p[4 * k + 1], p2 = p[4 * k + 2], p3 = p[4 * k + 3];
+                const uint32_t lo = __byte_perm(pick4(i0, i1, i2, i3, p0 >> 2),
+                                                pick4(i0, i1, i2, i3, p1 >> 2),
+                                                (p0 & 3u) | ((4u + (p1 & 3u)) << 4));
+                const uint32_t hi = __byte_perm(pick4(i0, i1, i2, i3, p2 >> 2),
+                                                pick4(i0, i1, i2, i3, p3 >> 2),
+                                                (p2 & 3u) | ((4u + (p3 & 3u)) << 4));
+                o[k] = __byte_perm(lo, hi, 0x5410);
+            }
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <int E, int MODE, bool LOCAL>
+__global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a) {
+    constexpr int LV = VecTraits<E>::LV;
+    constexpr uint64_t VM = (1u << LV) - 1u;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
+    uint4 r[4];
+    uint64_t yk[4];
+    uint32_t lx[4];
+    // all loads first, so that each thread keeps up to four 16-byte loads in flight
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if (k < a.per_thread && u < a.nvec) {
+            int64_t local = u, tile0 = 0;
+            if constexpr (LOCAL) {
+                local = u % a.tile_vecs;
+                tile0 = u - local;
+            }
+            const uint64_t y = static_cast<uint64_t>(local) << LV;
+            const uint64_t x = sw_inv(y, a.B, a.M, a.S, a.steps);
+            r[k] = ld_stream16(a.src + tile0 + static_cast<int64_t>(x >> LV));
+            yk[k] = y;
+            lx[k] = static_cast<uint32_t>((x ^ y) & VM);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if (k < a.per_thread && u < a.nvec) {
+            uint4 out;
+            if constexpr (MODE == kLanesFixed) out = r[k];
+            else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
+            else out = lanes_general<E>(r[k], yk[k], a);
+            st_stream16(a.dst + u, out);
+        }
+    }
+}
+
+template <int E>
+struct ElemType;
+template <> struct ElemType<1> { using T = uint8_t; };
+template <> struct ElemType<2> { using T = uint16_t; };
+template <> struct ElemType<4> { using T = uint32_t; };
+template <> struct ElemType<8> { using T = uint2; };
+template <> struct ElemType<16> { using T = uint4; };
+
+// One element per iteration; used when a tile is not a whole number of
+// 16-byte vectors or a pointer is not 16-byte aligned.
+template <int E>
+__global__ void __launch_bounds__(256)
+    relayout_scalar_kernel(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int B,
+                           int M, int S, int steps) {
+    using T = typename ElemType<E>::T;
+    T *d = static_cast<T *>(dst);
+    const T *s = static_cast<const T *>(src);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_elems;
+         i += stride) {
+        const int64_t local = i % tile_elems;
+        const int64_t tile0 = i - local;
+        const uint64_t x = sw_inv(static_cast<uint64_t>(local), B, M, S, steps);
+        d[i] = s[tile0 + static_cast<int64_t>(x)];
+    }
+}
+
+template <int E>
+swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, cudaStream_t st) {
+    const int threads = 256;
+    const int64_t per_cta = static_cast<int64_t>(threads) * a.per_thread;
+    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const dim3 g(static_cast<unsigned>(grid));
+#define SWZ_LAUNCH(MODE, LOCAL) relayout_vec_kernel<E, MODE, LOCAL><<<g, threads, 0, st>>>(a)
+    if (local) {
+        if (mode == kLanesFixed) SWZ_LAUNCH(kLanesFixed, true);
+        else if (mode == kLanesXor) SWZ_LAUNCH(kLanesXor, true);
+        else SWZ_LAUNCH(kLanesGeneral, true);
+    } else {
+        if (mode == kLanesFixed) SWZ_LAUNCH(kLanesFixed, false);
+        else if (mode == kLanesXor) SWZ_LAUNCH(kLanesXor, false);
+        else SWZ_LAUNCH(kLanesGeneral, false);
+    }
+#undef SWZ_LAUNCH
+    return launch_status();
+}
+
+template <int E>
+swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, int B, int M, int S,
+                         int steps, cudaStream_t st) {
+    const int threads = 256;
+    int64_t grid = (n + threads - 1) / threads;
+    if (grid > 152LL * 32) grid = 152LL * 32;
+    relayout_scalar_kernel<E><<<static_cast<unsigned>(grid), threads, 0, st>>>(dst, src, n, tile, B,
+                                                                                 M, S, steps);
+    return launch_status();
+}
+
+}  // namespace
+
+// Arguments are validated by the caller (swz_relayout in swz_abi.cu).
+swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems,
+                           int esize, int B, int M, int S, int direction, cudaStream_t st) {
+    const int64_t n_elems = n_tiles * tile_elems;
+    const int steps = (direction == 0 && B > 0 && S < B) ? (B + S - 1) / S : 1;
+    const int64_t tile_bytes = tile_elems * esize;
+    const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    if (tile_bytes % 16 == 0 && aligned16) {
+        int lv = 0;
+        while ((1 << lv) < 16 / esize) ++lv;
+        RelayoutArgs a;
+        a.dst = static_cast<uint4 *>(dst);
+        a.src = static_cast<const uint4 *>(src);
+        a.nvec = n_elems * esize / 16;
+        a.tile_vecs = tile_bytes / 16;
+        a.B = B; a.M = M; a.S = S;
+        a.steps = steps;
+        // keep each SM fed: up to four vectors per thread once the grid is
+        // several waves deep (152 SMs x 2048 threads per wave)
+        const int64_t wave = 152LL * 2048;
+        a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+        const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
+        const int period = B + M + S;
+        const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
+        switch (esize) {
+            case 1: return launch_vec<1>(a, mode, local, st);
+            case 2: return launch_vec<2>(a, mode, local, st);
+            case 4: return launch_vec<4>(a, mode, local, st);
+            case 8: return launch_vec<8>(a, mode, local, st);
+            case 16: return launch_vec<16>(a, mode, local, st);
+            default: return SWZ_ERR_PARAM;
+        }
+    }
+    switch (esize) {
+        case 1: return launch_scalar<1>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 2: return launch_scalar<2>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 4: return launch_scalar<4>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 8: return launch_scalar<8>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 16: return launch_scalar<16>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        default: return SWZ_ERR_PARAM;
+    }
+}
+
+}  // namespace swz

@@ -1,0 +1,304 @@
+// swz_tma.cu -- 16-bit transpose whose tiles enter shared memory through TMA
+// tensor copies with the hardware 128-byte swizzle (sm_103a).
+//
+// The hardware 128-byte swizzle mode places 16-byte chunk c of box row r at
+// chunk position c ^ (r mod 8) inside each 1024-byte span, which is the
+// byte-address Swizzle<3,4,3> ("CuTe Swizzle 学习手册", sections "Sw<3,4,3>
+// vs Sw<3,3,3>" and "H100 TMA + Swizzle"): with 64-element (128-byte) box
+// rows it is exactly the layout of the SWZ_T_SWIZZLED 16-bit kernel, so the
+// same conflict-free transposing matrix loads drain it.
+//
+// Persistent kernel: each CTA walks tiles blockIdx.x, +gridDim.x, ...; a
+// ring of kStages shared buffers keeps kStages tile loads in flight while the
+// current tile is drained.  One elected thread issues the copies; each buffer
+// has an mbarrier that the copy completes.  Every wait on an mbarrier is
+// bounded by a time limit; on expiry the kernel records SWZ_ERR_TIMEOUT in a
+// per-device status word, waits (again bounded) for its own copies still in
+// flight, and returns; swz_device_status() reports it to the host.
+#include "swz_common.cuh"
+
+#include <cuda.h>
+#include <mutex>
+
+namespace swz {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTile = 64;                        // 64 x 64 elements
+constexpr int kTileBytes = kTile * kTile * 2;    // 8 KiB
+constexpr int kThreads = 128;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &d0, uint32_t &d1,
+                                                  uint32_t &d2, uint32_t &d3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, int i) {
+    const uint32_t lo = (i & 1) ? a1 : a0;
+    const uint32_t hi = (i & 1) ? a3 : a2;
+    return (i & 2) ? hi : lo;
+}
+
+struct TmaArgs {
+    uint16_t *dst;
+    int64_t R, C, tiles_c, n_tiles;
+    int vec_store_ok;
+    int issue_copies;   // 0 only in the timeout self-test: no copy is issued, every wait expires
+    uint64_t wait_ns;
+    uint32_t *status;   // per-device status word
+};
+
+__global__ void __launch_bounds__(kThreads)
+    transpose16_tma_kernel(const __grid_constant__ CUtensorMap map, const TmaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kStages];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
+    uint8_t *const gbase = smem_raw + (base - raw);
+    const int tid = threadIdx.x;
+    const uint32_t bar0 = smem_u32(&bars[0]);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int s, int64_t t) {
+        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
+        mbar_expect_tx(bar0 + 8u * s, kTileBytes);
+        tma_load_2d(base + s * kTileBytes, &map, static_cast<int>(tc * kTile), static_cast<int>(tr * kTile),
+                    bar0 + 8u * s);
+    };
+    if (tid == 0 && a.issue_copies) {
+        for (int s = 0; s < kStages; ++s) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (t < a.n_tiles) issue(s, t);
+        }
+    }
+
+    const int lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, kk = lane & 3, m = lane >> 3, i8 = lane & 7;
+    int64_t it = 0;
+    for (;; ++it) {
+        const int64_t t = blockIdx.x + it * gridDim.x;
+        if (t >= a.n_tiles) break;
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t parity = static_cast<uint32_t>((it / kStages) & 1);
+        const bool ok = mbar_wait_bounded(bar0 + 8u * s, parity, a.wait_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
+            // let this CTA's copies still in flight land before the CTA exits
+            if (a.issue_copies) {
+                for (int64_t j = it; j < it + kStages; ++j) {
+                    const int64_t tj = blockIdx.x + j * gridDim.x;
+                    if (tj >= a.n_tiles) break;
+                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kStages),
+                                      static_cast<uint32_t>((j / kStages) & 1), a.wait_ns);
+                }
+            }
+            return;
+        }
+        const uint16_t *sm = reinterpret_cast<const uint16_t *>(gbase + s * kTileBytes);
+        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
+        const int64_t r0 = tr * kTile, c0 = tc * kTile;
+        if (a.vec_store_ok && r0 + kTile <= a.R && c0 + kTile <= a.C) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int xi = warp * 4 + k;
+                const int cb = xi & 7, rbg = (xi >> 3) * 4;
+                const int row = (rbg + m) * 8 + i8;
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(base + s * kTileBytes + row * 128 + ((cb ^ (row & 7)) << 4), a0, a1, a2, a3);
+                uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int from = kk ^ r;
+                    const uint32_t send = pick4(a0, a1, a2, a3, from);
+                    const uint32_t got = r ? __shfl_xor_sync(kFullMask, send, r) : send;
+                    b0 = (from == 0) ? got : b0;
+                    b1 = (from == 1) ? got : b1;
+                    b2 = (from == 2) ? got : b2;
+                    b3 = (from == 3) ? got : b3;
+                }
+                st_stream16(a.dst + (c0 + cb * 8 + g) * a.R + r0 + (rbg + kk) * 8, make_uint4(b0, b1, b2, b3));
+            }
+        } else {
+            for (int idx = tid; idx < kTile * kTile; idx += kThreads) {
+                const int ocl = idx / kTile, orow = idx % kTile;
+                if (c0 + ocl < a.C && r0 + orow < a.R)
+                    a.dst[(c0 + ocl) * a.R + r0 + orow] = sm[orow * 64 + (((ocl >> 3) ^ (orow & 7)) << 3) + (ocl & 7)];
+            }
+        }
+        __syncthreads();  // every thread is done with buffer s
+        if (tid == 0 && a.issue_copies) {
+            const int64_t tn = t + static_cast<int64_t>(kStages) * gridDim.x;
+            if (tn < a.n_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(s, tn);
+            }
+        }
+    }
+}
+
+// ---- host side ---------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+uint32_t *g_status[kMaxDevices] = {};
+
+}  // namespace
+
+// The per-device status word (allocated once per device, on first use).
+uint32_t *device_status_word(bool create) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status[dev] && create) {
+        uint32_t *p = nullptr;
+        if (cudaMalloc(&p, sizeof(uint32_t)) != cudaSuccess) return nullptr;
+        if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) { cudaFree(p); return nullptr; }
+        g_status[dev] = p;
+    }
+    return g_status[dev];
+}
+
+swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
+                            cudaStream_t st);
+
+swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st,
+                             int issue_copies, uint64_t wait_ns) {
+    // TMA needs 16-byte aligned source rows and int32 coordinates; otherwise
+    // the shared-memory-staged swizzled kernel does the same job.
+    const bool tma_ok = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (C % 8) == 0 && R < (1LL << 31) &&
+                        C < (1LL << 31);
+    EncodeTiledFn encode = encode_fn();
+    if (!tma_ok || !encode) return transpose_launch(dst, src, R, C, 2, SWZ_T_SWIZZLED, st);
+    uint32_t *status = device_status_word(true);
+    if (!status) return SWZ_ERR_CUDA;
+
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(C) * 2};
+    const cuuint32_t box[2] = {kTile, kTile};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(src), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SWZ_ERR_CUDA;
+
+    TmaArgs a;
+    a.dst = static_cast<uint16_t *>(dst);
+    a.R = R;
+    a.C = C;
+    a.tiles_c = (C + kTile - 1) / kTile;
+    a.n_tiles = ((R + kTile - 1) / kTile) * a.tiles_c;
+    a.vec_store_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (R % 8 == 0);
+    a.issue_copies = issue_copies;
+    a.wait_ns = wait_ns;
+    a.status = status;
+    const int smem = kStages * kTileBytes + 1024;
+    int grid = 152 * 4;
+    if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
+    transpose16_tma_kernel<<<grid, kThreads, smem, st>>>(map, a);
+    return launch_status();
+}
+
+swz_status transpose_tma_launch(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st) {
+    return transpose_tma_run(dst, src, R, C, st, 1, kWaitLimitNs);
+}
+
+}  // namespace swz
+
+extern "C" {
+
+// Waits for `stream`, then reads and clears the calling device's status word.
+swz_status swz_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SWZ_ERR_CUDA;
+    uint32_t *w = swz::device_status_word(false);
+    if (!w) return SWZ_OK;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SWZ_ERR_CUDA;
+    if (v && cudaMemset(w, 0, sizeof v) != cudaSuccess) return SWZ_ERR_CUDA;
+    return (v & (1u << SWZ_ERR_TIMEOUT)) ? SWZ_ERR_TIMEOUT : SWZ_OK;
+}
+
+// Self-test of the bounded wait: runs the TMA transpose kernel with no copy
+// issued, so every mbarrier wait expires after wait_ns nanoseconds and the
+// kernel must record SWZ_ERR_TIMEOUT and return.  dst is not written.
+swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, int64_t cols,
+                                    uint64_t wait_ns, void *stream) {
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (rows <= 0 || cols <= 0 || cols % 8 != 0) return SWZ_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) return SWZ_ERR_ALIGN;
+    return swz::transpose_tma_run(dst, src, rows, cols, static_cast<cudaStream_t>(stream), 0, wait_ns);
+}
+
+}  // extern "C"

@@ -1,0 +1,310 @@
+// swz_transpose.cu -- HBM -> shared memory -> HBM transpose with the tile
+// staged under a per-element-size swizzle (sm_103a).
+//
+// Every kernel fills the shared tile row-wise (coalesced 16-byte global
+// loads) and drains it column-wise (coalesced 16-byte global stores of the
+// transposed rows).  The column-wise drain is where a plain row-major tile
+// serialises: all rows of one column sit in one bank ("CuTe Swizzle 学习手册",
+// section "冲突的典型场景").  The variants differ only in where element
+// (row, col) of a tile lives in shared memory:
+//   SWZ_T_SWIZZLED    the column index is XOR-ed with the row index (the
+//                     swizzle of the element size, below);
+//   SWZ_T_UNSWIZZLED  plain [T][T];
+//   SWZ_T_PADDED      [T][T + 1] ("CUDA 013 - Swizzle 的工作原理", section
+//                     "如何避免 Bank Conflict").
+//
+// Element sizes 4 and 8: units of N x N elements with 128-byte rows (N = 32
+// for 4 bytes, 16 for 8 bytes) under element Swizzle<log2 N, 0, log2 N>, i.e.
+// physical column = column ^ row inside a unit ("CUDA 013 - Swizzle 的工作原理",
+// sections "swizzle 映射案例" and "行列位数": 32 x 32 units for 4-byte
+// elements, 16 x 16 for 8-byte ones).  Shared accesses are per element; with
+// the thread mapping below, each warp-wide store touches 4 rows x one unit
+// width and each warp-wide load 4 columns x one unit height, and the XOR
+// spreads both over all 32 banks.
+//
+// Element size 2: tiles of 64 x 64 with 128-byte rows under the
+// byte-address Swizzle<3,4,3> (16-byte chunk index XOR row mod 8, equal to
+// element Swizzle<3,3,3>; "CuTe Swizzle 学习手册", sections "Sw<3,4,3> vs
+// Sw<3,3,3>" and "不同矩阵配置的选择指南").  The tile is filled with 16-byte
+// stores and drained with transposing 8 x 8 matrix loads (ldmatrix .trans):
+// the eight rows of one 8 x 8 block are read from eight different chunk
+// positions, so each matrix load is one conflict-free pass.  Four lanes then
+// exchange 32-bit words so that each lane owns 16 contiguous output bytes.
+//
+// Element sizes 1 and 16: 32 x 32 units under element Swizzle<5,0,5>, one
+// element per access.
+//
+// Tiles that cross the matrix edge, and matrices whose rows are not whole
+// 16-byte vectors, go element by element with bounds checks through the same
+// shared layout.
+#include "swz_common.cuh"
+
+#include <cstring>
+
+namespace swz {
+namespace {
+
+// ---------------------------------------------------------------- 4 / 8 B --
+template <typename T, int VARIANT, int UR, int UC, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+    transpose_unit_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
+                          int64_t tiles_c, int vec_ok) {
+    constexpr int N = 128 / static_cast<int>(sizeof(T));    // unit edge: 32 (4 B) or 16 (8 B)
+    constexpr int VPE = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte vector
+    constexpr int P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;  // unit row pitch, elements
+    constexpr int TR = UR * N, TC = UC * N;                 // tile edge, elements
+    constexpr int NV = TR * TC / VPE;                       // 16-byte vectors per tile
+    constexpr int ITER = NV / THREADS;
+    static_assert(NV % THREADS == 0, "tile must divide evenly over the threads");
+    static_assert(8 * VPE == N, "a unit row is eight 16-byte vectors");
+    __shared__ T sm[UR * UC * N * P];
+
+    const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
+    const int64_t tc = static_cast<int64_t>(blockIdx.x) - tr * tiles_c;
+    const int64_t r0 = tr * TR, c0 = tc * TC;
+    const int tid = threadIdx.x;
+    auto phys = [](int ir, int ic) -> int { return VARIANT == SWZ_T_SWIZZLED ? (ic ^ ir) : ic; };
+
+    if (vec_ok && r0 + TR <= R && c0 + TC <= C) {
+        uint4 v[ITER];
+        // fill: a warp covers 4 tile rows x one unit width (8 vectors per row)
+#pragma unroll
+        for (int k = 0; k < ITER; ++k) {
+            const int id = k * THREADS + tid;
+            const int lane = id & 31, wb = id >> 5;
+            const int q = lane & 7, row = (wb / UC) * 4 + (lane >> 3), uc = wb % UC;
+            v[k] = ld_stream16(src + (r0 + row) * C + c0 + uc * N + q * VPE);
+        }
+#pragma unroll
+        for (int k = 0; k < ITER; ++k) {
+            const int id = k * THREADS + tid;
+            const int lane = id & 31, wb = id >> 5;
+            const int q = lane & 7, row = (wb / UC) * 4 + (lane >> 3), uc = wb % UC;
+            const int ur = row / N, ir = row % N;
+            T e[VPE];
+            memcpy(e, &v[k], 16);
+            T *unit = sm + (ur * UC + uc) * N * P + ir * P;
+#pragma unroll
+            for (int j = 0; j < VPE; ++j) unit[phys(ir, q * VPE + j)] = e[j];
+        }
+        __syncthreads();
+        // drain: a warp covers 4 output rows (tile columns) x one unit height
+#pragma unroll
+        for (int k = 0; k < ITER; ++k) {
+            const int id = k * THREADS + tid;
+            const int lane = id & 31, wb = id >> 5;
+            const int p = lane & 7, ocl = (wb / UR) * 4 + (lane >> 3), ur = wb % UR;
+            const int uc = ocl / N, ic = ocl % N;
+            const T *unit = sm + (ur * UC + uc) * N * P;
+            T e[VPE];
+#pragma unroll
+            for (int j = 0; j < VPE; ++j) {
+                const int ir = p * VPE + j;
+                e[j] = unit[ir * P + phys(ir, ic)];
+            }
+            uint4 o;
+            memcpy(&o, e, 16);
+            st_stream16(dst + (c0 + ocl) * R + r0 + ur * N + p * VPE, o);
+        }
+    } else {
+        for (int idx = tid; idx < TR * TC; idx += THREADS) {
+            const int row = idx / TC, cl = idx % TC;
+            if (r0 + row < R && c0 + cl < C) {
+                const int ur = row / N, ir = row % N, uc = cl / N, ic = cl % N;
+                sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)] = src[(r0 + row) * C + c0 + cl];
+            }
+        }
+        __syncthreads();
+        for (int idx = tid; idx < TR * TC; idx += THREADS) {
+            const int ocl = idx / TR, orow = idx % TR;
+            if (c0 + ocl < C && r0 + orow < R) {
+                const int ur = orow / N, ir = orow % N, uc = ocl / N, ic = ocl % N;
+                dst[(c0 + ocl) * R + r0 + orow] = sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------- 2 B --
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &d0, uint32_t &d1,
+                                                  uint32_t &d2, uint32_t &d3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          int i) {
+    const uint32_t lo = (i & 1) ? a1 : a0;
+    const uint32_t hi = (i & 1) ? a3 : a2;
+    return (i & 2) ? hi : lo;
+}
+
+// Tile 64 x 64 of 16-bit elements, 128 threads.
+template <int VARIANT>
+__global__ void __launch_bounds__(128)
+    transpose16_kernel(uint16_t *__restrict__ dst, const uint16_t *__restrict__ src, int64_t R,
+                       int64_t C, int64_t tiles_c, int vec_ok) {
+    constexpr int TR = 64, TC = 64, THREADS = 128;
+    constexpr int PITCH = (VARIANT == SWZ_T_PADDED) ? 72 : 64;  // elements per shared row
+    __shared__ __align__(1024) uint16_t sm[TR * PITCH];
+    const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
+    const int64_t tc = static_cast<int64_t>(blockIdx.x) - tr * tiles_c;
+    const int64_t r0 = tr * TR, c0 = tc * TC;
+    const int tid = threadIdx.x;
+    // 16-byte chunk position of chunk ch of tile row `row`
+    auto chunk = [](int row, int ch) -> int { return VARIANT == SWZ_T_SWIZZLED ? (ch ^ (row & 7)) : ch; };
+
+    if (vec_ok && r0 + TR <= R && c0 + TC <= C) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int id = k * THREADS + tid, ch = id & 7, row = id >> 3;
+            v[k] = ld_stream16(src + (r0 + row) * C + c0 + ch * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int id = k * THREADS + tid, ch = id & 7, row = id >> 3;
+            *reinterpret_cast<uint4 *>(sm + row * PITCH + chunk(row, ch) * 8) = v[k];
+        }
+        __syncthreads();
+        const int lane = tid & 31, warp = tid >> 5;
+        const int g = lane >> 2, kk = lane & 3;   // output row in the block, word slot
+        const int m = lane >> 3, i = lane & 7;    // matrix addressed by this lane, its row
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int xi = warp * 4 + k;          // 16 x4 loads cover the 64 blocks
+            const int cb = xi & 7, rbg = (xi >> 3) * 4;
+            const int row = (rbg + m) * 8 + i;
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(smem_u32(sm + row * PITCH + chunk(row, cb) * 8), a0, a1, a2, a3);
+            // a[mm] holds output row 8cb + g, columns 8(rbg + mm) + 2kk .. +1.
+            // 4 x 4 word transpose across lanes 4g .. 4g + 3: lane kk collects
+            // words for columns 8(rbg + kk) .. +7.
+            uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int from = kk ^ r;
+                const uint32_t send = pick4(a0, a1, a2, a3, from);
+                const uint32_t got = r ? __shfl_xor_sync(kFullMask, send, r) : send;
+                b0 = (from == 0) ? got : b0;
+                b1 = (from == 1) ? got : b1;
+                b2 = (from == 2) ? got : b2;
+                b3 = (from == 3) ? got : b3;
+            }
+            st_stream16(dst + (c0 + cb * 8 + g) * R + r0 + (rbg + kk) * 8, make_uint4(b0, b1, b2, b3));
+        }
+    } else {
+        for (int idx = tid; idx < TR * TC; idx += THREADS) {
+            const int row = idx / TC, cl = idx % TC;
+            if (r0 + row < R && c0 + cl < C)
+                sm[row * PITCH + chunk(row, cl >> 3) * 8 + (cl & 7)] = src[(r0 + row) * C + c0 + cl];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < TR * TC; idx += THREADS) {
+            const int ocl = idx / TR, orow = idx % TR;
+            if (c0 + ocl < C && r0 + orow < R)
+                dst[(c0 + ocl) * R + r0 + orow] = sm[orow * PITCH + chunk(orow, ocl >> 3) * 8 + (ocl & 7)];
+        }
+    }
+}
+
+// --------------------------------------------------------------- 1 / 16 B --
+template <typename T, int VARIANT>
+__global__ void __launch_bounds__(256)
+    transpose_generic_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
+                             int64_t tiles_c) {
+    constexpr int N = 32, P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;
+    __shared__ T sm[N * P];
+    const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
+    const int64_t tc = static_cast<int64_t>(blockIdx.x) - tr * tiles_c;
+    const int64_t r0 = tr * N, c0 = tc * N;
+    auto phys = [](int ir, int ic) -> int { return VARIANT == SWZ_T_SWIZZLED ? (ic ^ ir) : ic; };
+    for (int idx = threadIdx.x; idx < N * N; idx += 256) {
+        const int row = idx >> 5, cl = idx & 31;
+        if (r0 + row < R && c0 + cl < C) sm[row * P + phys(row, cl)] = src[(r0 + row) * C + c0 + cl];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < N * N; idx += 256) {
+        const int ocl = idx >> 5, orow = idx & 31;
+        if (c0 + ocl < C && r0 + orow < R)
+            dst[(c0 + ocl) * R + r0 + orow] = sm[orow * P + phys(orow, ocl)];
+    }
+}
+
+template <typename T, int UR, int UC, int THREADS>
+swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
+                       cudaStream_t st) {
+    constexpr int N = 128 / static_cast<int>(sizeof(T));
+    constexpr int VPE = 16 / static_cast<int>(sizeof(T));
+    const int64_t TR = UR * N, TC = UC * N;
+    const int64_t tiles_c = (C + TC - 1) / TC, tiles = ((R + TR - 1) / TR) * tiles_c;
+    if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const int vec_ok = aligned16 && (C % VPE == 0) && (R % VPE == 0);
+    T *d = static_cast<T *>(dst);
+    const T *s = static_cast<const T *>(src);
+    const unsigned g = static_cast<unsigned>(tiles);
+    if (variant == SWZ_T_SWIZZLED)
+        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    else if (variant == SWZ_T_UNSWIZZLED)
+        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    else
+        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    return launch_status();
+}
+
+swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
+                     cudaStream_t st) {
+    const int64_t tiles_c = (C + 63) / 64, tiles = ((R + 63) / 64) * tiles_c;
+    if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const int vec_ok = aligned16 && (C % 8 == 0) && (R % 8 == 0);
+    uint16_t *d = static_cast<uint16_t *>(dst);
+    const uint16_t *s = static_cast<const uint16_t *>(src);
+    const unsigned g = static_cast<unsigned>(tiles);
+    if (variant == SWZ_T_SWIZZLED)
+        transpose16_kernel<SWZ_T_SWIZZLED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    else if (variant == SWZ_T_UNSWIZZLED)
+        transpose16_kernel<SWZ_T_UNSWIZZLED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    else
+        transpose16_kernel<SWZ_T_PADDED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    return launch_status();
+}
+
+template <typename T>
+swz_status launch_generic(void *dst, const void *src, int64_t R, int64_t C, int variant,
+                          cudaStream_t st) {
+    const int64_t tiles_c = (C + 31) / 32, tiles = ((R + 31) / 32) * tiles_c;
+    if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    T *d = static_cast<T *>(dst);
+    const T *s = static_cast<const T *>(src);
+    const unsigned g = static_cast<unsigned>(tiles);
+    if (variant == SWZ_T_SWIZZLED)
+        transpose_generic_kernel<T, SWZ_T_SWIZZLED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+    else if (variant == SWZ_T_UNSWIZZLED)
+        transpose_generic_kernel<T, SWZ_T_UNSWIZZLED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+    else
+        transpose_generic_kernel<T, SWZ_T_PADDED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+    return launch_status();
+}
+
+}  // namespace
+
+swz_status transpose_tma_launch(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st);
+
+// Arguments are validated by the caller (swz_transpose in swz_abi.cu).
+swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize,
+                            int variant, cudaStream_t st) {
+    const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    switch (esize) {
+        case 1: return launch_generic<uint8_t>(dst, src, R, C, variant, st);
+        case 2:
+            if (variant == SWZ_T_TMA) return transpose_tma_launch(dst, src, R, C, st);
+            return launch_16(dst, src, R, C, variant, aligned16, st);
+        case 4: return launch_unit<uint32_t, 2, 2, 256>(dst, src, R, C, variant, aligned16, st);
+        case 8: return launch_unit<unsigned long long, 4, 4, 256>(dst, src, R, C, variant, aligned16, st);
+        case 16: return launch_generic<uint4>(dst, src, R, C, variant, st);
+        default: return SWZ_ERR_PARAM;
+    }
+}
+
+}  // namespace swz
