@@ -191,6 +191,47 @@ swz_status swz_device_status(void *stream);
 swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, int64_t cols,
                                     uint64_t wait_ns, void *stream);
 
+/*
+ * The SWZ_T_TMA transpose without any allocation by the library.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot let a library allocate device memory: a serving loop whose device
+ * memory is planned ahead and owned by its own pool, a process whose device
+ * memory is already fully reserved by another allocator, or code that must
+ * not block on the allocator.  swz_transpose(..., SWZ_T_TMA) makes one
+ * cudaMalloc (its 4-byte status word) on its first call on each device; this
+ * entry point instead keeps that status word in a fixed 256-byte array in
+ * the library's device data (every GPU that loads the library holds that
+ * array until the process exits).  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Computes the same result as swz_transpose(dst, src, rows, cols, 2,
+ * SWZ_T_TMA, stream): out[c][r] = in[r][c] for 16-bit elements (raw bits),
+ * through the same kernel, with the same fallback to the shared-memory-staged
+ * swizzled kernel when src is not 16-byte aligned or cols is not a multiple
+ * of 8.
+ *
+ * dst, src  : device buffers of rows x cols 2-byte elements (caller-owned).
+ * rows, cols: 0 <= rows, cols < 2^31 (the TMA coordinate range); larger
+ *             requests are refused with SWZ_ERR_SHAPE.  The call needs one
+ *             4-byte status word of the array for any matrix size.
+ * timed_out : optional host pointer.  NULL: the call returns once the work
+ *             is enqueued.  Non-NULL: the call waits for `stream`, stores 1
+ *             if one of the kernel's bounded waits gave up (dst is then
+ *             incomplete and SWZ_ERR_TIMEOUT is returned), 0 otherwise.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture.  Every call shares the array:
+ * each call clears the status word on `stream` before its kernel runs, and
+ * calls whose work overlaps on the GPU (on different streams) race on it.
+ *
+ * Errors: SWZ_ERR_NULL, SWZ_ERR_SHAPE, SWZ_ERR_ALIGN (dst or src not 2-byte
+ * aligned), SWZ_ERR_ALIAS, SWZ_ERR_CUDA, SWZ_ERR_TIMEOUT (timed_out only).
+ */
+swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
+                                     uint32_t *timed_out, void *stream);
+
 /* sw(x) on the host (the same function the kernels apply). */
 uint64_t swz_apply(uint64_t x, int B, int M, int S);
 

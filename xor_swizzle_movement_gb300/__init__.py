@@ -19,6 +19,7 @@ __all__ = [
     "SwzError", "lib", "library_path",
     "swz_relayout", "swz_transpose", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
+    "swz_transpose_tma_noalloc",
     "swz_status_string", "swz_version",
     "SWZ_OK", "SWZ_ERR_NULL", "SWZ_ERR_PARAM", "SWZ_ERR_SHAPE", "SWZ_ERR_ALIGN", "SWZ_ERR_ALIAS",
     "SWZ_ERR_CUDA", "SWZ_ERR_TIMEOUT", "SWZ_ERR_UNSUPPORTED",
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.swz_device_status.restype = i32
         L.swz_selftest_tma_timeout.argtypes = [vp, vp, i64, i64, u64, vp]
         L.swz_selftest_tma_timeout.restype = i32
+        L.swz_transpose_tma_noalloc.argtypes = [vp, vp, i64, i64, ctypes.POINTER(ctypes.c_uint32), vp]
+        L.swz_transpose_tma_noalloc.restype = i32
         L.swz_status_string.argtypes = [i32]
         L.swz_status_string.restype = ctypes.c_char_p
         L.swz_version.argtypes = []
@@ -160,6 +163,19 @@ def swz_device_status(stream=None) -> int:
 def swz_selftest_tma_timeout(dst, src, rows: int, cols: int, wait_ns: int, stream=None) -> None:
     _check(lib().swz_selftest_tma_timeout(_ptr(dst), _ptr(src), rows, cols, wait_ns, _stream(stream)),
            "swz_selftest_tma_timeout")
+
+
+def swz_transpose_tma_noalloc(dst, src, rows: int, cols: int, wait: bool = False, stream=None) -> int:
+    """The 16-bit TMA transpose with no allocation by the library (for callers
+    whose device memory is owned by their own pool).  With wait=True the call
+    waits for the stream and returns 1 if a bounded wait gave up, else 0."""
+    flag = ctypes.c_uint32(0)
+    status = lib().swz_transpose_tma_noalloc(_ptr(dst), _ptr(src), rows, cols,
+                                             ctypes.byref(flag) if wait else None, _stream(stream))
+    if status == SWZ_ERR_TIMEOUT:
+        return 1
+    _check(status, "swz_transpose_tma_noalloc")
+    return int(flag.value)
 
 
 def swz_status_string(status: int) -> str:

@@ -302,3 +302,104 @@ swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, in
 }
 
 }  // extern "C"
+
+// ---- allocation-free variant of the TMA transpose ------------------------
+//
+// For callers that must not have the library allocate device memory: the
+// SWZ_T_TMA path above makes one cudaMalloc (its status word) on the first
+// call on each device.  This variant runs the same kernel with its status
+// word taken from a fixed array in the library's own device data instead.
+namespace swz {
+namespace {
+
+// The scratch of the allocation-free call: word 0 is the status word the
+// kernel sets when a bounded wait gives up.  256 bytes at file scope; every
+// GPU that loads the library holds one copy until the process exits.
+constexpr int kNoAllocScratchWords = 64;
+constexpr int kNoAllocWordsNeeded = 1;  // one status word, whatever the matrix size
+static_assert(kNoAllocWordsNeeded <= kNoAllocScratchWords, "scratch array too small");
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+std::mutex g_noalloc_mu;
+uint32_t *g_noalloc_addr[kMaxDevices] = {};
+
+// Set-up, once per device, with that device current: the device address of
+// g_noalloc_scratch.  (In host code the array's name only stands for the
+// symbol; a kernel must be given this address.)
+uint32_t *noalloc_scratch(int dev) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_noalloc_addr[dev] = static_cast<uint32_t *>(p);
+    }
+    return g_noalloc_addr[dev];
+}
+
+}  // namespace
+}  // namespace swz
+
+extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
+                                                uint32_t *timed_out, void *stream) {
+    using namespace swz;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (timed_out) *timed_out = 0;
+    if (rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
+    // the largest request: TMA coordinates are 32-bit
+    if (rows >= (1LL << 31) || cols >= (1LL << 31)) return SWZ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return SWZ_OK;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 1u) return SWZ_ERR_ALIGN;
+    const int64_t n_bytes = rows * cols * 2;
+    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+
+    EncodeTiledFn encode = encode_fn();
+    const bool tma_ok = encode && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (cols % 8) == 0;
+    if (!tma_ok) {
+        // same fallback as SWZ_T_TMA: the shared-memory-staged swizzled kernel, no scratch
+        const swz_status s = transpose_launch(dst, src, rows, cols, 2, SWZ_T_SWIZZLED, st);
+        if (s == SWZ_OK && timed_out && cudaStreamSynchronize(st) != cudaSuccess) return SWZ_ERR_CUDA;
+        return s;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SWZ_ERR_CUDA;
+    uint32_t *scratch = noalloc_scratch(dev);
+    if (!scratch) return SWZ_ERR_CUDA;
+    // the array keeps the previous call's contents: the status word must start at zero
+    if (cudaMemsetAsync(scratch, 0, kNoAllocWordsNeeded * sizeof(uint32_t), st) != cudaSuccess)
+        return SWZ_ERR_CUDA;
+
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {kTile, kTile};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(src), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SWZ_ERR_CUDA;
+    TmaArgs a;
+    a.dst = static_cast<uint16_t *>(dst);
+    a.R = rows;
+    a.C = cols;
+    a.tiles_c = (cols + kTile - 1) / kTile;
+    a.n_tiles = ((rows + kTile - 1) / kTile) * a.tiles_c;
+    a.vec_store_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (rows % 8 == 0);
+    a.issue_copies = 1;
+    a.wait_ns = kWaitLimitNs;
+    a.status = scratch;
+    int grid = 152 * 4;
+    if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
+    transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
+    const swz_status s = launch_status();
+    if (s != SWZ_OK || !timed_out) return s;
+    uint32_t v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess ||
+        cudaMemcpy(&v, scratch, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SWZ_ERR_CUDA;
+    if (v & (1u << SWZ_ERR_TIMEOUT)) {
+        *timed_out = 1;
+        return SWZ_ERR_TIMEOUT;
+    }
+    return SWZ_OK;
+}
