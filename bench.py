@@ -65,6 +65,12 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--case", default=None,
+                   help="run one kernel case for a profiler and exit: relayout, relayout_bms, "
+                        "transposes, bank_profile")
+    p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
+    p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
+    p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
     return p.parse_args()
 
 
@@ -162,6 +168,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+
+
+def reduce_max_ms(torch, total_ms: float, dist, device) -> float:
+    """The slowest rank's timed milliseconds (all ranks get it)."""
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(world: int, bytes_per_step: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_step per step (weak scaling),
+    timed by the slowest rank."""
+    return world * bytes_per_step * steps / (max_total_ms * 1e-3) / GB
 
 
 def make_flush(torch, dev):
@@ -321,8 +340,64 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """Launch one kernel case `reps` times (no timing): the command a profiler wraps."""
+    import torch
+    import xor_swizzle_movement_gb300 as swz
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    swz.lib()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+
+    def rand_bytes(n):
+        return torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=gen)
+
+    done = []
+    if args.case == "relayout":            # the headline workload, forward + inverse
+        src = rand_bytes(TILES * ROWS * COLS * ESIZE)
+        a, b = torch.empty_like(src), torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_relayout(a, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
+            swz.swz_relayout(b, a, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
+        done.append("relayout fwd+inv")
+    elif args.case == "relayout_bms":      # one uint16 buffer as one tile, forward
+        n = args.n or (1 << 27)
+        Bq, Mq, Sq = (int(v) for v in args.bms.split(","))
+        src = rand_bytes(2 * n)
+        dst = torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0)
+        done.append(f"relayout uint16 n={n} Sw<{Bq},{Mq},{Sq}>")
+    elif args.case == "transposes":        # every staging of the fp32 / fp16 / fp64 transposes
+        for esize, n, variants in ((4, args.n or 8192, (0, 1, 2)), (2, args.n or 8192, (0, 3, 1, 2)),
+                                   (8, (args.n or 8192) // 2, (0, 1, 2))):
+            src = rand_bytes(n * n * esize)
+            dst = torch.empty_like(src)
+            for v in variants:
+                for _ in range(args.reps):
+                    swz.swz_transpose(dst, src, n, n, esize, v)
+                done.append(f"transpose esize={esize} n={n} variant={v}")
+            del src, dst
+    elif args.case == "bank_profile":
+        n = args.n or (1 << 20)
+        pats = torch.randint(0, 228 * 1024 // 4, (n, 32), dtype=torch.int32, device=dev, generator=gen) * 4
+        w = torch.empty(n, dtype=torch.int32, device=dev)
+        f = torch.empty(n, dtype=torch.int32, device=dev)
+        for _ in range(args.reps):
+            swz.swz_bank_profile(pats, None, n, 4, w, f)
+        done.append(f"bank_profile n={n}")
+    else:
+        raise SystemExit(f"unknown --case {args.case}")
+    torch.cuda.synchronize()
+    print(json.dumps({"case": args.case, "launched": done, "reps": args.reps}), flush=True)
+
+
 def main():
     args = parse()
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -340,7 +415,7 @@ def main():
     pg = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist.init_process_group("nccl")
         pg = dist
 
     peak, peak_kind = peaks()
@@ -393,11 +468,9 @@ def main():
     launch_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev] + [e1.elapsed_time(e2) for _, e1, e2 in ev]
     total_ms = sum(step_ms)
     if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = reduce_max_ms(torch, total_ms, pg, dev)
     ms_per_step = total_ms / args.steps
-    value = world * STEP_BYTES * args.steps / (total_ms * 1e-3) / GB
+    value = throughput(world, STEP_BYTES, args.steps, total_ms)
 
     # roofline of the relayout kernel (both launches of a step are that kernel)
     avg_launch_s = statistics.mean(launch_ms) * 1e-3
