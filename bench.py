@@ -185,7 +185,7 @@ def throughput(world: int, bytes_per_step: int, steps: int, max_total_ms: float)
 
 def make_flush(torch, dev):
     w = torch.empty(512 * MiB, dtype=torch.uint8, device=dev)
-    r = torch.ones(512 * MiB // 4, dtype=torch.int32, device=dev)
+    r = torch.ones(512 * MiB // 4, dtype=torch.float32, device=dev)
 
     def flush():
         w.fill_(1)
@@ -210,9 +210,58 @@ def timed_launches(torch, fn, reps, flush, warm=3):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def back_to_back_ms(torch, fn, reps=10, groups=3, warm=2):
+    """Mean ms per launch over `reps` back-to-back launches (best of `groups`).
+    For inputs larger than L2, where no launch finds the previous one's data
+    in L2; avoids the ~2 us quantum of single-launch event timings."""
+    st = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    best = None
+    for _ in range(groups):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        b.record(st)
+        b.synchronize()
+        ms = a.elapsed_time(b) / reps
+        best = ms if best is None else min(best, ms)
+    return best
+
+
+def staging_patterns(esize, variant):
+    """Warp-wide shared-memory access patterns (byte addresses of lanes 0..31)
+    of the transpose stagings: the first fill store and the first drain load
+    of warp 0, as the kernels index their tiles; returns
+    {access: (addresses, access_bytes)}."""
+    if esize in (4, 8):
+        n = 128 // esize                 # unit edge
+        vpe = 16 // esize                # elements per 16-byte vector
+        pitch = n + 1 if variant == 2 else n
+
+        def phys(ir, ic):
+            return ic ^ ir if variant == 0 else ic
+        fill = [esize * ((lane >> 3) * pitch + phys(lane >> 3, (lane & 7) * vpe)) for lane in range(32)]
+        drain = [esize * (((lane & 7) * vpe) * pitch + phys((lane & 7) * vpe, lane >> 3)) for lane in range(32)]
+        return {"fill_store": (fill, esize), "drain_load": (drain, esize)}
+    # 16-bit: 128-byte rows (144 with padding), 16-byte chunks
+    pitch_b = 144 if variant == 2 else 128
+
+    def chunk(row, ch):
+        return ch ^ (row & 7) if variant in (0, 3) else ch
+    fill = [(lane >> 3) * pitch_b + 16 * chunk(lane >> 3, lane & 7) for lane in range(32)]
+    rows = [(lane >> 3) * 8 + (lane & 7) for lane in range(32)]     # ldmatrix.x4 row addresses
+    drain = [r * pitch_b + 16 * chunk(r, 0) for r in rows]
+    return {"fill_store": (fill, 16), "drain_ldmatrix": (drain, 16)}
+
+
 def measure_rows(torch, swz, dev, flush, peak):
     """Each remaining row of the path at its full size (inputs drawn on the GPU
-    from the row's seed)."""
+    from the row's seed).  Inputs larger than L2 are timed back to back; the
+    2 MiB relayout is timed with L2 flushed (cold) and as a CUDA graph of 20
+    steps (warm, no launch gaps)."""
     out = {}
     gen = torch.Generator(device=dev)
 
@@ -220,30 +269,40 @@ def measure_rows(torch, swz, dev, flush, peak):
         gen.manual_seed(seed)
         return torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=gen)
 
-    def summary(ms_list, nbytes):
-        ms = statistics.median(ms_list)
+    def summary(ms, nbytes):
         gbs = nbytes / (ms * 1e-3) / GB
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3)}
 
     # small relayout: 256 fp16 tiles 64x64, Swizzle<3,3,3>, forward then inverse (4 MiB moved per launch)
     src = rand_bytes(256 * 64 * 64 * 2, 0)
     a, b = torch.empty_like(src), torch.empty_like(src)
-    cold = timed_launches(torch, lambda: (swz.swz_relayout(a, src, 256, 64, 64, 2, 3, 3, 3, 0),
-                                          swz.swz_relayout(b, a, 256, 64, 64, 2, 3, 3, 3, 1)), 50, flush)
-    warm_ms = timed_launches(torch, lambda: (swz.swz_relayout(a, src, 256, 64, 64, 2, 3, 3, 3, 0),
-                                             swz.swz_relayout(b, a, 256, 64, 64, 2, 3, 3, 3, 1)), 50,
-                             lambda: None)
-    out["relayout_fp16_64x64_sw333_2MiB"] = {"cold_l2": summary(cold, 4 * src.numel()),
-                                             "warm_l2": summary(warm_ms, 4 * src.numel()),
-                                             "note": "4 MiB per launch: launch-latency bound, % of HBM not meaningful"}
-    del src, a, b
+
+    def small_step():
+        swz.swz_relayout(a, src, 256, 64, 64, 2, 3, 3, 3, 0)
+        swz.swz_relayout(b, a, 256, 64, 64, 2, 3, 3, 3, 1)
+    cold = statistics.mean(timed_launches(torch, small_step, 100, flush))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            small_step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(20):
+            small_step()
+    warm = back_to_back_ms(torch, graph.replay, reps=10) / 20
+    out["relayout_fp16_64x64_sw333_2MiB"] = {
+        "cold_l2": summary(cold, 8 * src.numel()), "warm_l2_graph": summary(warm, 8 * src.numel()),
+        "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound"}
+    del src, a, b, graph
 
     # int8 tiles 64x128, Swizzle<5,2,5>, 1 GiB, forward and inverse
     src = rand_bytes(1 << 30, 4)
     dst = torch.empty_like(src)
     n_tiles = (1 << 30) // (64 * 128)
-    fwd = timed_launches(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0), 10, flush)
-    inv = timed_launches(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 1), 10, flush)
+    fwd = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0))
+    inv = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 1))
     out["relayout_int8_64x128_sw525_1GiB"] = {"forward": summary(fwd, 2 << 30), "inverse": summary(inv, 2 << 30)}
 
     # one 1 GiB uint16 buffer, every (B, M, S) with B 1..5, M 0..4, S B..7, forward
@@ -252,9 +311,9 @@ def measure_rows(torch, swz, dev, flush, peak):
     for Bq in range(1, 6):
         for Mq in range(0, 5):
             for Sq in range(Bq, 8):
-                ms = timed_launches(torch, lambda: swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0), 3,
-                                    flush, warm=1)
-                res.append(((2 << 30) / (statistics.median(ms) * 1e-3) / GB, (Bq, Mq, Sq)))
+                ms = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0),
+                                     reps=3, groups=2, warm=1)
+                res.append(((2 << 30) / (ms * 1e-3) / GB, (Bq, Mq, Sq)))
     res.sort()
     vals = [r[0] for r in res]
     out["relayout_uint16_1GiB_sweep125"] = {
@@ -264,14 +323,32 @@ def measure_rows(torch, swz, dev, flush, peak):
         "min_frac_of_hbm": round(vals[0] / peak, 3)}
     del src, dst
 
-    # transposes
+    # transposes, with the bank model's verdict on each staging's warp accesses
+    pat_rows, pat_keys = [], []
+    for esize, variants in ((4, (0, 1, 2)), (2, (0, 3, 1, 2)), (8, (0, 1, 2))):
+        for v in variants:
+            for access, (addrs, width) in staging_patterns(esize, v).items():
+                pat_rows.append((addrs, width))
+                pat_keys.append((esize, v, access))
+    ways_model = {}
+    for width in sorted({w for _, w in pat_rows}):
+        idx = [i for i, (_, w) in enumerate(pat_rows) if w == width]
+        pats = torch.tensor([pat_rows[i][0] for i in idx], dtype=torch.int32, device=dev)
+        wy = torch.empty(len(idx), dtype=torch.int32, device=dev)
+        wf = torch.empty(len(idx), dtype=torch.int32, device=dev)
+        swz.swz_bank_profile(pats, None, len(idx), width, wy, wf)
+        for j, i in enumerate(idx):
+            ways_model[pat_keys[i]] = int(wy[j].item())
+
     def transpose_rows(name, n, esize, variants, seed):
         s_ = rand_bytes(n * n * esize, seed)
         d_ = torch.empty_like(s_)
         r = {}
         for v, vname in variants:
-            ms = timed_launches(torch, lambda: swz.swz_transpose(d_, s_, n, n, esize, v), 10, flush)
+            ms = back_to_back_ms(torch, lambda: swz.swz_transpose(d_, s_, n, n, esize, v))
             r[vname] = summary(ms, 2 * n * n * esize)
+            r[vname]["bank_model_ways"] = {acc: ways_model[(esize, v, acc)]
+                                           for (e_, v_, acc) in pat_keys if e_ == esize and v_ == v}
         out[name] = r
 
     transpose_rows("transpose_fp32_8192", 8192, 4, [(0, "swizzled_sw505"), (1, "unswizzled"), (2, "padded_33")], 2)
@@ -279,16 +356,15 @@ def measure_rows(torch, swz, dev, flush, peak):
                    [(0, "swizzled_sw343_ldmatrix"), (3, "tma_swizzle128b"), (1, "unswizzled"), (2, "padded")], 3)
     transpose_rows("transpose_fp64_8192", 8192, 8, [(0, "swizzled_sw404"), (1, "unswizzled"), (2, "padded_17")], 4)
 
-    # bank profiler: 2^22 random aligned 4-byte patterns
+    # bank profiler: 2^22 random aligned 4-byte patterns (512 MiB of addresses)
     npat = 1 << 22
     gen.manual_seed(5)
     pats = (torch.randint(0, 228 * 1024 // 4, (npat, 32), dtype=torch.int32, device=dev, generator=gen) * 4)
     ways = torch.empty(npat, dtype=torch.int32, device=dev)
     wf = torch.empty(npat, dtype=torch.int32, device=dev)
-    ms = timed_launches(torch, lambda: swz.swz_bank_profile(pats, None, npat, 4, ways, wf), 10, flush)
-    med = statistics.median(ms)
-    out["bank_profile_4M_patterns_w4"] = {"ms": round(med, 4), "Gpatterns/s": round(npat / (med * 1e-3) / 1e9, 3),
-                                          "GB/s": round(npat * 136 / (med * 1e-3) / GB, 1)}
+    ms = back_to_back_ms(torch, lambda: swz.swz_bank_profile(pats, None, npat, 4, ways, wf))
+    out["bank_profile_4M_patterns_w4"] = {"ms": round(ms, 4), "Gpatterns/s": round(npat / (ms * 1e-3) / 1e9, 3),
+                                          "GB/s": round(npat * 136 / (ms * 1e-3) / GB, 1)}
     return out
 
 

@@ -22,7 +22,13 @@
 //                 the lanes are not moved at all;
 //   kLanesXor     M + S >= log2 V: the XOR constant is the same for every lane
 //                 of the vector, the permutation is lane -> lane ^ L;
-//   kLanesGeneral otherwise: per-lane source computed from the swizzle.
+//   kLanesGeneral otherwise: the swizzle and its inverse are linear maps over
+//                 GF(2) on the offset bits, and a vector's offset y (aligned)
+//                 and its lane index l share no bit, so the source of lane l is
+//                 g(y) ^ g(l): a per-vector constant k = g(y) mod V XOR-ed with
+//                 a lane map L(l) = g(l) that is the same for every vector.
+//                 The host tabulates L (V nibbles); the kernel reads lane
+//                 L(l) ^ k.
 #include "swz_common.cuh"
 
 namespace swz {
@@ -37,8 +43,11 @@ struct RelayoutArgs {
     int64_t tile_vecs;  // 16-byte vectors per tile
     int B, M, S;
     int steps;          // 1: source = sw(y); >1: source = sw^-1(y) by `steps` iterations
-    int per_thread;     // vectors per thread, 1..4
+    int per_thread;     // vectors per thread, 1..kMaxPerThread
+    uint64_t lane_tab;  // nibble l: lane map L(l) = g(l) mod V (kLanesGeneral)
 };
+
+constexpr int kMaxPerThread = 4;
 
 template <int E>
 struct VecTraits {
@@ -82,17 +91,16 @@ __device__ __forceinline__ uint4 lanes_xor(uint4 v, uint32_t L) {
     }
 }
 
-// out lane l = in lane (g(y + l) mod V), g = the gather function
+// out lane l = in lane L(l) ^ k  (= g(y + l) mod V, g = the gather function)
 template <int E>
-__device__ __forceinline__ uint4 lanes_general(uint4 v, uint64_t y, const RelayoutArgs &a) {
+__device__ __forceinline__ uint4 lanes_general(uint4 v, uint32_t k, uint64_t lane_tab) {
     constexpr int V = VecTraits<E>::V;
     if constexpr (E == 16) {
         return v;
     } else {
         uint32_t p[V];
 #pragma unroll
-        for (int l = 0; l < V; ++l)
-            p[l] = static_cast<uint32_t>(sw_inv(y + l, a.B, a.M, a.S, a.steps)) & (V - 1);
+        for (int l = 0; l < V; ++l) p[l] = (static_cast<uint32_t>(lane_tab >> (4 * l)) & 15u) ^ k;
         const uint32_t i0 = v.x, i1 = v.y, i2 = v.z, i3 = v.w;
         uint32_t o[4];
         if constexpr (E == 8) {
@@ -136,12 +144,12 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
     constexpr int LV = VecTraits<E>::LV;
     constexpr uint64_t VM = (1u << LV) - 1u;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
-    uint4 r[4];
-    uint64_t yk[4];
-    uint32_t lx[4];
-    // all loads first, so that each thread keeps up to four 16-byte loads in flight
+    uint4 r[kMaxPerThread];
+    uint32_t lx[kMaxPerThread];
+    const uint64_t policy = l2_evict_first_policy();
+    // all loads first, so that each thread keeps up to kMaxPerThread 16-byte loads in flight
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kMaxPerThread; ++k) {
         const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
         if (k < a.per_thread && u < a.nvec) {
             int64_t local = u, tile0 = 0;
@@ -151,19 +159,18 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
             }
             const uint64_t y = static_cast<uint64_t>(local) << LV;
             const uint64_t x = sw_inv(y, a.B, a.M, a.S, a.steps);
-            r[k] = ld_stream16(a.src + tile0 + static_cast<int64_t>(x >> LV));
-            yk[k] = y;
-            lx[k] = static_cast<uint32_t>((x ^ y) & VM);
+            r[k] = ld_stream16_hint(a.src + tile0 + static_cast<int64_t>(x >> LV), policy);
+            lx[k] = static_cast<uint32_t>(x & VM);
         }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kMaxPerThread; ++k) {
         const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
         if (k < a.per_thread && u < a.nvec) {
             uint4 out;
             if constexpr (MODE == kLanesFixed) out = r[k];
             else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
-            else out = lanes_general<E>(r[k], yk[k], a);
+            else out = lanes_general<E>(r[k], lx[k], a.lane_tab);
             st_stream16(a.dst + u, out);
         }
     }
@@ -251,6 +258,10 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // several waves deep (152 SMs x 2048 threads per wave)
         const int64_t wave = 152LL * 2048;
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+        a.lane_tab = 0;
+        for (int l = 0; l < (16 / esize); ++l)
+            a.lane_tab |= (sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & static_cast<uint64_t>((16 / esize) - 1))
+                          << (4 * l);
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
         const int period = B + M + S;
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);

@@ -20,7 +20,10 @@
 // elements, 16 x 16 for 8-byte ones).  Shared accesses are per element; with
 // the thread mapping below, each warp-wide store touches 4 rows x one unit
 // width and each warp-wide load 4 columns x one unit height, and the XOR
-// spreads both over all 32 banks.
+// spreads both over all 32 banks.  A CTA of 256 threads owns 2 x 2 units:
+// 64 x 64 fp32 (16 KiB, at most 6 CTAs per SM so that no register spills) or
+// 32 x 32 fp64 (8 KiB, 8 CTAs per SM: the 64 x 64 fp64 tile's 32 KiB held
+// occupancy down and ran 17% slower).
 //
 // Element size 2: tiles of 64 x 64 with 128-byte rows under the
 // byte-address Swizzle<3,4,3> (16-byte chunk index XOR row mod 8, equal to
@@ -45,8 +48,8 @@ namespace swz {
 namespace {
 
 // ---------------------------------------------------------------- 4 / 8 B --
-template <typename T, int VARIANT, int UR, int UC, int THREADS>
-__global__ void __launch_bounds__(THREADS)
+template <typename T, int VARIANT, int UR, int UC, int THREADS, int MIN_CTAS>
+__global__ void __launch_bounds__(THREADS, MIN_CTAS)
     transpose_unit_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
                           int64_t tiles_c, int vec_ok) {
     constexpr int N = 128 / static_cast<int>(sizeof(T));    // unit edge: 32 (4 B) or 16 (8 B)
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-template <typename T, int UR, int UC, int THREADS>
+template <typename T, int UR, int UC, int THREADS, int MIN_CTAS>
 swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
                        cudaStream_t st) {
     constexpr int N = 128 / static_cast<int>(sizeof(T));
@@ -245,11 +248,11 @@ swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int var
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
     if (variant == SWZ_T_SWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
     else
-        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
     return launch_status();
 }
 
@@ -300,8 +303,8 @@ swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, in
         case 2:
             if (variant == SWZ_T_TMA) return transpose_tma_launch(dst, src, R, C, st);
             return launch_16(dst, src, R, C, variant, aligned16, st);
-        case 4: return launch_unit<uint32_t, 2, 2, 256>(dst, src, R, C, variant, aligned16, st);
-        case 8: return launch_unit<unsigned long long, 4, 4, 256>(dst, src, R, C, variant, aligned16, st);
+        case 4: return launch_unit<uint32_t, 2, 2, 256, 6>(dst, src, R, C, variant, aligned16, st);
+        case 8: return launch_unit<unsigned long long, 2, 2, 256, 8>(dst, src, R, C, variant, aligned16, st);
         case 16: return launch_generic<uint4>(dst, src, R, C, variant, st);
         default: return SWZ_ERR_PARAM;
     }
