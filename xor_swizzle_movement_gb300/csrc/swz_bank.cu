@@ -9,12 +9,13 @@
 // Lane l of the warp holds lane l's address, so the pattern is read with one
 // coalesced 128-byte load.  Aligned patterns (the only ones real hardware
 // accepts: a w-byte access on a multiple of w, or a sub-word access that does
-// not straddle a word) are counted with two warp matches: the first keeps one
-// lane per distinct (pass, access unit), the second groups those leaders by
-// (pass, bank group) and its population count is the number of distinct
-// words in that bank.  Unaligned patterns, where one lane may touch up to
-// five words and neighbours may share some of them, are counted exactly with
-// a per-warp table in shared memory.
+// not straddle a word) are counted in claim rounds through a 32-slot per-warp
+// table (one slot per pass and bank group): a round costs one shared store,
+// one shared load and a ballot, and a pass takes exactly as many rounds as
+// its cost.  (Two warp-wide match instructions per pattern, the obvious
+// alternative, cost about 50 SM cycles each here.)  Unaligned patterns, where
+// one lane may touch up to five words and neighbours may share some of them,
+// are counted exactly with a per-warp table of word candidates.
 #include "swz_common.cuh"
 
 namespace swz {
@@ -22,47 +23,56 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 
-__device__ __forceinline__ int reduce_max_segment(int v, int seg) {
-    // max over aligned groups of `seg` lanes (seg = 8, 16 or 32)
-    for (int o = 1; o < seg; o <<= 1) v = max(v, __shfl_xor_sync(kFullMask, v, o));
-    return v;
-}
-
+// W = access bytes per lane (1, 2, 4, 8, 16)
+template <int W>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     bank_profile_kernel(const uint32_t *__restrict__ addrs, const uint32_t *__restrict__ active,
-                        int64_t n, int width, int32_t *__restrict__ ways,
-                        int32_t *__restrict__ wavefronts) {
+                        int64_t n, int32_t *__restrict__ ways, int32_t *__restrict__ wavefronts) {
+    constexpr int kPasses = W <= 4 ? 1 : W / 4;
+    constexpr int kLpp = 32 / kPasses;                       // lanes per pass
+    constexpr uint32_t kUnitShift = W <= 4 ? 2 : (W == 8 ? 3 : 4);  // log2 of the access unit (>= a word)
+    __shared__ uint32_t s_tab[kWarpsPerCta][32];
     __shared__ uint32_t s_first[kWarpsPerCta][32];
     __shared__ int s_nw[kWarpsPerCta][32];
     __shared__ int s_cnt[kWarpsPerCta][4][32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int passes = width <= 4 ? 1 : width / 4;
-    const int lpp = 32 / passes;  // lanes per pass
-    const int pass = lane / lpp;
+    const int pass = lane / kLpp;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
     for (int64_t p = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + wid; p < n; p += warps_total) {
         const uint32_t a = __ldcs(addrs + p * 32 + lane);
         const uint32_t mask = active ? __ldcs(active + p) : kFullMask;
         const bool on = (mask >> lane) & 1u;
-        const bool aligned = width <= 4 ? ((a & 3u) + static_cast<uint32_t>(width) <= 4u)
-                                        : ((a & static_cast<uint32_t>(width - 1)) == 0u);
+        const bool aligned = W <= 4 ? ((a & 3u) + static_cast<uint32_t>(W) <= 4u)
+                                    : ((a & static_cast<uint32_t>(W - 1)) == 0u);
         int cost;  // cost of this lane's pass, valid on every lane of the pass
         if (__all_sync(kFullMask, !on || aligned)) {
-            const uint32_t unit_bytes = width <= 4 ? 4u : static_cast<uint32_t>(width);
-            const uint32_t unit = a / unit_bytes;               // access unit (word or w-byte chunk)
-            const uint32_t groups = 32u / (unit_bytes / 4u);    // bank groups of unit_bytes
-            const unsigned long long solo = (1ull << 63) | static_cast<unsigned long long>(lane);
-            const unsigned long long k1 =
-                on ? ((static_cast<unsigned long long>(pass) << 40) | unit) : solo;
-            const unsigned m1 = __match_any_sync(kFullMask, k1);
-            const bool leader = on && (__ffs(m1) - 1 == lane);
-            const unsigned long long k2 =
-                leader ? ((static_cast<unsigned long long>(pass) << 40) | (unit % groups)) : solo;
-            const unsigned m2 = __match_any_sync(kFullMask, k2);
-            cost = reduce_max_segment(leader ? __popc(m2) : 0, lpp);
+            // An aligned access unit (a word, or a W-byte chunk) never shares a
+            // word with a different unit, so the pass cost is the largest
+            // number of distinct units in one bank group.  Count it by rounds:
+            // every lane still waiting writes its unit into its group's slot,
+            // one write per slot wins, and every lane whose unit is the one in
+            // its slot is served.  Each round serves exactly one distinct unit
+            // per slot, so a pass takes as many rounds as its worst group holds
+            // distinct units.
+            const uint32_t unit = a >> kUnitShift;
+            const int slot = pass * kLpp + static_cast<int>(unit & static_cast<uint32_t>(kLpp - 1));
+            const unsigned pass_lanes = (kLpp == 32) ? kFullMask : (((1u << (kLpp & 31)) - 1u) << (pass * kLpp));
+            volatile uint32_t *tab = s_tab[wid];
+            unsigned rem = __ballot_sync(kFullMask, on);
+            int rounds = 0;
+            while (rem) {  // warp-uniform; every round serves at least one lane
+                const bool waiting = (rem >> lane) & 1u;
+                if (waiting) tab[slot] = unit;
+                __syncwarp();
+                const bool served = waiting && tab[slot] == unit;
+                __syncwarp();
+                rounds += (rem & pass_lanes) != 0u;
+                rem &= ~__ballot_sync(kFullMask, served);
+            }
+            cost = rounds;
         } else {
             // exact count: candidate words first .. first + nw - 1 per lane
-            const unsigned long long last = (static_cast<unsigned long long>(a) + width - 1) >> 2;
+            const unsigned long long last = (static_cast<unsigned long long>(a) + W - 1) >> 2;
             const uint32_t first = a >> 2;
             const int nw = on ? static_cast<int>(last - first + 1) : 0;
             s_first[wid][lane] = first;
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
                 bool fresh = valid && (__ffs(m) - 1 == lane);
                 if (fresh && i > 0) {
                     // did a lane of this pass touch the same word in an earlier round?
-                    for (int l2 = pass * lpp; l2 < (pass + 1) * lpp; ++l2) {
+                    for (int l2 = pass * kLpp; l2 < (pass + 1) * kLpp; ++l2) {
                         const long long d = static_cast<long long>(wd) - static_cast<long long>(s_first[wid][l2]);
                         if (d >= 0 && d < i && d < s_nw[wid][l2]) fresh = false;
                     }
@@ -89,23 +99,26 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
             }
             __syncwarp();
             int mine = 0;
-            for (int q = 0; q < passes; ++q) {
-                const int c = reduce_max_segment(s_cnt[wid][q][lane], 32);
+#pragma unroll
+            for (int q = 0; q < kPasses; ++q) {
+                const int c = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(s_cnt[wid][q][lane])));
                 if (q == pass) mine = c;
             }
             cost = mine;
             __syncwarp();
         }
-        // one representative lane per pass carries that pass's cost
-        int worst = (lane % lpp == 0) ? cost : 0;
-        int total = worst;
-        for (int o = 1; o < 32; o <<= 1) {
-            worst = max(worst, __shfl_xor_sync(kFullMask, worst, o));
-            total += __shfl_xor_sync(kFullMask, total, o);
+        unsigned worst, total;
+        if constexpr (kPasses == 1) {
+            worst = total = static_cast<unsigned>(cost);  // already uniform across the warp
+        } else {
+            // one representative lane per pass carries that pass's cost
+            const unsigned rep = (lane % kLpp == 0) ? static_cast<unsigned>(cost) : 0u;
+            worst = __reduce_max_sync(kFullMask, rep);
+            total = __reduce_add_sync(kFullMask, rep);
         }
         if (lane == 0) {
-            ways[p] = worst;
-            wavefronts[p] = total;
+            ways[p] = static_cast<int32_t>(worst);
+            wavefronts[p] = static_cast<int32_t>(total);
         }
     }
 }
@@ -125,8 +138,15 @@ swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, in
                                int32_t *ways, int32_t *wavefronts, cudaStream_t st) {
     int64_t grid = (n + kWarpsPerCta - 1) / kWarpsPerCta;
     if (grid > 152LL * 64) grid = 152LL * 64;  // grid-stride beyond 64 CTAs per SM
-    bank_profile_kernel<<<static_cast<unsigned>(grid), kWarpsPerCta * 32, 0, st>>>(addrs, active, n, width,
-                                                                                ways, wavefronts);
+    const unsigned g = static_cast<unsigned>(grid);
+    switch (width) {
+        case 1: bank_profile_kernel<1><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        case 2: bank_profile_kernel<2><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        case 4: bank_profile_kernel<4><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        case 8: bank_profile_kernel<8><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        case 16: bank_profile_kernel<16><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        default: return SWZ_ERR_PARAM;
+    }
     return launch_status();
 }
 

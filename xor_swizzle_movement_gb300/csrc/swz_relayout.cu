@@ -27,8 +27,10 @@
 //                 and its lane index l share no bit, so the source of lane l is
 //                 g(y) ^ g(l): a per-vector constant k = g(y) mod V XOR-ed with
 //                 a lane map L(l) = g(l) that is the same for every vector.
-//                 The host tabulates L (V nibbles); the kernel reads lane
-//                 L(l) ^ k.
+//                 The kernel first XORs the lanes by k (as kLanesXor), then
+//                 applies the fixed permutation L as a byte permutation of the
+//                 16-byte vector: three prmt per output word with selectors the
+//                 host computes once per launch.
 #include "swz_common.cuh"
 
 namespace swz {
@@ -44,7 +46,7 @@ struct RelayoutArgs {
     int B, M, S;
     int steps;          // 1: source = sw(y); >1: source = sw^-1(y) by `steps` iterations
     int per_thread;     // vectors per thread, 1..kMaxPerThread
-    uint64_t lane_tab;  // nibble l: lane map L(l) = g(l) mod V (kLanesGeneral)
+    uint32_t perm_sel[12];  // kLanesGeneral: prmt selectors of the fixed lane map L, 3 per word
 };
 
 constexpr int kMaxPerThread = 4;
@@ -54,13 +56,6 @@ struct VecTraits {
     static constexpr int V = 16 / E;  // lanes (elements) per vector
     static constexpr int LV = (E == 1) ? 4 : (E == 2) ? 3 : (E == 4) ? 2 : (E == 8) ? 1 : 0;
 };
-
-__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t i) {
-    const uint32_t lo = (i & 1u) ? a1 : a0;
-    const uint32_t hi = (i & 1u) ? a3 : a2;
-    return (i & 2u) ? hi : lo;
-}
 
 // out lane l = in lane l ^ L
 template <int E>
@@ -91,52 +86,18 @@ __device__ __forceinline__ uint4 lanes_xor(uint4 v, uint32_t L) {
     }
 }
 
-// out lane l = in lane L(l) ^ k  (= g(y + l) mod V, g = the gather function)
-template <int E>
-__device__ __forceinline__ uint4 lanes_general(uint4 v, uint32_t k, uint64_t lane_tab) {
-    constexpr int V = VecTraits<E>::V;
-    if constexpr (E == 16) {
-        return v;
-    } else {
-        uint32_t p[V];
+// A fixed permutation of the 16 bytes of v: output byte 4w + i comes from the
+// input byte the host encoded in sel[3w .. 3w + 2] (two prmt pick from the low
+// and the high 8 bytes, a third merges them).
+__device__ __forceinline__ uint4 bytes_permute(uint4 v, const uint32_t *sel) {
+    uint32_t o[4];
 #pragma unroll
-        for (int l = 0; l < V; ++l) p[l] = (static_cast<uint32_t>(lane_tab >> (4 * l)) & 15u) ^ k;
-        const uint32_t i0 = v.x, i1 = v.y, i2 = v.z, i3 = v.w;
-        uint32_t o[4];
-        if constexpr (E == 8) {
-#pragma unroll
-            for (int l = 0; l < 2; ++l) {
-                o[2 * l] = p[l] ? i2 : i0;
-                o[2 * l + 1] = p[l] ? i3 : i1;
-            }
-        } else if constexpr (E == 4) {
-#pragma unroll
-            for (int l = 0; l < 4; ++l) o[l] = pick4(i0, i1, i2, i3, p[l]);
-        } else if constexpr (E == 2) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t pa = p[2 * k], pb = p[2 * k + 1];
-                const uint32_t wa = pick4(i0, i1, i2, i3, pa >> 1);
-                const uint32_t wb = pick4(i0, i1, i2, i3, pb >> 1);
-                const uint32_t ha = (pa & 1u) * 2u, hb = 4u + (pb & 1u) * 2u;
-                const uint32_t sel = ha | ((ha + 1u) << 4) | (hb << 8) | ((hb + 1u) << 12);
-                o[k] = __byte_perm(wa, wb, sel);
-            }
-        } else {  // E == 1
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t p0 = p[4 * k], p1 = p[4 * k + 1], p2 = p[4 * k + 2], p3 = p[4 * k + 3];
-                const uint32_t lo = __byte_perm(pick4(i0, i1, i2, i3, p0 >> 2),
-                                                pick4(i0, i1, i2, i3, p1 >> 2),
-                                                (p0 & 3u) | ((4u + (p1 & 3u)) << 4));
-                const uint32_t hi = __byte_perm(pick4(i0, i1, i2, i3, p2 >> 2),
-                                                pick4(i0, i1, i2, i3, p3 >> 2),
-                                                (p2 & 3u) | ((4u + (p3 & 3u)) << 4));
-                o[k] = __byte_perm(lo, hi, 0x5410);
-            }
-        }
-        return make_uint4(o[0], o[1], o[2], o[3]);
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = __byte_perm(v.x, v.y, sel[3 * w]);
+        const uint32_t hi = __byte_perm(v.z, v.w, sel[3 * w + 1]);
+        o[w] = __byte_perm(lo, hi, sel[3 * w + 2]);
     }
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int E, int MODE, bool LOCAL>
@@ -170,7 +131,7 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
             uint4 out;
             if constexpr (MODE == kLanesFixed) out = r[k];
             else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
-            else out = lanes_general<E>(r[k], lx[k], a.lane_tab);
+            else out = bytes_permute(lanes_xor<E>(r[k], lx[k]), a.perm_sel);
             st_stream16(a.dst + u, out);
         }
     }
@@ -258,10 +219,30 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // several waves deep (152 SMs x 2048 threads per wave)
         const int64_t wave = 152LL * 2048;
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
-        a.lane_tab = 0;
-        for (int l = 0; l < (16 / esize); ++l)
-            a.lane_tab |= (sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & static_cast<uint64_t>((16 / esize) - 1))
-                          << (4 * l);
+        // kLanesGeneral: out lane l = (lanes XOR-ed by k)[L(l)], L(l) = g(l) for a lane index l;
+        // as bytes: out byte l * esize + b <- in byte L(l) * esize + b
+        int src_byte[16];
+        const int lanes = 16 / esize;
+        for (int l = 0; l < lanes; ++l) {
+            const int Ll = static_cast<int>(sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & (lanes - 1));
+            for (int bb = 0; bb < esize; ++bb) src_byte[l * esize + bb] = Ll * esize + bb;
+        }
+        for (int w = 0; w < 4; ++w) {
+            uint32_t s_lo = 0, s_hi = 0, s_mix = 0;
+            for (int i = 0; i < 4; ++i) {
+                const int sb = src_byte[4 * w + i];
+                if (sb < 8) {
+                    s_lo |= static_cast<uint32_t>(sb) << (4 * i);
+                    s_mix |= static_cast<uint32_t>(i) << (4 * i);
+                } else {
+                    s_hi |= static_cast<uint32_t>(sb - 8) << (4 * i);
+                    s_mix |= static_cast<uint32_t>(4 + i) << (4 * i);
+                }
+            }
+            a.perm_sel[3 * w] = s_lo;
+            a.perm_sel[3 * w + 1] = s_hi;
+            a.perm_sel[3 * w + 2] = s_mix;
+        }
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
         const int period = B + M + S;
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
