@@ -8,7 +8,12 @@
 // rows it is exactly the layout of the SWZ_T_SWIZZLED 16-bit kernel, so the
 // same conflict-free transposing matrix loads drain it.
 //
-// Persistent kernel: each CTA walks tiles blockIdx.x, +gridDim.x, ...; a
+// When the output rows are whole 16-byte vectors the output leaves by TMA
+// too (transpose16_tma_ls_kernel): ldmatrix .trans, then stmatrix into an
+// output tile under the same 128-byte swizzle, then one tensor store per tile.
+// Otherwise the drained rows leave by 16-byte stores (transpose16_tma_kernel).
+//
+// Persistent kernels: each CTA walks tiles blockIdx.x, +gridDim.x, ...; a
 // ring of kStages shared buffers keeps kStages tile loads in flight while the
 // current tile is drained.  One elected thread issues the copies; each buffer
 // has an mbarrier that the copy completes.  Every wait on an mbarrier is
@@ -189,6 +194,106 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(d0), "r"(d1),
+                 "r"(d2), "r"(d3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t smem_src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(smem_src)
+                 : "memory");
+}
+
+constexpr int kOutBufs = 2;
+
+// Both directions through the tensor-memory accelerator: the input tile
+// arrives under the 128-byte swizzle, each warp transposes its 8 x 8 blocks
+// with ldmatrix .trans and writes them with stmatrix into an output tile laid
+// out under the same swizzle, and one thread stores that tile with a tensor
+// copy.  Edge tiles need no special case: the load fills out-of-range
+// elements with zeros and the store drops them.  Output buffers are double
+// buffered; a buffer is rewritten only after the store issued from it two
+// tiles earlier has finished reading it.
+__global__ void __launch_bounds__(kThreads)
+    transpose16_tma_ls_kernel(const __grid_constant__ CUtensorMap map_in, const __grid_constant__ CUtensorMap map_out,
+                              const TmaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[kStages];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t out_base = base + kStages * kTileBytes;
+    const int tid = threadIdx.x;
+    const uint32_t bar0 = smem_u32(&bars[0]);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    auto issue = [&](int s, int64_t t) {
+        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
+        mbar_expect_tx(bar0 + 8u * s, kTileBytes);
+        tma_load_2d(base + s * kTileBytes, &map_in, static_cast<int>(tc * kTile), static_cast<int>(tr * kTile),
+                    bar0 + 8u * s);
+    };
+    if (tid == 0 && a.issue_copies) {
+        for (int s = 0; s < kStages; ++s) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (t < a.n_tiles) issue(s, t);
+        }
+    }
+
+    const int lane = tid & 31, warp = tid >> 5;
+    const int m = lane >> 3, i8 = lane & 7;  // matrix addressed by this lane, its row
+    for (int64_t it = 0;; ++it) {
+        const int64_t t = blockIdx.x + it * gridDim.x;
+        if (t >= a.n_tiles) break;
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ob = out_base + static_cast<uint32_t>(it & 1) * kTileBytes;
+        const bool ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kStages) & 1), a.wait_ns);
+        if (tid == 0 && it >= kOutBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
+            if (a.issue_copies) {
+                for (int64_t j = it; j < it + kStages; ++j) {
+                    const int64_t tj = blockIdx.x + j * gridDim.x;
+                    if (tj >= a.n_tiles) break;
+                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kStages),
+                                      static_cast<uint32_t>((j / kStages) & 1), a.wait_ns);
+                }
+            }
+            if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            return;
+        }
+        const uint32_t ib = base + s * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int xi = warp * 4 + k;
+            const int cb = xi & 7, rbg = (xi >> 3) * 4;
+            const int row = (rbg + m) * 8 + i8;   // input tile row this lane addresses
+            uint32_t d0, d1, d2, d3;
+            ldmatrix_x4_trans(ib + row * 128 + ((cb ^ (row & 7)) << 4), d0, d1, d2, d3);
+            // block (rbg + m, cb) transposed lands at output block (cb, rbg + m)
+            const int orow = cb * 8 + i8;
+            stmatrix_x4(ob + orow * 128 + (((rbg + m) ^ (orow & 7)) << 4), d0, d1, d2, d3);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();  // output tile complete, input buffer s consumed
+        if (tid == 0) {
+            const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
+            tma_store_2d(&map_out, static_cast<int>(tr * kTile), static_cast<int>(tc * kTile), ob);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            const int64_t tn = t + static_cast<int64_t>(kStages) * gridDim.x;
+            if (a.issue_copies && tn < a.n_tiles) issue(s, tn);
+        }
+    }
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---- host side ---------------------------------------------------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -215,6 +320,23 @@ std::mutex g_status_mu;
 uint32_t *g_status[kMaxDevices] = {};
 
 }  // namespace
+
+// The load+store kernel needs more than the default 48 KiB of dynamic shared
+// memory; the attribute is set once per device.
+bool ls_smem_attribute_set(int smem) {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(transpose16_tma_ls_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
+}
 
 // The per-device status word (allocated once per device, on first use).
 uint32_t *device_status_word(bool create) {
@@ -264,10 +386,23 @@ swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, c
     a.issue_copies = issue_copies;
     a.wait_ns = wait_ns;
     a.status = status;
-    const int smem = kStages * kTileBytes + 1024;
     int grid = 152 * 4;
     if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
-    transpose16_tma_kernel<<<grid, kThreads, smem, st>>>(map, a);
+    if (a.vec_store_ok) {
+        // the output (C x R, rows of R elements) also goes out through a tensor map
+        CUtensorMap map_out;
+        const cuuint64_t odim[2] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(C)};
+        const cuuint64_t ostride[1] = {static_cast<cuuint64_t>(R) * 2};
+        if (encode(&map_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dst, odim, ostride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SWZ_ERR_CUDA;
+        const int smem = (kStages + kOutBufs) * kTileBytes + 1024;
+        if (!ls_smem_attribute_set(smem)) return SWZ_ERR_CUDA;
+        transpose16_tma_ls_kernel<<<grid, kThreads, smem, st>>>(map, map_out, a);
+        return launch_status();
+    }
+    transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
     return launch_status();
 }
 
