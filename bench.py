@@ -292,10 +292,27 @@ def measure_rows(torch, swz, dev, flush, peak):
         for _ in range(20):
             small_step()
     warm = back_to_back_ms(torch, graph.replay, reps=10) / 20
+    def small_step_tma():
+        swz.swz_relayout_tma(a, src, 256, 64, 64, 2, 3, 3, 3, 0)
+        swz.swz_relayout_tma(b, a, 256, 64, 64, 2, 3, 3, 3, 1)
+    cold_tma = statistics.mean(timed_launches(torch, small_step_tma, 100, flush))
     out["relayout_fp16_64x64_sw333_2MiB"] = {
         "cold_l2": summary(cold, 8 * src.numel()), "warm_l2_graph": summary(warm, 8 * src.numel()),
+        "tma_cold_l2": summary(cold_tma, 8 * src.numel()),
         "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound"}
     del src, a, b, graph
+
+    # the same Swizzle<3,3,3> fp16 64x64 tiles over 1 GiB: register path vs the TMA 128-byte mode
+    src = rand_bytes(1 << 30, 4)
+    dst = torch.empty_like(src)
+    nt = (1 << 30) // 8192
+    r = {}
+    for name, fn in (("register", swz.swz_relayout), ("tma_128B", swz.swz_relayout_tma)):
+        for d in (0, 1):
+            ms = back_to_back_ms(torch, lambda: fn(dst, src, nt, 64, 64, 2, 3, 3, 3, d))
+            r[f"{name}_{'forward' if d == 0 else 'inverse'}"] = summary(ms, 2 << 30)
+    out["relayout_fp16_64x64_sw333_1GiB"] = r
+    del src, dst
 
     # int8 tiles 64x128, Swizzle<5,2,5>, 1 GiB, forward and inverse
     src = rand_bytes(1 << 30, 4)

@@ -86,6 +86,28 @@ swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t row
                         void *stream);
 
 /*
+ * Batched tile relayout through the tensor-memory accelerator's hardware
+ * swizzle.
+ *
+ * Source: the TMA usage of "CuTe Swizzle 学习手册", sections "Sw<3,4,3> vs
+ * Sw<3,3,3>" (Sw<3,4,3> is the 128-byte pattern the TMA descriptor carries)
+ * and "H100 TMA + Swizzle".  The TMA 32-, 64- and 128-byte swizzle modes are
+ * the byte-address Swizzle<1,4,3>, <2,4,3> and <3,4,3>, i.e. element
+ * Swizzle<B, 4 - log2(esize), 3> for B = 1, 2, 3.
+ *
+ * Same arguments, rules, errors and result as swz_relayout.  The copy runs on
+ * the TMA (forward: a swizzled tensor load and a plain bulk store; inverse: a
+ * plain bulk load and a swizzled tensor store) when S = 3, M + log2(esize) = 4,
+ * 1 <= B <= 3, each tile holds a multiple of 2^(B+7) bytes and dst and src are
+ * 16-byte aligned; any other request runs swz_relayout's kernels.  The TMA
+ * path's bounded waits report to swz_device_status() (its status word is the
+ * one SWZ_T_TMA allocates on first use).
+ */
+swz_status swz_relayout_tma(void *dst, const void *src, int64_t n_tiles, int64_t rows,
+                            int64_t cols, int esize, int B, int M, int S, int direction,
+                            void *stream);
+
+/*
  * Matrix transpose HBM -> shared memory -> HBM.
  *
  * out[c][r] = in[r][c] for a rows x cols row-major matrix of esize-byte

@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "SwzError", "lib", "library_path",
-    "swz_relayout", "swz_transpose", "swz_bank_profile", "swz_slice_collision",
+    "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
     "swz_transpose_tma_noalloc",
     "swz_status_string", "swz_version",
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         i32, i64, u64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
         L.swz_relayout.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, i32, i32, vp]
         L.swz_relayout.restype = i32
+        L.swz_relayout_tma.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, i32, i32, vp]
+        L.swz_relayout_tma.restype = i32
         L.swz_transpose.argtypes = [vp, vp, i64, i64, i32, i32, vp]
         L.swz_transpose.restype = i32
         L.swz_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp, vp]
@@ -125,6 +127,14 @@ def swz_relayout(dst, src, n_tiles: int, rows: int, cols: int, esize: int, B: in
     """direction 0: dst[t][sw(i)] = src[t][i]; 1: dst[t][i] = src[t][sw(i)]."""
     _check(lib().swz_relayout(_ptr(dst), _ptr(src), n_tiles, rows, cols, esize, B, M, S, direction,
                               _stream(stream)), "swz_relayout")
+
+
+def swz_relayout_tma(dst, src, n_tiles: int, rows: int, cols: int, esize: int, B: int, M: int, S: int,
+                     direction: int, stream=None) -> None:
+    """swz_relayout through the TMA hardware swizzle where it applies
+    (S = 3, M + log2 esize = 4, 1 <= B <= 3); otherwise the same as swz_relayout."""
+    _check(lib().swz_relayout_tma(_ptr(dst), _ptr(src), n_tiles, rows, cols, esize, B, M, S, direction,
+                                  _stream(stream)), "swz_relayout_tma")
 
 
 def swz_transpose(dst, src, rows: int, cols: int, esize: int, variant: int = SWZ_T_SWIZZLED,

@@ -6,6 +6,8 @@ namespace swz {
 
 swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize,
                            int B, int M, int S, int direction, cudaStream_t st);
+swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize,
+                               int B, int M, int S, int direction, cudaStream_t st);
 swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
                             cudaStream_t st);
 swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, int64_t n, int width,
@@ -47,25 +49,53 @@ bool aligned_to(const void *p, int64_t n) { return (reinterpret_cast<uintptr_t>(
 }  // namespace
 }  // namespace swz
 
+namespace swz {
+namespace {
+// Validation shared by the relayout entry points; *launch is set when there
+// is work to launch (tile_elems then holds rows * cols).
+swz_status check_relayout(void *dst, const void *src, int64_t n_tiles, int64_t rows, int64_t cols, int esize, int B,
+                          int M, int S, int direction, int64_t *tile_elems, bool *launch) {
+    *launch = false;
+    if (!valid_esize(esize) || !valid_bms(B, M, S, 48) || (direction != 0 && direction != 1))
+        return SWZ_ERR_PARAM;
+    if (n_tiles < 0 || rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
+    int64_t n_elems, n_bytes;
+    if (!mul_ok(rows, cols, tile_elems) || !mul_ok(n_tiles, *tile_elems, &n_elems) ||
+        !mul_ok(n_elems, esize, &n_bytes))
+        return SWZ_ERR_SHAPE;
+    if (n_elems == 0) return SWZ_OK;
+    if (*tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
+    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+    *launch = true;
+    return SWZ_OK;
+}
+}  // namespace
+}  // namespace swz
+
 extern "C" {
 
 swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t rows, int64_t cols,
                         int esize, int B, int M, int S, int direction, void *stream) {
     using namespace swz;
-    if (!valid_esize(esize) || !valid_bms(B, M, S, 48) || (direction != 0 && direction != 1))
-        return SWZ_ERR_PARAM;
-    if (n_tiles < 0 || rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
-    int64_t tile_elems, n_elems, n_bytes;
-    if (!mul_ok(rows, cols, &tile_elems) || !mul_ok(n_tiles, tile_elems, &n_elems) ||
-        !mul_ok(n_elems, esize, &n_bytes))
-        return SWZ_ERR_SHAPE;
-    if (n_elems == 0) return SWZ_OK;
-    if (tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
-    if (!dst || !src) return SWZ_ERR_NULL;
-    if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
-    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+    int64_t tile_elems = 0;
+    bool launch = false;
+    const swz_status v = check_relayout(dst, src, n_tiles, rows, cols, esize, B, M, S, direction, &tile_elems, &launch);
+    if (v != SWZ_OK || !launch) return v;
     return relayout_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction,
                            static_cast<cudaStream_t>(stream));
+}
+
+swz_status swz_relayout_tma(void *dst, const void *src, int64_t n_tiles, int64_t rows, int64_t cols,
+                            int esize, int B, int M, int S, int direction, void *stream) {
+    using namespace swz;
+    int64_t tile_elems = 0;
+    bool launch = false;
+    const swz_status v = check_relayout(dst, src, n_tiles, rows, cols, esize, B, M, S, direction, &tile_elems, &launch);
+    if (v != SWZ_OK || !launch) return v;
+    return relayout_tma_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction,
+                               static_cast<cudaStream_t>(stream));
 }
 
 swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int esize, int variant,

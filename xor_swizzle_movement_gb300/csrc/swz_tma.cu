@@ -20,9 +20,8 @@
 // bounded by a time limit; on expiry the kernel records SWZ_ERR_TIMEOUT in a
 // per-device status word, waits (again bounded) for its own copies still in
 // flight, and returns; swz_device_status() reports it to the host.
-#include "swz_common.cuh"
+#include "swz_tma_common.cuh"
 
-#include <cuda.h>
 #include <mutex>
 
 namespace swz {
@@ -32,51 +31,6 @@ constexpr int kStages = 4;
 constexpr int kTile = 64;                        // 64 x 64 elements
 constexpr int kTileBytes = kTile * kTile * 2;    // 8 KiB
 constexpr int kThreads = 128;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > limit_ns) return false;
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &d0, uint32_t &d1,
                                                   uint32_t &d2, uint32_t &d3) {
@@ -200,12 +154,6 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t d0, uint32_t
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t smem_src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
-                 "r"(y), "r"(smem_src)
-                 : "memory");
-}
-
 constexpr int kOutBufs = 2;
 
 // Both directions through the tensor-memory accelerator: the input tile
@@ -296,10 +244,11 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---- host side ---------------------------------------------------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                   CUtensorMapFloatOOBfill);
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+uint32_t *g_status[kMaxDevices] = {};
+
+}  // namespace
 
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
@@ -314,12 +263,6 @@ EncodeTiledFn encode_fn() {
     });
     return fn;
 }
-
-constexpr int kMaxDevices = 64;
-std::mutex g_status_mu;
-uint32_t *g_status[kMaxDevices] = {};
-
-}  // namespace
 
 // The load+store kernel needs more than the default 48 KiB of dynamic shared
 // memory; the attribute is set once per device.
