@@ -40,33 +40,69 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    u64, i64, i32, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    L.orc_swizzle.argtypes = [u64, i32, i32, i32]
+    L.orc_swizzle.restype = u64
+    L.orc_relayout.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, i32]
+    L.orc_relayout.restype = i32
+    L.orc_relayout_positions.argtypes = [vp, i64, i64, i32, i32, i32, vp]
+    L.orc_relayout_positions.restype = i32
+    L.orc_transpose.argtypes = [vp, vp, i64, i64, i32]
+    L.orc_transpose.restype = i32
+    L.orc_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp]
+    L.orc_bank_profile.restype = i32
+    L.orc_slice_collision.argtypes = [u64, i32, i32, i32]
+    L.orc_slice_collision.restype = u64
+    L.orc_slice_is_layout.argtypes = [u64, i32, i32, i32]
+    L.orc_slice_is_layout.restype = i32
+    L.orc_dump_layout.argtypes = [ctypes.c_char_p, i64, i64, i64, i32, i32, i32, i32]
+    L.orc_dump_layout.restype = i64
+    return L
+
+
 _lib = None
 
 
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        path = build()
-        L = ctypes.CDLL(path)
-        u64, i64, i32, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
-        L.orc_swizzle.argtypes = [u64, i32, i32, i32]
-        L.orc_swizzle.restype = u64
-        L.orc_relayout.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, i32]
-        L.orc_relayout.restype = i32
-        L.orc_relayout_positions.argtypes = [vp, i64, i64, i32, i32, i32, vp]
-        L.orc_relayout_positions.restype = i32
-        L.orc_transpose.argtypes = [vp, vp, i64, i64, i32]
-        L.orc_transpose.restype = i32
-        L.orc_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp]
-        L.orc_bank_profile.restype = i32
-        L.orc_slice_collision.argtypes = [u64, i32, i32, i32]
-        L.orc_slice_collision.restype = u64
-        L.orc_slice_is_layout.argtypes = [u64, i32, i32, i32]
-        L.orc_slice_is_layout.restype = i32
-        L.orc_dump_layout.argtypes = [ctypes.c_char_p, i64, i64, i64, i32, i32, i32, i32]
-        L.orc_dump_layout.restype = i64
-        _lib = L
+        _lib = _bind(build())
     return _lib
+
+
+class Oracle:
+    """The oracle's functions bound to one compiled copy of it.  The
+    module-level functions use the default build; the tests that plant
+    mistakes in a copy of the C source bind that copy here."""
+
+    def __init__(self, path: str):
+        self.L = _bind(path)
+
+    def swizzle(self, offset, **kw):
+        return _swizzle(self.L, offset, **kw)
+
+    def relayout(self, src, **kw):
+        return _relayout(self.L, src, **kw)
+
+    def relayout_positions(self, idx, **kw):
+        return _relayout_positions(self.L, idx, **kw)
+
+    def transpose(self, src):
+        return _transpose(self.L, src)
+
+    def bank_profile(self, addrs, width, active=None):
+        return _bank_profile(self.L, addrs, width, active)
+
+    def slice_collision(self, A, **kw):
+        return _slice_collision(self.L, A, **kw)
+
+    def slice_is_layout(self, A, **kw):
+        return _slice_is_layout(self.L, A, **kw)
+
+    def dump_layout(self, rows, cols, esize, **kw):
+        return _dump_layout(self.L, rows, cols, esize, **kw)
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -78,45 +114,45 @@ def _ptr(a: np.ndarray) -> int:
 # i.e. (M, B, S).  The wrappers below take keyword arguments B, M, S so that a
 # caller cannot mix the orders up.
 
-def swizzle(offset: int, *, B: int, M: int, S: int) -> int:
-    return int(lib().orc_swizzle(offset, M, B, S))
+def _swizzle(L, offset: int, *, B: int, M: int, S: int) -> int:
+    return int(L.orc_swizzle(offset, M, B, S))
 
 
-def relayout(src: np.ndarray, *, tile_elems: int, B: int, M: int, S: int,
-             direction: int) -> np.ndarray:
+def _relayout(L, src: np.ndarray, *, tile_elems: int, B: int, M: int, S: int,
+              direction: int) -> np.ndarray:
     """src: contiguous array whose size is a multiple of tile_elems elements."""
     src = np.ascontiguousarray(src)
     dst = np.empty_like(src)
     esize = src.dtype.itemsize
     n_tiles = src.size // tile_elems if tile_elems else 0
     assert n_tiles * tile_elems == src.size
-    rc = lib().orc_relayout(_ptr(dst), _ptr(src), n_tiles, tile_elems, esize, M, B, S, direction)
+    rc = L.orc_relayout(_ptr(dst), _ptr(src), n_tiles, tile_elems, esize, M, B, S, direction)
     if rc != ORC_OK:
         raise ValueError(f"orc_relayout failed with {rc}")
     return dst
 
 
-def relayout_positions(idx: np.ndarray, *, tile_elems: int, B: int, M: int, S: int) -> np.ndarray:
+def _relayout_positions(L, idx: np.ndarray, *, tile_elems: int, B: int, M: int, S: int) -> np.ndarray:
     idx = np.ascontiguousarray(idx, dtype=np.int64)
     out = np.empty_like(idx)
-    rc = lib().orc_relayout_positions(_ptr(idx), idx.size, tile_elems, M, B, S, _ptr(out))
+    rc = L.orc_relayout_positions(_ptr(idx), idx.size, tile_elems, M, B, S, _ptr(out))
     if rc != ORC_OK:
         raise ValueError(f"orc_relayout_positions failed with {rc}")
     return out
 
 
-def transpose(src: np.ndarray) -> np.ndarray:
+def _transpose(L, src: np.ndarray) -> np.ndarray:
     """src: 2-D contiguous array; returns its transpose as a new contiguous array."""
     src = np.ascontiguousarray(src)
     rows, cols = src.shape
     dst = np.empty((cols, rows), dtype=src.dtype)
-    rc = lib().orc_transpose(_ptr(dst), _ptr(src), rows, cols, src.dtype.itemsize)
+    rc = L.orc_transpose(_ptr(dst), _ptr(src), rows, cols, src.dtype.itemsize)
     if rc != ORC_OK:
         raise ValueError(f"orc_transpose failed with {rc}")
     return dst
 
 
-def bank_profile(addrs: np.ndarray, width: int, active: np.ndarray | None = None):
+def _bank_profile(L, addrs: np.ndarray, width: int, active: np.ndarray | None = None):
     """addrs: (n, 32) uint32 byte addresses. Returns (ways, wavefronts) int32 arrays."""
     addrs = np.ascontiguousarray(addrs, dtype=np.uint32).reshape(-1, 32)
     n = addrs.shape[0]
@@ -127,22 +163,72 @@ def bank_profile(addrs: np.ndarray, width: int, active: np.ndarray | None = None
         active = np.ascontiguousarray(active, dtype=np.uint32)
         assert active.shape == (n,)
         act_ptr = _ptr(active)
-    rc = lib().orc_bank_profile(_ptr(addrs), act_ptr, n, width, _ptr(ways), _ptr(wf))
+    rc = L.orc_bank_profile(_ptr(addrs), act_ptr, n, width, _ptr(ways), _ptr(wf))
     if rc != ORC_OK:
         raise ValueError(f"orc_bank_profile failed with {rc}")
     return ways, wf
 
 
-def slice_collision(A: int, *, B: int, M: int, S: int) -> int:
-    return int(lib().orc_slice_collision(A, M, B, S))
+def _slice_collision(L, A: int, *, B: int, M: int, S: int) -> int:
+    return int(L.orc_slice_collision(A, M, B, S))
 
 
-def slice_is_layout(A: int, *, B: int, M: int, S: int) -> bool:
-    return bool(lib().orc_slice_is_layout(A, M, B, S))
+def _slice_is_layout(L, A: int, *, B: int, M: int, S: int) -> bool:
+    return bool(L.orc_slice_is_layout(A, M, B, S))
 
 
-def dump_layout(rows: int, cols: int, esize: int, *, B: int, M: int, S: int) -> str:
-    n = lib().orc_dump_layout(None, 0, rows, cols, esize, M, B, S)
+def _dump_layout(L, rows: int, cols: int, esize: int, *, B: int, M: int, S: int) -> str:
+    n = L.orc_dump_layout(None, 0, rows, cols, esize, M, B, S)
     buf = ctypes.create_string_buffer(int(n) + 1)
-    lib().orc_dump_layout(buf, n + 1, rows, cols, esize, M, B, S)
+    L.orc_dump_layout(buf, n + 1, rows, cols, esize, M, B, S)
     return buf.value.decode()
+
+
+# module-level functions on the default build
+def swizzle(offset, **kw):
+    return _swizzle(lib(), offset, **kw)
+
+
+def relayout(src, **kw):
+    return _relayout(lib(), src, **kw)
+
+
+def relayout_positions(idx, **kw):
+    return _relayout_positions(lib(), idx, **kw)
+
+
+def transpose(src):
+    return _transpose(lib(), src)
+
+
+def bank_profile(addrs, width, active=None):
+    return _bank_profile(lib(), addrs, width, active)
+
+
+def slice_collision(A, **kw):
+    return _slice_collision(lib(), A, **kw)
+
+
+def slice_is_layout(A, **kw):
+    return _slice_is_layout(lib(), A, **kw)
+
+
+def dump_layout(rows, cols, esize, **kw):
+    return _dump_layout(lib(), rows, cols, esize, **kw)
+
+
+def compile_copy(c_source: str, out_dir: str) -> str:
+    """Compile a (possibly edited) copy of the oracle's C source; returns the
+    shared library's path.  Used by the tests that plant mistakes."""
+    os.makedirs(out_dir, exist_ok=True)
+    src = os.path.join(out_dir, "swz_oracle_copy.c")
+    with open(src, "w") as f:
+        f.write(c_source)
+    out = os.path.join(out_dir, "liboracle_copy.so")
+    subprocess.check_call(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-o", out, src])
+    return out
+
+
+def c_source() -> str:
+    with open(_SRC) as f:
+        return f.read()

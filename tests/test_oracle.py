@@ -171,15 +171,20 @@ def test_relayout_roundtrip_and_closed(orc):
             assert inv2.tobytes() == src.tobytes()
 
 
-def test_relayout_tile_local(orc):
-    # two tiles relayout independently: the second tile equals a relayout of
-    # its own data
+@pytest.mark.parametrize("tile", [64, 48, 24])
+def test_relayout_tile_local(orc, tile):
+    """Tiles relayout independently: each tile of the batch equals a one-tile
+    relayout of its own data.  48 and 24 are multiples of 2^(M+B) = 8 but not
+    of the 64-element period of Swizzle<2,1,3>, so offsets taken over the
+    whole batch instead of the tile would differ."""
     B, M, S = 2, 1, 3
-    tile = 64
-    src = np.arange(2 * tile, dtype=np.int32)
-    out = orc.relayout(src, tile_elems=tile, B=B, M=M, S=S, direction=0)
-    second = orc.relayout(src[tile:] - tile, tile_elems=tile, B=B, M=M, S=S, direction=0)
-    assert np.array_equal(out[tile:] - tile, second)
+    src = np.arange(3 * tile, dtype=np.int32)
+    for direction in (0, 1):
+        out = orc.relayout(src, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        for t in range(3):
+            alone = orc.relayout(np.ascontiguousarray(src[t * tile:(t + 1) * tile]), tile_elems=tile,
+                                 B=B, M=M, S=S, direction=direction)
+            assert np.array_equal(out[t * tile:(t + 1) * tile], alone)
 
 
 def test_relayout_not_closed(orc):

@@ -1,0 +1,93 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source, on the CPU
+(a shifted field, a wrong mask, OR for XOR, a swapped direction, a wrong
+index, a wrong bank modulus, broken broadcast, ...), compiles the copy and
+runs the pin battery of test_oracle.py against it.  At least one pin must
+fail for every mistake; the unmodified copy must pass them all.
+"""
+import pytest
+
+import oracle
+import test_oracle as pins
+
+MUTATIONS = [
+    ("yy field one bit too high", "yy = (offset >> (base + shift)) & bits_mask;",
+     "yy = (offset >> (base + shift + 1)) & bits_mask;"),
+    ("yy field one bit too low", "yy = (offset >> (base + shift)) & bits_mask;",
+     "yy = (offset >> (base + shift - 1)) & bits_mask;"),
+    ("mask one bit short", "bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << bits) - 1);",
+     "bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << (bits - 1)) - 1);"),
+    ("OR instead of XOR", "aa = zz ^ yy;", "aa = zz | yy;"),
+    ("z field not cleared", "offset = offset & ~(bits_mask << base); /* clear the zz field */",
+     "offset = offset; /* clear the zz field */"),
+    ("aa written one bit off", "offset = offset | (aa << base);         /* set the aa field */",
+     "offset = offset | (aa << (base + 1));   /* set the aa field */"),
+    ("relayout forward as a gather",
+     "memcpy(d + (size_t)(tile0 + (int64_t)j) * esize,\n                       s + (size_t)(tile0 + i) * esize, (size_t)esize);",
+     "memcpy(d + (size_t)(tile0 + i) * esize,\n                       s + (size_t)(tile0 + (int64_t)j) * esize, (size_t)esize);"),
+    ("relayout on global offsets", "uint64_t j = orc_swizzle((uint64_t)i, base, bits, shift);",
+     "uint64_t j = orc_swizzle((uint64_t)(tile0 + i), base, bits, shift) - (uint64_t)tile0;"),
+    ("transpose writes with the wrong stride", "memcpy(d + (size_t)(c * rows + r) * esize,",
+     "memcpy(d + (size_t)(c * cols + r) * esize,"),
+    ("bank modulus 16", "if ((int)(words[k] % 32) == bank)", "if ((int)(words[k] % 16) == bank)"),
+    ("last word one too far", "last = (a + (uint64_t)width - 1) / 4;", "last = (a + (uint64_t)width) / 4;"),
+    ("16-byte accesses in two passes", "passes = (width <= 4) ? 1 : width / 4;",
+     "passes = (width <= 4) ? 1 : 2;"),
+    ("no broadcast: repeated words counted",
+     "for (k = 0; k < n_words; ++k)\n                        if (words[k] == wd)\n                            seen = 1;",
+     "(void)seen;"),
+    ("wavefronts = worst pass", "total += cost;", "total = worst;"),
+    ("collision keeps A & sw(A)", "return A & ~orc_swizzle(A, base, bits, shift);",
+     "return A & orc_swizzle(A, base, bits, shift);"),
+]
+
+
+def battery(orc):
+    """Run the pins on `orc`; return the names of the ones that fail."""
+    checks = [
+        ("worked_example", lambda: pins.test_worked_example_673(orc)),
+        ("mapping_32x32", lambda: pins.test_two_d_mappings(orc, 32, 32, pins._mapping_32x32, (5, 0, 5))),
+        ("mapping_64x32", lambda: pins.test_two_d_mappings(orc, 64, 32, pins._mapping_64x32, (5, 0, 5))),
+        ("mapping_32x64", lambda: pins.test_two_d_mappings(orc, 32, 64, pins._mapping_32x64, (5, 0, 6))),
+        ("mapping_half", lambda: pins.test_two_d_mappings(orc, 32, 64, pins._mapping_half_pairs, (5, 1, 5))),
+        ("bit_diagrams", lambda: pins.test_bit_diagrams(orc)),
+        ("invariants_333", lambda: pins.test_swizzle_invariants(orc, 3, 3, 3)),
+        ("invariants_525", lambda: pins.test_swizzle_invariants(orc, 5, 2, 5)),
+        ("degenerate", lambda: pins.test_swizzle_degenerate(orc)),
+        ("relayout_roundtrip", lambda: pins.test_relayout_roundtrip_and_closed(orc)),
+        ("relayout_tile_local", lambda: pins.test_relayout_tile_local(orc, 48)),
+        ("relayout_usage_loop", lambda: pins.test_relayout_usage_loop(orc)),
+        ("transpose_small", lambda: pins.test_transpose_small(orc)),
+        ("bank_column", lambda: pins.test_bank_column_fp32(orc)),
+        ("bank_padding_xor", lambda: pins.test_bank_padding_and_xor(orc)),
+        ("bank_fp16", lambda: pins.test_bank_fp16_64_columns(orc)),
+        ("bank_usage", lambda: pins.test_bank_usage_examples(orc)),
+        ("bank_broadcast", lambda: pins.test_bank_broadcast(orc)),
+        ("bank_passes", lambda: pins.test_bank_minimum_passes(orc)),
+        ("bank_unaligned", lambda: pins.test_bank_inactive_and_unaligned(orc)),
+        ("collision_table", lambda: pins.test_collision_truth_table(orc)),
+        ("collision_layout", lambda: pins.test_collision_predicts_layout(orc, 2, 0, 2)),
+        ("dump", lambda: pins.test_dump_layout(orc)),
+    ]
+    failed = []
+    for name, fn in checks:
+        try:
+            fn()
+        except (AssertionError, ValueError, OverflowError):
+            failed.append(name)
+    return failed
+
+
+def test_unmodified_copy_passes(tmp_path):
+    orc = oracle.Oracle(oracle.compile_copy(oracle.c_source(), str(tmp_path)))
+    assert battery(orc) == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = oracle.c_source()
+    assert src.count(old) == 1, name
+    orc = oracle.Oracle(oracle.compile_copy(src.replace(old, new), str(tmp_path)))
+    failed = battery(orc)
+    assert failed, f"no pin caught: {name}"
