@@ -373,6 +373,25 @@ def measure_rows(torch, swz, dev, flush, peak):
                    [(0, "swizzled_sw343_ldmatrix"), (3, "tma_swizzle128b"), (1, "unswizzled"), (2, "padded")], 3)
     transpose_rows("transpose_fp64_8192", 8192, 8, [(0, "swizzled_sw404"), (1, "unswizzled"), (2, "padded_17")], 4)
 
+    # transpose fused with the relayout: a 64 x 2^21 bf16 matrix (256 MiB) into K-major 128 x 64
+    # tiles under Swizzle<3,4,3>, in one pass, against the transpose and the relayout apart
+    kr, kc = 64, 1 << 21
+    s_ = rand_bytes(kr * kc * 2, 1)
+    d_ = torch.empty_like(s_)
+    t_ = torch.empty_like(s_)
+    fused = back_to_back_ms(torch, lambda: swz.swz_transpose_relayout(d_, s_, kr, kc, 2, 8192, 3, 4, 3))
+
+    def two_pass():
+        swz.swz_transpose(t_, s_, kr, kc, 2, 0)
+        swz.swz_relayout(d_, t_, kr * kc // 8192, 128, 64, 2, 3, 4, 3, 0)
+    two = back_to_back_ms(torch, two_pass)
+    plain = back_to_back_ms(torch, lambda: swz.swz_transpose(t_, s_, kr, kc, 2, 0))
+    nb = kr * kc * 2
+    out["transpose_relayout_bf16_64x2M_kmajor_sw343"] = {
+        "fused": summary(fused, 2 * nb), "transpose_alone": summary(plain, 2 * nb),
+        "two_pass": {"ms": round(two, 4), "speedup_of_fused": round(two / fused, 2)}}
+    del s_, d_, t_
+
     # bank profiler: 2^22 random aligned 4-byte patterns (512 MiB of addresses)
     npat = 1 << 22
     gen.manual_seed(5)

@@ -137,6 +137,30 @@ swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols,
                          int variant, void *stream);
 
 /*
+ * Transpose fused with a forward relayout of its result.
+ *
+ * Sources: the transpose of swz_transpose, then the relayout of swz_relayout
+ * ("CUDA 013 - Swizzle 的工作原理", sections "更通用的映射规则" and "使用示例");
+ * the use is producing swizzled operand tiles directly, as in the
+ * composition of Swizzle<3,4,3> with a (128, 64) row-major tile in "CuTe
+ * Swizzle 学习手册", section "CuTe 中如何使用 Swizzle".
+ *
+ * Let T be the cols x rows transpose of src (rows x cols, row-major).  T is
+ * cut into tiles of tile_elems consecutive elements and each tile is stored
+ * in swizzled order: dst[t * tile_elems + sw(i)] = T[t * tile_elems + i].
+ * One pass over HBM (the two steps apart would make two).  The staging is
+ * SWZ_T_SWIZZLED's.
+ *
+ * rows, cols >= 0; tile_elems > 0 divides rows * cols and is a multiple of
+ * 2^(M + B); B, M, S as in swz_relayout; esize 1, 2, 4, 8 or 16.
+ * Errors: as swz_transpose, SWZ_ERR_PARAM for B, M, S, and SWZ_ERR_SHAPE
+ * when tile_elems breaks the rules above.
+ */
+swz_status swz_transpose_relayout(void *dst, const void *src, int64_t rows, int64_t cols,
+                                  int esize, int64_t tile_elems, int B, int M, int S,
+                                  void *stream);
+
+/*
  * Shared-memory bank-conflict profiler for warp access patterns.
  *
  * Model: 32 banks of 4 bytes, bank = (byte_addr / 4) % 32 ("CuTe Swizzle

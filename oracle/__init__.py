@@ -51,6 +51,8 @@ def _bind(path: str) -> ctypes.CDLL:
     L.orc_relayout_positions.restype = i32
     L.orc_transpose.argtypes = [vp, vp, i64, i64, i32]
     L.orc_transpose.restype = i32
+    L.orc_transpose_relayout.argtypes = [vp, vp, vp, i64, i64, i32, i64, i32, i32, i32]
+    L.orc_transpose_relayout.restype = i32
     L.orc_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp]
     L.orc_bank_profile.restype = i32
     L.orc_slice_collision.argtypes = [u64, i32, i32, i32]
@@ -91,6 +93,9 @@ class Oracle:
 
     def transpose(self, src):
         return _transpose(self.L, src)
+
+    def transpose_relayout(self, src, **kw):
+        return _transpose_relayout(self.L, src, **kw)
 
     def bank_profile(self, addrs, width, active=None):
         return _bank_profile(self.L, addrs, width, active)
@@ -152,6 +157,19 @@ def _transpose(L, src: np.ndarray) -> np.ndarray:
     return dst
 
 
+def _transpose_relayout(L, src: np.ndarray, *, tile_elems: int, B: int, M: int, S: int) -> np.ndarray:
+    """src: 2-D contiguous (rows, cols); returns the flat cols*rows result."""
+    src = np.ascontiguousarray(src)
+    rows, cols = src.shape
+    dst = np.empty(rows * cols, dtype=src.dtype)
+    tmp = np.empty(rows * cols, dtype=src.dtype)
+    rc = L.orc_transpose_relayout(_ptr(dst), _ptr(src), _ptr(tmp), rows, cols, src.dtype.itemsize,
+                                  tile_elems, M, B, S)
+    if rc != ORC_OK:
+        raise ValueError(f"orc_transpose_relayout failed with {rc}")
+    return dst
+
+
 def _bank_profile(L, addrs: np.ndarray, width: int, active: np.ndarray | None = None):
     """addrs: (n, 32) uint32 byte addresses. Returns (ways, wavefronts) int32 arrays."""
     addrs = np.ascontiguousarray(addrs, dtype=np.uint32).reshape(-1, 32)
@@ -199,6 +217,10 @@ def relayout_positions(idx, **kw):
 
 def transpose(src):
     return _transpose(lib(), src)
+
+
+def transpose_relayout(src, **kw):
+    return _transpose_relayout(lib(), src, **kw)
 
 
 def bank_profile(addrs, width, active=None):

@@ -21,6 +21,7 @@
  *   orc_swizzle            pinned (worked example, 2-D closed forms, bit diagrams)
  *   orc_relayout           pinned (reduces to orc_swizzle + byte copies)
  *   orc_transpose          pinned (textbook transpose, explicit small cases)
+ *   orc_transpose_relayout the two pinned steps above, in that order
  *   orc_bank_profile       pinned for access widths 1,2,4; the phase split
  *                          used for 8- and 16-byte accesses is a reading the
  *                          pages do not fix: "parity unpinned" for w = 8, 16.
@@ -127,6 +128,24 @@ int orc_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int es
             memcpy(d + (size_t)(c * rows + r) * esize,
                    s + (size_t)(r * cols + c) * esize, (size_t)esize);
     return ORC_OK;
+}
+
+/*
+ * Transpose, then forward relayout of the transposed matrix: the cols x rows
+ * result is cut into tiles of tile_elems consecutive elements and each tile is
+ * stored in swizzled order.  The two steps in that order, through a scratch
+ * copy of the transposed matrix (tmp, rows * cols elements, caller-owned).
+ */
+int orc_transpose_relayout(void *dst, const void *src, void *tmp, int64_t rows, int64_t cols, int esize,
+                           int64_t tile_elems, int base, int bits, int shift)
+{
+    int rc;
+    if (tile_elems <= 0 || (rows * cols) % tile_elems != 0)
+        return ORC_BAD_ARG;
+    rc = orc_transpose(tmp, src, rows, cols, esize);
+    if (rc != ORC_OK)
+        return rc;
+    return orc_relayout(dst, tmp, (rows * cols) / tile_elems, tile_elems, esize, base, bits, shift, 0);
 }
 
 /*

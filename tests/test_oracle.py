@@ -231,6 +231,24 @@ def test_transpose_matches_library(orc, dtype):
     assert np.array_equal(orc.transpose(t), a)
 
 
+def test_transpose_relayout_composes(orc):
+    """The fused operation is the transpose followed by the forward relayout
+    of the transposed matrix in tiles of tile_elems elements."""
+    rng = np.random.default_rng(3)
+    a = rng.integers(0, 2**16, size=(24, 40)).astype(np.uint16)
+    got = orc.transpose_relayout(a, tile_elems=8 * 24, B=3, M=0, S=3)
+    t = orc.transpose(a).ravel()
+    assert np.array_equal(got, orc.relayout(t, tile_elems=8 * 24, B=3, M=0, S=3, direction=0))
+    # the untouched case: B = 0 is the plain transpose
+    assert np.array_equal(orc.transpose_relayout(a, tile_elems=24, B=0, M=0, S=3), a.T.ravel())
+    # element (r, c) of the input lands in tile (c*rows + r) // te at sw(offset within the tile)
+    te = 8 * 24
+    for r, c in [(0, 0), (5, 7), (23, 39), (11, 20)]:
+        off = c * 24 + r
+        tile, loc = divmod(off, te)
+        assert got[tile * te + orc.swizzle(loc, B=3, M=0, S=3)] == a[r, c]
+
+
 # ------------------------------------------------------------- bank model ---
 
 def _ways(orc, addrs, width, active=None):

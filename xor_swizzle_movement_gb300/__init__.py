@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "SwzError", "lib", "library_path",
-    "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_bank_profile", "swz_slice_collision",
+    "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
     "swz_transpose_tma_noalloc",
     "swz_status_string", "swz_version",
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.swz_relayout_tma.restype = i32
         L.swz_transpose.argtypes = [vp, vp, i64, i64, i32, i32, vp]
         L.swz_transpose.restype = i32
+        L.swz_transpose_relayout.argtypes = [vp, vp, i64, i64, i32, i64, i32, i32, i32, vp]
+        L.swz_transpose_relayout.restype = i32
         L.swz_bank_profile.argtypes = [vp, vp, i64, i32, vp, vp, vp]
         L.swz_bank_profile.restype = i32
         L.swz_slice_collision.argtypes = [u64, i32, i32, i32, ctypes.POINTER(u64)]
@@ -142,6 +144,14 @@ def swz_transpose(dst, src, rows: int, cols: int, esize: int, variant: int = SWZ
     """dst (cols x rows) = transpose of src (rows x cols), raw esize-byte elements."""
     _check(lib().swz_transpose(_ptr(dst), _ptr(src), rows, cols, esize, variant, _stream(stream)),
            "swz_transpose")
+
+
+def swz_transpose_relayout(dst, src, rows: int, cols: int, esize: int, tile_elems: int, B: int, M: int,
+                           S: int, stream=None) -> None:
+    """dst = the transpose of src (rows x cols), cut into tiles of tile_elems
+    elements, each tile in Swizzle<B,M,S> order (forward relayout)."""
+    _check(lib().swz_transpose_relayout(_ptr(dst), _ptr(src), rows, cols, esize, tile_elems, B, M, S,
+                                        _stream(stream)), "swz_transpose_relayout")
 
 
 def swz_bank_profile(byte_addrs, active, n: int, access_bytes: int, ways, wavefronts,

@@ -10,6 +10,8 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
                                int B, int M, int S, int direction, cudaStream_t st);
 swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
                             cudaStream_t st);
+swz_status transpose_relayout_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int64_t te,
+                                     int B, int M, int S, cudaStream_t st);
 swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, int64_t n, int width,
                                int32_t *ways, int32_t *wavefronts, cudaStream_t st);
 swz_status slice_collision_launch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
@@ -111,6 +113,22 @@ swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols,
     if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
     if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
     return transpose_launch(dst, src, rows, cols, esize, variant, static_cast<cudaStream_t>(stream));
+}
+
+swz_status swz_transpose_relayout(void *dst, const void *src, int64_t rows, int64_t cols, int esize,
+                                  int64_t tile_elems, int B, int M, int S, void *stream) {
+    using namespace swz;
+    if (!valid_esize(esize) || !valid_bms(B, M, S, 48)) return SWZ_ERR_PARAM;
+    if (rows < 0 || cols < 0 || tile_elems <= 0) return SWZ_ERR_SHAPE;
+    int64_t n_elems, n_bytes;
+    if (!mul_ok(rows, cols, &n_elems) || !mul_ok(n_elems, esize, &n_bytes)) return SWZ_ERR_SHAPE;
+    if (n_elems % tile_elems != 0 || tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
+    if (n_elems == 0) return SWZ_OK;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
+    if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
+    return transpose_relayout_launch(dst, src, rows, cols, esize, tile_elems, B, M, S,
+                                     static_cast<cudaStream_t>(stream));
 }
 
 swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, int64_t n,

@@ -63,6 +63,82 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+
+// 16-byte vectors of E-byte elements: V lanes, log2 V.
+template <int E>
+struct VecTraits {
+    static constexpr int V = 16 / E;  // lanes (elements) per vector
+    static constexpr int LV = (E == 1) ? 4 : (E == 2) ? 3 : (E == 4) ? 2 : (E == 8) ? 1 : 0;
+};
+
+// out lane l = in lane l ^ L
+template <int E>
+__device__ __forceinline__ uint4 lanes_xor(uint4 v, uint32_t L) {
+    if constexpr (E == 16) {
+        return v;
+    } else {
+        uint32_t wx;
+        if constexpr (E == 8) wx = L << 1;
+        else if constexpr (E == 4) wx = L;
+        else if constexpr (E == 2) wx = L >> 1;
+        else wx = L >> 2;
+        uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w, t;
+        if (wx & 1u) { t = w0; w0 = w1; w1 = t; t = w2; w2 = w3; w3 = t; }
+        if (wx & 2u) { t = w0; w0 = w2; w2 = t; t = w1; w1 = w3; w3 = t; }
+        if constexpr (E == 2) {
+            if (L & 1u) {
+                w0 = __byte_perm(w0, 0, 0x1032); w1 = __byte_perm(w1, 0, 0x1032);
+                w2 = __byte_perm(w2, 0, 0x1032); w3 = __byte_perm(w3, 0, 0x1032);
+            }
+        }
+        if constexpr (E == 1) {
+            const uint32_t sel = 0x3210u ^ (0x1111u * (L & 3u));
+            w0 = __byte_perm(w0, 0, sel); w1 = __byte_perm(w1, 0, sel);
+            w2 = __byte_perm(w2, 0, sel); w3 = __byte_perm(w3, 0, sel);
+        }
+        return make_uint4(w0, w1, w2, w3);
+    }
+}
+
+// A fixed permutation of the 16 bytes of v: output byte 4w + i comes from the
+// input byte the host encoded in sel[3w .. 3w + 2] (two prmt pick from the low
+// and the high 8 bytes, a third merges them).
+__device__ __forceinline__ uint4 bytes_permute(uint4 v, const uint32_t *sel) {
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = __byte_perm(v.x, v.y, sel[3 * w]);
+        const uint32_t hi = __byte_perm(v.z, v.w, sel[3 * w + 1]);
+        o[w] = __byte_perm(lo, hi, sel[3 * w + 2]);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+
+// Host side: the prmt selectors that make bytes_permute move lane l of a
+// 16-byte vector of esize-byte elements from lane src_lane[l].
+inline void lane_map_selectors(const int *src_lane, int esize, uint32_t sel[12]) {
+    int src_byte[16];
+    const int lanes = 16 / esize;
+    for (int l = 0; l < lanes; ++l)
+        for (int bb = 0; bb < esize; ++bb) src_byte[l * esize + bb] = src_lane[l] * esize + bb;
+    for (int w = 0; w < 4; ++w) {
+        uint32_t s_lo = 0, s_hi = 0, s_mix = 0;
+        for (int i = 0; i < 4; ++i) {
+            const int sb = src_byte[4 * w + i];
+            if (sb < 8) {
+                s_lo |= static_cast<uint32_t>(sb) << (4 * i);
+                s_mix |= static_cast<uint32_t>(i) << (4 * i);
+            } else {
+                s_hi |= static_cast<uint32_t>(sb - 8) << (4 * i);
+                s_mix |= static_cast<uint32_t>(4 + i) << (4 * i);
+            }
+        }
+        sel[3 * w] = s_lo;
+        sel[3 * w + 1] = s_hi;
+        sel[3 * w + 2] = s_mix;
+    }
+}
 }  // namespace swz
 
 // Host-side helpers shared by the launchers (defined in swz_abi.cu).

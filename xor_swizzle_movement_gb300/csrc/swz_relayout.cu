@@ -51,54 +51,6 @@ struct RelayoutArgs {
 
 constexpr int kMaxPerThread = 4;
 
-template <int E>
-struct VecTraits {
-    static constexpr int V = 16 / E;  // lanes (elements) per vector
-    static constexpr int LV = (E == 1) ? 4 : (E == 2) ? 3 : (E == 4) ? 2 : (E == 8) ? 1 : 0;
-};
-
-// out lane l = in lane l ^ L
-template <int E>
-__device__ __forceinline__ uint4 lanes_xor(uint4 v, uint32_t L) {
-    if constexpr (E == 16) {
-        return v;
-    } else {
-        uint32_t wx;
-        if constexpr (E == 8) wx = L << 1;
-        else if constexpr (E == 4) wx = L;
-        else if constexpr (E == 2) wx = L >> 1;
-        else wx = L >> 2;
-        uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w, t;
-        if (wx & 1u) { t = w0; w0 = w1; w1 = t; t = w2; w2 = w3; w3 = t; }
-        if (wx & 2u) { t = w0; w0 = w2; w2 = t; t = w1; w1 = w3; w3 = t; }
-        if constexpr (E == 2) {
-            if (L & 1u) {
-                w0 = __byte_perm(w0, 0, 0x1032); w1 = __byte_perm(w1, 0, 0x1032);
-                w2 = __byte_perm(w2, 0, 0x1032); w3 = __byte_perm(w3, 0, 0x1032);
-            }
-        }
-        if constexpr (E == 1) {
-            const uint32_t sel = 0x3210u ^ (0x1111u * (L & 3u));
-            w0 = __byte_perm(w0, 0, sel); w1 = __byte_perm(w1, 0, sel);
-            w2 = __byte_perm(w2, 0, sel); w3 = __byte_perm(w3, 0, sel);
-        }
-        return make_uint4(w0, w1, w2, w3);
-    }
-}
-
-// A fixed permutation of the 16 bytes of v: output byte 4w + i comes from the
-// input byte the host encoded in sel[3w .. 3w + 2] (two prmt pick from the low
-// and the high 8 bytes, a third merges them).
-__device__ __forceinline__ uint4 bytes_permute(uint4 v, const uint32_t *sel) {
-    uint32_t o[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const uint32_t lo = __byte_perm(v.x, v.y, sel[3 * w]);
-        const uint32_t hi = __byte_perm(v.z, v.w, sel[3 * w + 1]);
-        o[w] = __byte_perm(lo, hi, sel[3 * w + 2]);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
 
 template <int E, int MODE, bool LOCAL>
 __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a) {
@@ -219,30 +171,11 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // several waves deep (152 SMs x 2048 threads per wave)
         const int64_t wave = 152LL * 2048;
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
-        // kLanesGeneral: out lane l = (lanes XOR-ed by k)[L(l)], L(l) = g(l) for a lane index l;
-        // as bytes: out byte l * esize + b <- in byte L(l) * esize + b
-        int src_byte[16];
-        const int lanes = 16 / esize;
-        for (int l = 0; l < lanes; ++l) {
-            const int Ll = static_cast<int>(sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & (lanes - 1));
-            for (int bb = 0; bb < esize; ++bb) src_byte[l * esize + bb] = Ll * esize + bb;
-        }
-        for (int w = 0; w < 4; ++w) {
-            uint32_t s_lo = 0, s_hi = 0, s_mix = 0;
-            for (int i = 0; i < 4; ++i) {
-                const int sb = src_byte[4 * w + i];
-                if (sb < 8) {
-                    s_lo |= static_cast<uint32_t>(sb) << (4 * i);
-                    s_mix |= static_cast<uint32_t>(i) << (4 * i);
-                } else {
-                    s_hi |= static_cast<uint32_t>(sb - 8) << (4 * i);
-                    s_mix |= static_cast<uint32_t>(4 + i) << (4 * i);
-                }
-            }
-            a.perm_sel[3 * w] = s_lo;
-            a.perm_sel[3 * w + 1] = s_hi;
-            a.perm_sel[3 * w + 2] = s_mix;
-        }
+        // kLanesGeneral: out lane l = (lanes XOR-ed by k)[L(l)], L(l) = g(l) for a lane index l
+        int src_lane[16];
+        for (int l = 0; l < 16 / esize; ++l)
+            src_lane[l] = static_cast<int>(sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & ((16 / esize) - 1));
+        lane_map_selectors(src_lane, esize, a.perm_sel);
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
         const int period = B + M + S;
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);

@@ -45,13 +45,44 @@
 #include <cstring>
 
 namespace swz {
+
+// A transpose can hand its output straight to a forward relayout: the
+// transposed matrix, cut into tiles of `te` consecutive elements, each tile
+// stored in Swizzle<B,M,S> order.  Transposed element y then lands at
+// fused_pos(y); a 16-byte vector of it lands in one 16-byte vector (the
+// swizzle only reads bits above the bits it writes), with its lanes moved by
+// the inverse lane map L^-1 (fixed, `sel`) and then XOR-ed by the vector's k.
+struct FuseArgs {
+    int64_t te;         // relayout tile, elements
+    int B, M, S;
+    int global;         // te is a multiple of 2^(B+M+S): the whole-matrix offset may be swizzled directly
+    int lanes;          // 0: lanes stay (M >= log2 V); 1: lanes XOR-ed by k only (M + S >= log2 V); 2: general
+    uint32_t sel[12];   // bytes_permute selectors of L^-1, L(l) = sw(l) mod V
+};
+
 namespace {
 
+__device__ __forceinline__ uint64_t fused_pos(uint64_t y, const FuseArgs &f) {
+    if (f.global) return sw_fwd(y, f.B, f.M, f.S);
+    const uint64_t loc = y % static_cast<uint64_t>(f.te);
+    return (y - loc) + sw_fwd(loc, f.B, f.M, f.S);
+}
+
+template <int E>
+__device__ __forceinline__ void store16_fused(void *dst, uint64_t y, uint4 v, const FuseArgs &f) {
+    constexpr uint64_t VM = VecTraits<E>::V - 1;
+    const uint64_t x = fused_pos(y, f);
+    uint4 o = v;  // f.lanes is uniform over the launch: no divergence
+    if (f.lanes == 2) o = bytes_permute(o, f.sel);
+    if (f.lanes != 0) o = lanes_xor<E>(o, static_cast<uint32_t>(x & VM));
+    st_stream16(static_cast<uint8_t *>(dst) + (x & ~VM) * E, o);
+}
+
 // ---------------------------------------------------------------- 4 / 8 B --
-template <typename T, int VARIANT, int UR, int UC, int THREADS, int MIN_CTAS>
+template <typename T, int VARIANT, int UR, int UC, int THREADS, int MIN_CTAS, bool FUSE>
 __global__ void __launch_bounds__(THREADS, MIN_CTAS)
     transpose_unit_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
-                          int64_t tiles_c, int vec_ok) {
+                          int64_t tiles_c, int vec_ok, const FuseArgs f) {
     constexpr int N = 128 / static_cast<int>(sizeof(T));    // unit edge: 32 (4 B) or 16 (8 B)
     constexpr int VPE = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte vector
     constexpr int P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;  // unit row pitch, elements
@@ -107,7 +138,9 @@ __global__ void __launch_bounds__(THREADS, MIN_CTAS)
             }
             uint4 o;
             memcpy(&o, e, 16);
-            st_stream16(dst + (c0 + ocl) * R + r0 + ur * N + p * VPE, o);
+            const int64_t y = (c0 + ocl) * R + r0 + ur * N + p * VPE;
+            if constexpr (FUSE) store16_fused<static_cast<int>(sizeof(T))>(dst, static_cast<uint64_t>(y), o, f);
+            else st_stream16(dst + y, o);
         }
     } else {
         for (int idx = tid; idx < TR * TC; idx += THREADS) {
@@ -122,7 +155,9 @@ __global__ void __launch_bounds__(THREADS, MIN_CTAS)
             const int ocl = idx / TR, orow = idx % TR;
             if (c0 + ocl < C && r0 + orow < R) {
                 const int ur = orow / N, ir = orow % N, uc = ocl / N, ic = ocl % N;
-                dst[(c0 + ocl) * R + r0 + orow] = sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)];
+                const int64_t y = (c0 + ocl) * R + r0 + orow;
+                dst[FUSE ? static_cast<int64_t>(fused_pos(static_cast<uint64_t>(y), f)) : y] =
+                    sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)];
             }
         }
     }
@@ -144,10 +179,10 @@ __device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2,
 }
 
 // Tile 64 x 64 of 16-bit elements, 128 threads.
-template <int VARIANT>
+template <int VARIANT, bool FUSE>
 __global__ void __launch_bounds__(128)
     transpose16_kernel(uint16_t *__restrict__ dst, const uint16_t *__restrict__ src, int64_t R,
-                       int64_t C, int64_t tiles_c, int vec_ok) {
+                       int64_t C, int64_t tiles_c, int vec_ok, const FuseArgs f) {
     constexpr int TR = 64, TC = 64, THREADS = 128;
     constexpr int PITCH = (VARIANT == SWZ_T_PADDED) ? 72 : 64;  // elements per shared row
     __shared__ __align__(1024) uint16_t sm[TR * PITCH];
@@ -195,7 +230,9 @@ __global__ void __launch_bounds__(128)
                 b2 = (from == 2) ? got : b2;
                 b3 = (from == 3) ? got : b3;
             }
-            st_stream16(dst + (c0 + cb * 8 + g) * R + r0 + (rbg + kk) * 8, make_uint4(b0, b1, b2, b3));
+            const int64_t y = (c0 + cb * 8 + g) * R + r0 + (rbg + kk) * 8;
+            if constexpr (FUSE) store16_fused<2>(dst, static_cast<uint64_t>(y), make_uint4(b0, b1, b2, b3), f);
+            else st_stream16(dst + y, make_uint4(b0, b1, b2, b3));
         }
     } else {
         for (int idx = tid; idx < TR * TC; idx += THREADS) {
@@ -206,17 +243,20 @@ __global__ void __launch_bounds__(128)
         __syncthreads();
         for (int idx = tid; idx < TR * TC; idx += THREADS) {
             const int ocl = idx / TR, orow = idx % TR;
-            if (c0 + ocl < C && r0 + orow < R)
-                dst[(c0 + ocl) * R + r0 + orow] = sm[orow * PITCH + chunk(orow, ocl >> 3) * 8 + (ocl & 7)];
+            if (c0 + ocl < C && r0 + orow < R) {
+                const int64_t y = (c0 + ocl) * R + r0 + orow;
+                dst[FUSE ? static_cast<int64_t>(fused_pos(static_cast<uint64_t>(y), f)) : y] =
+                    sm[orow * PITCH + chunk(orow, ocl >> 3) * 8 + (ocl & 7)];
+            }
         }
     }
 }
 
 // --------------------------------------------------------------- 1 / 16 B --
-template <typename T, int VARIANT>
+template <typename T, int VARIANT, bool FUSE>
 __global__ void __launch_bounds__(256)
     transpose_generic_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
-                             int64_t tiles_c) {
+                             int64_t tiles_c, const FuseArgs f) {
     constexpr int N = 32, P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;
     __shared__ T sm[N * P];
     const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
@@ -230,84 +270,128 @@ __global__ void __launch_bounds__(256)
     __syncthreads();
     for (int idx = threadIdx.x; idx < N * N; idx += 256) {
         const int ocl = idx >> 5, orow = idx & 31;
-        if (c0 + ocl < C && r0 + orow < R)
-            dst[(c0 + ocl) * R + r0 + orow] = sm[orow * P + phys(orow, ocl)];
+        if (c0 + ocl < C && r0 + orow < R) {
+            const int64_t y = (c0 + ocl) * R + r0 + orow;
+            dst[FUSE ? static_cast<int64_t>(fused_pos(static_cast<uint64_t>(y), f)) : y] = sm[orow * P + phys(orow, ocl)];
+        }
     }
 }
 
 template <typename T, int UR, int UC, int THREADS, int MIN_CTAS>
 swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
-                       cudaStream_t st) {
+                       const FuseArgs *fuse, cudaStream_t st) {
     constexpr int N = 128 / static_cast<int>(sizeof(T));
     constexpr int VPE = 16 / static_cast<int>(sizeof(T));
     const int64_t TR = UR * N, TC = UC * N;
     const int64_t tiles_c = (C + TC - 1) / TC, tiles = ((R + TR - 1) / TR) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    const int vec_ok = aligned16 && (C % VPE == 0) && (R % VPE == 0);
+    // a fused relayout needs its tiles to hold whole 16-byte vectors
+    const int vec_ok = aligned16 && (C % VPE == 0) && (R % VPE == 0) && (!fuse || fuse->te % VPE == 0);
     T *d = static_cast<T *>(dst);
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
-    if (variant == SWZ_T_SWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    if (fuse)
+        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, true><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+    else if (variant == SWZ_T_SWIZZLED)
+        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     else
-        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS, MIN_CTAS><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     return launch_status();
 }
 
 swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
-                     cudaStream_t st) {
+                     const FuseArgs *fuse, cudaStream_t st) {
     const int64_t tiles_c = (C + 63) / 64, tiles = ((R + 63) / 64) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    const int vec_ok = aligned16 && (C % 8 == 0) && (R % 8 == 0);
+    const int vec_ok = aligned16 && (C % 8 == 0) && (R % 8 == 0) && (!fuse || fuse->te % 8 == 0);
     uint16_t *d = static_cast<uint16_t *>(dst);
     const uint16_t *s = static_cast<const uint16_t *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
-    if (variant == SWZ_T_SWIZZLED)
-        transpose16_kernel<SWZ_T_SWIZZLED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+    const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    if (fuse)
+        transpose16_kernel<SWZ_T_SWIZZLED, true><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+    else if (variant == SWZ_T_SWIZZLED)
+        transpose16_kernel<SWZ_T_SWIZZLED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose16_kernel<SWZ_T_UNSWIZZLED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose16_kernel<SWZ_T_UNSWIZZLED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     else
-        transpose16_kernel<SWZ_T_PADDED><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok);
+        transpose16_kernel<SWZ_T_PADDED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
     return launch_status();
 }
 
 template <typename T>
-swz_status launch_generic(void *dst, const void *src, int64_t R, int64_t C, int variant,
+swz_status launch_generic(void *dst, const void *src, int64_t R, int64_t C, int variant, const FuseArgs *fuse,
                           cudaStream_t st) {
     const int64_t tiles_c = (C + 31) / 32, tiles = ((R + 31) / 32) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     T *d = static_cast<T *>(dst);
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
-    if (variant == SWZ_T_SWIZZLED)
-        transpose_generic_kernel<T, SWZ_T_SWIZZLED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+    const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    if (fuse)
+        transpose_generic_kernel<T, SWZ_T_SWIZZLED, true><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
+    else if (variant == SWZ_T_SWIZZLED)
+        transpose_generic_kernel<T, SWZ_T_SWIZZLED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose_generic_kernel<T, SWZ_T_UNSWIZZLED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+        transpose_generic_kernel<T, SWZ_T_UNSWIZZLED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
     else
-        transpose_generic_kernel<T, SWZ_T_PADDED><<<g, 256, 0, st>>>(d, s, R, C, tiles_c);
+        transpose_generic_kernel<T, SWZ_T_PADDED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
     return launch_status();
 }
+
+swz_status dispatch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant, const FuseArgs *fuse,
+                    cudaStream_t st);
 
 }  // namespace
 
 swz_status transpose_tma_launch(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st);
 
-// Arguments are validated by the caller (swz_transpose in swz_abi.cu).
-swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize,
-                            int variant, cudaStream_t st) {
+namespace {
+swz_status dispatch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant, const FuseArgs *fuse,
+                    cudaStream_t st) {
     const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
     switch (esize) {
-        case 1: return launch_generic<uint8_t>(dst, src, R, C, variant, st);
+        case 1: return launch_generic<uint8_t>(dst, src, R, C, variant, fuse, st);
         case 2:
-            if (variant == SWZ_T_TMA) return transpose_tma_launch(dst, src, R, C, st);
-            return launch_16(dst, src, R, C, variant, aligned16, st);
-        case 4: return launch_unit<uint32_t, 2, 2, 256, 6>(dst, src, R, C, variant, aligned16, st);
-        case 8: return launch_unit<unsigned long long, 2, 2, 256, 8>(dst, src, R, C, variant, aligned16, st);
-        case 16: return launch_generic<uint4>(dst, src, R, C, variant, st);
+            if (variant == SWZ_T_TMA && !fuse) return transpose_tma_launch(dst, src, R, C, st);
+            return launch_16(dst, src, R, C, variant, aligned16, fuse, st);
+        case 4: return launch_unit<uint32_t, 2, 2, 256, 6>(dst, src, R, C, variant, aligned16, fuse, st);
+        case 8: return launch_unit<unsigned long long, 2, 2, 256, 8>(dst, src, R, C, variant, aligned16, fuse, st);
+        case 16: return launch_generic<uint4>(dst, src, R, C, variant, fuse, st);
         default: return SWZ_ERR_PARAM;
     }
+}
+}  // namespace
+
+// Arguments are validated by the caller (swz_transpose in swz_abi.cu).
+swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
+                            cudaStream_t st) {
+    return dispatch(dst, src, R, C, esize, variant, nullptr, st);
+}
+
+// Arguments are validated by the caller (swz_transpose_relayout in swz_abi.cu).
+swz_status transpose_relayout_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int64_t te,
+                                     int B, int M, int S, cudaStream_t st) {
+    FuseArgs f{};
+    f.te = te;
+    f.B = B;
+    f.M = M;
+    f.S = S;
+    const int period = B + M + S;
+    f.global = (B == 0) || (period < 62 && te % (int64_t(1) << period) == 0);
+    // L(l) = sw(l) mod V on the lanes of a 16-byte vector; bytes_permute needs L^-1
+    const int lanes = 16 / esize;
+    int L[16], Linv[16];
+    for (int l = 0; l < lanes; ++l) L[l] = static_cast<int>(sw_fwd(static_cast<uint64_t>(l), B, M, S) & (lanes - 1));
+    for (int l = 0; l < lanes; ++l) Linv[L[l]] = l;
+    lane_map_selectors(Linv, esize, f.sel);
+    int lv = 0;
+    while ((1 << lv) < lanes) ++lv;
+    f.lanes = (B == 0 || M >= lv) ? 0 : (M + S >= lv) ? 1 : 2;
+    return dispatch(dst, src, R, C, esize, SWZ_T_SWIZZLED, &f, st);
 }
 
 }  // namespace swz
