@@ -206,6 +206,21 @@ swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, 
 swz_status swz_slice_collision(uint64_t A, int B, int M, int S, uint64_t *C_out);
 
 /*
+ * The plain layout that replaces the swizzle on a slice ("cutlass 入门",
+ * section "swizzle 融入 layout 优化": when no (Y_i, Z_i) pair is active, the
+ * swizzle composed with the slice equals a plain layout).
+ *
+ * If swz_slice_collision(A) is 0, writes for each set bit of A, from the
+ * lowest, its stride strides[k] = sw(2^bit) and the count to *n_bits, so that
+ * sw(x) = sum over the set bits of x of their strides, for every x whose bits
+ * are a subset of A; returns SWZ_OK.  Otherwise writes nothing and returns
+ * SWZ_ERR_UNSUPPORTED (the slice keeps a real XOR).  strides: host array of
+ * at least 64 entries.  Host function, synchronous.
+ * Errors: SWZ_ERR_NULL, SWZ_ERR_PARAM (as swz_slice_collision).
+ */
+swz_status swz_slice_layout(uint64_t A, int B, int M, int S, uint64_t *strides, int *n_bits);
+
+/*
  * Batched slice collision on the GPU: C[k] = A[k] & ~sw(A[k]) for n masks.
  * A, C: device arrays of n uint64.  Same parameter rules as
  * swz_slice_collision; SWZ_ERR_SHAPE for n < 0.

@@ -106,3 +106,21 @@ def test_status_strings(swz):
         assert s.startswith("SWZ_")
     assert "unknown" in swz.swz_status_string(99)
     assert swz.swz_version() >= 100
+
+
+@pytest.mark.parametrize("B,M,S", [(2, 0, 2), (3, 1, 2), (2, 1, 3), (3, 0, 1)])
+def test_slice_layout(swz, orc, B, M, S):
+    """Slices whose collision mask is 0 come back as per-bit strides that
+    reproduce the swizzle on every subset (the oracle's brute force agrees);
+    the others are refused."""
+    import itertools
+    for A in range(1 << (B + M + S + 1)):
+        strides = swz.swz_slice_layout(A, B, M, S)
+        assert (strides is not None) == orc.slice_is_layout(A, B=B, M=M, S=S), A
+        if strides is None:
+            continue
+        bits = [i for i in range(64) if (A >> i) & 1]
+        assert len(strides) == len(bits)
+        for pick in itertools.product((0, 1), repeat=len(bits)):
+            x = sum(b << i for b, i in zip(pick, bits))
+            assert sum(b * st for b, st in zip(pick, strides)) == orc.swizzle(x, B=B, M=M, S=S)

@@ -18,7 +18,7 @@ import os
 __all__ = [
     "SwzError", "lib", "library_path",
     "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
-    "swz_slice_collision_batch", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
+    "swz_slice_collision_batch", "swz_slice_layout", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
     "swz_transpose_tma_noalloc",
     "swz_status_string", "swz_version",
     "SWZ_OK", "SWZ_ERR_NULL", "SWZ_ERR_PARAM", "SWZ_ERR_SHAPE", "SWZ_ERR_ALIGN", "SWZ_ERR_ALIAS",
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.swz_bank_profile.restype = i32
         L.swz_slice_collision.argtypes = [u64, i32, i32, i32, ctypes.POINTER(u64)]
         L.swz_slice_collision.restype = i32
+        L.swz_slice_layout.argtypes = [u64, i32, i32, i32, ctypes.POINTER(u64), ctypes.POINTER(i32)]
+        L.swz_slice_layout.restype = i32
         L.swz_slice_collision_batch.argtypes = [vp, i64, i32, i32, i32, vp, vp]
         L.swz_slice_collision_batch.restype = i32
         L.swz_apply.argtypes = [u64, i32, i32, i32]
@@ -164,6 +166,18 @@ def swz_slice_collision(A: int, B: int, M: int, S: int) -> int:
     out = ctypes.c_uint64(0)
     _check(lib().swz_slice_collision(A, B, M, S, ctypes.byref(out)), "swz_slice_collision")
     return int(out.value)
+
+
+def swz_slice_layout(A: int, B: int, M: int, S: int):
+    """Per-bit strides of the plain layout equal to the swizzle on slice A, or
+    None when the slice collides (A & ~sw(A) != 0)."""
+    strides = (ctypes.c_uint64 * 64)()
+    n = ctypes.c_int(0)
+    status = lib().swz_slice_layout(A, B, M, S, strides, ctypes.byref(n))
+    if status == SWZ_ERR_UNSUPPORTED:
+        return None
+    _check(status, "swz_slice_layout")
+    return [int(strides[i]) for i in range(n.value)]
 
 
 def swz_slice_collision_batch(A, n: int, B: int, M: int, S: int, C, stream=None) -> None:

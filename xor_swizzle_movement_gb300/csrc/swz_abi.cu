@@ -153,6 +153,18 @@ swz_status swz_slice_collision(uint64_t A, int B, int M, int S, uint64_t *C_out)
     return SWZ_OK;
 }
 
+swz_status swz_slice_layout(uint64_t A, int B, int M, int S, uint64_t *strides, int *n_bits) {
+    using namespace swz;
+    if (!valid_bms(B, M, S, 64)) return SWZ_ERR_PARAM;
+    if (!strides || !n_bits) return SWZ_ERR_NULL;
+    if ((A & ~sw_fwd(A, B, M, S)) != 0) return SWZ_ERR_UNSUPPORTED;
+    int k = 0;
+    for (int bit = 0; bit < 64; ++bit)
+        if ((A >> bit) & 1u) strides[k++] = sw_fwd(uint64_t(1) << bit, B, M, S);
+    *n_bits = k;
+    return SWZ_OK;
+}
+
 swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
                                      void *stream) {
     using namespace swz;
