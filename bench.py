@@ -550,7 +550,7 @@ def main():
     torch.cuda.synchronize()
     assert torch.equal(back, src), "relayout round trip failed"
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     gpu_id = None
     try:
         gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
@@ -564,7 +564,29 @@ def main():
         pg.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for e0, e1, e2 in ev:
+    # one event pair per step: an event between the two launches would keep the
+    # inverse from launching under the forward's last wave (programmatic
+    # dependent launch)
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    total_ms = sum(step_ms)
+    if pg:
+        total_ms = reduce_max_ms(torch, total_ms, pg, dev)
+    ms_per_step = total_ms / args.steps
+    value = throughput(world, STEP_BYTES, args.steps, total_ms)
+
+    # each direction on its own (events around each launch; not part of the value)
+    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(50)]
+    for e0, e1, e2 in iso:
         flush()
         e0.record(stream)
         swz.swz_relayout(phys, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
@@ -572,28 +594,25 @@ def main():
         swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
         e2.record(stream)
     torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
-    launch_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev] + [e1.elapsed_time(e2) for _, e1, e2 in ev]
-    total_ms = sum(step_ms)
-    if pg:
-        total_ms = reduce_max_ms(torch, total_ms, pg, dev)
-    ms_per_step = total_ms / args.steps
-    value = throughput(world, STEP_BYTES, args.steps, total_ms)
+    fwd_iso = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in iso)
+    inv_iso = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in iso)
 
-    # roofline of the relayout kernel (both launches of a step are that kernel)
-    avg_launch_s = statistics.mean(launch_ms) * 1e-3
+    # roofline of the relayout kernel: both launches of a step are that kernel,
+    # so its mean launch duration over the timed region is the step time / 2
+    avg_launch_s = statistics.mean(step_ms) / 2 * 1e-3
     achieved = LAUNCH_BYTES / avg_launch_s / GB
     src_hash = source_hash("swz_relayout.cu", "swz_common.cuh")
     traffic = committed_traffic("relayout_vec_kernel<2,0,false> 4096x128x64 bf16 Sw<3,4,3>", src_hash)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 3), "traffic": traffic,
+                # the DRAM side alone: ncu's bytes per launch over the same mean duration
+                # (64 MiB of output fits in L2, so fewer bytes reach DRAM than the algorithm moves)
+                "dram_achieved": None if traffic is None else round(traffic / avg_launch_s / GB, 1),
+                "dram_frac": None if traffic is None else round(traffic / avg_launch_s / GB / peak, 3),
                 "peak_kind": f"{peak_kind} HBM copy bandwidth", "kernel": "relayout_vec_kernel",
-                "forward_ms": round(statistics.mean(launch_ms[: args.steps]), 4),
-                "inverse_ms": round(statistics.mean(launch_ms[args.steps:]), 4)}
+                "mean_launch_ms": round(avg_launch_s * 1e3, 5),
+                "isolated_ms": {"forward": round(fwd_iso, 4), "inverse": round(inv_iso, 4),
+                                "note": "events around each launch, outside the timed region"}}
 
     # end to end from pinned host buffers: the step's input is copied in and its
     # result copied out inside the timed region.  The tiles go in 8 chunks over

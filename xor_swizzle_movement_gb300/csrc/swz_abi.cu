@@ -22,6 +22,14 @@ swz_status launch_status() {
     return e == cudaSuccess ? SWZ_OK : SWZ_ERR_CUDA;
 }
 
+swz_status launched(cudaError_t launch_result) {
+    if (launch_result != cudaSuccess) {
+        cudaGetLastError();  // clear it: the status carries it
+        return SWZ_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     __shared__ uint32_t s_first[kWarpsPerCta][32];
     __shared__ int s_nw[kWarpsPerCta][32];
     __shared__ int s_cnt[kWarpsPerCta][4][32];
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int pass = lane / kLpp;
     const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
@@ -125,6 +127,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 
 __global__ void slice_collision_kernel(const uint64_t *__restrict__ A, int64_t n, int B, int M,
                                        int S, uint64_t *__restrict__ C) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint64_t a = A[i];
@@ -139,23 +143,24 @@ swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, in
     int64_t grid = (n + kWarpsPerCta - 1) / kWarpsPerCta;
     if (grid > 152LL * 64) grid = 152LL * 64;  // grid-stride beyond 64 CTAs per SM
     const unsigned g = static_cast<unsigned>(grid);
+    cudaError_t e;
     switch (width) {
-        case 1: bank_profile_kernel<1><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
-        case 2: bank_profile_kernel<2><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
-        case 4: bank_profile_kernel<4><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
-        case 8: bank_profile_kernel<8><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
-        case 16: bank_profile_kernel<16><<<g, kWarpsPerCta * 32, 0, st>>>(addrs, active, n, ways, wavefronts); break;
+        case 1: e = launch_pdl(bank_profile_kernel<1>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
+        case 2: e = launch_pdl(bank_profile_kernel<2>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
+        case 4: e = launch_pdl(bank_profile_kernel<4>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
+        case 8: e = launch_pdl(bank_profile_kernel<8>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
+        case 16: e = launch_pdl(bank_profile_kernel<16>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
         default: return SWZ_ERR_PARAM;
     }
-    return launch_status();
+    return launched(e);
 }
 
 swz_status slice_collision_launch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
                                   cudaStream_t st) {
     int64_t grid = (n + 255) / 256;
     if (grid > 152LL * 16) grid = 152LL * 16;
-    slice_collision_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(A, n, B, M, S, C);
-    return launch_status();
+    return launched(launch_pdl(slice_collision_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, A, n, B, M,
+                               S, C));
 }
 
 }  // namespace swz

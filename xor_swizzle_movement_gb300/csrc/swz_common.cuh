@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "swz.h"
@@ -58,6 +59,17 @@ __device__ __forceinline__ void st_stream16(void *p, uint4 v) {
                  "r"(v.w)
                  : "memory");
 }
+
+// Programmatic dependent launch.  A kernel launched with the
+// programmatic-stream-serialization attribute may start while the previous
+// kernel on its stream is still running; pdl_wait() blocks until that kernel
+// has completed and its writes are visible, so it must precede every global
+// memory access (reads of its results and writes it might still read).
+// pdl_launch_dependents() lets the next such kernel start launching; called on
+// entry, it lets the next grid fill SMs during this grid's last wave.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -141,8 +153,26 @@ inline void lane_map_selectors(const int *src_lane, int esize, uint32_t sel[12])
 }
 }  // namespace swz
 
+// Launch `kernel` with programmatic dependent launch allowed (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Host-side helpers shared by the launchers (defined in swz_abi.cu).
 namespace swz {
 swz_status launch_status();
+swz_status launched(cudaError_t launch_result);  // status of a launch_pdl call
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes);
 }  // namespace swz

@@ -56,6 +56,8 @@ template <int E, int MODE, bool LOCAL>
 __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a) {
     constexpr int LV = VecTraits<E>::LV;
     constexpr uint64_t VM = (1u << LV) - 1u;
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
     uint4 r[kMaxPerThread];
     uint32_t lx[kMaxPerThread];
@@ -103,6 +105,8 @@ template <int E>
 __global__ void __launch_bounds__(256)
     relayout_scalar_kernel(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int B,
                            int M, int S, int steps) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     using T = typename ElemType<E>::T;
     T *d = static_cast<T *>(dst);
     const T *s = static_cast<const T *>(src);
@@ -123,18 +127,19 @@ swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, cudaStream_t 
     const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     const dim3 g(static_cast<unsigned>(grid));
-#define SWZ_LAUNCH(MODE, LOCAL) relayout_vec_kernel<E, MODE, LOCAL><<<g, threads, 0, st>>>(a)
+#define SWZ_LAUNCH(MODE, LOCAL) launch_pdl(relayout_vec_kernel<E, MODE, LOCAL>, g, dim3(threads), 0, st, a)
+    cudaError_t e;
     if (local) {
-        if (mode == kLanesFixed) SWZ_LAUNCH(kLanesFixed, true);
-        else if (mode == kLanesXor) SWZ_LAUNCH(kLanesXor, true);
-        else SWZ_LAUNCH(kLanesGeneral, true);
+        if (mode == kLanesFixed) e = SWZ_LAUNCH(kLanesFixed, true);
+        else if (mode == kLanesXor) e = SWZ_LAUNCH(kLanesXor, true);
+        else e = SWZ_LAUNCH(kLanesGeneral, true);
     } else {
-        if (mode == kLanesFixed) SWZ_LAUNCH(kLanesFixed, false);
-        else if (mode == kLanesXor) SWZ_LAUNCH(kLanesXor, false);
-        else SWZ_LAUNCH(kLanesGeneral, false);
+        if (mode == kLanesFixed) e = SWZ_LAUNCH(kLanesFixed, false);
+        else if (mode == kLanesXor) e = SWZ_LAUNCH(kLanesXor, false);
+        else e = SWZ_LAUNCH(kLanesGeneral, false);
     }
 #undef SWZ_LAUNCH
-    return launch_status();
+    return launched(e);
 }
 
 template <int E>
@@ -143,9 +148,8 @@ swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, in
     const int threads = 256;
     int64_t grid = (n + threads - 1) / threads;
     if (grid > 152LL * 32) grid = 152LL * 32;
-    relayout_scalar_kernel<E><<<static_cast<unsigned>(grid), threads, 0, st>>>(dst, src, n, tile, B,
-                                                                                 M, S, steps);
-    return launch_status();
+    return launched(launch_pdl(relayout_scalar_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st,
+                               dst, src, n, tile, B, M, S, steps));
 }
 
 }  // namespace

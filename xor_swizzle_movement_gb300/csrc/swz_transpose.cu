@@ -83,6 +83,8 @@ template <typename T, int VARIANT, int UR, int UC, int THREADS, int MIN_CTAS, bo
 __global__ void __launch_bounds__(THREADS, MIN_CTAS)
     transpose_unit_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
                           int64_t tiles_c, int vec_ok, const FuseArgs f) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     constexpr int N = 128 / static_cast<int>(sizeof(T));    // unit edge: 32 (4 B) or 16 (8 B)
     constexpr int VPE = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte vector
     constexpr int P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;  // unit row pitch, elements
@@ -183,6 +185,8 @@ template <int VARIANT, bool FUSE>
 __global__ void __launch_bounds__(128)
     transpose16_kernel(uint16_t *__restrict__ dst, const uint16_t *__restrict__ src, int64_t R,
                        int64_t C, int64_t tiles_c, int vec_ok, const FuseArgs f) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     constexpr int TR = 64, TC = 64, THREADS = 128;
     constexpr int PITCH = (VARIANT == SWZ_T_PADDED) ? 72 : 64;  // elements per shared row
     __shared__ __align__(1024) uint16_t sm[TR * PITCH];
@@ -257,6 +261,8 @@ template <typename T, int VARIANT, bool FUSE>
 __global__ void __launch_bounds__(256)
     transpose_generic_kernel(T *__restrict__ dst, const T *__restrict__ src, int64_t R, int64_t C,
                              int64_t tiles_c, const FuseArgs f) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     constexpr int N = 32, P = (VARIANT == SWZ_T_PADDED) ? N + 1 : N;
     __shared__ T sm[N * P];
     const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
@@ -291,15 +297,16 @@ swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int var
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
     const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    cudaError_t e;
     if (fuse)
-        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, true><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, true>, g, dim3(THREADS), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_SWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose_unit_kernel<T, SWZ_T_SWIZZLED, UR, UC, THREADS, MIN_CTAS, false>, g, dim3(THREADS), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose_unit_kernel<T, SWZ_T_UNSWIZZLED, UR, UC, THREADS, MIN_CTAS, false>, g, dim3(THREADS), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else
-        transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS, MIN_CTAS, false><<<g, THREADS, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
-    return launch_status();
+        e = launch_pdl(transpose_unit_kernel<T, SWZ_T_PADDED, UR, UC, THREADS, MIN_CTAS, false>, g, dim3(THREADS), 0, st, d, s, R, C, tiles_c, vec_ok, f);
+    return launched(e);
 }
 
 swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int variant, bool aligned16,
@@ -311,15 +318,16 @@ swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int varia
     const uint16_t *s = static_cast<const uint16_t *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
     const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    cudaError_t e;
     if (fuse)
-        transpose16_kernel<SWZ_T_SWIZZLED, true><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose16_kernel<SWZ_T_SWIZZLED, true>, g, dim3(128), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_SWIZZLED)
-        transpose16_kernel<SWZ_T_SWIZZLED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose16_kernel<SWZ_T_SWIZZLED, false>, g, dim3(128), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose16_kernel<SWZ_T_UNSWIZZLED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
+        e = launch_pdl(transpose16_kernel<SWZ_T_UNSWIZZLED, false>, g, dim3(128), 0, st, d, s, R, C, tiles_c, vec_ok, f);
     else
-        transpose16_kernel<SWZ_T_PADDED, false><<<g, 128, 0, st>>>(d, s, R, C, tiles_c, vec_ok, f);
-    return launch_status();
+        e = launch_pdl(transpose16_kernel<SWZ_T_PADDED, false>, g, dim3(128), 0, st, d, s, R, C, tiles_c, vec_ok, f);
+    return launched(e);
 }
 
 template <typename T>
@@ -331,15 +339,16 @@ swz_status launch_generic(void *dst, const void *src, int64_t R, int64_t C, int 
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
     const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    cudaError_t e;
     if (fuse)
-        transpose_generic_kernel<T, SWZ_T_SWIZZLED, true><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
+        e = launch_pdl(transpose_generic_kernel<T, SWZ_T_SWIZZLED, true>, g, dim3(256), 0, st, d, s, R, C, tiles_c, f);
     else if (variant == SWZ_T_SWIZZLED)
-        transpose_generic_kernel<T, SWZ_T_SWIZZLED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
+        e = launch_pdl(transpose_generic_kernel<T, SWZ_T_SWIZZLED, false>, g, dim3(256), 0, st, d, s, R, C, tiles_c, f);
     else if (variant == SWZ_T_UNSWIZZLED)
-        transpose_generic_kernel<T, SWZ_T_UNSWIZZLED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
+        e = launch_pdl(transpose_generic_kernel<T, SWZ_T_UNSWIZZLED, false>, g, dim3(256), 0, st, d, s, R, C, tiles_c, f);
     else
-        transpose_generic_kernel<T, SWZ_T_PADDED, false><<<g, 256, 0, st>>>(d, s, R, C, tiles_c, f);
-    return launch_status();
+        e = launch_pdl(transpose_generic_kernel<T, SWZ_T_PADDED, false>, g, dim3(256), 0, st, d, s, R, C, tiles_c, f);
+    return launched(e);
 }
 
 swz_status dispatch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant, const FuseArgs *fuse,
