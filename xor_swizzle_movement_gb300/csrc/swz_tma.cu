@@ -167,6 +167,8 @@ constexpr int kOutBufs = 2;
 __global__ void __launch_bounds__(kThreads)
     transpose16_tma_ls_kernel(const __grid_constant__ CUtensorMap map_in, const __grid_constant__ CUtensorMap map_out,
                               const TmaArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before the first tensor copy
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[kStages];
     const uint32_t raw = smem_u32(smem_raw);
@@ -342,8 +344,7 @@ swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, c
             return SWZ_ERR_CUDA;
         const int smem = (kStages + kOutBufs) * kTileBytes + 1024;
         if (!ls_smem_attribute_set(smem)) return SWZ_ERR_CUDA;
-        transpose16_tma_ls_kernel<<<grid, kThreads, smem, st>>>(map, map_out, a);
-        return launch_status();
+        return launched(launch_pdl(transpose16_tma_ls_kernel, dim3(grid), dim3(kThreads), smem, st, map, map_out, a));
     }
     transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
     return launch_status();

@@ -40,9 +40,11 @@ struct TmaRelayoutArgs {
 
 __global__ void __launch_bounds__(32)
     relayout_tma_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
+    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bars[kRing];
     if (threadIdx.x != 0) return;  // one thread issues every copy
+    pdl_wait();                    // before the first copy
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // the swizzle is computed from address bits
     const uint32_t bar0 = smem_u32(&bars[0]);
@@ -149,8 +151,8 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     a.status = status;
     int64_t grid = 152LL * kCtasPerSm;
     if (a.n_chunks < grid) grid = a.n_chunks;
-    relayout_tma_kernel<<<static_cast<unsigned>(grid), 32, kRing * kChunk + 1024, st>>>(map, a);
-    return launch_status();
+    return launched(launch_pdl(relayout_tma_kernel, dim3(static_cast<unsigned>(grid)), dim3(32), kRing * kChunk + 1024,
+                               st, map, a));
 }
 
 }  // namespace swz
