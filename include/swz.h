@@ -293,6 +293,22 @@ swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, in
 swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
                                      uint32_t *timed_out, void *stream);
 
+/*
+ * Text map of a swizzled tile, the counterpart of CuTe's print_layout
+ * ("CuTe Swizzle 学习手册", section "如何验证 Swizzle 是否正确消除冲突": print
+ * each element's swizzled offset and its bank; with no bank repeated within
+ * a 128-byte row segment the layout is conflict-free for row access).
+ *
+ * One line per tile row; for each column "physical_offset/bank", separated
+ * by single spaces, where physical_offset = sw(r * cols + c) and bank =
+ * (physical_offset * esize / 4) % 32.  Writes at most cap bytes including
+ * the terminating NUL into buf (buf may be NULL when cap is 0) and returns
+ * the length of the whole text, excluding the NUL, or -1 for bad arguments
+ * (rows, cols < 0, esize < 1, B, M, S out of range).  Host function.
+ */
+int64_t swz_layout_text(char *buf, int64_t cap, int64_t rows, int64_t cols, int esize, int B, int M,
+                        int S);
+
 /* sw(x) on the host (the same function the kernels apply). */
 uint64_t swz_apply(uint64_t x, int B, int M, int S);
 

@@ -124,3 +124,15 @@ def test_slice_layout(swz, orc, B, M, S):
         for pick in itertools.product((0, 1), repeat=len(bits)):
             x = sum(b << i for b, i in zip(pick, bits))
             assert sum(b * st for b, st in zip(pick, strides)) == orc.swizzle(x, B=B, M=M, S=S)
+
+
+def test_layout_text_matches_oracle_dump(swz, orc):
+    for (rows, cols, esize, B, M, S) in [(32, 64, 4, 5, 0, 6), (8, 64, 2, 3, 3, 3), (16, 16, 8, 4, 0, 4)]:
+        assert swz.swz_layout_text(rows, cols, esize, B, M, S) == orc.dump_layout(rows, cols, esize, B=B, M=M, S=S)
+    assert swz.lib().swz_layout_text(None, 0, -1, 4, 4, 3, 0, 3) == -1
+    # truncation: the returned length is the whole text, the buffer holds a prefix
+    import ctypes
+    full = swz.swz_layout_text(4, 4, 4, 2, 0, 2)
+    buf = ctypes.create_string_buffer(10)
+    assert swz.lib().swz_layout_text(buf, 10, 4, 4, 4, 2, 0, 2) == len(full)
+    assert buf.value.decode() == full[:9]

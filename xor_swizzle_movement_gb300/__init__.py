@@ -18,7 +18,7 @@ import os
 __all__ = [
     "SwzError", "lib", "library_path",
     "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
-    "swz_slice_collision_batch", "swz_slice_layout", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
+    "swz_slice_collision_batch", "swz_slice_layout", "swz_layout_text", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
     "swz_transpose_tma_noalloc",
     "swz_status_string", "swz_version",
     "SWZ_OK", "SWZ_ERR_NULL", "SWZ_ERR_PARAM", "SWZ_ERR_SHAPE", "SWZ_ERR_ALIGN", "SWZ_ERR_ALIAS",
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.swz_slice_layout.restype = i32
         L.swz_slice_collision_batch.argtypes = [vp, i64, i32, i32, i32, vp, vp]
         L.swz_slice_collision_batch.restype = i32
+        L.swz_layout_text.argtypes = [ctypes.c_char_p, i64, i64, i64, i32, i32, i32, i32]
+        L.swz_layout_text.restype = i64
         L.swz_apply.argtypes = [u64, i32, i32, i32]
         L.swz_apply.restype = u64
         L.swz_device_status.argtypes = [vp]
@@ -183,6 +185,16 @@ def swz_slice_layout(A: int, B: int, M: int, S: int):
 def swz_slice_collision_batch(A, n: int, B: int, M: int, S: int, C, stream=None) -> None:
     _check(lib().swz_slice_collision_batch(_ptr(A), n, B, M, S, _ptr(C), _stream(stream)),
            "swz_slice_collision_batch")
+
+
+def swz_layout_text(rows: int, cols: int, esize: int, B: int, M: int, S: int) -> str:
+    """Text map of a swizzled rows x cols tile: "physical_offset/bank" per element."""
+    n = lib().swz_layout_text(None, 0, rows, cols, esize, B, M, S)
+    if n < 0:
+        raise SwzError(SWZ_ERR_PARAM, "swz_layout_text")
+    buf = ctypes.create_string_buffer(int(n) + 1)
+    lib().swz_layout_text(buf, n + 1, rows, cols, esize, B, M, S)
+    return buf.value.decode()
 
 
 def swz_apply(x: int, B: int, M: int, S: int) -> int:

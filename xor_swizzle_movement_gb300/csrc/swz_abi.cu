@@ -2,6 +2,8 @@
 // dispatch to the kernels, status codes.  Nothing here allocates memory.
 #include "swz_common.cuh"
 
+#include <cstdio>
+
 namespace swz {
 
 swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize,
@@ -183,6 +185,29 @@ swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M,
     if (!aligned_to(A, 8) || !aligned_to(C, 8)) return SWZ_ERR_ALIGN;
     if (ranges_overlap(A, n * 8, C, n * 8) && A != C) return SWZ_ERR_ALIAS;
     return slice_collision_launch(A, n, B, M, S, C, static_cast<cudaStream_t>(stream));
+}
+
+int64_t swz_layout_text(char *buf, int64_t cap, int64_t rows, int64_t cols, int esize, int B, int M, int S) {
+    using namespace swz;
+    if (rows < 0 || cols < 0 || esize < 1 || cap < 0 || (cap > 0 && !buf) || !valid_bms(B, M, S, 64)) return -1;
+    int64_t len = 0;
+    auto put = [&](const char *text, int n) {
+        for (int i = 0; i < n; ++i, ++len)
+            if (len < cap - 1) buf[len] = text[i];
+    };
+    char cell[48];
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            const uint64_t phys = sw_fwd(static_cast<uint64_t>(r * cols + c), B, M, S);
+            const uint64_t bank = (phys * static_cast<uint64_t>(esize) / 4) % 32;
+            const int n = snprintf(cell, sizeof cell, c ? " %llu/%llu" : "%llu/%llu",
+                                   static_cast<unsigned long long>(phys), static_cast<unsigned long long>(bank));
+            put(cell, n);
+        }
+        put("\n", 1);
+    }
+    if (cap > 0) buf[len < cap - 1 ? len : cap - 1] = '\0';
+    return len;
 }
 
 uint64_t swz_apply(uint64_t x, int B, int M, int S) {
