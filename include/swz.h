@@ -222,8 +222,9 @@ swz_status swz_slice_layout(uint64_t A, int B, int M, int S, uint64_t *strides, 
 
 /*
  * Batched slice collision on the GPU: C[k] = A[k] & ~sw(A[k]) for n masks.
- * A, C: device arrays of n uint64.  Same parameter rules as
- * swz_slice_collision; SWZ_ERR_SHAPE for n < 0.
+ * A, C: device arrays of n uint64; C may be A itself (in place), otherwise
+ * the two must not overlap (SWZ_ERR_ALIAS).  Same parameter rules as
+ * swz_slice_collision; SWZ_ERR_SHAPE for n < 0 or n * 8 bytes overflowing.
  */
 swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M, int S,
                                      uint64_t *C, void *stream);

@@ -179,7 +179,7 @@ swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M,
                                      void *stream) {
     using namespace swz;
     if (!valid_bms(B, M, S, 64)) return SWZ_ERR_PARAM;
-    if (n < 0) return SWZ_ERR_SHAPE;
+    if (n < 0 || n > INT64_MAX / 8) return SWZ_ERR_SHAPE;
     if (n == 0) return SWZ_OK;
     if (!A || !C) return SWZ_ERR_NULL;
     if (!aligned_to(A, 8) || !aligned_to(C, 8)) return SWZ_ERR_ALIGN;
@@ -189,7 +189,10 @@ swz_status swz_slice_collision_batch(const uint64_t *A, int64_t n, int B, int M,
 
 int64_t swz_layout_text(char *buf, int64_t cap, int64_t rows, int64_t cols, int esize, int B, int M, int S) {
     using namespace swz;
-    if (rows < 0 || cols < 0 || esize < 1 || cap < 0 || (cap > 0 && !buf) || !valid_bms(B, M, S, 64)) return -1;
+    int64_t n_elems;
+    if (rows < 0 || cols < 0 || esize < 1 || cap < 0 || (cap > 0 && !buf) || !valid_bms(B, M, S, 64) ||
+        !mul_ok(rows, cols, &n_elems))
+        return -1;
     int64_t len = 0;
     auto put = [&](const char *text, int n) {
         for (int i = 0; i < n; ++i, ++len)
