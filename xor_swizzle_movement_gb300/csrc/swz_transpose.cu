@@ -32,7 +32,8 @@
 // stores and drained with transposing 8 x 8 matrix loads (ldmatrix .trans):
 // the eight rows of one 8 x 8 block are read from eight different chunk
 // positions, so each matrix load is one conflict-free pass.  Four lanes then
-// exchange 32-bit words so that each lane owns 16 contiguous output bytes.
+// exchange 32-bit words (a two-step XOR butterfly) so that each lane owns 16
+// contiguous output bytes.
 //
 // Element sizes 1 and 16: 32 x 32 units under element Swizzle<5,0,5>, one
 // element per access.
@@ -173,11 +174,20 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &d0, u
                  : "r"(addr));
 }
 
-__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          int i) {
-    const uint32_t lo = (i & 1) ? a1 : a0;
-    const uint32_t hi = (i & 1) ? a3 : a2;
-    return (i & 2) ? hi : lo;
+// 4 x 4 transpose of 32-bit words across the 4 lanes of a group (lane kk
+// holds row kk on entry, column kk on exit): an XOR butterfly, first swapping
+// 2 x 2 blocks with the lane 2 away, then single words with the neighbour.
+__device__ __forceinline__ void transpose4_lanes(uint32_t &x0, uint32_t &x1, uint32_t &x2, uint32_t &x3, int kk) {
+    const bool hi2 = kk & 2;
+    uint32_t s0 = hi2 ? x0 : x2, s1 = hi2 ? x1 : x3;
+    s0 = __shfl_xor_sync(kFullMask, s0, 2);
+    s1 = __shfl_xor_sync(kFullMask, s1, 2);
+    if (hi2) { x0 = s0; x1 = s1; } else { x2 = s0; x3 = s1; }
+    const bool hi1 = kk & 1;
+    uint32_t t0 = hi1 ? x0 : x1, t1 = hi1 ? x2 : x3;
+    t0 = __shfl_xor_sync(kFullMask, t0, 1);
+    t1 = __shfl_xor_sync(kFullMask, t1, 1);
+    if (hi1) { x0 = t0; x2 = t1; } else { x1 = t0; x3 = t1; }
 }
 
 // Tile 64 x 64 of 16-bit elements, 128 threads.
@@ -223,17 +233,8 @@ __global__ void __launch_bounds__(128)
             // a[mm] holds output row 8cb + g, columns 8(rbg + mm) + 2kk .. +1.
             // 4 x 4 word transpose across lanes 4g .. 4g + 3: lane kk collects
             // words for columns 8(rbg + kk) .. +7.
-            uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int from = kk ^ r;
-                const uint32_t send = pick4(a0, a1, a2, a3, from);
-                const uint32_t got = r ? __shfl_xor_sync(kFullMask, send, r) : send;
-                b0 = (from == 0) ? got : b0;
-                b1 = (from == 1) ? got : b1;
-                b2 = (from == 2) ? got : b2;
-                b3 = (from == 3) ? got : b3;
-            }
+            uint32_t b0 = a0, b1 = a1, b2 = a2, b3 = a3;
+            transpose4_lanes(b0, b1, b2, b3, kk);
             const int64_t y = (c0 + cb * 8 + g) * R + r0 + (rbg + kk) * 8;
             if constexpr (FUSE) store16_fused<2>(dst, static_cast<uint64_t>(y), make_uint4(b0, b1, b2, b3), f);
             else st_stream16(dst + y, make_uint4(b0, b1, b2, b3));
