@@ -67,7 +67,7 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--case", default=None,
                    help="run one kernel case for a profiler and exit: relayout, relayout_bms, "
-                        "transposes, bank_profile")
+                        "relayout_tma, transposes, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
@@ -491,6 +491,21 @@ def run_case(args):
                     swz.swz_transpose(dst, src, n, n, esize, v)
                 done.append(f"transpose esize={esize} n={n} variant={v}")
             del src, dst
+    elif args.case == "relayout_tma":      # 16-bit 64 x 64 tiles, Swizzle<3,3,3> on the TMA 128-byte mode
+        nbytes = args.n or (256 << 20)
+        src = rand_bytes(nbytes)
+        a, b = torch.empty_like(src), torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_relayout_tma(a, src, nbytes // 8192, 64, 64, 2, 3, 3, 3, 0)
+            swz.swz_relayout_tma(b, a, nbytes // 8192, 64, 64, 2, 3, 3, 3, 1)
+        done.append(f"relayout_tma fwd+inv bytes={nbytes}")
+    elif args.case == "transpose_relayout":  # 64 x n bf16 into K-major 128 x 64 Swizzle<3,4,3> tiles
+        cols = args.n or (1 << 20)
+        src = rand_bytes(64 * cols * 2)
+        dst = torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_transpose_relayout(dst, src, 64, cols, 2, 8192, 3, 4, 3)
+        done.append(f"transpose_relayout 64 x {cols}")
     elif args.case == "bank_profile":
         n = args.n or (1 << 20)
         pats = torch.randint(0, 228 * 1024 // 4, (n, 32), dtype=torch.int32, device=dev, generator=gen) * 4

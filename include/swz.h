@@ -42,7 +42,7 @@ typedef enum swz_status {
     SWZ_ERR_ALIAS = 5,       /* dst and src overlap (in-place is not supported) */
     SWZ_ERR_CUDA = 6,        /* the CUDA runtime reported an error at launch */
     SWZ_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (see swz_transpose) */
-    SWZ_ERR_UNSUPPORTED = 8  /* a valid request this build has no kernel for */
+    SWZ_ERR_UNSUPPORTED = 8  /* a valid request the library has no kernel for */
 } swz_status;
 
 /* Transpose staging variants (see swz_transpose). */
