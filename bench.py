@@ -11,7 +11,7 @@ barrier and a device synchronisation.  L2 is flushed before every step
 (write 512 MiB, then read another 512 MiB so that no dirty line is left for
 the timed kernels to write back); each step is timed on its launch stream
 with CUDA events and the flushes are outside those intervals.  SM clocks and
-throttle reasons are sampled with nvidia-smi during the timed steps.
+throttle reasons are sampled (NVML, else nvidia-smi) during the timed steps.
 
 The JSON line also carries:
   roofline      the relayout kernel's achieved GB/s against the measured HBM
@@ -115,19 +115,96 @@ def committed_traffic(kernel_key: str, src_hash: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+    """SM clocks, power and clock-event (throttle) reasons during the timed
+    region.  Polls NVML every 1 ms through ctypes when the driver's library
+    is present (read-only queries), else runs nvidia-smi at its fastest
+    interval (50 ms).  Only samples taken between the region's start and end
+    are kept."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of NVML's public API
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_slowdown"}
+    NVML_CLOCK_SM = 1
 
     def __init__(self, gpu_id: str | None):
-        self.rows = []
+        self.rows = []          # (t, sm_mhz, max_mhz, power_w, {reasons})
         self.proc = None
         self.gpu_id = gpu_id
+        self.source = None
+        self._stop = threading.Event()
+        self.thread = None
+
+    # -- NVML --------------------------------------------------------------
+    def _nvml_open(self):
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if nv.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.gpu_id:
+            ok = nv.nvmlDeviceGetHandleByUUID(self.gpu_id.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            idx = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+            ok = idx.isdigit() and nv.nvmlDeviceGetHandleByIndex_v2(int(idx), ctypes.byref(h)) == 0
+        if not ok:
+            nv.nvmlShutdown()
+            return None
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        return nv, h, reasons_fn
+
+    def _nvml_poll(self, nv, h, reasons_fn):
+        import ctypes
+        clk, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        # the maximum clock is a fixed property and its query is slow: once
+        top = mx.value if nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0 else None
+        k = 0
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            sm = clk.value if nv.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0 else None
+            bits = rs.value if reasons_fn is not None and reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+            pw = None
+            if k % 8 == 0 and nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0:
+                pw = mw.value / 1000.0
+            names = {n for b, n in self.REASON_BITS.items() if bits & b}
+            self.rows.append((t, sm, top, pw, names))
+            k += 1
+            self._stop.wait(0.001)
+        nv.nvmlShutdown()
+
+    # -- nvidia-smi ----------------------------------------------------------
+    def _smi_read(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        for line in self.proc.stdout:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 8:
+                self.rows.append((time.perf_counter(), num(p[0]), num(p[1]), num(p[2]),
+                                  {names[i] for i in range(4) if p[4 + i].lower() == "active"}))
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        nvml = self._nvml_open()
+        if nvml is not None:
+            self.source = "nvml, 1 ms"
+            # let the polling thread take the interpreter lock often while the
+            # main thread launches (the default switch interval is 5 ms)
+            self._switch = sys.getswitchinterval()
+            sys.setswitchinterval(0.0005)
+            self.thread = threading.Thread(target=self._nvml_poll, args=nvml, daemon=True)
+            self.thread.start()
+            return
+        cmd = ["nvidia-smi", f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -135,36 +212,39 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi, 50 ms"
+        self.thread = threading.Thread(target=self._smi_read, daemon=True)
         self.thread.start()
         t0 = time.time()
         while not self.rows and time.time() - t0 < 5:
             time.sleep(0.02)
-        self.rows.clear()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 8:
-                self.rows.append(parts)
-
-    def stop(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.06)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = list(self.rows)
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+    def stop(self, t0: float, t1: float):
+        """Summary of the samples taken in [t0, t1] (time.perf_counter)."""
+        if self.thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        if self.proc is not None:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self._stop.set()
+        self.thread.join(timeout=5)
+        if getattr(self, "_switch", None):
+            sys.setswitchinterval(self._switch)
+        rows = [r for r in list(self.rows) if t0 <= r[0] <= t1]
+        if not rows and self.proc is not None:   # region shorter than one nvidia-smi interval
+            after = [r for r in list(self.rows) if r[0] > t1]
+            rows = after[:1]
+        sm = [r[1] for r in rows if r[1] is not None]
+        mx = [r[2] for r in rows if r[2] is not None]
+        pw = [r[3] for r in rows if r[3] is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)}
+                "reasons": sorted(set().union(*[r[4] for r in rows])) if rows else [],
+                "samples": len(rows), "source": self.source,
+                "power_w_max": max(pw) if pw else None}
 
 
 # ----------------------------------------------------------------------------
@@ -590,8 +670,9 @@ def main():
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
+    clk = clocks.stop(wall0, wall1)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     total_ms = sum(step_ms)
     if pg:

@@ -41,3 +41,34 @@ def test_throughput_and_traffic_record(tmp_path, monkeypatch):
     assert (got == rec["dram_bytes_per_launch"]) == (rec["source_hash"] == current)
     assert bench.committed_traffic(key, "0" * 16) is None
     assert bench.committed_traffic("no such kernel", current) is None
+
+
+def test_clock_sampler_keeps_only_the_timed_region():
+    """Samples outside [t0, t1] are dropped; reasons are the union over the
+    region; no sampler at all reports itself as unavailable."""
+    cs = bench.ClockSampler(None)
+    assert cs.stop(0.0, 1.0)["reasons"] == ["clock sampling unavailable"]
+
+    class Done:
+        def join(self, timeout=None):
+            pass
+    cs = bench.ClockSampler(None)
+    cs.thread, cs.source = Done(), "test"
+    cs.rows = [(0.5, 900.0, 2070.0, 100.0, {"hw_slowdown"}),      # before the region
+               (1.0, 2070.0, 2070.0, 600.0, set()),
+               (1.5, 2055.0, 2070.0, 900.0, {"sw_power_cap"}),
+               (2.0, 2070.0, 2070.0, 700.0, set()),
+               (2.5, 800.0, 2070.0, 100.0, {"sw_thermal_slowdown"})]  # after it
+    got = cs.stop(1.0, 2.0)
+    assert got["samples"] == 3
+    assert got["sm_mhz"] == 2070.0 and got["sm_max_mhz"] == 2070.0
+    assert got["reasons"] == ["sw_power_cap"]
+    assert got["power_w_max"] == 900.0
+
+
+def test_clock_sampler_reason_bits():
+    """NVML's clock-event reason bits map onto the names the JSON line uses."""
+    bits = bench.ClockSampler.REASON_BITS
+    assert bits[0x4] == "sw_power_cap" and bits[0x8] == "hw_slowdown"
+    assert bits[0x20] == "sw_thermal_slowdown" and bits[0x40] == "hw_thermal_slowdown"
+    assert 0x1 not in bits  # idle is not a slowdown
