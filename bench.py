@@ -382,6 +382,23 @@ def measure_rows(torch, swz, dev, flush, peak):
         "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound"}
     del src, a, b, graph
 
+    # what bounds the headline step: the fixed cost of an event-timed launch
+    # after a flush (one 16 KiB tile), and the same kernel copying 32 MiB that
+    # stays in L2 (Swizzle<3,4,3> and the identity, back to back)
+    src = rand_bytes(32 * MiB, 1)
+    a = torch.empty_like(src)
+    floor = statistics.mean(timed_launches(
+        torch, lambda: swz.swz_relayout(a, src, 1, 128, 64, 2, 3, 4, 3, 0), 100, flush))
+    l2_sw = back_to_back_ms(torch, lambda: swz.swz_relayout(a, src, 2048, 128, 64, 2, 3, 4, 3, 0), reps=50)
+    l2_id = back_to_back_ms(torch, lambda: swz.swz_relayout(a, src, 2048, 128, 64, 2, 0, 0, 1, 0), reps=50)
+    out["headline_context"] = {
+        "one_tile_launch_after_flush_ms": round(floor, 4),
+        "l2_resident_32MiB_sw343": summary(l2_sw, 2 * src.numel()),
+        "l2_resident_32MiB_identity": summary(l2_id, 2 * src.numel()),
+        "note": "fixed event-to-event cost of one launch after the flush, and the kernel's rate on "
+                "data that stays in L2 (64 MiB of read + write per launch)"}
+    del src, a
+
     # the same Swizzle<3,3,3> fp16 64x64 tiles over 1 GiB: register path vs the TMA 128-byte mode
     src = rand_bytes(1 << 30, 4)
     dst = torch.empty_like(src)
