@@ -8,8 +8,8 @@ from the product package: the two share no code.
 The arithmetic lives in ``swz_oracle.c`` (plain C, one element per loop
 iteration); this module only compiles it with gcc and marshals numpy arrays
 through ctypes.  The parity status of every function is stated in the C
-file's header: everything is pinned except the bank model's pass split for
-8- and 16-byte accesses ("parity unpinned" for w = 8, 16).
+file's header: every function is pinned (the grouping of 8-byte bank-model
+passes into consecutive half-warps is a reading the pins constrain).
 """
 from __future__ import annotations
 

@@ -22,9 +22,11 @@
  *   orc_relayout           pinned (reduces to orc_swizzle + byte copies)
  *   orc_transpose          pinned (textbook transpose, explicit small cases)
  *   orc_transpose_relayout the two pinned steps above, in that order
- *   orc_bank_profile       pinned for access widths 1,2,4; the phase split
- *                          used for 8- and 16-byte accesses is a reading the
- *                          pages do not fix: "parity unpinned" for w = 8, 16.
+ *   orc_bank_profile       pinned for every access width: 1, 2, 4 by the
+ *                          pages' bank rules; 16 by the ldmatrix.m8n8.x4
+ *                          note of [P1] (four reads, one per 8 x 8 matrix);
+ *                          8 by [P1]'s 128-byte operation size (its grouping
+ *                          into consecutive half-warps is a reading).
  *   orc_slice_collision    pinned (truth tables, brute-force additivity)
  */
 #include <stdint.h>
@@ -163,9 +165,13 @@ int orc_transpose_relayout(void *dst, const void *src, void *tmp, int64_t rows, 
  *   several passes; that minimum is not a conflict.  Conflicts are counted
  *   within each pass.
  *
- * Reading where the pages are silent (parity unpinned for w = 8, 16): a warp
- * access of w <= 4 bytes per lane is one pass over all 32 lanes; w = 8 is two
- * passes (lanes 0-15, 16-31); w = 16 is four passes of 8 lanes.  In each pass
+ * [P1], the ldmatrix.m8n8.x4 note: a 16 x 16 fp16 block (512 bytes) is read
+ *   in four warp reads, one per 8 x 8 matrix; matrix m's row addresses come
+ *   from lanes 8m .. 8m+7 (PTX ISA), so w = 16 is four passes of 8 lanes.
+ * [P1]: one operation serves at most 64 fp16 values (128 bytes), so w = 8 is
+ *   two passes of 16 lanes; taking them as lanes 0-15 and 16-31 is the
+ *   reading (the pages do not name the lanes).  w <= 4 is one pass over all
+ *   32 lanes.  In each pass
  * every active lane touches the words floor(a/4) .. floor((a+w-1)/4); the
  * pass costs the largest number of distinct words that fall in one bank.
  * ways = largest pass cost, wavefronts = sum of pass costs.

@@ -341,6 +341,36 @@ def test_bank_minimum_passes(orc):
     assert ways == 1 and wavefronts == 4
 
 
+def test_bank_ldmatrix_x4_passes(orc):
+    """"NVIDIA CuTe Swizzle", the note on ldmatrix.m8n8.x4: the 16 x 16 fp16
+    block (512 bytes) is four warp reads, one per 8 x 8 matrix, and only a
+    conflict inside one of them counts.  ldmatrix .x4 takes matrix m's eight
+    row addresses from lanes 8m .. 8m+7 (PTX ISA, ldmatrix).  In the page's
+    (-1, 64) fp16 layout under Swizzle<3,3,3>, lanes i and 8 + i hit the same
+    banks (rows i and 8 + i share a chunk position) but sit in different
+    matrices: no conflict, four passes.  Unswizzled, each matrix's eight rows
+    share one chunk position: 8-way in every pass."""
+    for r0, c0 in [(0, 0), (16, 8), (40, 48)]:
+        rows = [(r0 + 8 * (m & 1) + i, c0 + 8 * (m >> 1)) for m in range(4) for i in range(8)]
+        sw = [2 * orc.swizzle(r * 64 + c, B=3, M=3, S=3) for r, c in rows]
+        assert _ways(orc, sw, 16) == (1, 4)
+        plain = [2 * (r * 64 + c) for r, c in rows]
+        assert _ways(orc, plain, 16) == (8, 32)
+
+
+def test_bank_8byte_passes(orc):
+    """"NVIDIA CuTe Swizzle": one operation serves at most 64 fp16 values of
+    distinct columns, i.e. 128 bytes; more takes further passes, and that
+    minimum is not a conflict.  A warp reading 32 consecutive 8-byte words
+    (256 bytes) therefore takes two passes and has no conflict.  Reading
+    down an 8-byte column of 128-byte rows puts each half-warp pass on one
+    bank pair: 16 distinct words per bank in each of the two passes."""
+    assert _ways(orc, [8 * l for l in range(32)], 8) == (1, 2)
+    assert _ways(orc, [128 * l + 8 for l in range(32)], 8) == (16, 32)
+    # the same 256 bytes as 4-byte accesses: one pass (two words per lane pair)
+    assert _ways(orc, [4 * l for l in range(32)], 4) == (1, 1)
+
+
 def test_bank_inactive_and_unaligned(orc):
     # inactive lanes do not count
     col = [4 * (r * 32) for r in range(32)]

@@ -34,6 +34,11 @@ MUTATIONS = [
     ("last word one too far", "last = (a + (uint64_t)width - 1) / 4;", "last = (a + (uint64_t)width) / 4;"),
     ("16-byte accesses in two passes", "passes = (width <= 4) ? 1 : width / 4;",
      "passes = (width <= 4) ? 1 : 2;"),
+    ("8-byte accesses in one pass", "passes = (width <= 4) ? 1 : width / 4;",
+     "passes = (width <= 8) ? 1 : width / 4;"),
+    ("passes interleave the lanes",
+     "for (lane = pass * lanes_per_pass; lane < (pass + 1) * lanes_per_pass; ++lane) {",
+     "for (lane = pass; lane < 32; lane += passes) {"),
     ("no broadcast: repeated words counted",
      "for (k = 0; k < n_words; ++k)\n                        if (words[k] == wd)\n                            seen = 1;",
      "(void)seen;"),
@@ -65,6 +70,8 @@ def battery(orc):
         ("bank_usage", lambda: pins.test_bank_usage_examples(orc)),
         ("bank_broadcast", lambda: pins.test_bank_broadcast(orc)),
         ("bank_passes", lambda: pins.test_bank_minimum_passes(orc)),
+        ("bank_ldmatrix", lambda: pins.test_bank_ldmatrix_x4_passes(orc)),
+        ("bank_8byte", lambda: pins.test_bank_8byte_passes(orc)),
         ("bank_unaligned", lambda: pins.test_bank_inactive_and_unaligned(orc)),
         ("collision_table", lambda: pins.test_collision_truth_table(orc)),
         ("collision_layout", lambda: pins.test_collision_predicts_layout(orc, 2, 0, 2)),
