@@ -470,6 +470,17 @@ def measure_rows(torch, swz, dev, flush, peak):
                    [(0, "swizzled_sw343_ldmatrix"), (3, "tma_swizzle128b"), (1, "unswizzled"), (2, "padded")], 3)
     transpose_rows("transpose_fp64_8192", 8192, 8, [(0, "swizzled_sw404"), (1, "unswizzled"), (2, "padded_17")], 4)
 
+    # the same swizzled fp32 kernel when the output rows are not 32 KiB apart:
+    # 8256 x 8192 (output pitch 33 KiB) and 16384 x 16384 (64 KiB)
+    pitch = {}
+    for r_, c_ in ((8256, 8192), (16384, 16384)):
+        s_ = rand_bytes(r_ * c_ * 4, 2)
+        d_ = torch.empty_like(s_)
+        ms = back_to_back_ms(torch, lambda: swz.swz_transpose(d_, s_, r_, c_, 4, 0))
+        pitch[f"{r_}x{c_}_output_pitch_{r_ * 4 // 1024}KiB"] = summary(ms, 2 * r_ * c_ * 4)
+        del s_, d_
+    out["transpose_fp32_swizzled_output_pitch"] = pitch
+
     # transpose fused with the relayout: a 64 x 2^21 bf16 matrix (256 MiB) into K-major 128 x 64
     # tiles under Swizzle<3,4,3>, in one pass, against the transpose and the relayout apart
     kr, kc = 64, 1 << 21
