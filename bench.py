@@ -477,7 +477,7 @@ def measure_rows(torch, swz, dev, flush, peak):
         s_ = rand_bytes(r_ * c_ * 4, 2)
         d_ = torch.empty_like(s_)
         ms = back_to_back_ms(torch, lambda: swz.swz_transpose(d_, s_, r_, c_, 4, 0))
-        pitch[f"{r_}x{c_}_output_pitch_{r_ * 4 // 1024}KiB"] = summary(ms, 2 * r_ * c_ * 4)
+        pitch[f"{r_}x{c_}_output_pitch_{r_ * 4}B"] = summary(ms, 2 * r_ * c_ * 4)
         del s_, d_
     out["transpose_fp32_swizzled_output_pitch"] = pitch
 
