@@ -20,7 +20,9 @@ The JSON line also carries:
                 current kernel source;
   e2e           the same metric through the C ABI from pinned host buffers,
                 host->device and device->host copies inside the timed region;
-  cpu_baseline  the CPU oracle (single thread) on the same workload;
+  cpu_baseline  the CPU oracle on the same workload: single thread, and split
+                over every host core (spawned processes); the 125-set sweep on
+                a 64 MiB sample;
   rows          every other row of the path measured in the same run: the
                 small relayout, the 1 GiB int8 and uint16-sweep relayouts, the
                 fp32 / fp16 / fp64 transposes with each staging, the bank
@@ -512,23 +514,115 @@ def measure_rows(torch, swz, dev, flush, peak):
     return out
 
 
-def cpu_baseline(host_src, seconds=10.0):
-    """The CPU oracle (single thread, as it stands) on the whole workload,
-    forward then inverse, repeated for about `seconds`."""
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+# The oracle over every host core: spawned worker processes (no CUDA state is
+# inherited) attach to the input in shared memory and each runs the oracle,
+# unchanged, on its own run of tiles: the oracle's outer loop split across
+# processes.
+_POOL = {}
+
+
+def _pool_init(shm_name, n_el):
+    import numpy as np
+    from multiprocessing import shared_memory
+    shm = shared_memory.SharedMemory(name=shm_name)
+    _POOL["shm"] = shm
+    _POOL["src"] = np.ndarray((n_el,), dtype=np.uint16, buffer=shm.buf)
+
+
+def _pool_job(job):
+    """('pair', e0, e1, tile, B, M, S): forward then inverse of elements
+    [e0, e1); ('fwd', ...): the forward relayout alone."""
     import oracle
+    kind, e0, e1, te, b, m, s = job
+    out = oracle.relayout(_POOL["src"][e0:e1], tile_elems=te, B=b, M=m, S=s, direction=0)
+    if kind == "pair":
+        oracle.relayout(out, tile_elems=te, B=b, M=m, S=s, direction=1)
+    return e1 - e0
+
+
+def _timed_rounds(fn, seconds):
     t_end = time.perf_counter() + seconds
     times = []
     while True:
         t0 = time.perf_counter()
-        fwd = oracle.relayout(host_src, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
-        oracle.relayout(fwd, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
+        fn()
         times.append(time.perf_counter() - t0)
         if time.perf_counter() > t_end:
-            break
+            return times
+
+
+def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25):
+    """The CPU oracle, as it stands, on the whole workload (forward then
+    inverse): single thread for about `seconds`, then split over every core
+    of this process's affinity set for about `seconds_all`.  Also the
+    relayout sweep's 125 parameter sets on a 64 MiB uint16 sample, over all
+    cores, and single-threaded on three of them."""
+    import numpy as np
+    import multiprocessing as mp
+    from multiprocessing import shared_memory
+    import oracle
+    from xor_swizzle_movement_gb300 import inputs
+    te = ROWS * COLS
+    times = _timed_rounds(lambda: oracle.relayout(
+        oracle.relayout(host_src, tile_elems=te, B=B, M=M, S=S, direction=0),
+        tile_elems=te, B=B, M=M, S=S, direction=1), seconds)
     mean = sum(times) / len(times)
-    return {"value": round(STEP_BYTES / mean / GB, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"whole workload (forward + inverse of {TILES} tiles), {len(times)} repetitions, "
-                      f"{mean * 1e3:.1f} ms each, single thread"}
+    res = {"value": round(STEP_BYTES / mean / GB, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"whole workload (forward + inverse of {TILES} tiles), {len(times)} repetitions, "
+                     f"{mean * 1e3:.1f} ms each, single thread",
+           "cpu_model": cpu_model()}
+
+    cores = len(os.sched_getaffinity(0))
+    n_el = max(host_src.size, sweep_el)
+    shm = shared_memory.SharedMemory(create=True, size=n_el * 2)
+    try:
+        buf = np.ndarray((n_el,), dtype=np.uint16, buffer=shm.buf)
+        with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(shm.name, n_el)) as pool:
+            # the headline workload, tiles split into 4 runs per core
+            buf[:host_src.size] = host_src.view(np.uint16).reshape(-1)
+            n_runs = 4 * cores
+            cuts = [TILES * i // n_runs for i in range(n_runs + 1)]
+            jobs = [("pair", cuts[i] * te, cuts[i + 1] * te, te, B, M, S) for i in range(n_runs) if cuts[i + 1] > cuts[i]]
+            pool.map(_pool_job, jobs)                    # warm: every worker has loaded the oracle
+            t_all = _timed_rounds(lambda: pool.map(_pool_job, jobs), seconds_all)
+            m_all = sum(t_all) / len(t_all)
+            res["all_cores"] = {"value": round(STEP_BYTES / m_all / GB, 3), "unit": "GB/s", "cores": cores,
+                                "sample": f"whole workload, {len(t_all)} repetitions, {m_all * 1e3:.1f} ms each, "
+                                          f"{len(jobs)} runs of tiles over {cores} processes"}
+            # the relayout sweep: one 2^25-element tile (a prefix of the 2^29-element buffer; every
+            # swizzle period divides it), forward, all 125 parameter sets
+            buf[:sweep_el] = inputs.uint16_bits(sweep_el, seed=4)
+            combos = [(b, m, s) for b in range(1, 6) for m in range(5) for s in range(b, 8)]
+            sweep_jobs = [("fwd", 0, sweep_el, sweep_el, b, m, s) for (b, m, s) in combos]
+            t0 = time.perf_counter()
+            pool.map(_pool_job, sweep_jobs, chunksize=1)
+            t_sweep = time.perf_counter() - t0
+        one = {}
+        for (b, m, s) in ((1, 4, 7), (3, 3, 3), (5, 2, 5)):
+            t0 = time.perf_counter()
+            oracle.relayout(buf[:sweep_el], tile_elems=sweep_el, B=b, M=m, S=s, direction=0)
+            one[f"{b},{m},{s}"] = round(2 * sweep_el * 2 / (time.perf_counter() - t0) / GB, 3)
+        res["sweep125_uint16"] = {
+            "all_cores_GB/s": round(len(combos) * 2 * sweep_el * 2 / t_sweep / GB, 3), "cores": cores,
+            "single_thread_GB/s": one,
+            "sample": f"forward relayout of a {sweep_el * 2 / MiB:g} MiB prefix of the 1 GiB buffer, "
+                      f"{len(combos)} parameter sets"}
+    finally:
+        shm.close()
+        shm.unlink()
+    return res
 
 
 def run_reference(args):

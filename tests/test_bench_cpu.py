@@ -72,3 +72,17 @@ def test_clock_sampler_reason_bits():
     assert bits[0x4] == "sw_power_cap" and bits[0x8] == "hw_slowdown"
     assert bits[0x20] == "sw_thermal_slowdown" and bits[0x40] == "hw_thermal_slowdown"
     assert 0x1 not in bits  # idle is not a slowdown
+
+
+def test_cpu_baseline_single_and_all_cores():
+    """The CPU baseline runs the oracle single-threaded and over every core
+    (spawned workers on shared memory) on the headline workload, and the
+    125-set sweep on a small sample; all report positive rates."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.bf16_normal(bench.TILES * bench.ROWS * bench.COLS, seed=1)
+    res = bench.cpu_baseline(host, seconds=0.01, seconds_all=0.01, sweep_el=1 << 16)
+    assert res["kind"] == "oracle" and res["cores"] == 1 and res["value"] > 0
+    assert res["all_cores"]["cores"] == len(os.sched_getaffinity(0)) and res["all_cores"]["value"] > 0
+    sw = res["sweep125_uint16"]
+    assert sw["all_cores_GB/s"] > 0 and set(sw["single_thread_GB/s"]) == {"1,4,7", "3,3,3", "5,2,5"}
+    assert isinstance(res["cpu_model"], str) and res["cpu_model"]
