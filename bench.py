@@ -632,8 +632,15 @@ def run_reference(args):
     from xor_swizzle_movement_gb300 import inputs
     import oracle
     host = inputs.bf16_normal(TILES * ROWS * COLS, seed=1)
-    # one step = forward + inverse of a bounded sample (512 of the 4096 tiles)
-    sample_tiles = 512
+    # one step = forward + inverse of a bounded sample of the 4096 tiles: at
+    # most 512, fewer when K + W steps of 512 would take over about a minute
+    probe = host[: 64 * ROWS * COLS]
+    t0 = time.perf_counter()
+    oracle.relayout(oracle.relayout(probe, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0),
+                    tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
+    per_tile = (time.perf_counter() - t0) / 64
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    sample_tiles = int(max(16, min(512, budget / per_tile)))
     part = host[: sample_tiles * ROWS * COLS]
     step_bytes = STEP_BYTES * sample_tiles // TILES
     for _ in range(args.warmup):
