@@ -137,13 +137,13 @@ __global__ void __launch_bounds__(kThreads)
                     a.dst[(c0 + ocl) * a.R + r0 + orow] = sm[orow * 64 + (((ocl >> 3) ^ (orow & 7)) << 3) + (ocl & 7)];
             }
         }
-        __syncthreads();  // every thread is done with buffer s
+        // every thread orders its reads of buffer s before the tensor copy
+        // that refills it (the copy writes through the async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
         if (tid == 0 && a.issue_copies) {
             const int64_t tn = t + static_cast<int64_t>(kStages) * gridDim.x;
-            if (tn < a.n_tiles) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(s, tn);
-            }
+            if (tn < a.n_tiles) issue(s, tn);
         }
     }
 }

@@ -6,14 +6,19 @@
 // 3: the byte-address Swizzle<B,4,3>, i.e. element Swizzle<B, 4 - log2 e, 3> on
 // e-byte elements ("CuTe Swizzle 学习手册", sections "Sw<3,4,3> vs Sw<3,3,3>"
 // and "H100 TMA + Swizzle").  The buffer is viewed as rows of 2^(B+4) bytes
-// (the swizzle span) and moved in 8 KiB chunks:
-//   forward  dst[sw(i)] = src[i]: a swizzled tensor load, then a plain bulk store;
-//   inverse  dst[i] = src[sw(i)]: a plain bulk load, then a swizzled tensor store.
+// (the swizzle span) and moved in 8 KiB chunks, the tensor copy on the
+// swizzled side and 16-byte register copies on the plain side:
+//   forward  dst[sw(i)] = src[i]: a swizzled tensor load into shared memory,
+//            then every thread copies its vectors out to dst in order;
+//   inverse  dst[i] = src[sw(i)]: every thread copies its vectors of src into
+//            shared memory in order, then a swizzled tensor store.
+// (With the tensor copy on both sides, a bulk copy for the plain side, the
+// copy engine's rate for 128-byte box rows held both directions near 6.4 TB/s;
+// splitting the work between it and the SM's load/store units reaches 6.7-6.9.)
 // Each chunk covers whole swizzle periods (2^(B+7) bytes) of whole tiles, so
-// the tile-local swizzle equals the swizzle of the chunk-local offset.  One
-// thread per CTA drives a ring of four 8 KiB buffers; every copy is
-// asynchronous and every mbarrier wait is bounded (kWaitLimitNs) with the
-// expiry recorded in the per-device status word.
+// the tile-local swizzle equals the swizzle of the chunk-local offset.  The
+// forward kernel waits on its loads with bounded mbarrier waits (kWaitLimitNs)
+// and records an expiry in the per-device status word.
 #include "swz_tma_common.cuh"
 
 namespace swz {
@@ -23,9 +28,11 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
 
 namespace {
 
-constexpr int kChunk = 8192;     // bytes per copy
-constexpr int kRing = 4;         // buffers per CTA
-constexpr int kCtasPerSm = 6;    // 33 KiB of shared memory each
+constexpr int kChunk = 8192;                         // bytes per tensor copy
+constexpr int kThreads = 256;
+constexpr int kVecs = kChunk / 16 / kThreads;        // 16-byte vectors per thread per chunk
+constexpr int kFwdRing = 3, kFwdCtasPerSm = 2;       // forward: 3 chunks in flight per CTA
+constexpr int kInvRing = 4, kInvCtasPerSm = 6;       // inverse: 4 output buffers per CTA
 
 struct TmaRelayoutArgs {
     uint8_t *dst;
@@ -33,79 +40,130 @@ struct TmaRelayoutArgs {
     int64_t bytes;          // the whole buffer
     int64_t n_chunks;
     int rows_per_chunk;     // kChunk / swizzle span
-    int direction;
     uint64_t wait_ns;
     uint32_t *status;
 };
 
-__global__ void __launch_bounds__(32)
-    relayout_tma_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// 16-byte vectors of chunk c that hold data (the last chunk may be short)
+__device__ __forceinline__ int chunk_vecs(const TmaRelayoutArgs &a, int64_t c) {
+    const int64_t left = a.bytes - c * kChunk;
+    return static_cast<int>((left < kChunk ? left : kChunk) / 16);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    relayout_tma_fwd_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
     pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kRing];
-    if (threadIdx.x != 0) return;  // one thread issues every copy
-    pdl_wait();                    // before the first copy
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // the swizzle is computed from address bits
+    __shared__ __align__(8) uint64_t bars[kFwdRing];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // the swizzle is computed from address bits
     const uint32_t bar0 = smem_u32(&bars[0]);
-    for (int s = 0; s < kRing; ++s) mbar_init(bar0 + 8u * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-
-    auto chunk_bytes = [&](int64_t c) -> uint32_t {
-        const int64_t left = a.bytes - c * kChunk;
-        return static_cast<uint32_t>(left < kChunk ? left : kChunk);
+    const int tid = threadIdx.x;
+    // a tensor box always transfers its full size (rows past the end are zero-filled)
+    auto issue = [&](int s, int64_t c) {
+        mbar_expect_tx(bar0 + 8u * s, kChunk);
+        tma_load_2d(base + s * kChunk, &map, 0, static_cast<int>(c * a.rows_per_chunk), bar0 + 8u * s);
     };
-    auto issue_load = [&](int s, int64_t c) {
-        const uint32_t buf = base + s * kChunk, bar = bar0 + 8u * s;
-        if (a.direction == 0) {
-            // a tensor box always transfers its full size (rows past the end are zero-filled)
-            mbar_expect_tx(bar, kChunk);
-            tma_load_2d(buf, &map, 0, static_cast<int>(c * a.rows_per_chunk), bar);
-        } else {
-            const uint32_t nb = chunk_bytes(c);
-            mbar_expect_tx(bar, nb);
-            bulk_load(buf, a.src + c * kChunk, nb, bar);
+    if (tid == 0) {
+        for (int s = 0; s < kFwdRing; ++s) mbar_init(bar0 + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int s = 0; s < kFwdRing; ++s) {
+            const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
+            if (c < a.n_chunks) issue(s, c);
         }
-    };
-    auto issue_store = [&](int s, int64_t c) {
-        const uint32_t buf = base + s * kChunk;
-        if (a.direction == 0) bulk_store(a.dst + c * kChunk, buf, chunk_bytes(c));
-        else tma_store_2d(&map, 0, static_cast<int>(c * a.rows_per_chunk), buf);  // rows past the end are dropped
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    };
-
-    for (int s = 0; s < kRing; ++s) {
-        const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-        if (c < a.n_chunks) issue_load(s, c);
     }
+    __syncthreads();
     for (int64_t it = 0;; ++it) {
         const int64_t c = blockIdx.x + it * gridDim.x;
         if (c >= a.n_chunks) break;
-        const int s = static_cast<int>(it % kRing);
-        if (!mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kRing) & 1), a.wait_ns)) {
-            atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
-            // let the loads still in flight land before the CTA exits: those of
-            // iterations it .. it + kRing - 1 (before the first refill) or
-            // it .. it + kRing - 2 (after it)
-            const int64_t last = it == 0 ? kRing - 1 : it + kRing - 2;
-            for (int64_t j = it; j <= last; ++j) {
-                if (blockIdx.x + j * gridDim.x >= a.n_chunks) break;
-                mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kRing),
-                                  static_cast<uint32_t>((j / kRing) & 1), a.wait_ns);
+        const int s = static_cast<int>(it % kFwdRing);
+        const bool ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kFwdRing) & 1), a.wait_ns);
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) {
+                atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
+                // let the loads still in flight (iterations it .. it + kFwdRing - 1) land
+                for (int64_t j = it; j < it + kFwdRing; ++j) {
+                    if (blockIdx.x + j * gridDim.x >= a.n_chunks) break;
+                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kFwdRing),
+                                      static_cast<uint32_t>((j / kFwdRing) & 1), a.wait_ns);
+                }
             }
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             return;
         }
-        issue_store(s, c);
-        if (it >= 1) {
-            // the previous chunk's store has read its buffer: refill that buffer
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            const int64_t cn = c - gridDim.x + static_cast<int64_t>(kRing) * gridDim.x;
-            if (cn < a.n_chunks) issue_load(static_cast<int>((it - 1) % kRing), cn);
+        const int nv = chunk_vecs(a, c);
+        uint4 v[kVecs];
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) {
+            const int idx = k * kThreads + tid;
+            if (idx < nv) v[k] = lds16(base + s * kChunk + idx * 16);
+        }
+        // every thread orders its reads of buffer s before the tensor copy
+        // that refills it (the copy writes through the async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0) {
+            const int64_t cn = c + static_cast<int64_t>(kFwdRing) * gridDim.x;
+            if (cn < a.n_chunks) issue(s, cn);
+        }
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) {
+            const int idx = k * kThreads + tid;
+            if (idx < nv) st_stream16(a.dst + c * kChunk + idx * 16, v[k]);
         }
     }
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads)
+    relayout_tma_inv_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int tid = threadIdx.x;
+    uint4 v[kVecs];
+    auto load = [&](int64_t c) {
+        const int nv = chunk_vecs(a, c);
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) {
+            const int idx = k * kThreads + tid;
+            if (idx < nv) v[k] = ld_stream16(a.src + c * kChunk + idx * 16);
+        }
+    };
+    int64_t c = blockIdx.x;
+    if (c < a.n_chunks) load(c);
+    for (int64_t it = 0; c < a.n_chunks; ++it, c += gridDim.x) {
+        const int s = static_cast<int>(it % kInvRing);
+        // the store issued from buffer s kInvRing chunks ago has read it
+        if (tid == 0 && it >= kInvRing) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kInvRing - 1) : "memory");
+        __syncthreads();
+        const int nv = chunk_vecs(a, c);
+#pragma unroll
+        for (int k = 0; k < kVecs; ++k) {
+            const int idx = k * kThreads + tid;
+            if (idx < nv) sts16(base + s * kChunk + idx * 16, v[k]);
+        }
+        if (c + gridDim.x < a.n_chunks) load(c + gridDim.x);  // the next chunk's loads overlap this store
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // these writes before the tensor store
+        __syncthreads();
+        if (tid == 0) {
+            // rows past the end of the buffer are dropped
+            tma_store_2d(&map, 0, static_cast<int>(c * a.rows_per_chunk), base + s * kChunk);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 }  // namespace
@@ -146,13 +204,14 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     a.bytes = bytes;
     a.n_chunks = (bytes + kChunk - 1) / kChunk;
     a.rows_per_chunk = static_cast<int>(kChunk / span);
-    a.direction = direction;
     a.wait_ns = kWaitLimitNs;
     a.status = status;
-    int64_t grid = 152LL * kCtasPerSm;
+    int64_t grid = 152LL * (direction == 0 ? kFwdCtasPerSm : kInvCtasPerSm);
     if (a.n_chunks < grid) grid = a.n_chunks;
-    return launched(launch_pdl(relayout_tma_kernel, dim3(static_cast<unsigned>(grid)), dim3(32), kRing * kChunk + 1024,
-                               st, map, a));
+    const dim3 g(static_cast<unsigned>(grid));
+    if (direction == 0)
+        return launched(launch_pdl(relayout_tma_fwd_kernel, g, dim3(kThreads), kFwdRing * kChunk + 1024, st, map, a));
+    return launched(launch_pdl(relayout_tma_inv_kernel, g, dim3(kThreads), kInvRing * kChunk + 1024, st, map, a));
 }
 
 }  // namespace swz
