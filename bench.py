@@ -563,12 +563,13 @@ def _timed_rounds(fn, seconds):
             return times
 
 
-def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25):
+def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, sample_scale=1):
     """The CPU oracle, as it stands, on the whole workload (forward then
     inverse): single thread for about `seconds`, then split over every core
     of this process's affinity set for about `seconds_all`.  Also the
     relayout sweep's 125 parameter sets on a 64 MiB uint16 sample, over all
-    cores, and single-threaded on three of them."""
+    cores, and single-threaded on three of them; and, single-threaded, a
+    bounded sample of every other row's workload."""
     import numpy as np
     import multiprocessing as mp
     from multiprocessing import shared_memory
@@ -622,7 +623,43 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25):
     finally:
         shm.close()
         shm.unlink()
+    res["other_rows_single_thread"] = cpu_rows(scale=sample_scale)
     return res
+
+
+def cpu_rows(scale=1):
+    """The oracle, single thread, on a bounded sample of every other row's
+    workload (GB/s = bytes read + written / time).  `scale` divides the
+    samples (tests)."""
+    import numpy as np
+    import oracle
+    from xor_swizzle_movement_gb300 import inputs
+
+    def rate(nbytes, fn):
+        t0 = time.perf_counter()
+        fn()
+        return round(2 * nbytes / (time.perf_counter() - t0) / GB, 3)
+    out = {}
+    small = inputs.uint16_bits(256 * 64 * 64, seed=0)
+    out["relayout_fp16_64x64_sw333_2MiB"] = {
+        "GB/s": rate(2 * small.nbytes, lambda: oracle.relayout(
+            oracle.relayout(small, tile_elems=4096, B=3, M=3, S=3, direction=0),
+            tile_elems=4096, B=3, M=3, S=3, direction=1)),
+        "sample": "whole workload, forward + inverse"}
+    n_i8 = (2048 // scale) * 64 * 128
+    i8 = inputs.random_bytes(n_i8, seed=4)
+    out["relayout_int8_64x128_sw525"] = {
+        "GB/s": rate(i8.nbytes, lambda: oracle.relayout(i8, tile_elems=64 * 128, B=5, M=2, S=5, direction=0)),
+        "sample": f"{n_i8 // (64 * 128)} of the 131072 tiles, forward"}
+    for name, n, esize, gen in (("transpose_fp32_8192", 8192, 4, lambda k: inputs.f32_uniform(k, seed=2)),
+                                ("transpose_fp16_16384", 16384, 2, lambda k: inputs.f16_bits_no_nan(k, seed=3)),
+                                ("transpose_fp64_8192", 8192, 8,
+                                 lambda k: inputs.random_bytes(8 * k, seed=4).view(np.uint64))):
+        rows = max(8, 512 // scale)
+        a = gen(rows * n).reshape(rows, n)
+        out[name] = {"GB/s": rate(a.nbytes, lambda: oracle.transpose(a)),
+                     "sample": f"{rows} of the {n} rows"}
+    return out
 
 
 def run_reference(args):

@@ -80,9 +80,13 @@ def test_cpu_baseline_single_and_all_cores():
     125-set sweep on a small sample; all report positive rates."""
     from xor_swizzle_movement_gb300 import inputs
     host = inputs.bf16_normal(bench.TILES * bench.ROWS * bench.COLS, seed=1)
-    res = bench.cpu_baseline(host, seconds=0.01, seconds_all=0.01, sweep_el=1 << 16)
+    res = bench.cpu_baseline(host, seconds=0.01, seconds_all=0.01, sweep_el=1 << 16, sample_scale=64)
     assert res["kind"] == "oracle" and res["cores"] == 1 and res["value"] > 0
     assert res["all_cores"]["cores"] == len(os.sched_getaffinity(0)) and res["all_cores"]["value"] > 0
     sw = res["sweep125_uint16"]
     assert sw["all_cores_GB/s"] > 0 and set(sw["single_thread_GB/s"]) == {"1,4,7", "3,3,3", "5,2,5"}
     assert isinstance(res["cpu_model"], str) and res["cpu_model"]
+    assert set(res["other_rows_single_thread"]) == {
+        "relayout_fp16_64x64_sw333_2MiB", "relayout_int8_64x128_sw525", "transpose_fp32_8192",
+        "transpose_fp16_16384", "transpose_fp64_8192"}
+    assert all(v["GB/s"] > 0 for v in res["other_rows_single_thread"].values())
