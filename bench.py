@@ -533,20 +533,29 @@ def cpu_model() -> str:
 _POOL = {}
 
 
-def _pool_init(shm_name, n_el):
+def _pool_init(shm_name, nbytes):
     import numpy as np
     from multiprocessing import shared_memory
     shm = shared_memory.SharedMemory(name=shm_name)
     _POOL["shm"] = shm
-    _POOL["src"] = np.ndarray((n_el,), dtype=np.uint16, buffer=shm.buf)
+    _POOL["buf"] = np.ndarray((nbytes,), dtype=np.uint8, buffer=shm.buf)
 
 
 def _pool_job(job):
-    """('pair', e0, e1, tile, B, M, S): forward then inverse of elements
-    [e0, e1); ('fwd', ...): the forward relayout alone."""
+    """('pair' | 'fwd', dtype, e0, e1, tile, B, M, S): forward (then inverse,
+    for 'pair') relayout of elements [e0, e1) of the shared buffer viewed as
+    dtype; ('transpose', dtype, r0, r1, cols): transpose of rows [r0, r1) of a
+    row-major matrix with `cols` columns at the start of the buffer."""
+    import numpy as np
     import oracle
-    kind, e0, e1, te, b, m, s = job
-    out = oracle.relayout(_POOL["src"][e0:e1], tile_elems=te, B=b, M=m, S=s, direction=0)
+    kind, dtype = job[0], np.dtype(job[1])
+    view = _POOL["buf"].view(dtype)
+    if kind == "transpose":
+        _, _, r0, r1, cols = job
+        oracle.transpose(view[r0 * cols:r1 * cols].reshape(r1 - r0, cols))
+        return (r1 - r0) * cols
+    _, _, e0, e1, te, b, m, s = job
+    out = oracle.relayout(view[e0:e1], tile_elems=te, B=b, M=m, S=s, direction=0)
     if kind == "pair":
         oracle.relayout(out, tile_elems=te, B=b, M=m, S=s, direction=1)
     return e1 - e0
@@ -568,8 +577,9 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
     inverse): single thread for about `seconds`, then split over every core
     of this process's affinity set for about `seconds_all`.  Also the
     relayout sweep's 125 parameter sets on a 64 MiB uint16 sample, over all
-    cores, and single-threaded on three of them; and, single-threaded, a
-    bounded sample of every other row's workload."""
+    cores and single-threaded on three of them; and every other row's
+    workload on a bounded sample, single thread and over all cores.
+    `sample_scale` divides the other rows' samples (tests)."""
     import numpy as np
     import multiprocessing as mp
     from multiprocessing import shared_memory
@@ -586,16 +596,26 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
            "cpu_model": cpu_model()}
 
     cores = len(os.sched_getaffinity(0))
-    n_el = max(host_src.size, sweep_el)
-    shm = shared_memory.SharedMemory(create=True, size=n_el * 2)
+    band = max(8, 256 // sample_scale)                   # transpose rows per worker
+    i8_tiles = max(1, 2048 // sample_scale)              # int8 64 x 128 tiles per worker
+    nbytes = max(host_src.nbytes, sweep_el * 2, band * cores * 8192 * 8, band * cores * 16384 * 2,
+                 i8_tiles * cores * 8192)
+    shm = shared_memory.SharedMemory(create=True, size=nbytes)
+
+    def wall(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
     try:
-        buf = np.ndarray((n_el,), dtype=np.uint16, buffer=shm.buf)
-        with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(shm.name, n_el)) as pool:
+        buf = np.ndarray((nbytes,), dtype=np.uint8, buffer=shm.buf)
+        u16 = buf.view(np.uint16)
+        with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(shm.name, nbytes)) as pool:
             # the headline workload, tiles split into 4 runs per core
-            buf[:host_src.size] = host_src.view(np.uint16).reshape(-1)
+            u16[:host_src.size] = host_src.view(np.uint16).reshape(-1)
             n_runs = 4 * cores
             cuts = [TILES * i // n_runs for i in range(n_runs + 1)]
-            jobs = [("pair", cuts[i] * te, cuts[i + 1] * te, te, B, M, S) for i in range(n_runs) if cuts[i + 1] > cuts[i]]
+            jobs = [("pair", "<u2", cuts[i] * te, cuts[i + 1] * te, te, B, M, S)
+                    for i in range(n_runs) if cuts[i + 1] > cuts[i]]
             pool.map(_pool_job, jobs)                    # warm: every worker has loaded the oracle
             t_all = _timed_rounds(lambda: pool.map(_pool_job, jobs), seconds_all)
             m_all = sum(t_all) / len(t_all)
@@ -604,62 +624,61 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
                                           f"{len(jobs)} runs of tiles over {cores} processes"}
             # the relayout sweep: one 2^25-element tile (a prefix of the 2^29-element buffer; every
             # swizzle period divides it), forward, all 125 parameter sets
-            buf[:sweep_el] = inputs.uint16_bits(sweep_el, seed=4)
+            u16[:sweep_el] = inputs.uint16_bits(sweep_el, seed=4)
             combos = [(b, m, s) for b in range(1, 6) for m in range(5) for s in range(b, 8)]
-            sweep_jobs = [("fwd", 0, sweep_el, sweep_el, b, m, s) for (b, m, s) in combos]
-            t0 = time.perf_counter()
-            pool.map(_pool_job, sweep_jobs, chunksize=1)
-            t_sweep = time.perf_counter() - t0
-        one = {}
-        for (b, m, s) in ((1, 4, 7), (3, 3, 3), (5, 2, 5)):
-            t0 = time.perf_counter()
-            oracle.relayout(buf[:sweep_el], tile_elems=sweep_el, B=b, M=m, S=s, direction=0)
-            one[f"{b},{m},{s}"] = round(2 * sweep_el * 2 / (time.perf_counter() - t0) / GB, 3)
-        res["sweep125_uint16"] = {
-            "all_cores_GB/s": round(len(combos) * 2 * sweep_el * 2 / t_sweep / GB, 3), "cores": cores,
-            "single_thread_GB/s": one,
-            "sample": f"forward relayout of a {sweep_el * 2 / MiB:g} MiB prefix of the 1 GiB buffer, "
-                      f"{len(combos)} parameter sets"}
+            sweep_jobs = [("fwd", "<u2", 0, sweep_el, sweep_el, b, m, s) for (b, m, s) in combos]
+            t_sweep = wall(lambda: pool.map(_pool_job, sweep_jobs, chunksize=1))
+            one = {}
+            for (b, m, s) in ((1, 4, 7), (3, 3, 3), (5, 2, 5)):
+                t = wall(lambda: oracle.relayout(u16[:sweep_el], tile_elems=sweep_el, B=b, M=m, S=s, direction=0))
+                one[f"{b},{m},{s}"] = round(2 * sweep_el * 2 / t / GB, 3)
+            res["sweep125_uint16"] = {
+                "all_cores_GB/s": round(len(combos) * 2 * sweep_el * 2 / t_sweep / GB, 3), "cores": cores,
+                "single_thread_GB/s": one,
+                "sample": f"forward relayout of a {sweep_el * 2 / MiB:g} MiB prefix of the 1 GiB buffer, "
+                          f"{len(combos)} parameter sets"}
+
+            # every other row: one run on one core, then one band per core at once
+            other = {}
+
+            def row(name, moved_one, run_one, moved_all, all_jobs, sample):
+                pool.map(_pool_job, all_jobs)            # warm
+                other[name] = {"single_thread_GB/s": round(moved_one / wall(run_one) / GB, 3),
+                               "all_cores_GB/s": round(moved_all / wall(lambda: pool.map(_pool_job, all_jobs)) / GB, 3),
+                               "cores": cores, "sample": sample}
+            small = inputs.uint16_bits(256 * 4096, seed=0)
+            u16[:small.size] = small
+            cut = [256 * i // cores for i in range(cores + 1)]
+            row("relayout_fp16_64x64_sw333_2MiB", 4 * small.nbytes,
+                lambda: oracle.relayout(oracle.relayout(u16[:small.size], tile_elems=4096, B=3, M=3, S=3, direction=0),
+                                        tile_elems=4096, B=3, M=3, S=3, direction=1),
+                4 * small.nbytes,
+                [("pair", "<u2", cut[i] * 4096, cut[i + 1] * 4096, 4096, 3, 3, 3)
+                 for i in range(cores) if cut[i + 1] > cut[i]],
+                "whole workload, forward + inverse; all cores: its 256 tiles split over the cores")
+            n8 = i8_tiles * 8192
+            buf[:n8 * cores] = inputs.random_bytes(n8 * cores, seed=4)
+            row("relayout_int8_64x128_sw525", 2 * n8,
+                lambda: oracle.relayout(buf[:n8], tile_elems=8192, B=5, M=2, S=5, direction=0),
+                2 * n8 * cores, [("fwd", "u1", i * n8, (i + 1) * n8, 8192, 5, 2, 5) for i in range(cores)],
+                f"forward; {i8_tiles} of the 131072 tiles per core")
+            for name, n, esize, dt, gen in (
+                    ("transpose_fp32_8192", 8192, 4, "<u4", lambda k: inputs.f32_uniform(k, seed=2).view(np.uint32)),
+                    ("transpose_fp16_16384", 16384, 2, "<u2", lambda k: inputs.f16_bits_no_nan(k, seed=3)),
+                    ("transpose_fp64_8192", 8192, 8, "<u8",
+                     lambda k: inputs.random_bytes(8 * k, seed=4).view(np.uint64))):
+                rows = min(n, band * cores)
+                view = buf.view(np.dtype(dt))
+                view[:rows * n] = gen(rows * n)
+                row(name, 2 * band * n * esize, lambda: oracle.transpose(view[:band * n].reshape(band, n)),
+                    2 * rows * n * esize,
+                    [("transpose", dt, r0, min(rows, r0 + band), n) for r0 in range(0, rows, band)],
+                    f"{band} rows; all cores: {rows} rows of the {n} in bands of {band}")
+            res["other_rows"] = other
     finally:
         shm.close()
         shm.unlink()
-    res["other_rows_single_thread"] = cpu_rows(scale=sample_scale)
     return res
-
-
-def cpu_rows(scale=1):
-    """The oracle, single thread, on a bounded sample of every other row's
-    workload (GB/s = bytes read + written / time).  `scale` divides the
-    samples (tests)."""
-    import numpy as np
-    import oracle
-    from xor_swizzle_movement_gb300 import inputs
-
-    def rate(nbytes, fn):
-        t0 = time.perf_counter()
-        fn()
-        return round(2 * nbytes / (time.perf_counter() - t0) / GB, 3)
-    out = {}
-    small = inputs.uint16_bits(256 * 64 * 64, seed=0)
-    out["relayout_fp16_64x64_sw333_2MiB"] = {
-        "GB/s": rate(2 * small.nbytes, lambda: oracle.relayout(
-            oracle.relayout(small, tile_elems=4096, B=3, M=3, S=3, direction=0),
-            tile_elems=4096, B=3, M=3, S=3, direction=1)),
-        "sample": "whole workload, forward + inverse"}
-    n_i8 = (2048 // scale) * 64 * 128
-    i8 = inputs.random_bytes(n_i8, seed=4)
-    out["relayout_int8_64x128_sw525"] = {
-        "GB/s": rate(i8.nbytes, lambda: oracle.relayout(i8, tile_elems=64 * 128, B=5, M=2, S=5, direction=0)),
-        "sample": f"{n_i8 // (64 * 128)} of the 131072 tiles, forward"}
-    for name, n, esize, gen in (("transpose_fp32_8192", 8192, 4, lambda k: inputs.f32_uniform(k, seed=2)),
-                                ("transpose_fp16_16384", 16384, 2, lambda k: inputs.f16_bits_no_nan(k, seed=3)),
-                                ("transpose_fp64_8192", 8192, 8,
-                                 lambda k: inputs.random_bytes(8 * k, seed=4).view(np.uint64))):
-        rows = max(8, 512 // scale)
-        a = gen(rows * n).reshape(rows, n)
-        out[name] = {"GB/s": rate(a.nbytes, lambda: oracle.transpose(a)),
-                     "sample": f"{rows} of the {n} rows"}
-    return out
 
 
 def run_reference(args):
