@@ -52,6 +52,23 @@ def test_hardware_modes(swz, orc, esize, B, tile_bytes, n_tiles):
     assert swz.swz_device_status() == swz.SWZ_OK
 
 
+@pytest.mark.parametrize("B", [1, 2, 3])
+@pytest.mark.parametrize("n_tiles", [1, 3])
+def test_buffer_smaller_than_one_chunk(swz, orc, B, n_tiles):
+    """Tiles of one swizzle period (2^(B+7) bytes) and a whole buffer below
+    one 8 KiB chunk: the tensor box is taller than the tensor."""
+    from xor_swizzle_movement_gb300 import inputs
+    tile_bytes = 1 << (B + 7)
+    cols = 64
+    rows = tile_bytes // 2 // cols
+    host = inputs.uint16_bits(n_tiles * tile_bytes // 2, seed=12)
+    for direction in (0, 1):
+        got = run(swz, host, n_tiles, rows, cols, 2, B, 3, 3, direction)
+        want = orc.relayout(host, tile_elems=tile_bytes // 2, B=B, M=3, S=3, direction=direction)
+        assert np.array_equal(got, want), direction
+    assert swz.swz_device_status() == swz.SWZ_OK
+
+
 def test_small_fp16_tiles_sw333(swz, orc):
     """256 tiles of 64 x 64 16-bit elements, Swizzle<3,3,3>: the 128-byte mode."""
     from xor_swizzle_movement_gb300 import inputs
