@@ -144,6 +144,21 @@ def test_ragged_tiles(swz, orc, esize, rows, cols, B, M, S, n_tiles):
         assert got.tobytes() == want.tobytes()
 
 
+@pytest.mark.parametrize("esize,tile,B,M,S", [
+    (1, 2, 1, 0, 1), (1, 4, 1, 0, 1), (1, 4, 2, 0, 1), (1, 8, 1, 0, 2), (1, 8, 2, 1, 1), (1, 8, 3, 0, 1),
+    (2, 2, 1, 0, 3), (2, 4, 2, 0, 1), (2, 4, 1, 1, 1), (4, 2, 1, 0, 1), (8, 1, 0, 0, 1)])
+@pytest.mark.parametrize("n_tiles", [4096, 4099])
+def test_tiles_smaller_than_a_vector(swz, orc, esize, tile, B, M, S, n_tiles):
+    """Tiles of 1 to 8 bytes: whole tiles inside every 16-byte vector (a fixed
+    lane permutation), and a count that leaves a partial vector (element path)."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=9).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, 1, tile, esize, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), direction
+
+
 @pytest.mark.parametrize("esize", [1, 2, 4, 8])
 def test_misaligned_pointers(swz, orc, esize):
     """Pointers aligned to the element size but not to 16 bytes."""

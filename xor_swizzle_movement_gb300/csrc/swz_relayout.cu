@@ -161,6 +161,32 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
     const int steps = (direction == 0 && B > 0 && S < B) ? (B + S - 1) / S : 1;
     const int64_t tile_bytes = tile_elems * esize;
     const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    if (tile_bytes < 16 && 16 % tile_bytes == 0 && aligned16 && (n_elems * esize) % 16 == 0) {
+        // Every 16-byte vector holds whole tiles, so each vector stays where it
+        // is and its lanes move by one fixed permutation: the vector kernel
+        // with the identity at vector level (B = 0) and that permutation as
+        // its lane map.
+        const int lanes = 16 / esize, te = static_cast<int>(tile_elems);
+        int src_lane[16];
+        for (int l = 0; l < lanes; ++l)
+            src_lane[l] = (l - l % te) + static_cast<int>(sw_inv(static_cast<uint64_t>(l % te), B, M, S, steps));
+        RelayoutArgs a;
+        a.dst = static_cast<uint4 *>(dst);
+        a.src = static_cast<const uint4 *>(src);
+        a.nvec = n_elems * esize / 16;
+        a.tile_vecs = 1;
+        a.B = 0; a.M = 0; a.S = 1;
+        a.steps = 1;
+        const int64_t wave = 152LL * 2048;
+        a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+        lane_map_selectors(src_lane, esize, a.perm_sel);
+        switch (esize) {
+            case 1: return launch_vec<1>(a, kLanesGeneral, false, st);
+            case 2: return launch_vec<2>(a, kLanesGeneral, false, st);
+            case 4: return launch_vec<4>(a, kLanesGeneral, false, st);
+            default: return launch_vec<8>(a, kLanesGeneral, false, st);
+        }
+    }
     if (tile_bytes % 16 == 0 && aligned16) {
         int lv = 0;
         while ((1 << lv) < 16 / esize) ++lv;
