@@ -123,9 +123,12 @@ swz_status swz_relayout_tma(void *dst, const void *src, int64_t n_tiles, int64_t
  *   esize 2 : 128-byte rows (64 elements) under the byte-address Swizzle<3,4,3>
  *             (16-byte chunk index XOR row mod 8; element Swizzle<3,3,3>),
  *             drained by 8 x 8 transposing matrix loads;
- *   esize 1, 16 : 32 x 32 units, element Swizzle<5,0,5>.
+ *   esize 1 : 128 x 128-byte tiles under the byte-address Swizzle<3,4,7>
+ *             (16-byte chunk index XOR (row / 16) mod 8), drained as 4 x 4
+ *             byte blocks transposed in registers;
+ *   esize 16 : 32 x 32 units, element Swizzle<5,0,5>.
  * SWZ_T_UNSWIZZLED uses the plain layout, SWZ_T_PADDED pads each row by one
- * element (by 16 bytes for esize 2).  SWZ_T_TMA is accepted for esize 2 only.
+ * element (by 16 bytes for esize 2); for esize 1 both run on 32 x 32 units.  SWZ_T_TMA is accepted for esize 2 only.
  *
  * dst: cols x rows elements; src: rows x cols elements; both device buffers.
  * rows, cols >= 0 (any value: edge tiles are handled element by element).

@@ -55,6 +55,18 @@ def test_misaligned(swz, orc, esize):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("shape", [(2048, 4096), (384, 640), (4096, 2048 + 16)])
+def test_u8_full_tiles(swz, orc, shape):
+    """1-byte elements through 128 x 128 byte tiles: whole tiles (register 4 x 4
+    byte transposes), and a column count that leaves a ragged last tile."""
+    from xor_swizzle_movement_gb300 import inputs
+    rows, cols = shape
+    host = inputs.random_bytes(rows * cols, seed=17).reshape(rows, cols)
+    for variant in VARIANTS:
+        got = run_transpose(swz, host, 1, variant)
+        assert np.array_equal(got, orc.transpose(host)), variant
+
+
 def test_fp32_8192_all_variants(swz, orc):
     from xor_swizzle_movement_gb300 import inputs
     n = 8192

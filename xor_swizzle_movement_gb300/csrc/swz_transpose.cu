@@ -35,8 +35,15 @@
 // exchange 32-bit words (a two-step XOR butterfly) so that each lane owns 16
 // contiguous output bytes.
 //
-// Element sizes 1 and 16: 32 x 32 units under element Swizzle<5,0,5>, one
-// element per access.
+// Element size 1: tiles of 128 x 128 bytes with 128-byte rows under the
+// byte-address Swizzle<3,4,7> (16-byte chunk index XOR (row / 16) mod 8).
+// The tile is filled with 16-byte stores; each thread of the drain reads one
+// 32-bit word (4 columns) from 16 consecutive rows, transposes the 4 x 4 byte
+// blocks in registers with byte permutes and stores 4 output vectors of 16
+// bytes.  A warp's drain load covers 8 row groups x 4 words, which the XOR
+// spreads over all 32 banks.  The unswizzled and padded stagings of 1-byte
+// elements, and the 16-byte elements, use 32 x 32 units under element
+// Swizzle<5,0,5>, one element per access.
 //
 // Tiles that cross the matrix edge, and matrices whose rows are not whole
 // 16-byte vectors, go element by element with bounds checks through the same
@@ -257,6 +264,86 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// --------------------------------------------------------------------- 1 B --
+// 4 x 4 byte transpose: row k of the block is w[k]; on return t[j] holds
+// column j (byte k of t[j] is byte j of w[k]).
+__device__ __forceinline__ void transpose4x4_bytes(const uint32_t w[4], uint32_t t[4]) {
+    const uint32_t a = __byte_perm(w[0], w[1], 0x5140), b = __byte_perm(w[0], w[1], 0x7362);
+    const uint32_t c = __byte_perm(w[2], w[3], 0x5140), d = __byte_perm(w[2], w[3], 0x7362);
+    t[0] = __byte_perm(a, c, 0x5410);
+    t[1] = __byte_perm(a, c, 0x7632);
+    t[2] = __byte_perm(b, d, 0x5410);
+    t[3] = __byte_perm(b, d, 0x7632);
+}
+
+// Tile 128 x 128 bytes, 256 threads.
+template <bool FUSE>
+__global__ void __launch_bounds__(256)
+    transpose8_kernel(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src, int64_t R, int64_t C,
+                      int64_t tiles_c, int vec_ok, const FuseArgs f) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    constexpr int T = 128, THREADS = 256;
+    __shared__ __align__(16) uint8_t sm[T * T];
+    const int64_t tr = static_cast<int64_t>(blockIdx.x) / tiles_c;
+    const int64_t tc = static_cast<int64_t>(blockIdx.x) - tr * tiles_c;
+    const int64_t r0 = tr * T, c0 = tc * T;
+    const int tid = threadIdx.x;
+    // byte offset of (row, col) in the staged tile
+    auto at = [](int row, int col) -> int { return row * T + ((((col >> 4) ^ (row >> 4)) & 7) << 4) + (col & 15); };
+
+    if (vec_ok && r0 + T <= R && c0 + T <= C) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int id = k * THREADS + tid, row = id >> 3, ch = id & 7;
+            v[k] = ld_stream16(src + (r0 + row) * C + c0 + ch * 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int id = k * THREADS + tid, row = id >> 3, ch = id & 7;
+            *reinterpret_cast<uint4 *>(sm + at(row, ch * 16)) = v[k];
+        }
+        __syncthreads();
+        // thread: word q (columns 4q .. 4q + 3) of rows 16g .. 16g + 15
+        const int lane = tid & 31, warp = tid >> 5;
+        const int g = lane & 7, q = 4 * warp + (lane >> 3);
+        uint32_t col[4][4];  // col[j][a]: column 4q + j, rows 16g + 4a .. + 3
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            uint32_t w[4], t[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int row = 16 * g + 4 * a + k;
+                w[k] = *reinterpret_cast<const uint32_t *>(sm + at(row, 4 * q));
+            }
+            transpose4x4_bytes(w, t);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) col[j][a] = t[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t y = (c0 + 4 * q + j) * R + r0 + 16 * g;
+            const uint4 o = make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+            if constexpr (FUSE) store16_fused<1>(dst, static_cast<uint64_t>(y), o, f);
+            else st_stream16(dst + y, o);
+        }
+    } else {
+        for (int idx = tid; idx < T * T; idx += THREADS) {
+            const int row = idx / T, cl = idx % T;
+            if (r0 + row < R && c0 + cl < C) sm[at(row, cl)] = src[(r0 + row) * C + c0 + cl];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < T * T; idx += THREADS) {
+            const int ocl = idx / T, orow = idx % T;
+            if (c0 + ocl < C && r0 + orow < R) {
+                const int64_t y = (c0 + ocl) * R + r0 + orow;
+                dst[FUSE ? static_cast<int64_t>(fused_pos(static_cast<uint64_t>(y), f)) : y] = sm[at(orow, ocl)];
+            }
+        }
+    }
+}
+
 // --------------------------------------------------------------- 1 / 16 B --
 template <typename T, int VARIANT, bool FUSE>
 __global__ void __launch_bounds__(256)
@@ -331,6 +418,21 @@ swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int varia
     return launched(e);
 }
 
+swz_status launch_8(void *dst, const void *src, int64_t R, int64_t C, bool aligned16, const FuseArgs *fuse,
+                    cudaStream_t st) {
+    const int64_t tiles_c = (C + 127) / 128, tiles = ((R + 127) / 128) * tiles_c;
+    if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const int vec_ok = aligned16 && (C % 16 == 0) && (R % 16 == 0) && (!fuse || fuse->te % 16 == 0);
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    const uint8_t *s = static_cast<const uint8_t *>(src);
+    const unsigned g = static_cast<unsigned>(tiles);
+    const FuseArgs f = fuse ? *fuse : FuseArgs{};
+    cudaError_t e;
+    if (fuse) e = launch_pdl(transpose8_kernel<true>, g, dim3(256), 0, st, d, s, R, C, tiles_c, vec_ok, f);
+    else e = launch_pdl(transpose8_kernel<false>, g, dim3(256), 0, st, d, s, R, C, tiles_c, vec_ok, f);
+    return launched(e);
+}
+
 template <typename T>
 swz_status launch_generic(void *dst, const void *src, int64_t R, int64_t C, int variant, const FuseArgs *fuse,
                           cudaStream_t st) {
@@ -364,7 +466,9 @@ swz_status dispatch(void *dst, const void *src, int64_t R, int64_t C, int esize,
                     cudaStream_t st) {
     const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
     switch (esize) {
-        case 1: return launch_generic<uint8_t>(dst, src, R, C, variant, fuse, st);
+        case 1:
+            if (fuse || variant == SWZ_T_SWIZZLED) return launch_8(dst, src, R, C, aligned16, fuse, st);
+            return launch_generic<uint8_t>(dst, src, R, C, variant, fuse, st);
         case 2:
             if (variant == SWZ_T_TMA && !fuse) return transpose_tma_launch(dst, src, R, C, st);
             return launch_16(dst, src, R, C, variant, aligned16, fuse, st);
