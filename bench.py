@@ -483,6 +483,17 @@ def measure_rows(torch, swz, dev, flush, peak):
         del s_, d_
     out["transpose_fp32_swizzled_output_pitch"] = pitch
 
+    # 1-byte elements (not a configured workload): 16384 x 16384 bytes, the
+    # swizzled 128 x 128 byte tiles against the element-wise unswizzled staging
+    s_ = rand_bytes(16384 * 16384, 4)
+    d_ = torch.empty_like(s_)
+    u8 = {}
+    for v, vname in ((0, "swizzled_byte_sw347"), (1, "unswizzled")):
+        ms = back_to_back_ms(torch, lambda: swz.swz_transpose(d_, s_, 16384, 16384, 1, v))
+        u8[vname] = summary(ms, 2 * 16384 * 16384)
+    out["transpose_u8_16384"] = u8
+    del s_, d_
+
     # transpose fused with the relayout: a 64 x 2^21 bf16 matrix (256 MiB) into K-major 128 x 64
     # tiles under Swizzle<3,4,3>, in one pass, against the transpose and the relayout apart
     kr, kc = 64, 1 << 21
