@@ -25,8 +25,8 @@ The JSON line also carries:
                 a 64 MiB sample;
   rows          every other row of the path measured in the same run: the
                 small relayout, the 1 GiB int8 and uint16-sweep relayouts, the
-                fp32 / fp16 / fp64 transposes with each staging, the bank
-                profiler (skip with --no-rows).
+                fp32 / fp16 / fp64 (and 1-byte) transposes with each staging,
+                the bank profiler (skip with --no-rows).
 
 --impl reference times the CPU oracle as the reference arm.
 Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak
