@@ -99,24 +99,42 @@ template <> struct ElemType<4> { using T = uint32_t; };
 template <> struct ElemType<8> { using T = uint2; };
 template <> struct ElemType<16> { using T = uint4; };
 
-// One element per iteration; used when a tile is not a whole number of
-// 16-byte vectors or a pointer is not 16-byte aligned.
-template <int E>
+// Element by element; used when a tile is not a whole number of 16-byte
+// vectors or a pointer is not 16-byte aligned.  Each thread keeps four
+// independent elements in flight, and tile-local offsets (a 64-bit remainder)
+// are taken only when the tile does not hold whole swizzle periods.
+template <int E, bool LOCAL>
 __global__ void __launch_bounds__(256)
     relayout_scalar_kernel(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int B,
                            int M, int S, int steps) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     using T = typename ElemType<E>::T;
+    constexpr int U = 4;
     T *d = static_cast<T *>(dst);
     const T *s = static_cast<const T *>(src);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_elems;
-         i += stride) {
-        const int64_t local = i % tile_elems;
-        const int64_t tile0 = i - local;
-        const uint64_t x = sw_inv(static_cast<uint64_t>(local), B, M, S, steps);
-        d[i] = s[tile0 + static_cast<int64_t>(x)];
+    for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n_elems;
+         i0 += U * stride) {
+        T v[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < n_elems) {
+                int64_t local = i, tile0 = 0;
+                if constexpr (LOCAL) {
+                    local = i % tile_elems;
+                    tile0 = i - local;
+                }
+                const uint64_t x = sw_inv(static_cast<uint64_t>(local), B, M, S, steps);
+                v[k] = s[tile0 + static_cast<int64_t>(x)];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t i = i0 + k * stride;
+            if (i < n_elems) d[i] = v[k];
+        }
     }
 }
 
@@ -148,8 +166,14 @@ swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, in
     const int threads = 256;
     int64_t grid = (n + threads - 1) / threads;
     if (grid > 152LL * 32) grid = 152LL * 32;
-    return launched(launch_pdl(relayout_scalar_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st,
-                               dst, src, n, tile, B, M, S, steps));
+    const int period = B + M + S;
+    const bool local = B > 0 && (period >= 62 || (tile & ((int64_t(1) << period) - 1)) != 0);
+    const dim3 g(static_cast<unsigned>(grid));
+    if (local)
+        return launched(launch_pdl(relayout_scalar_kernel<E, true>, g, dim3(threads), 0, st, dst, src, n, tile, B,
+                                   M, S, steps));
+    return launched(launch_pdl(relayout_scalar_kernel<E, false>, g, dim3(threads), 0, st, dst, src, n, tile, B, M,
+                               S, steps));
 }
 
 }  // namespace
