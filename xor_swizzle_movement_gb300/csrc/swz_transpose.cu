@@ -153,11 +153,20 @@ __global__ void __launch_bounds__(THREADS, MIN_CTAS)
             else st_stream16(dst + y, o);
         }
     } else {
-        for (int idx = tid; idx < TR * TC; idx += THREADS) {
-            const int row = idx / TC, cl = idx % TC;
+        // all loads first: each thread keeps its elements of the tile in flight
+        constexpr int EI = TR * TC / THREADS;
+        T ev[EI];
+#pragma unroll
+        for (int k = 0; k < EI; ++k) {
+            const int idx = k * THREADS + tid, row = idx / TC, cl = idx % TC;
+            if (r0 + row < R && c0 + cl < C) ev[k] = src[(r0 + row) * C + c0 + cl];
+        }
+#pragma unroll
+        for (int k = 0; k < EI; ++k) {
+            const int idx = k * THREADS + tid, row = idx / TC, cl = idx % TC;
             if (r0 + row < R && c0 + cl < C) {
                 const int ur = row / N, ir = row % N, uc = cl / N, ic = cl % N;
-                sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)] = src[(r0 + row) * C + c0 + cl];
+                sm[(ur * UC + uc) * N * P + ir * P + phys(ir, ic)] = ev[k];
             }
         }
         __syncthreads();
