@@ -69,7 +69,7 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--case", default=None,
                    help="run one kernel case for a profiler and exit: relayout, relayout_bms, "
-                        "relayout_tma, transposes, transpose_relayout, bank_profile")
+                        "relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
@@ -775,6 +775,14 @@ def run_case(args):
             swz.swz_relayout_tma(a, src, nbytes // 8192, 64, 64, 2, 3, 3, 3, 0)
             swz.swz_relayout_tma(b, a, nbytes // 8192, 64, 64, 2, 3, 3, 3, 1)
         done.append(f"relayout_tma fwd+inv bytes={nbytes}")
+    elif args.case == "transpose_u8":  # n x n bytes, swizzled and unswizzled stagings
+        n = args.n or 8192
+        src = rand_bytes(n * n)
+        dst = torch.empty_like(src)
+        for v in (0, 1):
+            for _ in range(args.reps):
+                swz.swz_transpose(dst, src, n, n, 1, v)
+            done.append(f"transpose esize=1 n={n} variant={v}")
     elif args.case == "transpose_relayout":  # 64 x n bf16 into K-major 128 x 64 Swizzle<3,4,3> tiles
         cols = args.n or (1 << 20)
         src = rand_bytes(64 * cols * 2)
