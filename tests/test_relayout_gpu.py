@@ -159,6 +159,26 @@ def test_tiles_smaller_than_a_vector(swz, orc, esize, tile, B, M, S, n_tiles):
         assert got.tobytes() == want.tobytes(), direction
 
 
+@pytest.mark.parametrize("esize,tile,B,M,S", [
+    (1, 24, 2, 0, 1), (1, 40, 3, 0, 2), (1, 12, 2, 0, 3), (1, 1000, 3, 0, 3), (2, 12, 2, 0, 1),
+    (2, 20, 2, 0, 2), (2, 76, 2, 0, 3), (4, 6, 1, 0, 1), (4, 10, 1, 0, 1), (4, 30, 1, 0, 5),
+    (8, 3, 0, 0, 1), (8, 10, 1, 0, 2), (8, 6, 1, 0, 1),
+    # groups of 2^M elements gathered as units of 2, 4 or 8 bytes
+    (1, 40, 2, 1, 2), (1, 24, 1, 2, 3), (2, 12, 1, 1, 2), (1, 56, 0, 3, 1), (4, 14, 0, 1, 1),
+    (2, 28, 1, 1, 3)])
+@pytest.mark.parametrize("n_tiles", [1, 1000, 4099])
+def test_ragged_tiles_staged(swz, orc, esize, tile, B, M, S, n_tiles):
+    """Tiles whose byte size is not a multiple of 16 (aligned pointers): whole
+    tiles staged in shared memory in blocks of lcm(tile bytes, 16) x k bytes,
+    including a last block that is partial and not a multiple of 16 bytes."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=10).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, 1, tile, esize, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), direction
+
+
 @pytest.mark.parametrize("esize", [1, 2, 4, 8])
 def test_misaligned_pointers(swz, orc, esize):
     """Pointers aligned to the element size but not to 16 bytes."""

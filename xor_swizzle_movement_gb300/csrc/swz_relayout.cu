@@ -33,6 +33,8 @@
 //                 host computes once per launch.
 #include "swz_common.cuh"
 
+#include <cstring>
+
 namespace swz {
 namespace {
 
@@ -160,6 +162,75 @@ swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, cudaStream_t 
     return launched(e);
 }
 
+// Tiles whose byte size is not a multiple of 16, with 16-byte aligned
+// pointers: a CTA stages a block of whole tiles (a multiple of
+// lcm(tile bytes, 16), at most kStageBytes) in shared memory with 16-byte
+// loads; each thread then gathers one 16-byte output vector element by
+// element from the staged block and stores it with one 16-byte store.  The
+// block starts on a tile boundary, so an element's tile-local offset is its
+// block offset modulo the tile: a multiply-high by a precomputed reciprocal
+// (exact while offset x tile < 2^32) for a vector's first element, then a
+// running count.
+constexpr int kStageBytes = 8192;
+
+template <int E>
+__global__ void __launch_bounds__(256)
+    relayout_staged_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes, int block_bytes, uint32_t te,
+                           uint32_t te_recip, int B, int M, int S, int steps) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    using T = typename ElemType<E>::T;
+    constexpr int V = 16 / E;  // elements per output vector
+    __shared__ __align__(16) uint8_t a_s[kStageBytes];
+    const int tid = threadIdx.x;
+    for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * block_bytes; b0 < bytes;
+         b0 += static_cast<int64_t>(gridDim.x) * block_bytes) {
+        const int nb = static_cast<int>(bytes - b0 < block_bytes ? bytes - b0 : block_bytes);
+        const int nv = nb / 16;
+        for (int v = tid; v < nv; v += 256)
+            *reinterpret_cast<uint4 *>(a_s + 16 * v) = ld_stream16(src + b0 + 16 * v);
+        for (int t = 16 * nv + tid; t < nb; t += 256) a_s[t] = src[b0 + t];
+        __syncthreads();
+        auto local_of = [&](uint32_t e) -> uint32_t { return te == 1 ? 0u : e - __umulhi(e, te_recip) * te; };
+        for (int v = tid; v < nv; v += 256) {
+            uint32_t e = static_cast<uint32_t>(v) * V;
+            uint32_t local = local_of(e), tile0 = e - local;
+            T lanes[V];
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const uint32_t x = static_cast<uint32_t>(sw_inv(local, B, M, S, steps));
+                lanes[k] = *reinterpret_cast<const T *>(a_s + (tile0 + x) * E);
+                if (++local == te) {
+                    local = 0;
+                    tile0 += te;
+                }
+            }
+            uint4 o;
+            memcpy(&o, lanes, 16);
+            st_stream16(dst + b0 + 16 * v, o);
+        }
+        const uint32_t ne = static_cast<uint32_t>(nb / E);
+        for (uint32_t e = static_cast<uint32_t>(nv) * V + tid; e < ne; e += 256) {
+            const uint32_t local = local_of(e);
+            const uint32_t x = static_cast<uint32_t>(sw_inv(local, B, M, S, steps));
+            *reinterpret_cast<T *>(dst + b0 + e * E) = *reinterpret_cast<const T *>(a_s + (e - local + x) * E);
+        }
+        __syncthreads();  // the buffer is refilled for the next block
+    }
+}
+
+template <int E>
+swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_bytes, int64_t tile_elems, int B,
+                         int M, int S, int steps, cudaStream_t st) {
+    int64_t grid = (bytes + block_bytes - 1) / block_bytes;
+    if (grid > 152LL * 8) grid = 152LL * 8;
+    const uint32_t te = static_cast<uint32_t>(tile_elems);
+    const uint32_t recip = te == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / te + 1);
+    return launched(launch_pdl(relayout_staged_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
+                               static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), bytes, block_bytes,
+                               te, recip, B, M, S, steps));
+}
+
 template <int E>
 swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, int B, int M, int S,
                          int steps, cudaStream_t st) {
@@ -209,6 +280,27 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
             case 2: return launch_vec<2>(a, kLanesGeneral, false, st);
             case 4: return launch_vec<4>(a, kLanesGeneral, false, st);
             default: return launch_vec<8>(a, kLanesGeneral, false, st);
+        }
+    }
+    if (tile_bytes % 16 != 0 && aligned16) {
+        int64_t g = tile_bytes, h = 16;
+        while (h) { const int64_t r = g % h; g = h; h = r; }
+        const int64_t l = tile_bytes / g * 16;  // lcm(tile bytes, 16)
+        if (l <= kStageBytes) {
+            const int block = static_cast<int>(l * (kStageBytes / l));
+            const int64_t bytes = n_elems * esize;
+            // groups of 2^M elements move intact: gather units of 2^k elements,
+            // k = min(M, log2(16 / esize)), under Swizzle<B, M - k, S> on unit
+            // offsets (tiles hold a multiple of 2^M elements)
+            int k = 0;
+            while (k < M && (esize << (k + 1)) <= 8) ++k;
+            const int64_t te_u = tile_elems >> k;
+            switch (esize << k) {
+                case 1: return launch_staged<1>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+                case 2: return launch_staged<2>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+                case 4: return launch_staged<4>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+                default: return launch_staged<8>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+            }
         }
     }
     if (tile_bytes % 16 == 0 && aligned16) {
