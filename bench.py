@@ -439,7 +439,7 @@ def measure_rows(torch, swz, dev, flush, peak):
         "min_frac_of_hbm": round(vals[0] / peak, 3)}
     del src, dst
 
-    # transposes, with the bank model's verdict on each staging's warp accesses
+    # transposes, with the bank model's prediction for each staging's warp accesses
     pat_rows, pat_keys = [], []
     for esize, variants in ((4, (0, 1, 2)), (2, (0, 3, 1, 2)), (8, (0, 1, 2))):
         for v in variants:

@@ -20,9 +20,9 @@ import bench
     (2, 2, {"fill_store": 1, "drain_ldmatrix": 1}),
     (2, 3, {"fill_store": 1, "drain_ldmatrix": 1}),
 ])
-def test_staging_patterns_bank_verdicts(orc, esize, variant, expect):
+def test_staging_patterns_bank_predictions(orc, esize, variant, expect):
     """The warp accesses the bench feeds to the GPU profiler get, from the
-    oracle's bank model, the verdicts the transpose stagings are built for."""
+    oracle's bank model, the predictions the transpose stagings are built for."""
     got = {}
     for access, (addrs, width) in bench.staging_patterns(esize, variant).items():
         ways, _ = orc.bank_profile(np.array([addrs], dtype=np.uint32), width)
