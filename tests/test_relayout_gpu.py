@@ -165,7 +165,9 @@ def test_tiles_smaller_than_a_vector(swz, orc, esize, tile, B, M, S, n_tiles):
     (8, 3, 0, 0, 1), (8, 10, 1, 0, 2), (8, 6, 1, 0, 1),
     # groups of 2^M elements gathered as units of 2, 4 or 8 bytes
     (1, 40, 2, 1, 2), (1, 24, 1, 2, 3), (2, 12, 1, 1, 2), (1, 56, 0, 3, 1), (4, 14, 0, 1, 1),
-    (2, 28, 1, 1, 3)])
+    (2, 28, 1, 1, 3),
+    # S < B: the forward gathers through the exact inverse
+    (1, 24, 2, 1, 1), (2, 20, 2, 0, 1)])
 @pytest.mark.parametrize("n_tiles", [1, 1000, 4099])
 def test_ragged_tiles_staged(swz, orc, esize, tile, B, M, S, n_tiles):
     """Tiles whose byte size is not a multiple of 16 (aligned pointers): whole
