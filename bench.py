@@ -69,7 +69,7 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--case", default=None,
                    help="run one kernel case for a profiler and exit: relayout, relayout_bms, "
-                        "relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
+                        "relayout_staged, relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
@@ -757,6 +757,14 @@ def run_case(args):
         for _ in range(args.reps):
             swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0)
         done.append(f"relayout uint16 n={n} Sw<{Bq},{Mq},{Sq}>")
+    elif args.case == "relayout_staged":   # ragged 24-byte tiles staged in shared memory
+        nbytes = (args.n or (256 << 20)) // 24 * 24
+        src = rand_bytes(nbytes)
+        dst = torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_relayout(dst, src, nbytes // 24, 3, 4, 2, 2, 0, 1, 0)     # uint16 3 x 4, Sw<2,0,1>
+            swz.swz_relayout(dst, src, nbytes // 24, 1, 24, 1, 1, 2, 3, 0)    # int8 24, Sw<1,2,3>
+        done.append(f"relayout staged bytes={nbytes}")
     elif args.case == "transposes":        # every staging of the fp32 / fp16 / fp64 transposes
         for esize, n, variants in ((4, args.n or 8192, (0, 1, 2)), (2, args.n or 8192, (0, 3, 1, 2)),
                                    (8, (args.n or 8192) // 2, (0, 1, 2))):
