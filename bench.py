@@ -483,6 +483,25 @@ def measure_rows(torch, swz, dev, flush, peak):
         del s_, d_
     out["transpose_fp32_swizzled_output_pitch"] = pitch
 
+    # tiles that are not whole 16-byte vectors (not a configured workload): 256 MiB
+    # each, staged in shared memory (aligned pointers) or element by element
+    # (a source 2 bytes off 16-byte alignment)
+    rag = {}
+    nb = (256 * MiB) // 120 * 120
+    s_ = rand_bytes(nb + 64, 4)
+    d_ = torch.empty_like(s_)
+    for name, args_ in (("u8_tile24_sw201", (nb // 24, 1, 24, 1, 2, 0, 1)),
+                        ("u8_tile24_sw123_4byte_units", (nb // 24, 1, 24, 1, 1, 2, 3)),
+                        ("u16_tile3x4_sw201", (nb // 24, 3, 4, 2, 2, 0, 1)),
+                        ("u32_tile30_sw105", (nb // 120, 1, 30, 4, 1, 0, 5))):
+        ms = back_to_back_ms(torch, lambda: swz.swz_relayout(d_, s_[:nb], *args_, 0))
+        rag[name] = summary(ms, 2 * nb)
+    src_off = s_[2:2 + 64 * MiB]
+    ms = back_to_back_ms(torch, lambda: swz.swz_relayout(d_[:64 * MiB], src_off, 64 * MiB // 8192, 64, 64, 2, 3, 3, 3, 0))
+    rag["u16_64x64_sw333_source_plus_2B"] = summary(ms, 2 * 64 * MiB)
+    out["relayout_ragged_or_unaligned"] = rag
+    del s_, d_, src_off
+
     # 1-byte elements (not a configured workload): 16384 x 16384 bytes, the
     # swizzled 128 x 128 byte tiles against the element-wise unswizzled staging
     s_ = rand_bytes(16384 * 16384, 4)
