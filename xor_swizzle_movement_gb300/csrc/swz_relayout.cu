@@ -173,6 +173,16 @@ swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, cudaStream_t 
 // running count.
 constexpr int kStageBytes = 8192;
 
+// sw_inv on offsets below 2^16 in 32-bit arithmetic; the launcher passes
+// B = 0 when the read field starts at or above bit 16 (the swizzle is then the
+// identity on every offset of a staged block).
+__device__ __forceinline__ uint32_t sw_inv32(uint32_t y, int B, int M, int S, int steps) {
+    const uint32_t mask = (1u << B) - 1u;
+    uint32_t x = y;
+    for (int i = 0; i < steps; ++i) x = y ^ (((x >> (M + S)) & mask) << M);
+    return x;
+}
+
 template <int E>
 __global__ void __launch_bounds__(256)
     relayout_staged_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes, int block_bytes, uint32_t te,
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(256)
             T lanes[V];
 #pragma unroll
             for (int k = 0; k < V; ++k) {
-                const uint32_t x = static_cast<uint32_t>(sw_inv(local, B, M, S, steps));
+                const uint32_t x = sw_inv32(local, B, M, S, steps);
                 lanes[k] = *reinterpret_cast<const T *>(a_s + (tile0 + x) * E);
                 if (++local == te) {
                     local = 0;
@@ -212,7 +222,7 @@ __global__ void __launch_bounds__(256)
         const uint32_t ne = static_cast<uint32_t>(nb / E);
         for (uint32_t e = static_cast<uint32_t>(nv) * V + tid; e < ne; e += 256) {
             const uint32_t local = local_of(e);
-            const uint32_t x = static_cast<uint32_t>(sw_inv(local, B, M, S, steps));
+            const uint32_t x = sw_inv32(local, B, M, S, steps);
             *reinterpret_cast<T *>(dst + b0 + e * E) = *reinterpret_cast<const T *>(a_s + (e - local + x) * E);
         }
         __syncthreads();  // the buffer is refilled for the next block
@@ -226,6 +236,9 @@ swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_by
     if (grid > 152LL * 8) grid = 152LL * 8;
     const uint32_t te = static_cast<uint32_t>(tile_elems);
     const uint32_t recip = te == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / te + 1);
+    // staged offsets are below kStageBytes <= 2^16: a read field at or above
+    // bit 16 is all zero there, and the swizzle is the identity
+    if (M + S >= 16) { B = 0; M = 0; S = 1; steps = 1; }
     return launched(launch_pdl(relayout_staged_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
                                static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), bytes, block_bytes,
                                te, recip, B, M, S, steps));
