@@ -25,7 +25,7 @@ constexpr int kWarpsPerCta = 8;
 
 // W = access bytes per lane (1, 2, 4, 8, 16)
 template <int W>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, 8)  // 8 CTAs (64 warps) per SM: 32 registers
     bank_profile_kernel(const uint32_t *__restrict__ addrs, const uint32_t *__restrict__ active,
                         int64_t n, int32_t *__restrict__ ways, int32_t *__restrict__ wavefronts) {
     constexpr int kPasses = W <= 4 ? 1 : W / 4;
