@@ -61,8 +61,11 @@ enum {
  * "使用示例" (an element whose logical offset is o lives at the swizzled
  * offset sw(o)); "NVIDIA CuTe Swizzle" and "cutlass 入门" for the parameters.
  *
- * dst, src : device buffers of n_tiles * rows * cols elements of esize bytes,
- *            each tile stored contiguously, row-major (offset o = r * cols + c).
+ * dst, src : buffers of n_tiles * rows * cols elements of esize bytes, each
+ *            tile stored contiguously, row-major (offset o = r * cols + c).
+ *            Normally device memory; host memory the device can address
+ *            (pinned, or any on systems with address translation) also works,
+ *            at the host link's rate.
  * esize    : 1, 2, 4, 8 or 16 bytes.  Elements are copied as raw bits.
  * B, M, S  : swizzle parameters in element units; 0 <= B <= 16,
  *            0 <= M <= 32, and when B > 0: 1 <= S <= 32, B + M + S <= 48.
