@@ -13,8 +13,9 @@
  * in ELEMENT-offset units.
  *
  * Conventions shared by every entry point:
- *   - Pointers named dst/src/out are DEVICE pointers owned by the caller; the
- *     library never allocates, frees or retains them.
+ *   - Pointers named dst/src/out are DEVICE pointers owned by the caller (the
+ *     relayout also accepts host memory the device can address); the library
+ *     never allocates, frees or retains them.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  GPU work is enqueued on it and the call returns without
  *     waiting; the caller synchronises.
