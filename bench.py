@@ -355,6 +355,11 @@ def measure_rows(torch, swz, dev, flush, peak):
         gbs = nbytes / (ms * 1e-3) / GB
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 3)}
 
+    def flushed_median(fn, nbytes):
+        """Median of 20 single launches, each after an L2 flush and timed by
+        its own event pair (event resolution about 2 us)."""
+        return summary(statistics.median(timed_launches(torch, fn, 20, flush)), nbytes)
+
     # small relayout: 256 fp16 tiles 64x64, Swizzle<3,3,3>, forward then inverse (4 MiB moved per launch)
     src = rand_bytes(256 * 64 * 64 * 2, 0)
     a, b = torch.empty_like(src), torch.empty_like(src)
@@ -419,7 +424,10 @@ def measure_rows(torch, swz, dev, flush, peak):
     n_tiles = (1 << 30) // (64 * 128)
     fwd = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0))
     inv = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 1))
-    out["relayout_int8_64x128_sw525_1GiB"] = {"forward": summary(fwd, 2 << 30), "inverse": summary(inv, 2 << 30)}
+    out["relayout_int8_64x128_sw525_1GiB"] = {
+        "forward": summary(fwd, 2 << 30), "inverse": summary(inv, 2 << 30),
+        "forward_flushed_median_20": flushed_median(
+            lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0), 2 << 30)}
 
     # one 1 GiB uint16 buffer, every (B, M, S) with B 1..5, M 0..4, S B..7, forward
     n = 1 << 29
@@ -463,6 +471,8 @@ def measure_rows(torch, swz, dev, flush, peak):
         for v, vname in variants:
             ms = back_to_back_ms(torch, lambda: swz.swz_transpose(d_, s_, n, n, esize, v))
             r[vname] = summary(ms, 2 * n * n * esize)
+            r[vname]["flushed_median_20"] = flushed_median(
+                lambda: swz.swz_transpose(d_, s_, n, n, esize, v), 2 * n * n * esize)
             r[vname]["bank_model_ways"] = {acc: ways_model[(esize, v, acc)]
                                            for (e_, v_, acc) in pat_keys if e_ == esize and v_ == v}
         out[name] = r
