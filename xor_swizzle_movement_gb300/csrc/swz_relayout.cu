@@ -186,13 +186,25 @@ __device__ __forceinline__ uint32_t sw_inv32(uint32_t y, int B, int M, int S, in
 template <int E>
 __global__ void __launch_bounds__(256)
     relayout_staged_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes, int block_bytes, uint32_t te,
-                           uint32_t te_recip, int B, int M, int S, int steps) {
+                           uint32_t te_recip, uint32_t pat, uint32_t pat_recip, int B, int M, int S,
+                           int steps) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     using T = typename ElemType<E>::T;
     constexpr int V = 16 / E;  // elements per output vector
     __shared__ __align__(16) uint8_t a_s[kStageBytes];
+    // Source of each element of an output vector, relative to the vector's
+    // first element.  Blocks start on multiples of lcm(tile bytes, 16), so the
+    // pattern repeats every `pat` vectors; it is computed once per CTA.
+    __shared__ __align__(16) int16_t rel_s[kStageBytes / E];
     const int tid = threadIdx.x;
+    auto local_of = [&](uint32_t e) -> uint32_t { return te == 1 ? 0u : e - __umulhi(e, te_recip) * te; };
+    for (uint32_t i = tid; i < pat * V; i += 256) {
+        const uint32_t local = local_of(i);
+        rel_s[i] = static_cast<int16_t>(static_cast<int>(i - local + sw_inv32(local, B, M, S, steps)) -
+                                        static_cast<int>(i));
+    }
+    __syncthreads();
     for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * block_bytes; b0 < bytes;
          b0 += static_cast<int64_t>(gridDim.x) * block_bytes) {
         const int nb = static_cast<int>(bytes - b0 < block_bytes ? bytes - b0 : block_bytes);
@@ -201,20 +213,15 @@ __global__ void __launch_bounds__(256)
             *reinterpret_cast<uint4 *>(a_s + 16 * v) = ld_stream16(src + b0 + 16 * v);
         for (int t = 16 * nv + tid; t < nb; t += 256) a_s[t] = src[b0 + t];
         __syncthreads();
-        auto local_of = [&](uint32_t e) -> uint32_t { return te == 1 ? 0u : e - __umulhi(e, te_recip) * te; };
         for (int v = tid; v < nv; v += 256) {
-            uint32_t e = static_cast<uint32_t>(v) * V;
-            uint32_t local = local_of(e), tile0 = e - local;
+            const uint32_t e = static_cast<uint32_t>(v) * V;
+            const uint32_t p = pat == 1 ? 0u : static_cast<uint32_t>(v) - __umulhi(static_cast<uint32_t>(v), pat_recip) * pat;
+            int16_t rel[V];
+            memcpy(rel, rel_s + p * V, sizeof rel);
             T lanes[V];
 #pragma unroll
-            for (int k = 0; k < V; ++k) {
-                const uint32_t x = sw_inv32(local, B, M, S, steps);
-                lanes[k] = *reinterpret_cast<const T *>(a_s + (tile0 + x) * E);
-                if (++local == te) {
-                    local = 0;
-                    tile0 += te;
-                }
-            }
+            for (int k = 0; k < V; ++k)
+                lanes[k] = *reinterpret_cast<const T *>(a_s + (static_cast<int>(e + k) + rel[k]) * E);
             uint4 o;
             memcpy(&o, lanes, 16);
             st_stream16(dst + b0 + 16 * v, o);
@@ -239,9 +246,14 @@ swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_by
     // staged offsets are below kStageBytes <= 2^16: a read field at or above
     // bit 16 is all zero there, and the swizzle is the identity
     if (M + S >= 16) { B = 0; M = 0; S = 1; steps = 1; }
+    // the source pattern of output vectors repeats every lcm(tile bytes, 16) bytes
+    int64_t g = te * E, h = 16;
+    while (h) { const int64_t r = g % h; g = h; h = r; }
+    const uint32_t pat = static_cast<uint32_t>(te * E / g);  // lcm / 16 vectors
+    const uint32_t pat_recip = pat == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / pat + 1);
     return launched(launch_pdl(relayout_staged_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
                                static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), bytes, block_bytes,
-                               te, recip, B, M, S, steps));
+                               te, recip, pat, pat_recip, B, M, S, steps));
 }
 
 template <int E>
