@@ -247,6 +247,13 @@ def test_transpose_relayout_composes(orc):
         off = c * 24 + r
         tile, loc = divmod(off, te)
         assert got[tile * te + orc.swizzle(loc, B=3, M=0, S=3)] == a[r, c]
+    # a swizzle that is not its own inverse (S < B): the forward relayout puts
+    # every element at sw(offset), which the inverse would not
+    got1 = orc.transpose_relayout(a, tile_elems=te, B=3, M=0, S=1)
+    for r in range(24):
+        for c in range(40):
+            tile, loc = divmod(c * 24 + r, te)
+            assert got1[tile * te + orc.swizzle(loc, B=3, M=0, S=1)] == a[r, c]
 
 
 # ------------------------------------------------------------- bank model ---

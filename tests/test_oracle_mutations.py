@@ -43,6 +43,12 @@ MUTATIONS = [
      "for (k = 0; k < n_words; ++k)\n                        if (words[k] == wd)\n                            seen = 1;",
      "(void)seen;"),
     ("wavefronts = worst pass", "total += cost;", "total = worst;"),
+    ("fused: relayout before the transpose",
+     "rc = orc_transpose(tmp, src, rows, cols, esize);\n    if (rc != ORC_OK)\n        return rc;\n    return orc_relayout(dst, tmp, (rows * cols) / tile_elems, tile_elems, esize, base, bits, shift, 0);",
+     "rc = orc_relayout(tmp, src, (rows * cols) / tile_elems, tile_elems, esize, base, bits, shift, 0);\n    if (rc != ORC_OK)\n        return rc;\n    return orc_transpose(dst, tmp, rows, cols, esize);"),
+    ("fused: inverse relayout",
+     "return orc_relayout(dst, tmp, (rows * cols) / tile_elems, tile_elems, esize, base, bits, shift, 0);",
+     "return orc_relayout(dst, tmp, (rows * cols) / tile_elems, tile_elems, esize, base, bits, shift, 1);"),
     ("collision keeps A & sw(A)", "return A & ~orc_swizzle(A, base, bits, shift);",
      "return A & orc_swizzle(A, base, bits, shift);"),
 ]
@@ -64,6 +70,7 @@ def battery(orc):
         ("relayout_tile_local", lambda: pins.test_relayout_tile_local(orc, 48)),
         ("relayout_usage_loop", lambda: pins.test_relayout_usage_loop(orc)),
         ("transpose_small", lambda: pins.test_transpose_small(orc)),
+        ("transpose_relayout", lambda: pins.test_transpose_relayout_composes(orc)),
         ("bank_column", lambda: pins.test_bank_column_fp32(orc)),
         ("bank_padding_xor", lambda: pins.test_bank_padding_and_xor(orc)),
         ("bank_fp16", lambda: pins.test_bank_fp16_64_columns(orc)),
@@ -91,10 +98,29 @@ def test_unmodified_copy_passes(tmp_path):
     assert battery(orc) == []
 
 
+_CHILD = """
+import json, sys
+sys.path[:0] = [{tests!r}, {root!r}]
+import oracle, test_oracle_mutations as tm
+print(json.dumps(tm.battery(oracle.Oracle({lib!r}))))
+"""
+
+
 @pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
 def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    """The battery runs on the mutated copy in a child process: a mistake
+    that writes out of bounds may crash it, and a crash counts as caught."""
+    import json
+    import os
+    import subprocess
+    import sys
     src = oracle.c_source()
     assert src.count(old) == 1, name
-    orc = oracle.Oracle(oracle.compile_copy(src.replace(old, new), str(tmp_path)))
-    failed = battery(orc)
+    lib = oracle.compile_copy(src.replace(old, new), str(tmp_path))
+    tests = os.path.dirname(os.path.abspath(__file__))
+    code = _CHILD.format(tests=tests, root=os.path.dirname(tests), lib=lib)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return  # the planted mistake crashed the pins: caught
+    failed = json.loads(r.stdout.strip().splitlines()[-1])
     assert failed, f"no pin caught: {name}"
