@@ -94,10 +94,16 @@ def peaks():
 
 
 def source_hash(*names) -> str:
+    """Hash of the code in the named sources, comments and blank space
+    removed: a comment edit does not make a committed ncu record stale."""
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "xor_swizzle_movement_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "xor_swizzle_movement_gb300", "csrc", n), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -90,3 +90,17 @@ def test_cpu_baseline_single_and_all_cores():
         "relayout_fp16_64x64_sw333_2MiB", "relayout_int8_64x128_sw525", "transpose_fp32_8192",
         "transpose_fp16_16384", "transpose_fp64_8192"}
     assert all(v["single_thread_GB/s"] > 0 and v["all_cores_GB/s"] > 0 for v in res["other_rows"].values())
+
+
+def test_source_hash_ignores_comments(tmp_path, monkeypatch):
+    """A comment edit keeps a committed ncu record valid; a code edit does not."""
+    csrc = tmp_path / "xor_swizzle_movement_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    f = csrc / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f.write_text("// header\n__global__ void k(int *p) {\n    p[0] = 1;  /* store */\n}\n")
+    h0 = bench.source_hash("k.cu")
+    f.write_text("// another header\n/* a block\n comment */\n__global__ void k(int *p) {\n    p[0] = 1;\n}\n")
+    assert bench.source_hash("k.cu") == h0
+    f.write_text("__global__ void k(int *p) {\n    p[0] = 2;\n}\n")
+    assert bench.source_hash("k.cu") != h0

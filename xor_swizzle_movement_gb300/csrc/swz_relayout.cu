@@ -31,6 +31,14 @@
 //                 applies the fixed permutation L as a byte permutation of the
 //                 16-byte vector: three prmt per output word with selectors the
 //                 host computes once per launch.
+//
+// Other requests (relayout_launch picks the path):
+//   tiles of 1-8 bytes that divide 16: every vector holds whole tiles, so the
+//     same kernel runs with the identity at vector level and one fixed lane map;
+//   other tiles that are not whole 16-byte vectors, aligned pointers: the
+//     staged kernel (blocks of whole tiles in shared memory, 16-byte output
+//     vectors gathered through a per-CTA table of their sources);
+//   pointers that are not 16-byte aligned: element by element.
 #include "swz_common.cuh"
 
 #include <cstring>
