@@ -84,7 +84,7 @@ def test_k_major_operand_tiles(swz, orc):
     assert np.array_equal(two.cpu().numpy().view(np.uint16), got)
 
 
-@pytest.mark.parametrize("esize", [2, 4, 8])
+@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
 def test_misaligned(swz, orc, esize):
     from xor_swizzle_movement_gb300 import inputs
     rows, cols = 64, 128
