@@ -32,23 +32,30 @@ BMS = [(3, 4, 3), (3, 3, 3), (5, 0, 5), (2, 1, 3), (3, 0, 1), (4, 1, 2), (0, 0, 
 SHAPES = [(64, 128), (128, 64), (96, 160), (200, 136), (48, 256)]
 
 
-@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("B,M,S", BMS)
-@pytest.mark.parametrize("shape", SHAPES)
-def test_matches_oracle(swz, orc, esize, B, M, S, shape):
-    from xor_swizzle_movement_gb300 import inputs
-    rows, cols = shape
+def tile_for(rows, cols, B, M):
+    """Relayout tiles of whole rows of the transposed matrix where they close
+    under the swizzle, else the smallest closed multiple that divides the
+    matrix; None when the matrix cannot be cut into closed tiles that way."""
     n = rows * cols
-    # relayout tiles: whole rows of the transposed matrix where they close under the swizzle,
-    # else the smallest closed multiple that divides the matrix
-    te = None
     for k in (8, 4, 2, 1, 16, 32, 64):
         cand = k * rows
         if n % cand == 0 and cand % (1 << (M + B)) == 0:
-            te = cand
-            break
-    if te is None:
-        pytest.skip("no tile size closes under this swizzle for this shape")
+            return cand
+    return None
+
+
+# only the (swizzle, shape) pairs whose matrix splits into closed tiles
+CASES = [(bms, shape) for bms in BMS for shape in SHAPES if tile_for(*shape, bms[0], bms[1]) is not None]
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("bms,shape", CASES)
+def test_matches_oracle(swz, orc, esize, bms, shape):
+    from xor_swizzle_movement_gb300 import inputs
+    B, M, S = bms
+    rows, cols = shape
+    n = rows * cols
+    te = tile_for(rows, cols, B, M)
     host = inputs.random_bytes(n * esize, seed=14).view(void_dtype(esize)).reshape(rows, cols)
     got = run(swz, host, esize, te, B, M, S)
     want = orc.transpose_relayout(host, tile_elems=te, B=B, M=M, S=S)
