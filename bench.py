@@ -957,67 +957,72 @@ def main():
                 "isolated_ms": {"forward": round(fwd_iso, 4), "inverse": round(inv_iso, 4),
                                 "note": "events around each launch, outside the timed region"}}
 
-    # end to end from pinned host buffers: the step's input is copied in and its
-    # result copied out inside the timed region.  The tiles go in 8 chunks over
-    # three streams (copy in / relayout forward+inverse / copy out), so the two
-    # copy directions and the kernels overlap; each chunk waits only for its
-    # own buffers.
-    out_host = torch.empty_like(host_t).pin_memory()
-    n_chunks = 8
+    # end to end from pinned host buffers: every step copies its input in and
+    # its result out inside the timed region.  A step's tiles go in 4 chunks
+    # over three streams (copy in / relayout forward+inverse / copy out), so
+    # the two copy directions and the kernels overlap; each chunk waits only
+    # for its own buffers.  Consecutive steps alternate between two buffer
+    # sets, and 8 steps form one CUDA graph, so a step's copies start while the
+    # previous step's tail is still in flight.  (Host memory is reached at
+    # about 200 GB/s per direction here, about 300 GB/s with both at once; one
+    # step per graph with 8 chunks ran at 516 GB/s, this at about 600.)
+    n_chunks, per_graph = 4, 8
     ct = TILES // n_chunks
     ce = ct * ROWS * COLS
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    # (host memory is reached at ~200 GB/s per direction here, by copy engines and by
-    # SM loads alike; 8 chunks beat 4 and 16)
-    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
-    ev_run = [torch.cuda.Event() for _ in range(n_chunks)]
-    ev_out = [torch.cuda.Event() for _ in range(n_chunks)]
-    d_in = torch.empty_like(src)
+    buf_sets = [(torch.empty_like(src), phys, back),
+                (torch.empty_like(src), torch.empty_like(src), torch.empty_like(src))]
+    out_hosts = [torch.empty_like(host_t).pin_memory() for _ in range(2)]
+    ev = {key: [[torch.cuda.Event() for _ in range(n_chunks)] for _ in range(per_graph)]
+          for key in ("in", "run", "out")}
 
-    def e2e_step(capturing=False):
-        for c in range(n_chunks):
-            sl = slice(c * ce, (c + 1) * ce)
-            if not capturing:
-                s_in.wait_event(ev_run[c])      # previous step's relayout of this chunk read d_in
-            with torch.cuda.stream(s_in):
-                d_in[sl].copy_(host_t[sl], non_blocking=True)
-                ev_in[c].record(s_in)
-            s_run.wait_event(ev_in[c])
-            if not capturing:
-                s_run.wait_event(ev_out[c])     # previous step's copy-out of this chunk read back
-            with torch.cuda.stream(s_run):
-                swz.swz_relayout(phys[sl], d_in[sl], ct, ROWS, COLS, ESIZE, B, M, S, 0, stream=s_run)
-                swz.swz_relayout(back[sl], phys[sl], ct, ROWS, COLS, ESIZE, B, M, S, 1, stream=s_run)
-                ev_run[c].record(s_run)
-            s_out.wait_event(ev_run[c])
-            with torch.cuda.stream(s_out):
-                out_host[sl].copy_(back[sl], non_blocking=True)
-                ev_out[c].record(s_out)
+    def e2e_steps_enqueue():
+        for k in range(per_graph):
+            d_in_k, phys_k, back_k = buf_sets[k % 2]
+            out_k = out_hosts[k % 2]
+            for c in range(n_chunks):
+                sl = slice(c * ce, (c + 1) * ce)
+                if k >= 2:
+                    s_in.wait_event(ev["run"][k - 2][c])   # that step's relayout has read d_in
+                with torch.cuda.stream(s_in):
+                    d_in_k[sl].copy_(host_t[sl], non_blocking=True)
+                    ev["in"][k][c].record(s_in)
+                s_run.wait_event(ev["in"][k][c])
+                if k >= 2:
+                    s_run.wait_event(ev["out"][k - 2][c])  # that step's copy-out has read back
+                with torch.cuda.stream(s_run):
+                    swz.swz_relayout(phys_k[sl], d_in_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 0, stream=s_run)
+                    swz.swz_relayout(back_k[sl], phys_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 1, stream=s_run)
+                    ev["run"][k][c].record(s_run)
+                s_out.wait_event(ev["run"][k][c])
+                with torch.cuda.stream(s_out):
+                    out_k[sl].copy_(back_k[sl], non_blocking=True)
+                    ev["out"][k][c].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    # the whole pipelined step as one CUDA graph: one launch per step instead of
-    # ~60 host-side calls, so the host never limits the copy engines
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
     with torch.cuda.graph(graph, stream=cap):
         for s_ in (s_in, s_run, s_out):
             s_.wait_stream(cap)
-        e2e_step(capturing=True)
+        e2e_steps_enqueue()
         for s_ in (s_in, s_run, s_out):
             cap.wait_stream(s_)
-    out_host.zero_()
-    e2e_steps = max(10, min(100, args.steps // 20))
-    for _ in range(3):
+    for o in out_hosts:
+        o.zero_()
+    replays = -(-max(10, min(100, args.steps // 20)) // per_graph)
+    for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    for _ in range(replays):
         graph.replay()
     torch.cuda.synchronize()
+    e2e_steps = replays * per_graph
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    assert torch.equal(out_host, host_t), "end-to-end round trip failed"
+    for o in out_hosts:
+        assert torch.equal(o, host_t), "end-to-end round trip failed"
+    d_in, out_host = buf_sets[1][0], out_hosts[0]
     # the copy rates alone, for context
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -1033,6 +1038,7 @@ def main():
     e2e = {"value": round(STEP_BYTES / e2e_s / GB, 1), "unit": "GB/s",
            "h2d_bytes_per_step": n_el * ESIZE, "d2h_bytes_per_step": n_el * ESIZE,
            "ms_per_step": round(e2e_s * 1e3, 4), "chunks": n_chunks, "cuda_graph": True,
+           "steps_per_graph": per_graph, "buffer_sets": 2, "steps": e2e_steps,
            "copy_GB/s": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1)}}
 
     rows = None
