@@ -366,9 +366,18 @@ __global__ void __launch_bounds__(256)
     const int64_t tc = static_cast<int64_t>(blockIdx.x) - tr * tiles_c;
     const int64_t r0 = tr * N, c0 = tc * N;
     auto phys = [](int ir, int ic) -> int { return VARIANT == SWZ_T_SWIZZLED ? (ic ^ ir) : ic; };
-    for (int idx = threadIdx.x; idx < N * N; idx += 256) {
-        const int row = idx >> 5, cl = idx & 31;
-        if (r0 + row < R && c0 + cl < C) sm[row * P + phys(row, cl)] = src[(r0 + row) * C + c0 + cl];
+    // all loads first: each thread keeps its elements of the tile in flight
+    constexpr int EI = N * N / 256;
+    T ev[EI];
+#pragma unroll
+    for (int k = 0; k < EI; ++k) {
+        const int idx = k * 256 + threadIdx.x, row = idx >> 5, cl = idx & 31;
+        if (r0 + row < R && c0 + cl < C) ev[k] = src[(r0 + row) * C + c0 + cl];
+    }
+#pragma unroll
+    for (int k = 0; k < EI; ++k) {
+        const int idx = k * 256 + threadIdx.x, row = idx >> 5, cl = idx & 31;
+        if (r0 + row < R && c0 + cl < C) sm[row * P + phys(row, cl)] = ev[k];
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < N * N; idx += 256) {
