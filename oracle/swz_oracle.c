@@ -13,9 +13,10 @@
  *   [P2] "CuTe Swizzle 学习手册" -- bank structure, conflict rules,
  *        "Swizzle 数学公式".
  *   [P3] "cutlass 入门" -- "swizzle 融入 layout 优化" (slice collision).
- *   [P4] "CUDA 013 - Swizzle 的工作原理" -- "计算公式" (the base/bits/shift
- *        function), "更通用的映射规则" (offset-based rule, worked example),
- *        "什么是 Bank Conflict".
+ *   [P4] "CUDA 013 - Swizzle 的工作原理" -- "CuTe 通用 swizzle 映射规则解析"
+ *        (the Z and Y fields, AA = ZZ xor YY), "计算公式" (the names base,
+ *        bits, shift), "更通用的映射规则" (offset-based rule, worked
+ *        example), "什么是 Bank Conflict".
  *
  * Parity status per function (what pins it is listed in the test suite):
  *   orc_swizzle            pinned (worked example, 2-D closed forms, bit diagrams)
@@ -39,25 +40,40 @@
 #define ORC_BAD_ARG 1
 #define ORC_NOT_CLOSED 2
 
+/* Bit p of v (0 beyond the 64 bits of an offset). */
+static int orc_bit(uint64_t v, int p)
+{
+    if (p < 0 || p >= 64)
+        return 0;
+    return (int)((v >> p) & 1u);
+}
+
 /*
- * [P4] "计算公式": the function is parameterised by base (low bits kept as
- * they are), bits (width of the two fields) and shift (distance between the
- * fields).  The zz field starts at bit `base`, the yy field at bit
- * `base + shift`; aa = zz ^ yy replaces zz, every other bit is kept.
- * Written in the clear-then-set form of that section.
+ * The swizzle of one offset, bit by bit, as [P1]'s bit diagram and
+ * [P4] "CuTe 通用 swizzle 映射规则解析" define it: the lowest `base` bits
+ * take no part; a field Z of `bits` bits starts at bit `base`, a field Y of
+ * the same width starts `shift` bits above it; in the result, bit i of Z
+ * becomes (bit i of Z) xor (bit i of Y), and every bit outside Z is the
+ * input's.  The output is built one bit at a time from the input, so no
+ * written bit feeds a later read.
  */
 uint64_t orc_swizzle(uint64_t offset, int base, int bits, int shift)
 {
-    uint64_t bits_mask, zz, yy, aa;
-    if (bits <= 0)
-        return offset;
-    bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << bits) - 1);
-    zz = (offset >> base) & bits_mask;
-    yy = (offset >> (base + shift)) & bits_mask;
-    aa = zz ^ yy;
-    offset = offset & ~(bits_mask << base); /* clear the zz field */
-    offset = offset | (aa << base);         /* set the aa field */
-    return offset;
+    uint64_t out = offset;
+    int i;
+    for (i = 0; i < bits; ++i) {
+        int zpos = base + i;
+        int ypos = base + shift + i;
+        int v;
+        if (zpos >= 64)
+            break;
+        v = orc_bit(offset, zpos) ^ orc_bit(offset, ypos);
+        if (v)
+            out |= (uint64_t)1 << zpos;
+        else
+            out &= ~((uint64_t)1 << zpos);
+    }
+    return out;
 }
 
 /*

@@ -12,17 +12,14 @@ import oracle
 import test_oracle as pins
 
 MUTATIONS = [
-    ("yy field one bit too high", "yy = (offset >> (base + shift)) & bits_mask;",
-     "yy = (offset >> (base + shift + 1)) & bits_mask;"),
-    ("yy field one bit too low", "yy = (offset >> (base + shift)) & bits_mask;",
-     "yy = (offset >> (base + shift - 1)) & bits_mask;"),
-    ("mask one bit short", "bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << bits) - 1);",
-     "bits_mask = (bits >= 64) ? ~(uint64_t)0 : (((uint64_t)1 << (bits - 1)) - 1);"),
-    ("OR instead of XOR", "aa = zz ^ yy;", "aa = zz | yy;"),
-    ("z field not cleared", "offset = offset & ~(bits_mask << base); /* clear the zz field */",
-     "offset = offset; /* clear the zz field */"),
-    ("aa written one bit off", "offset = offset | (aa << base);         /* set the aa field */",
-     "offset = offset | (aa << (base + 1));   /* set the aa field */"),
+    ("y field one bit too high", "int ypos = base + shift + i;", "int ypos = base + shift + 1 + i;"),
+    ("y field one bit too low", "int ypos = base + shift + i;", "int ypos = base + shift - 1 + i;"),
+    ("z field one bit too high", "int zpos = base + i;", "int zpos = base + 1 + i;"),
+    ("field one bit short", "for (i = 0; i < bits; ++i) {", "for (i = 0; i < bits - 1; ++i) {"),
+    ("OR instead of XOR", "v = orc_bit(offset, zpos) ^ orc_bit(offset, ypos);",
+     "v = orc_bit(offset, zpos) | orc_bit(offset, ypos);"),
+    ("z bit never cleared", "out &= ~((uint64_t)1 << zpos);", "out = out;"),
+    ("set bit written one place up", "out |= (uint64_t)1 << zpos;", "out |= (uint64_t)1 << (zpos + 1);"),
     ("relayout forward as a gather",
      "memcpy(d + (size_t)(tile0 + (int64_t)j) * esize,\n                       s + (size_t)(tile0 + i) * esize, (size_t)esize);",
      "memcpy(d + (size_t)(tile0 + i) * esize,\n                       s + (size_t)(tile0 + (int64_t)j) * esize, (size_t)esize);"),
