@@ -276,19 +276,25 @@ swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, in
  * allocating routine.
  *
  * Computes the same result as swz_transpose(dst, src, rows, cols, 2,
- * SWZ_T_TMA, stream): out[c][r] = in[r][c] for 16-bit elements (raw bits),
- * through the same kernel, with the same fallback to the shared-memory-staged
- * swizzled kernel when src is not 16-byte aligned or cols is not a multiple
- * of 8.
+ * SWZ_T_TMA, stream): out[c][r] = in[r][c] for 16-bit elements (raw bits).
+ * It always runs the TMA-loaded kernel that stores with 16-byte stores
+ * (tensor loads under the hardware 128-byte swizzle, conflict-free
+ * transposing matrix reads); SWZ_T_TMA runs that kernel too, except when dst
+ * is 16-byte aligned and rows is a multiple of 8, where it also stores
+ * through a tensor map.  The two calls can differ in speed, never in result.
+ * Both fall back to the shared-memory-staged swizzled kernel when src is not
+ * 16-byte aligned or cols is not a multiple of 8.
  *
  * dst, src  : device buffers of rows x cols 2-byte elements (caller-owned).
  * rows, cols: 0 <= rows, cols < 2^31 (the TMA coordinate range); larger
  *             requests are refused with SWZ_ERR_SHAPE.  The call needs one
  *             4-byte status word of the array for any matrix size.
  * timed_out : optional host pointer.  NULL: the call returns once the work
- *             is enqueued.  Non-NULL: the call waits for `stream`, stores 1
- *             if one of the kernel's bounded waits gave up (dst is then
- *             incomplete and SWZ_ERR_TIMEOUT is returned), 0 otherwise.
+ *             is enqueued, and a bounded wait that gives up goes unreported
+ *             (dst is then incomplete; the next call clears the status
+ *             word).  Non-NULL: the call waits for `stream`, stores 1 if one
+ *             of the kernel's bounded waits gave up (dst is then incomplete
+ *             and SWZ_ERR_TIMEOUT is returned), 0 otherwise.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, once per device, with that device current); make
@@ -301,6 +307,19 @@ swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, in
  */
 swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
                                      uint32_t *timed_out, void *stream);
+
+/*
+ * Self-test of swz_transpose_tma_noalloc's timeout report: the same call with
+ * no tensor copy issued, so each bounded wait of its kernel gives up after
+ * wait_ns nanoseconds and the kernel records the expiry in the fixed array's
+ * status word and returns without writing dst.  Waits for `stream`; stores 1
+ * in *timed_out and returns SWZ_ERR_TIMEOUT when the expiry was reported.
+ * rows, cols > 0, cols a multiple of 8, src 16-byte aligned (SWZ_ERR_SHAPE,
+ * SWZ_ERR_ALIGN); timed_out must not be NULL (SWZ_ERR_NULL).  Allocates
+ * nothing.  Host function that launches one kernel.
+ */
+swz_status swz_selftest_noalloc_timeout(void *dst, const void *src, int64_t rows, int64_t cols,
+                                        uint64_t wait_ns, uint32_t *timed_out, void *stream);
 
 /*
  * Text map of a swizzled tile, the counterpart of CuTe's print_layout

@@ -19,7 +19,7 @@ __all__ = [
     "SwzError", "lib", "library_path",
     "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_slice_layout", "swz_layout_text", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
-    "swz_transpose_tma_noalloc",
+    "swz_transpose_tma_noalloc", "swz_selftest_noalloc_timeout",
     "swz_status_string", "swz_version",
     "SWZ_OK", "SWZ_ERR_NULL", "SWZ_ERR_PARAM", "SWZ_ERR_SHAPE", "SWZ_ERR_ALIGN", "SWZ_ERR_ALIAS",
     "SWZ_ERR_CUDA", "SWZ_ERR_TIMEOUT", "SWZ_ERR_UNSUPPORTED",
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
         L.swz_selftest_tma_timeout.restype = i32
         L.swz_transpose_tma_noalloc.argtypes = [vp, vp, i64, i64, ctypes.POINTER(ctypes.c_uint32), vp]
         L.swz_transpose_tma_noalloc.restype = i32
+        L.swz_selftest_noalloc_timeout.argtypes = [vp, vp, i64, i64, u64, ctypes.POINTER(ctypes.c_uint32), vp]
+        L.swz_selftest_noalloc_timeout.restype = i32
         L.swz_status_string.argtypes = [i32]
         L.swz_status_string.restype = ctypes.c_char_p
         L.swz_version.argtypes = []
@@ -222,6 +224,17 @@ def swz_transpose_tma_noalloc(dst, src, rows: int, cols: int, wait: bool = False
         return 1
     _check(status, "swz_transpose_tma_noalloc")
     return int(flag.value)
+
+
+def swz_selftest_noalloc_timeout(dst, src, rows: int, cols: int, wait_ns: int, stream=None) -> int:
+    """Runs swz_transpose_tma_noalloc's kernel with no copy issued; returns the
+    timed_out flag (1 when the expiry was reported) and the status code."""
+    flag = ctypes.c_uint32(0)
+    status = lib().swz_selftest_noalloc_timeout(_ptr(dst), _ptr(src), rows, cols, wait_ns, ctypes.byref(flag),
+                                                _stream(stream))
+    if status != SWZ_ERR_TIMEOUT:
+        _check(status, "swz_selftest_noalloc_timeout")
+    return int(flag.value), int(status)
 
 
 def swz_status_string(status: int) -> str:

@@ -2,6 +2,7 @@
 // dispatch to the kernels, status codes.  Nothing here allocates memory.
 #include "swz_common.cuh"
 
+#include <atomic>
 #include <cstdio>
 
 namespace swz {
@@ -30,6 +31,30 @@ swz_status launched(cudaError_t launch_result) {
         return SWZ_ERR_CUDA;
     }
     return launch_status();
+}
+
+// Streaming multiprocessors of the current device, queried once per device
+// and cached (launch geometry is sized in multiples of it).  Returns 1 if the
+// query fails; the launch that follows then reports the error.
+int sm_count() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes) {

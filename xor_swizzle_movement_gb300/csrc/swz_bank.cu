@@ -141,7 +141,8 @@ __global__ void slice_collision_kernel(const uint64_t *__restrict__ A, int64_t n
 swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, int64_t n, int width,
                                int32_t *ways, int32_t *wavefronts, cudaStream_t st) {
     int64_t grid = (n + kWarpsPerCta - 1) / kWarpsPerCta;
-    if (grid > 152LL * 64) grid = 152LL * 64;  // grid-stride beyond 64 CTAs per SM
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 64;  // grid-stride beyond 64 CTAs per SM
+    if (grid > cap) grid = cap;
     const unsigned g = static_cast<unsigned>(grid);
     cudaError_t e;
     switch (width) {
@@ -158,7 +159,8 @@ swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, in
 swz_status slice_collision_launch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
                                   cudaStream_t st) {
     int64_t grid = (n + 255) / 256;
-    if (grid > 152LL * 16) grid = 152LL * 16;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+    if (grid > cap) grid = cap;
     return launched(launch_pdl(slice_collision_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, A, n, B, M,
                                S, C));
 }

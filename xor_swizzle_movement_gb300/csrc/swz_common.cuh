@@ -175,4 +175,5 @@ namespace swz {
 swz_status launch_status();
 swz_status launched(cudaError_t launch_result);  // status of a launch_pdl call
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes);
+int sm_count();  // SMs of the current device (cached per device)
 }  // namespace swz

@@ -248,7 +248,8 @@ template <int E>
 swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_bytes, int64_t tile_elems, int B,
                          int M, int S, int steps, cudaStream_t st) {
     int64_t grid = (bytes + block_bytes - 1) / block_bytes;
-    if (grid > 152LL * 8) grid = 152LL * 8;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+    if (grid > cap) grid = cap;
     const uint32_t te = static_cast<uint32_t>(tile_elems);
     const uint32_t recip = te == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / te + 1);
     // staged offsets are below kStageBytes <= 2^16: a read field at or above
@@ -269,7 +270,8 @@ swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, in
                          int steps, cudaStream_t st) {
     const int threads = 256;
     int64_t grid = (n + threads - 1) / threads;
-    if (grid > 152LL * 32) grid = 152LL * 32;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 32;
+    if (grid > cap) grid = cap;
     const int period = B + M + S;
     const bool local = B > 0 && (period >= 62 || (tile & ((int64_t(1) << period) - 1)) != 0);
     const dim3 g(static_cast<unsigned>(grid));
@@ -305,7 +307,7 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         a.tile_vecs = 1;
         a.B = 0; a.M = 0; a.S = 1;
         a.steps = 1;
-        const int64_t wave = 152LL * 2048;
+        const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
         lane_map_selectors(src_lane, esize, a.perm_sel);
         switch (esize) {
@@ -347,8 +349,8 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         a.B = B; a.M = M; a.S = S;
         a.steps = steps;
         // keep each SM fed: up to four vectors per thread once the grid is
-        // several waves deep (152 SMs x 2048 threads per wave)
-        const int64_t wave = 152LL * 2048;
+        // several waves deep (every SM x 2048 threads per wave)
+        const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
         // kLanesGeneral: out lane l = (lanes XOR-ed by k)[L(l)], L(l) = g(l) for a lane index l
         int src_lane[16];

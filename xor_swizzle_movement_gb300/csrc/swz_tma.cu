@@ -331,7 +331,7 @@ swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, c
     a.issue_copies = issue_copies;
     a.wait_ns = wait_ns;
     a.status = status;
-    int grid = 152 * 4;
+    int grid = sm_count() * 4;
     if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
     if (a.vec_store_ok) {
         // the output (C x R, rows of R elements) also goes out through a tensor map
@@ -418,15 +418,20 @@ uint32_t *noalloc_scratch(int dev) {
 }  // namespace
 }  // namespace swz
 
-extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
-                                                uint32_t *timed_out, void *stream) {
-    using namespace swz;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace swz {
+namespace {
+
+// The allocation-free call; issue_copies = 0 and a short wait_ns only in its
+// timeout self-test (no copy is issued, so every bounded wait expires).
+swz_status noalloc_run(void *dst, const void *src, int64_t rows, int64_t cols, uint32_t *timed_out,
+                       cudaStream_t st, int issue_copies, uint64_t wait_ns) {
     if (timed_out) *timed_out = 0;
     if (rows < 0 || cols < 0) return SWZ_ERR_SHAPE;
     // the largest request: TMA coordinates are 32-bit
     if (rows >= (1LL << 31) || cols >= (1LL << 31)) return SWZ_ERR_SHAPE;
     if (rows == 0 || cols == 0) return SWZ_OK;
+    // rows * cols * 2 stays below 2^63 for rows, cols < 2^31; checked all the same
+    if (rows > INT64_MAX / 2 / cols) return SWZ_ERR_SHAPE;
     if (!dst || !src) return SWZ_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 1u) return SWZ_ERR_ALIGN;
     const int64_t n_bytes = rows * cols * 2;
@@ -435,6 +440,7 @@ extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int6
     EncodeTiledFn encode = encode_fn();
     const bool tma_ok = encode && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (cols % 8) == 0;
     if (!tma_ok) {
+        if (!issue_copies) return encode ? SWZ_ERR_SHAPE : SWZ_ERR_CUDA;  // the self-test needs the TMA kernel
         // same fallback as SWZ_T_TMA: the shared-memory-staged swizzled kernel, no scratch
         const swz_status s = transpose_launch(dst, src, rows, cols, 2, SWZ_T_SWIZZLED, st);
         if (s == SWZ_OK && timed_out && cudaStreamSynchronize(st) != cudaSuccess) return SWZ_ERR_CUDA;
@@ -464,10 +470,10 @@ extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int6
     a.tiles_c = (cols + kTile - 1) / kTile;
     a.n_tiles = ((rows + kTile - 1) / kTile) * a.tiles_c;
     a.vec_store_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (rows % 8 == 0);
-    a.issue_copies = 1;
-    a.wait_ns = kWaitLimitNs;
+    a.issue_copies = issue_copies;
+    a.wait_ns = wait_ns;
     a.status = scratch;
-    int grid = 152 * 4;
+    int grid = sm_count() * 4;
     if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
     transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
     const swz_status s = launch_status();
@@ -481,4 +487,25 @@ extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int6
         return SWZ_ERR_TIMEOUT;
     }
     return SWZ_OK;
+}
+
+}  // namespace
+}  // namespace swz
+
+extern "C" swz_status swz_transpose_tma_noalloc(void *dst, const void *src, int64_t rows, int64_t cols,
+                                                uint32_t *timed_out, void *stream) {
+    return swz::noalloc_run(dst, src, rows, cols, timed_out, static_cast<cudaStream_t>(stream), 1,
+                            swz::kWaitLimitNs);
+}
+
+// Self-test of the allocation-free call's timeout report: the same call with
+// no tensor copy issued, so every bounded wait gives up after wait_ns and the
+// kernel records the expiry in the fixed array's status word.
+extern "C" swz_status swz_selftest_noalloc_timeout(void *dst, const void *src, int64_t rows, int64_t cols,
+                                                   uint64_t wait_ns, uint32_t *timed_out, void *stream) {
+    if (!timed_out) return SWZ_ERR_NULL;
+    if (!dst || !src) return SWZ_ERR_NULL;
+    if (rows <= 0 || cols <= 0 || cols % 8 != 0) return SWZ_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) return SWZ_ERR_ALIGN;
+    return swz::noalloc_run(dst, src, rows, cols, timed_out, static_cast<cudaStream_t>(stream), 0, wait_ns);
 }

@@ -206,7 +206,7 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     a.rows_per_chunk = static_cast<int>(kChunk / span);
     a.wait_ns = kWaitLimitNs;
     a.status = status;
-    int64_t grid = 152LL * (direction == 0 ? kFwdCtasPerSm : kInvCtasPerSm);
+    int64_t grid = static_cast<int64_t>(sm_count()) * (direction == 0 ? kFwdCtasPerSm : kInvCtasPerSm);
     if (a.n_chunks < grid) grid = a.n_chunks;
     const dim3 g(static_cast<unsigned>(grid));
     if (direction == 0)
