@@ -1,36 +1,42 @@
 #!/usr/bin/env python3
 """Benchmark of the XOR-swizzle data-movement path on GB300.
 
-One step = the headline workload: Swizzle<3,4,3> relayout of 4096 bf16 tiles
-of 128 x 64 (64 MiB, N(0,1) values from seed 1), forward (logical ->
-swizzled) then inverse (swizzled -> logical), through the C ABI.  The metric
-is algorithmic bytes moved (read + write, 2 x 64 MiB per launch) per second.
+One step = the headline workload: Swizzle<5,2,5> relayout of 131072 int8
+tiles of 64 x 128 (1 GiB of random bytes from seed 4; groups of 4 bytes move
+intact), forward (logical -> swizzled) then inverse (swizzled -> logical),
+through the C ABI.  The metric is algorithmic bytes moved (read + write,
+2 x 1 GiB per launch) per second.
 
-Timing: W untimed warm-up steps, then exactly K timed steps bracketed by a
-barrier and a device synchronisation.  L2 is flushed before every step
-(write 512 MiB, then read another 512 MiB so that no dirty line is left for
-the timed kernels to write back); each step is timed on its launch stream
-with CUDA events and the flushes are outside those intervals.  SM clocks and
-throttle reasons are sampled (NVML, else nvidia-smi) during the timed steps.
+Timing: W untimed warm-up steps, then exactly K timed steps back to back,
+bracketed by a barrier and a device synchronisation and timed by one CUDA
+event pair on the launch stream.  Every buffer is 1 GiB, larger than the
+126 MB L2, so no step finds the previous one's data in L2 (no flush).  SM
+clocks and throttle reasons are sampled (NVML, else nvidia-smi) during the
+timed steps.
 
 The JSON line also carries:
   roofline      the relayout kernel's achieved GB/s against the measured HBM
                 copy bandwidth (MEASURED_PEAKS.json), with the DRAM traffic per
                 launch from the committed ncu summary when it matches the
                 current kernel source;
-  e2e           the same metric through the C ABI from pinned host buffers,
-                host->device and device->host copies inside the timed region;
-  cpu_baseline  the CPU oracle on the same workload: single thread, and split
-                over every host core (spawned processes); the 125-set sweep on
-                a 64 MiB sample;
+  e2e           the same metric through the C ABI on pinned HOST buffers: the
+                forward launch reads the host input and the inverse launch
+                writes the host output over the host link, inside the timed
+                region; a copy-engine pipeline of the same step is reported
+                beside it;
+  cpu_baseline  the CPU oracle on the same workload: single thread on a
+                bounded sample of tiles, and the whole workload split over
+                every host core (spawned processes); the 125-set sweep on a
+                64 MiB sample; every other row on a bounded sample;
   rows          every other row of the path measured in the same run: the
-                small relayout, the 1 GiB int8 and uint16-sweep relayouts, the
-                fp32 / fp16 / fp64 (and 1-byte) transposes with each staging,
-                the bank profiler (skip with --no-rows).
+                64 MiB bf16 relayout (L2-assisted), the small relayout, the
+                uint16 sweep, the fp32 / fp16 / fp64 (and 1-byte) transposes
+                with each staging, the bank profiler (skip with --no-rows).
 
 --impl reference times the CPU oracle as the reference arm.
-Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak
-scaling, no collective on the data path); value = all ranks' bytes / max time.
+--gpus N without torchrun relaunches itself under torch.distributed.run.
+Multi-GPU: every rank runs the same per-GPU workload (weak scaling, no
+collective on the data path); value = all ranks' bytes / max time.
 """
 from __future__ import annotations
 
@@ -51,28 +57,35 @@ if ROOT not in sys.path:
 MiB = 1 << 20
 GB = 1e9
 METRIC = "relayout/transpose GB/s (read+write) & % of GB300 HBM peak; smem bank conflicts"
-TILES, ROWS, COLS, ESIZE = 4096, 128, 64, 2
-B, M, S = 3, 4, 3
-WORKLOAD = ("Swizzle<3,4,3> relayout forward then inverse of 4096 bf16 tiles of 128x64 "
-            "(64 MiB, N(0,1) from seed 1)")
-STEP_BYTES = 2 * 2 * TILES * ROWS * COLS * ESIZE     # two launches, each reads and writes 64 MiB
-LAUNCH_BYTES = 2 * TILES * ROWS * COLS * ESIZE
+TILES, ROWS, COLS, ESIZE = 131072, 64, 128, 1
+B, M, S = 5, 2, 5
+WORKLOAD = ("Swizzle<5,2,5> relayout forward then inverse of 131072 int8 tiles of 64x128 "
+            "(1 GiB, random bytes from seed 4)")
+N_BYTES = TILES * ROWS * COLS * ESIZE                 # 1 GiB
+LAUNCH_BYTES = 2 * N_BYTES                            # each launch reads and writes 1 GiB
+STEP_BYTES = 2 * LAUNCH_BYTES                         # forward launch + inverse launch
+HEADLINE_KERNEL = "relayout_vec_kernel<1,1,false> 131072x64x128 int8 Sw<5,2,5>"
+# the 64 MiB bf16 workload (its output stays in L2): a row of the bench
+BF16 = dict(tiles=4096, rows=128, cols=64, esize=2, bms=(3, 4, 3))
 
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--case", default=None,
-                   help="run one kernel case for a profiler and exit: relayout, relayout_bms, "
+                   help="run one kernel case for a profiler and exit: relayout, relayout_bf16, relayout_bms, "
                         "relayout_staged, relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
+    p.add_argument("--launcher-check", action="store_true",
+                   help="check the multi-rank launch on CPU (gloo): each rank reports a fixed time, rank 0 "
+                        "prints the world size and the slowest rank's time; no GPU, no bench line")
     return p.parse_args()
 
 
@@ -395,22 +408,39 @@ def measure_rows(torch, swz, dev, flush, peak):
         "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound"}
     del src, a, b, graph
 
-    # what bounds the headline step: the fixed cost of an event-timed launch
-    # after a flush (one 16 KiB tile), and the same kernel copying 32 MiB that
-    # stays in L2 (Swizzle<3,4,3> and the identity, back to back)
-    src = rand_bytes(32 * MiB, 1)
-    a = torch.empty_like(src)
-    floor = statistics.mean(timed_launches(
-        torch, lambda: swz.swz_relayout(a, src, 1, 128, 64, 2, 3, 4, 3, 0), 100, flush))
-    l2_sw = back_to_back_ms(torch, lambda: swz.swz_relayout(a, src, 2048, 128, 64, 2, 3, 4, 3, 0), reps=50)
-    l2_id = back_to_back_ms(torch, lambda: swz.swz_relayout(a, src, 2048, 128, 64, 2, 0, 0, 1, 0), reps=50)
-    out["headline_context"] = {
-        "one_tile_launch_after_flush_ms": round(floor, 4),
-        "l2_resident_32MiB_sw343": summary(l2_sw, 2 * src.numel()),
-        "l2_resident_32MiB_identity": summary(l2_id, 2 * src.numel()),
-        "note": "fixed event-to-event cost of one launch after the flush, and the kernel's rate on "
-                "data that stays in L2 (64 MiB of read + write per launch)"}
-    del src, a
+    # the 64 MiB bf16 workload: Swizzle<3,4,3> relayout of 4096 tiles of 128 x 64
+    # (N(0,1) from seed 1), forward then inverse, L2 flushed before every step
+    # (one event pair per step).  64 MiB of output stays in the 126 MB L2, so
+    # the inverse reads much of the forward's output from L2: L2-assisted.
+    import numpy as np
+    from xor_swizzle_movement_gb300 import inputs
+    nt, nr, nc, ne = BF16["tiles"], BF16["rows"], BF16["cols"], BF16["esize"]
+    bq, mq, sq = BF16["bms"]
+    host = inputs.bf16_normal(nt * nr * nc, seed=1)
+    src = torch.from_numpy(host.view(np.int16)).to(dev)
+    a, b = torch.empty_like(src), torch.empty_like(src)
+
+    def bf16_step():
+        swz.swz_relayout(a, src, nt, nr, nc, ne, bq, mq, sq, 0)
+        swz.swz_relayout(b, a, nt, nr, nc, ne, bq, mq, sq, 1)
+    step_ms = statistics.mean(timed_launches(torch, bf16_step, 200, flush))
+    torch.cuda.synchronize()
+    assert torch.equal(b, src), "bf16 relayout round trip failed"
+    moved = 4 * src.numel() * ne
+    # what bounds it: the fixed cost of an event-timed launch after the flush
+    # (one 16 KiB tile), and the same kernel copying 32 MiB that stays in L2
+    one = statistics.mean(timed_launches(
+        torch, lambda: swz.swz_relayout(a, src, 1, nr, nc, ne, bq, mq, sq, 0), 100, flush))
+    half = src[: src.numel() // 2]
+    l2_sw = back_to_back_ms(torch, lambda: swz.swz_relayout(a[: half.numel()], half, nt // 2, nr, nc, ne,
+                                                            bq, mq, sq, 0), reps=50)
+    out["relayout_bf16_4096x128x64_sw343_64MiB"] = {
+        "step": summary(step_ms, moved),
+        "note": "forward + inverse, L2 flushed before each step; L2-assisted: the 64 MiB output stays in "
+                "the 126 MB L2, so the fraction is not an HBM figure",
+        "one_tile_launch_after_flush_ms": round(one, 4),
+        "l2_resident_32MiB_forward": summary(l2_sw, 2 * half.numel() * ne)}
+    del src, a, b, half
 
     # the same Swizzle<3,3,3> fp16 64x64 tiles over 1 GiB: register path vs the TMA 128-byte mode
     src = rand_bytes(1 << 30, 4)
@@ -424,16 +454,13 @@ def measure_rows(torch, swz, dev, flush, peak):
     out["relayout_fp16_64x64_sw333_1GiB"] = r
     del src, dst
 
-    # int8 tiles 64x128, Swizzle<5,2,5>, 1 GiB, forward and inverse
     src = rand_bytes(1 << 30, 4)
     dst = torch.empty_like(src)
     n_tiles = (1 << 30) // (64 * 128)
-    fwd = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0))
-    inv = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 1))
-    out["relayout_int8_64x128_sw525_1GiB"] = {
-        "forward": summary(fwd, 2 << 30), "inverse": summary(inv, 2 << 30),
+    out["relayout_int8_64x128_sw525_1GiB_flushed"] = {
         "forward_flushed_median_20": flushed_median(
-            lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0), 2 << 30)}
+            lambda: swz.swz_relayout(dst, src, n_tiles, 64, 128, 1, 5, 2, 5, 0), 2 << 30),
+        "note": "the headline's forward launch, each after an L2 flush, timed by its own event pair"}
 
     # one 1 GiB uint16 buffer, every (B, M, S) with B 1..5, M 0..4, S B..7, forward
     n = 1 << 29
@@ -618,34 +645,39 @@ def _timed_rounds(fn, seconds):
             return times
 
 
-def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, sample_scale=1):
-    """The CPU oracle, as it stands, on the whole workload (forward then
-    inverse): single thread for about `seconds`, then split over every core
-    of this process's affinity set for about `seconds_all`.  Also the
-    relayout sweep's 125 parameter sets on a 64 MiB uint16 sample, over all
-    cores and single-threaded on three of them; and every other row's
-    workload on a bounded sample, single thread and over all cores.
-    `sample_scale` divides the other rows' samples (tests)."""
+def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, sample_scale=1,
+                 sample_tiles=4096):
+    """The CPU oracle, as it stands, on the headline workload (forward then
+    inverse): single thread on a bounded sample of `sample_tiles` tiles for
+    about `seconds`, then the whole workload split over every core of this
+    process's affinity set for about `seconds_all`.  Also the relayout
+    sweep's 125 parameter sets on a 64 MiB uint16 sample, over all cores and
+    single-threaded on three of them; and every other row's workload on a
+    bounded sample, single thread and over all cores.  `sample_scale`
+    divides the other rows' samples (tests)."""
     import numpy as np
     import multiprocessing as mp
     from multiprocessing import shared_memory
     import oracle
     from xor_swizzle_movement_gb300 import inputs
     te = ROWS * COLS
+    n_tiles = host_src.size // te
+    sample_tiles = min(sample_tiles, n_tiles)
+    part = host_src[: sample_tiles * te]
     times = _timed_rounds(lambda: oracle.relayout(
-        oracle.relayout(host_src, tile_elems=te, B=B, M=M, S=S, direction=0),
+        oracle.relayout(part, tile_elems=te, B=B, M=M, S=S, direction=0),
         tile_elems=te, B=B, M=M, S=S, direction=1), seconds)
     mean = sum(times) / len(times)
-    res = {"value": round(STEP_BYTES / mean / GB, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"whole workload (forward + inverse of {TILES} tiles), {len(times)} repetitions, "
+    moved = 4 * part.nbytes
+    res = {"value": round(moved / mean / GB, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"forward + inverse of {sample_tiles} of the {n_tiles} tiles, {len(times)} repetitions, "
                      f"{mean * 1e3:.1f} ms each, single thread",
            "cpu_model": cpu_model()}
 
     cores = len(os.sched_getaffinity(0))
     band = max(8, 256 // sample_scale)                   # transpose rows per worker
-    i8_tiles = max(1, 2048 // sample_scale)              # int8 64 x 128 tiles per worker
-    nbytes = max(host_src.nbytes, sweep_el * 2, band * cores * 8192 * 8, band * cores * 16384 * 2,
-                 i8_tiles * cores * 8192)
+    bf = BF16["tiles"] * BF16["rows"] * BF16["cols"] * BF16["esize"]
+    nbytes = max(host_src.nbytes, sweep_el * 2, band * cores * 8192 * 8, band * cores * 16384 * 2, bf)
     shm = shared_memory.SharedMemory(create=True, size=nbytes)
 
     def wall(fn):
@@ -657,15 +689,15 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
         u16 = buf.view(np.uint16)
         with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(shm.name, nbytes)) as pool:
             # the headline workload, tiles split into 4 runs per core
-            u16[:host_src.size] = host_src.view(np.uint16).reshape(-1)
+            buf[:host_src.size] = host_src.reshape(-1)
             n_runs = 4 * cores
-            cuts = [TILES * i // n_runs for i in range(n_runs + 1)]
-            jobs = [("pair", "<u2", cuts[i] * te, cuts[i + 1] * te, te, B, M, S)
+            cuts = [n_tiles * i // n_runs for i in range(n_runs + 1)]
+            jobs = [("pair", "u1", cuts[i] * te, cuts[i + 1] * te, te, B, M, S)
                     for i in range(n_runs) if cuts[i + 1] > cuts[i]]
             pool.map(_pool_job, jobs)                    # warm: every worker has loaded the oracle
             t_all = _timed_rounds(lambda: pool.map(_pool_job, jobs), seconds_all)
             m_all = sum(t_all) / len(t_all)
-            res["all_cores"] = {"value": round(STEP_BYTES / m_all / GB, 3), "unit": "GB/s", "cores": cores,
+            res["all_cores"] = {"value": round(4 * host_src.nbytes / m_all / GB, 3), "unit": "GB/s", "cores": cores,
                                 "sample": f"whole workload, {len(t_all)} repetitions, {m_all * 1e3:.1f} ms each, "
                                           f"{len(jobs)} runs of tiles over {cores} processes"}
             # the relayout sweep: one 2^25-element tile (a prefix of the 2^29-element buffer; every
@@ -702,12 +734,20 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
                 [("pair", "<u2", cut[i] * 4096, cut[i + 1] * 4096, 4096, 3, 3, 3)
                  for i in range(cores) if cut[i + 1] > cut[i]],
                 "whole workload, forward + inverse; all cores: its 256 tiles split over the cores")
-            n8 = i8_tiles * 8192
-            buf[:n8 * cores] = inputs.random_bytes(n8 * cores, seed=4)
-            row("relayout_int8_64x128_sw525", 2 * n8,
-                lambda: oracle.relayout(buf[:n8], tile_elems=8192, B=5, M=2, S=5, direction=0),
-                2 * n8 * cores, [("fwd", "u1", i * n8, (i + 1) * n8, 8192, 5, 2, 5) for i in range(cores)],
-                f"forward; {i8_tiles} of the 131072 tiles per core")
+            hb = inputs.bf16_normal(bf // 2, seed=1)
+            u16[:hb.size] = hb
+            bt = BF16["tiles"]
+            bte = BF16["rows"] * BF16["cols"]
+            bq, mq, sq = BF16["bms"]
+            cut = [bt * i // cores for i in range(cores + 1)]
+            one_tiles = max(16, 512 // sample_scale)
+            row("relayout_bf16_4096x128x64_sw343_64MiB", 4 * one_tiles * bte * 2,
+                lambda: oracle.relayout(oracle.relayout(u16[:one_tiles * bte], tile_elems=bte, B=bq, M=mq, S=sq,
+                                                        direction=0), tile_elems=bte, B=bq, M=mq, S=sq, direction=1),
+                4 * bf,
+                [("pair", "<u2", cut[i] * bte, cut[i + 1] * bte, bte, bq, mq, sq)
+                 for i in range(cores) if cut[i + 1] > cut[i]],
+                f"forward + inverse; single thread {one_tiles} of the {bt} tiles; all cores: the whole workload")
             for name, n, esize, dt, gen in (
                     ("transpose_fp32_8192", 8192, 4, "<u4", lambda k: inputs.f32_uniform(k, seed=2).view(np.uint32)),
                     ("transpose_fp16_16384", 16384, 2, "<u2", lambda k: inputs.f16_bits_no_nan(k, seed=3)),
@@ -728,34 +768,38 @@ def cpu_baseline(host_src, seconds=10.0, seconds_all=5.0, sweep_el=1 << 25, samp
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, single thread, on a
+    bounded sample of the headline workload's tiles per step (at most 4096,
+    fewer when K + W steps would take over about a minute)."""
     rank, world, _ = dist_info()
     if rank != 0:
         return
     from xor_swizzle_movement_gb300 import inputs
     import oracle
-    host = inputs.bf16_normal(TILES * ROWS * COLS, seed=1)
-    # one step = forward + inverse of a bounded sample of the 4096 tiles: at
-    # most 512, fewer when K + W steps of 512 would take over about a minute
-    probe = host[: 64 * ROWS * COLS]
+    te = ROWS * COLS
+    probe_tiles = 256
+    host = inputs.random_bytes(4096 * te, seed=4)   # the first 4096 tiles of the 1 GiB buffer
+    probe = host[: probe_tiles * te]
     t0 = time.perf_counter()
-    oracle.relayout(oracle.relayout(probe, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0),
-                    tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
-    per_tile = (time.perf_counter() - t0) / 64
+    oracle.relayout(oracle.relayout(probe, tile_elems=te, B=B, M=M, S=S, direction=0),
+                    tile_elems=te, B=B, M=M, S=S, direction=1)
+    per_tile = (time.perf_counter() - t0) / probe_tiles
     budget = 60.0 / max(1, args.steps + args.warmup)
-    sample_tiles = int(max(16, min(512, budget / per_tile)))
-    part = host[: sample_tiles * ROWS * COLS]
-    step_bytes = STEP_BYTES * sample_tiles // TILES
+    sample_tiles = int(max(16, min(4096, budget / per_tile)))
+    part = host[: sample_tiles * te]
+    step_bytes = 4 * part.nbytes
     for _ in range(args.warmup):
-        oracle.relayout(part, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
+        oracle.relayout(oracle.relayout(part, tile_elems=te, B=B, M=M, S=S, direction=0),
+                        tile_elems=te, B=B, M=M, S=S, direction=1)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        f = oracle.relayout(part, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=0)
-        oracle.relayout(f, tile_elems=ROWS * COLS, B=B, M=M, S=S, direction=1)
+        f = oracle.relayout(part, tile_elems=te, B=B, M=M, S=S, direction=0)
+        oracle.relayout(f, tile_elems=te, B=B, M=M, S=S, direction=1)
     dt = time.perf_counter() - t0
     value = step_bytes * args.steps / dt / GB
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tiles": sample_tiles},
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{sample_tiles} of {TILES} tiles per step, forward + inverse, single thread"},
@@ -778,12 +822,20 @@ def run_case(args):
 
     done = []
     if args.case == "relayout":            # the headline workload, forward + inverse
-        src = rand_bytes(TILES * ROWS * COLS * ESIZE)
+        src = rand_bytes(N_BYTES)
         a, b = torch.empty_like(src), torch.empty_like(src)
         for _ in range(args.reps):
             swz.swz_relayout(a, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
             swz.swz_relayout(b, a, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
-        done.append("relayout fwd+inv")
+        done.append("relayout int8 1 GiB Sw<5,2,5> fwd+inv")
+    elif args.case == "relayout_bf16":     # the 64 MiB bf16 workload, forward + inverse
+        nt, nr, nc, ne = BF16["tiles"], BF16["rows"], BF16["cols"], BF16["esize"]
+        src = rand_bytes(nt * nr * nc * ne)
+        a, b = torch.empty_like(src), torch.empty_like(src)
+        for _ in range(args.reps):
+            swz.swz_relayout(a, src, nt, nr, nc, ne, *BF16["bms"], 0)
+            swz.swz_relayout(b, a, nt, nr, nc, ne, *BF16["bms"], 1)
+        done.append("relayout bf16 64 MiB Sw<3,4,3> fwd+inv")
     elif args.case == "relayout_bms":      # one uint16 buffer as one tile, forward
         n = args.n or (1 << 27)
         Bq, Mq, Sq = (int(v) for v in args.bms.split(","))
@@ -847,10 +899,163 @@ def run_case(args):
     print(json.dumps({"case": args.case, "launched": done, "reps": args.reps}), flush=True)
 
 
+def relaunch_command(argv, n_gpus: int, port: int):
+    """The torch.distributed.run command that runs this script on n_gpus
+    ranks of one node (used when --gpus N > 1 is given without torchrun)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def e2e_host_abi(torch, swz, host_in, steps: int):
+    """The step through the C ABI on pinned host buffers: the forward launch
+    reads the host input over the host link, the inverse launch writes the
+    host output.  Consecutive steps alternate between two streams (and two
+    device buffers and two host outputs), so one step's inverse (writing the
+    host) overlaps the next step's forward (reading it).  Returns seconds per
+    step (CUDA events) and checks both outputs."""
+    dev = torch.cuda.current_device()
+    phys = [torch.empty(N_BYTES, dtype=torch.uint8, device=dev) for _ in range(2)]
+    outs = [torch.zeros(N_BYTES, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    main = torch.cuda.current_stream()
+
+    def run(n):
+        for k in range(n):
+            st, j = streams[k % 2], k % 2
+            swz.swz_relayout(phys[j], host_in.data_ptr(), TILES, ROWS, COLS, ESIZE, B, M, S, 0, stream=st)
+            swz.swz_relayout(outs[j].data_ptr(), phys[j], TILES, ROWS, COLS, ESIZE, B, M, S, 1, stream=st)
+    for st in streams:
+        st.wait_stream(main)
+    run(2)
+    for st in streams:
+        main.wait_stream(st)
+    torch.cuda.synchronize()
+    for o in outs:
+        o.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for st in streams:
+        st.wait_stream(main)
+    run(steps)
+    for st in streams:
+        main.wait_stream(st)
+    e1.record(main)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, host_in), "end-to-end round trip through host buffers failed"
+    return e0.elapsed_time(e1) * 1e-3 / steps
+
+
+def e2e_copy_engine(torch, swz, host_in, src, steps_per_graph=4, n_chunks=8, replays=3):
+    """The same step fed by the copy engines: each step's input goes in by
+    chunks over three streams (copy in / relayout forward + inverse / copy
+    out), consecutive steps alternate between two buffer sets, and several
+    steps form one CUDA graph.  Returns seconds per step (host clock) and the
+    plain copy rates."""
+    ct = TILES // n_chunks
+    ce = ct * ROWS * COLS * ESIZE
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    buf_sets = [tuple(torch.empty_like(src) for _ in range(3)) for _ in range(2)]
+    out_hosts = [torch.empty_like(host_in).pin_memory() for _ in range(2)]
+    ev = {key: [[torch.cuda.Event() for _ in range(n_chunks)] for _ in range(steps_per_graph)]
+          for key in ("in", "run", "out")}
+
+    def enqueue():
+        for k in range(steps_per_graph):
+            d_in_k, phys_k, back_k = buf_sets[k % 2]
+            out_k = out_hosts[k % 2]
+            for c in range(n_chunks):
+                sl = slice(c * ce, (c + 1) * ce)
+                if k >= 2:
+                    s_in.wait_event(ev["run"][k - 2][c])   # that step's relayout has read d_in
+                with torch.cuda.stream(s_in):
+                    d_in_k[sl].copy_(host_in[sl], non_blocking=True)
+                    ev["in"][k][c].record(s_in)
+                s_run.wait_event(ev["in"][k][c])
+                if k >= 2:
+                    s_run.wait_event(ev["out"][k - 2][c])  # that step's copy-out has read back
+                with torch.cuda.stream(s_run):
+                    swz.swz_relayout(phys_k[sl], d_in_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 0, stream=s_run)
+                    swz.swz_relayout(back_k[sl], phys_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 1, stream=s_run)
+                    ev["run"][k][c].record(s_run)
+                s_out.wait_event(ev["run"][k][c])
+                with torch.cuda.stream(s_out):
+                    out_k[sl].copy_(back_k[sl], non_blocking=True)
+                    ev["out"][k][c].record(s_out)
+
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=cap):
+        for s_ in (s_in, s_run, s_out):
+            s_.wait_stream(cap)
+        enqueue()
+        for s_ in (s_in, s_run, s_out):
+            cap.wait_stream(s_)
+    for o in out_hosts:
+        o.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(replays):
+        graph.replay()
+    torch.cuda.synchronize()
+    per_step = (time.perf_counter() - t0) / (replays * steps_per_graph)
+    for o in out_hosts:
+        assert torch.equal(o, host_in), "copy-engine end-to-end round trip failed"
+    d_in, out_host = buf_sets[1][0], out_hosts[0]
+    t0 = time.perf_counter()
+    for _ in range(2):
+        d_in.copy_(host_in, non_blocking=True)
+    torch.cuda.synchronize()
+    h2d = 2 * N_BYTES / (time.perf_counter() - t0) / GB
+    t0 = time.perf_counter()
+    for _ in range(2):
+        out_host.copy_(d_in, non_blocking=True)
+    torch.cuda.synchronize()
+    d2h = 2 * N_BYTES / (time.perf_counter() - t0) / GB
+    del buf_sets, out_hosts, graph
+    return per_step, {"h2d": round(h2d, 1), "d2h": round(d2h, 1)}
+
+
+def launcher_check():
+    """The multi-rank plumbing without a GPU: a gloo process group over the
+    ranks the launcher started, each rank's time 10 + 5 * rank ms, the
+    max-over-ranks reduction and rank 0's report."""
+    import torch
+    import torch.distributed as dist
+    rank, world, _ = dist_info()
+    if world > 1:
+        dist.init_process_group("gloo")
+    mx = 10.0 + 5.0 * rank
+    if world > 1:
+        mx = reduce_max_ms(torch, mx, dist, torch.device("cpu"))
+        dist.barrier()
+    if rank == 0:
+        print(json.dumps({"launcher_check": True, "world": world, "max_ms": mx,
+                          "value": throughput(world, STEP_BYTES, 1, mx)}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.case:
         run_case(args)
+        return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: run this same command under torch.distributed.run
+        cmd = relaunch_command(sys.argv[1:], args.gpus, _free_port())
+        raise SystemExit(subprocess.call(cmd))
+    if args.launcher_check:
+        launcher_check()
         return
     if args.impl == "reference":
         run_reference(args)
@@ -873,13 +1078,11 @@ def main():
         pg = dist
 
     peak, peak_kind = peaks()
-    n_el = TILES * ROWS * COLS
-    host = inputs.bf16_normal(n_el, seed=1)
-    host_t = torch.from_numpy(host.view(np.int16)).pin_memory()
+    host = inputs.random_bytes(N_BYTES, seed=4)
+    host_t = torch.from_numpy(host).pin_memory()
     src = host_t.to(dev)
     phys = torch.empty_like(src)
     back = torch.empty_like(src)
-    flush = make_flush(torch, dev)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -887,12 +1090,10 @@ def main():
         swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
 
     for _ in range(max(args.warmup, 3)):
-        flush()
         step()
     torch.cuda.synchronize()
     assert torch.equal(back, src), "relayout round trip failed"
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     gpu_id = None
     try:
         gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
@@ -902,156 +1103,78 @@ def main():
         gpu_id = None
     clocks = ClockSampler(gpu_id)
     clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    # one event pair per step: an event between the two launches would keep the
-    # inverse from launching under the forward's last wave (programmatic
-    # dependent launch)
-    for e0, e1 in ev:
-        flush()
-        e0.record(stream)
+    # one event pair around the K steps: an event between launches would keep
+    # the next launch from starting under this one's last wave (programmatic
+    # dependent launch); every buffer is larger than L2, so no flush
+    e0.record(stream)
+    for _ in range(args.steps):
         step()
-        e1.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     wall1 = time.perf_counter()
     wall = wall1 - wall0
     clk = clocks.stop(wall0, wall1)
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    total_ms = sum(step_ms)
+    total_ms = e0.elapsed_time(e1)
     if pg:
         total_ms = reduce_max_ms(torch, total_ms, pg, dev)
     ms_per_step = total_ms / args.steps
     value = throughput(world, STEP_BYTES, args.steps, total_ms)
 
-    # each direction on its own (events around each launch; not part of the value)
-    iso = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(50)]
-    for e0, e1, e2 in iso:
-        flush()
-        e0.record(stream)
-        swz.swz_relayout(phys, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
-        e1.record(stream)
-        swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
-        e2.record(stream)
-    torch.cuda.synchronize()
-    fwd_iso = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in iso)
-    inv_iso = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in iso)
+    # each direction on its own, 20 launches back to back (not part of the value)
+    fwd_ms = back_to_back_ms(torch, lambda: swz.swz_relayout(phys, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0),
+                             reps=20)
+    inv_ms = back_to_back_ms(torch, lambda: swz.swz_relayout(back, phys, TILES, ROWS, COLS, ESIZE, B, M, S, 1),
+                             reps=20)
 
-    # roofline of the relayout kernel: both launches of a step are that kernel,
-    # so its mean launch duration over the timed region is the step time / 2
-    avg_launch_s = statistics.mean(step_ms) / 2 * 1e-3
+    # roofline of the relayout kernel: both launches of a step are that kernel
+    # (Swizzle<5,2,5> is its own inverse), so its mean launch duration over the
+    # timed region is the step time / 2
+    avg_launch_s = ms_per_step / 2 * 1e-3
     achieved = LAUNCH_BYTES / avg_launch_s / GB
     src_hash = source_hash("swz_relayout.cu", "swz_common.cuh")
-    traffic = committed_traffic("relayout_vec_kernel<2,0,false> 4096x128x64 bf16 Sw<3,4,3>", src_hash)
+    traffic = committed_traffic(HEADLINE_KERNEL, src_hash)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 3), "traffic": traffic,
-                # the DRAM side alone: ncu's bytes per launch over the same mean duration
-                # (64 MiB of output fits in L2, so fewer bytes reach DRAM than the algorithm moves)
-                "dram_achieved": None if traffic is None else round(traffic / avg_launch_s / GB, 1),
-                "dram_frac": None if traffic is None else round(traffic / avg_launch_s / GB / peak, 3),
-                "peak_kind": f"{peak_kind} HBM copy bandwidth", "kernel": "relayout_vec_kernel",
+                "algorithmic_bytes_per_launch": LAUNCH_BYTES,
+                "peak_kind": f"{peak_kind} HBM copy bandwidth", "kernel": "relayout_vec_kernel<1,1,false>",
                 "mean_launch_ms": round(avg_launch_s * 1e3, 5),
-                "isolated_ms": {"forward": round(fwd_iso, 4), "inverse": round(inv_iso, 4),
-                                "note": "events around each launch, outside the timed region"}}
+                "back_to_back_ms": {"forward": round(fwd_ms, 5), "inverse": round(inv_ms, 5),
+                                    "note": "20 launches of one direction, outside the timed region"}}
 
-    # end to end from pinned host buffers: every step copies its input in and
-    # its result out inside the timed region.  A step's tiles go in 4 chunks
-    # over three streams (copy in / relayout forward+inverse / copy out), so
-    # the two copy directions and the kernels overlap; each chunk waits only
-    # for its own buffers.  Consecutive steps alternate between two buffer
-    # sets, and 8 steps form one CUDA graph, so a step's copies start while the
-    # previous step's tail is still in flight.  (Host memory is reached at
-    # about 200 GB/s per direction here, about 300 GB/s with both at once; one
-    # step per graph with 8 chunks ran at 516 GB/s, this at about 600.)
-    n_chunks, per_graph = 4, 8
-    ct = TILES // n_chunks
-    ce = ct * ROWS * COLS
-    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    buf_sets = [(torch.empty_like(src), phys, back),
-                (torch.empty_like(src), torch.empty_like(src), torch.empty_like(src))]
-    out_hosts = [torch.empty_like(host_t).pin_memory() for _ in range(2)]
-    ev = {key: [[torch.cuda.Event() for _ in range(n_chunks)] for _ in range(per_graph)]
-          for key in ("in", "run", "out")}
-
-    def e2e_steps_enqueue():
-        for k in range(per_graph):
-            d_in_k, phys_k, back_k = buf_sets[k % 2]
-            out_k = out_hosts[k % 2]
-            for c in range(n_chunks):
-                sl = slice(c * ce, (c + 1) * ce)
-                if k >= 2:
-                    s_in.wait_event(ev["run"][k - 2][c])   # that step's relayout has read d_in
-                with torch.cuda.stream(s_in):
-                    d_in_k[sl].copy_(host_t[sl], non_blocking=True)
-                    ev["in"][k][c].record(s_in)
-                s_run.wait_event(ev["in"][k][c])
-                if k >= 2:
-                    s_run.wait_event(ev["out"][k - 2][c])  # that step's copy-out has read back
-                with torch.cuda.stream(s_run):
-                    swz.swz_relayout(phys_k[sl], d_in_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 0, stream=s_run)
-                    swz.swz_relayout(back_k[sl], phys_k[sl], ct, ROWS, COLS, ESIZE, B, M, S, 1, stream=s_run)
-                    ev["run"][k][c].record(s_run)
-                s_out.wait_event(ev["run"][k][c])
-                with torch.cuda.stream(s_out):
-                    out_k[sl].copy_(back_k[sl], non_blocking=True)
-                    ev["out"][k][c].record(s_out)
-
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream()
-    cap.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.graph(graph, stream=cap):
-        for s_ in (s_in, s_run, s_out):
-            s_.wait_stream(cap)
-        e2e_steps_enqueue()
-        for s_ in (s_in, s_run, s_out):
-            cap.wait_stream(s_)
-    for o in out_hosts:
-        o.zero_()
-    replays = -(-max(10, min(100, args.steps // 20)) // per_graph)
-    for _ in range(2):
-        graph.replay()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(replays):
-        graph.replay()
-    torch.cuda.synchronize()
-    e2e_steps = replays * per_graph
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    for o in out_hosts:
-        assert torch.equal(o, host_t), "end-to-end round trip failed"
-    d_in, out_host = buf_sets[1][0], out_hosts[0]
-    # the copy rates alone, for context
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(5):
-        d_in.copy_(host_t, non_blocking=True)
-    torch.cuda.synchronize()
-    h2d_gbs = 5 * n_el * ESIZE / (time.perf_counter() - t0) / GB
-    t0 = time.perf_counter()
-    for _ in range(5):
-        out_host.copy_(back, non_blocking=True)
-    torch.cuda.synchronize()
-    d2h_gbs = 5 * n_el * ESIZE / (time.perf_counter() - t0) / GB
+    # end to end through the C ABI on pinned host buffers (the headline e2e),
+    # and the copy-engine pipeline of the same step for context
+    e2e_s = e2e_host_abi(torch, swz, host_t, steps=16)
+    ce_s, copy_rates = e2e_copy_engine(torch, swz, host_t, src)
     e2e = {"value": round(STEP_BYTES / e2e_s / GB, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": n_el * ESIZE, "d2h_bytes_per_step": n_el * ESIZE,
-           "ms_per_step": round(e2e_s * 1e3, 4), "chunks": n_chunks, "cuda_graph": True,
-           "steps_per_graph": per_graph, "buffer_sets": 2, "steps": e2e_steps,
-           "copy_GB/s": {"h2d": round(h2d_gbs, 1), "d2h": round(d2h_gbs, 1)}}
+           "h2d_bytes_per_step": N_BYTES, "d2h_bytes_per_step": N_BYTES,
+           "ms_per_step": round(e2e_s * 1e3, 4), "steps": 16,
+           "how": "swz_relayout forward reading the pinned host input, inverse writing the pinned host "
+                  "output (kernels on host memory over the host link); consecutive steps on two streams",
+           "copy_engine_pipeline": {"value": round(STEP_BYTES / ce_s / GB, 1), "unit": "GB/s",
+                                    "ms_per_step": round(ce_s * 1e3, 4),
+                                    "how": "cudaMemcpyAsync chunks in and out over three streams around "
+                                           "the two launches, 4 steps per CUDA graph"},
+           "copy_GB/s": copy_rates}
 
     rows = None
     if not args.no_rows and rank == 0:
-        rows = measure_rows(torch, swz, dev, flush, peak)
+        del phys, back
+        rows = measure_rows(torch, swz, dev, make_flush(torch, dev), peak)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
             "config": {"workload": WORKLOAD, "tiles": TILES, "rows": ROWS, "cols": COLS, "elem_bytes": ESIZE,
                        "swizzle_BMS": [B, M, S], "step": "forward launch + inverse launch",
                        "bytes_per_step": STEP_BYTES,
-                       "l2": "flushed before every step (512 MiB write + 512 MiB read, untimed)",
+                       "l2": "inputs larger than L2 (three 1 GiB buffers against a 126 MB L2); no flush",
                        "parallelism": f"replicas x{world}"},
             "frac_of_hbm_peak": round(value / world / peak, 3),
             "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * args.steps,

@@ -32,13 +32,16 @@ def test_staging_patterns_bank_predictions(orc, esize, variant, expect):
 
 def test_throughput_and_traffic_record(tmp_path, monkeypatch):
     assert bench.throughput(2, 1 << 30, 10, 1000.0) == pytest.approx(2 * (1 << 30) * 10 / 1.0 / 1e9)
-    key = "relayout_vec_kernel<2,0,false> 4096x128x64 bf16 Sw<3,4,3>"
+    key = bench.HEADLINE_KERNEL
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
-        rec = json.load(f)[key]
+        rec = json.load(f).get(key)
     current = bench.source_hash("swz_relayout.cu", "swz_common.cuh")
     got = bench.committed_traffic(key, current)
     # the committed record is used only while it matches the kernel source
-    assert (got == rec["dram_bytes_per_launch"]) == (rec["source_hash"] == current)
+    if rec is None:
+        assert got is None
+    else:
+        assert (got == rec["dram_bytes_per_launch"]) == (rec["source_hash"] == current)
     assert bench.committed_traffic(key, "0" * 16) is None
     assert bench.committed_traffic("no such kernel", current) is None
 
@@ -76,18 +79,20 @@ def test_clock_sampler_reason_bits():
 
 def test_cpu_baseline_single_and_all_cores():
     """The CPU baseline runs the oracle single-threaded and over every core
-    (spawned workers on shared memory) on the headline workload, and the
-    125-set sweep on a small sample; all report positive rates."""
+    (spawned workers on shared memory) on (a prefix of) the headline
+    workload, and the 125-set sweep on a small sample; all report positive
+    rates."""
     from xor_swizzle_movement_gb300 import inputs
-    host = inputs.bf16_normal(bench.TILES * bench.ROWS * bench.COLS, seed=1)
-    res = bench.cpu_baseline(host, seconds=0.01, seconds_all=0.01, sweep_el=1 << 16, sample_scale=64)
+    host = inputs.random_bytes(256 * bench.ROWS * bench.COLS, seed=4)
+    res = bench.cpu_baseline(host, seconds=0.01, seconds_all=0.01, sweep_el=1 << 16, sample_scale=64,
+                             sample_tiles=16)
     assert res["kind"] == "oracle" and res["cores"] == 1 and res["value"] > 0
     assert res["all_cores"]["cores"] == len(os.sched_getaffinity(0)) and res["all_cores"]["value"] > 0
     sw = res["sweep125_uint16"]
     assert sw["all_cores_GB/s"] > 0 and set(sw["single_thread_GB/s"]) == {"1,4,7", "3,3,3", "5,2,5"}
     assert isinstance(res["cpu_model"], str) and res["cpu_model"]
     assert set(res["other_rows"]) == {
-        "relayout_fp16_64x64_sw333_2MiB", "relayout_int8_64x128_sw525", "transpose_fp32_8192",
+        "relayout_fp16_64x64_sw333_2MiB", "relayout_bf16_4096x128x64_sw343_64MiB", "transpose_fp32_8192",
         "transpose_fp16_16384", "transpose_fp64_8192"}
     assert all(v["single_thread_GB/s"] > 0 and v["all_cores_GB/s"] > 0 for v in res["other_rows"].values())
 
@@ -104,3 +109,15 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.source_hash("k.cu") == h0
     f.write_text("__global__ void k(int *p) {\n    p[0] = 2;\n}\n")
     assert bench.source_hash("k.cu") != h0
+
+
+def test_relaunch_command_runs_one_rank_per_gpu():
+    """--gpus N without torchrun becomes a torch.distributed.run command on
+    one node with N processes, on the loopback address, with the same
+    arguments."""
+    cmd = bench.relaunch_command(["--gpus", "4", "--steps", "7"], 4, 29555)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nnodes=1" in cmd and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[cmd.index("--master-port") + 1] == "29555"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "7"] and cmd[-5].endswith("bench.py")

@@ -44,3 +44,22 @@ def test_two_rank_max_and_throughput():
     for rank, mx, val in results:
         assert mx == 15.0
         assert val == pytest.approx(2 * bench.STEP_BYTES * 100 / 15e-3 / 1e9)
+
+
+def test_bench_launcher_starts_one_rank_per_gpu():
+    """bench.py --gpus 2, run without torchrun, relaunches itself under
+    torch.distributed.run with two ranks; with --launcher-check the ranks form
+    a gloo group, reduce their times and rank 0 alone prints the whole-job
+    figure."""
+    import json
+    import subprocess
+    import sys
+    import bench
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2", "--launcher-check"],
+                       capture_output=True, text=True, timeout=240, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["world"] == 2 and lines[0]["max_ms"] == 15.0
+    assert lines[0]["value"] == pytest.approx(2 * bench.STEP_BYTES / 15e-3 / 1e9)
