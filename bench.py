@@ -822,12 +822,14 @@ def run_case(args):
 
     done = []
     if args.case == "relayout":            # the headline workload, forward + inverse
-        src = rand_bytes(N_BYTES)
+        nbytes = (args.n or N_BYTES) // (ROWS * COLS) * (ROWS * COLS)
+        src = rand_bytes(nbytes)
         a, b = torch.empty_like(src), torch.empty_like(src)
+        nt = nbytes // (ROWS * COLS * ESIZE)
         for _ in range(args.reps):
-            swz.swz_relayout(a, src, TILES, ROWS, COLS, ESIZE, B, M, S, 0)
-            swz.swz_relayout(b, a, TILES, ROWS, COLS, ESIZE, B, M, S, 1)
-        done.append("relayout int8 1 GiB Sw<5,2,5> fwd+inv")
+            swz.swz_relayout(a, src, nt, ROWS, COLS, ESIZE, B, M, S, 0)
+            swz.swz_relayout(b, a, nt, ROWS, COLS, ESIZE, B, M, S, 1)
+        done.append(f"relayout int8 {nt} tiles of 64x128 Sw<5,2,5> fwd+inv")
     elif args.case == "relayout_bf16":     # the 64 MiB bf16 workload, forward + inverse
         nt, nr, nc, ne = BF16["tiles"], BF16["rows"], BF16["cols"], BF16["esize"]
         src = rand_bytes(nt * nr * nc * ne)
