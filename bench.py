@@ -78,7 +78,7 @@ def parse():
     p.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--case", default=None,
-                   help="run one kernel case for a profiler and exit: relayout, relayout_bf16, relayout_bms, "
+                   help="run one kernel case for a profiler and exit: relayout, relayout_bf16, relayout_bms, staging_probe, "
                         "relayout_staged, relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
@@ -887,6 +887,20 @@ def run_case(args):
         for _ in range(args.reps):
             swz.swz_transpose_relayout(dst, src, 64, cols, 2, 8192, 3, 4, 3)
         done.append(f"transpose_relayout 64 x {cols}")
+    elif args.case == "staging_probe":     # every transpose staging on registers, then with global traffic
+        iters = args.n or 64
+        ctas = torch.cuda.get_device_properties(dev).multi_processor_count * 4
+        gbytes = 1 << 30
+        gsrc, gdst = rand_bytes(gbytes), torch.empty(gbytes, dtype=torch.uint8, device=dev)
+        stagings = [(4, 0), (4, 1), (4, 2), (2, 0), (2, 1), (2, 2), (8, 0), (8, 1), (8, 2), (1, 0)]
+        for mode in ("shared_only", "with_global"):
+            for esize, v in stagings:
+                for _ in range(args.reps):
+                    if mode == "shared_only":
+                        swz.swz_staging_probe(esize, v, iters, ctas)     # no global access at all
+                    else:
+                        swz.swz_staging_probe(esize, v, iters, ctas, gsrc=gsrc, gdst=gdst, gbytes=gbytes)
+                done.append(f"staging_probe esize={esize} variant={v} {mode} iters={iters} ctas={ctas}")
     elif args.case == "bank_profile":
         n = args.n or (1 << 20)
         pats = torch.randint(0, 228 * 1024 // 4, (n, 32), dtype=torch.int32, device=dev, generator=gen) * 4

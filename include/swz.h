@@ -200,6 +200,33 @@ swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, 
                             void *stream);
 
 /*
+ * Shared-memory staging probe: a diagnostic for hardware bank-conflict
+ * counters, not a data path.  A column read of a row-major shared tile puts
+ * every lane in one bank ("CuTe Swizzle 学习手册", section "冲突的典型场景");
+ * the transpose stagings avoid it by XOR-ing the column ("Swizzle 数学公式")
+ * or padding the rows ("CUDA 013 - Swizzle 的工作原理", section "如何避免
+ * Bank Conflict").  This call launches `ctas` CTAs that each fill and drain
+ * one shared tile `iters` times with exactly the shared-memory instructions
+ * and addresses of the swz_transpose staging of that element size and
+ * variant (esize 4 / 8 / 2: SWZ_T_SWIZZLED, SWZ_T_UNSWIZZLED, SWZ_T_PADDED;
+ * esize 1: SWZ_T_SWIZZLED, the 128 x 128-byte tile), on values held in
+ * registers.
+ *
+ * gsrc, gdst, gbytes: optional device buffers of gbytes bytes (a multiple of
+ * 16, 16-byte aligned, not overlapping).  NULL: the kernel makes no global
+ * memory access at all.  Given: each iteration also streams one 16-byte load
+ * from gsrc per fill vector and one 16-byte store to gdst per drain vector,
+ * as the transpose does, cycling through the buffers.
+ * sink: optional device array of `ctas` words; each CTA writes a checksum of
+ * what it read after its last iteration (NULL: nothing is written).
+ *
+ * Errors: SWZ_ERR_PARAM (esize, variant), SWZ_ERR_SHAPE (iters, ctas < 0,
+ * ctas >= 2^31, gbytes), SWZ_ERR_ALIGN, SWZ_ERR_ALIAS, SWZ_ERR_CUDA.
+ */
+swz_status swz_staging_probe(int esize, int variant, int iters, const void *gsrc, void *gdst,
+                             int64_t gbytes, uint32_t *sink, int64_t ctas, void *stream);
+
+/*
  * Slice collision ("cutlass 入门", section "swizzle 融入 layout 优化").
  *
  * A is the largest index of a slice, so its set bits are the bits that can

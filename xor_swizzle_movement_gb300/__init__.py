@@ -19,7 +19,7 @@ __all__ = [
     "SwzError", "lib", "library_path",
     "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_slice_layout", "swz_layout_text", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
-    "swz_transpose_tma_noalloc", "swz_selftest_noalloc_timeout",
+    "swz_transpose_tma_noalloc", "swz_selftest_noalloc_timeout", "swz_staging_probe",
     "swz_status_string", "swz_version",
     "SWZ_OK", "SWZ_ERR_NULL", "SWZ_ERR_PARAM", "SWZ_ERR_SHAPE", "SWZ_ERR_ALIGN", "SWZ_ERR_ALIAS",
     "SWZ_ERR_CUDA", "SWZ_ERR_TIMEOUT", "SWZ_ERR_UNSUPPORTED",
@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.swz_transpose_tma_noalloc.restype = i32
         L.swz_selftest_noalloc_timeout.argtypes = [vp, vp, i64, i64, u64, ctypes.POINTER(ctypes.c_uint32), vp]
         L.swz_selftest_noalloc_timeout.restype = i32
+        L.swz_staging_probe.argtypes = [i32, i32, i32, vp, vp, i64, vp, i64, vp]
+        L.swz_staging_probe.restype = i32
         L.swz_status_string.argtypes = [i32]
         L.swz_status_string.restype = ctypes.c_char_p
         L.swz_version.argtypes = []
@@ -235,6 +237,15 @@ def swz_selftest_noalloc_timeout(dst, src, rows: int, cols: int, wait_ns: int, s
     if status != SWZ_ERR_TIMEOUT:
         _check(status, "swz_selftest_noalloc_timeout")
     return int(flag.value), int(status)
+
+
+def swz_staging_probe(esize: int, variant: int, iters: int, ctas: int, gsrc=None, gdst=None, gbytes: int = 0,
+                      sink=None, stream=None) -> None:
+    """Fill and drain one transpose staging `iters` times per CTA on register
+    data (a diagnostic for the shared-memory bank-conflict counters); with
+    gsrc / gdst, 16-byte global traffic streams alongside."""
+    _check(lib().swz_staging_probe(esize, variant, iters, _ptr(gsrc), _ptr(gdst), gbytes, _ptr(sink), ctas,
+                                   _stream(stream)), "swz_staging_probe")
 
 
 def swz_status_string(status: int) -> str:
