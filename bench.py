@@ -890,7 +890,7 @@ def run_case(args):
     elif args.case == "staging_probe":     # every transpose staging on registers, then with global traffic
         iters = args.n or 64
         ctas = torch.cuda.get_device_properties(dev).multi_processor_count * 4
-        gbytes = 1 << 30
+        gbytes = 256 << 20                 # larger than L2: the streamed data comes from DRAM
         gsrc, gdst = rand_bytes(gbytes), torch.empty(gbytes, dtype=torch.uint8, device=dev)
         stagings = [(4, 0), (4, 1), (4, 2), (2, 0), (2, 1), (2, 2), (8, 0), (8, 1), (8, 2), (1, 0)]
         for mode in ("shared_only", "with_global"):
