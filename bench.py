@@ -888,19 +888,22 @@ def run_case(args):
             swz.swz_transpose_relayout(dst, src, 64, cols, 2, 8192, 3, 4, 3)
         done.append(f"transpose_relayout 64 x {cols}")
     elif args.case == "staging_probe":     # every transpose staging on registers, then with global traffic
+        # two shapes: persistent CTAs that repeat the staging (4 per SM, `iters` rounds), and one round
+        # per CTA over as many CTAs as the 8192^2 fp32 transpose launches (16384)
         iters = args.n or 64
-        ctas = torch.cuda.get_device_properties(dev).multi_processor_count * 4
+        shapes = [(iters, torch.cuda.get_device_properties(dev).multi_processor_count * 4), (1, 16384)]
         gbytes = 256 << 20                 # larger than L2: the streamed data comes from DRAM
         gsrc, gdst = rand_bytes(gbytes), torch.empty(gbytes, dtype=torch.uint8, device=dev)
         stagings = [(4, 0), (4, 1), (4, 2), (2, 0), (2, 1), (2, 2), (8, 0), (8, 1), (8, 2), (1, 0)]
-        for mode in ("shared_only", "with_global"):
-            for esize, v in stagings:
-                for _ in range(args.reps):
-                    if mode == "shared_only":
-                        swz.swz_staging_probe(esize, v, iters, ctas)     # no global access at all
-                    else:
-                        swz.swz_staging_probe(esize, v, iters, ctas, gsrc=gsrc, gdst=gdst, gbytes=gbytes)
-                done.append(f"staging_probe esize={esize} variant={v} {mode} iters={iters} ctas={ctas}")
+        for it_, ctas in shapes:
+            for mode in ("shared_only", "with_global"):
+                for esize, v in stagings:
+                    for _ in range(args.reps):
+                        if mode == "shared_only":
+                            swz.swz_staging_probe(esize, v, it_, ctas)     # no global access at all
+                        else:
+                            swz.swz_staging_probe(esize, v, it_, ctas, gsrc=gsrc, gdst=gdst, gbytes=gbytes)
+                    done.append(f"staging_probe esize={esize} variant={v} {mode} iters={it_} ctas={ctas}")
     elif args.case == "bank_profile":
         n = args.n or (1 << 20)
         pats = torch.randint(0, 228 * 1024 // 4, (n, 32), dtype=torch.int32, device=dev, generator=gen) * 4

@@ -100,9 +100,9 @@ swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t row
  * Swizzle<B, 4 - log2(esize), 3> for B = 1, 2, 3.
  *
  * Same arguments, rules, errors and result as swz_relayout.  The swizzled side
- * of the copy runs on the TMA (forward: a swizzled tensor load into shared
- * memory, then 16-byte stores of it in order; inverse: 16-byte loads in order
- * into shared memory, then a swizzled tensor store) when S = 3, M + log2(esize) = 4,
+ * of the copy runs on the TMA (a swizzled tensor load into shared memory, then
+ * 16-byte stores of it in order; each mode is its own inverse, so both
+ * directions are this copy) when S = 3, M + log2(esize) = 4,
  * 1 <= B <= 3, each tile holds a multiple of 2^(B+7) bytes and dst and src are
  * 16-byte aligned; any other request runs swz_relayout's kernels.  The TMA
  * path's bounded waits report to swz_device_status() (its status word is the

@@ -3,7 +3,8 @@
 Where it applies, the relayout runs on the TMA's hardware swizzle modes, so
 these tests also pin the hardware: the 32-, 64- and 128-byte modes must
 produce exactly the oracle's element Swizzle<B, 4 - log2(esize), 3>, B = 1, 2, 3,
-in both directions (swizzled tensor load, and swizzled tensor store)."""
+in both directions (each mode is its own inverse: both run as a swizzled
+tensor load)."""
 import numpy as np
 import pytest
 

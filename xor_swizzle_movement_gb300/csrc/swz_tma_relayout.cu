@@ -6,19 +6,19 @@
 // 3: the byte-address Swizzle<B,4,3>, i.e. element Swizzle<B, 4 - log2 e, 3> on
 // e-byte elements ("CuTe Swizzle 学习手册", sections "Sw<3,4,3> vs Sw<3,3,3>"
 // and "H100 TMA + Swizzle").  The buffer is viewed as rows of 2^(B+4) bytes
-// (the swizzle span) and moved in 8 KiB chunks, the tensor copy on the
-// swizzled side and 16-byte register copies on the plain side:
-//   forward  dst[sw(i)] = src[i]: a swizzled tensor load into shared memory,
-//            then every thread copies its vectors out to dst in order;
-//   inverse  dst[i] = src[sw(i)]: every thread copies its vectors of src into
-//            shared memory in order, then a swizzled tensor store.
-// (With the tensor copy on both sides, a bulk copy for the plain side, the
-// copy engine's rate for 128-byte box rows held both directions near 6.4 TB/s;
-// splitting the work between it and the SM's load/store units reaches 6.7-6.9.)
+// (the swizzle span) and moved in 8 KiB chunks: a swizzled tensor load puts
+// the logical byte at offset i of a chunk at shared offset sw(i), then every
+// thread copies its 16-byte vectors out to dst in order, so dst[sw(i)] =
+// src[i].  Every hardware mode is its own inverse (the field it reads sits
+// at or above the field it writes plus its width), so the inverse relayout
+// dst[i] = src[sw(i)] is the same copy.  (An inverse that filled shared
+// memory with 16-byte stores and left by a swizzled tensor store ran at 6.73
+// against 6.9 TB/s, and its shared stores collided with the tensor store's
+// shared reads on 11% of their wavefronts.)
 // Each chunk covers whole swizzle periods (2^(B+7) bytes) of whole tiles, so
 // the tile-local swizzle equals the swizzle of the chunk-local offset.  The
-// forward kernel waits on its loads with bounded mbarrier waits (kWaitLimitNs)
-// and records an expiry in the per-device status word.
+// kernel waits on its loads with bounded mbarrier waits (kWaitLimitNs) and
+// records an expiry in the per-device status word.
 #include "swz_tma_common.cuh"
 
 namespace swz {
@@ -31,8 +31,7 @@ namespace {
 constexpr int kChunk = 8192;                         // bytes per tensor copy
 constexpr int kThreads = 256;
 constexpr int kVecs = kChunk / 16 / kThreads;        // 16-byte vectors per thread per chunk
-constexpr int kFwdRing = 3, kFwdCtasPerSm = 2;       // forward: 3 chunks in flight per CTA
-constexpr int kInvRing = 4, kInvCtasPerSm = 6;       // inverse: 4 output buffers per CTA
+constexpr int kRing = 3, kCtasPerSm = 2;           // 3 chunks in flight per CTA
 
 struct TmaRelayoutArgs {
     uint8_t *dst;
@@ -50,11 +49,6 @@ __device__ __forceinline__ uint4 lds16(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 // 16-byte vectors of chunk c that hold data (the last chunk may be short)
 __device__ __forceinline__ int chunk_vecs(const TmaRelayoutArgs &a, int64_t c) {
     const int64_t left = a.bytes - c * kChunk;
@@ -62,11 +56,11 @@ __device__ __forceinline__ int chunk_vecs(const TmaRelayoutArgs &a, int64_t c) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-    relayout_tma_fwd_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
+    relayout_tma_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kFwdRing];
+    __shared__ __align__(8) uint64_t bars[kRing];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;  // the swizzle is computed from address bits
     const uint32_t bar0 = smem_u32(&bars[0]);
     const int tid = threadIdx.x;
@@ -76,10 +70,10 @@ __global__ void __launch_bounds__(kThreads)
         tma_load_2d(base + s * kChunk, &map, 0, static_cast<int>(c * a.rows_per_chunk), bar0 + 8u * s);
     };
     if (tid == 0) {
-        for (int s = 0; s < kFwdRing; ++s) mbar_init(bar0 + 8u * s, 1);
+        for (int s = 0; s < kRing; ++s) mbar_init(bar0 + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (int s = 0; s < kFwdRing; ++s) {
+        for (int s = 0; s < kRing; ++s) {
             const int64_t c = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
             if (c < a.n_chunks) issue(s, c);
         }
@@ -88,16 +82,16 @@ __global__ void __launch_bounds__(kThreads)
     for (int64_t it = 0;; ++it) {
         const int64_t c = blockIdx.x + it * gridDim.x;
         if (c >= a.n_chunks) break;
-        const int s = static_cast<int>(it % kFwdRing);
-        const bool ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kFwdRing) & 1), a.wait_ns);
+        const int s = static_cast<int>(it % kRing);
+        const bool ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kRing) & 1), a.wait_ns);
         if (!__syncthreads_and(ok)) {
             if (tid == 0) {
                 atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
-                // let the loads still in flight (iterations it .. it + kFwdRing - 1) land
-                for (int64_t j = it; j < it + kFwdRing; ++j) {
+                // let the loads still in flight (iterations it .. it + kRing - 1) land
+                for (int64_t j = it; j < it + kRing; ++j) {
                     if (blockIdx.x + j * gridDim.x >= a.n_chunks) break;
-                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kFwdRing),
-                                      static_cast<uint32_t>((j / kFwdRing) & 1), a.wait_ns);
+                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kRing),
+                                      static_cast<uint32_t>((j / kRing) & 1), a.wait_ns);
                 }
             }
             return;
@@ -114,7 +108,7 @@ __global__ void __launch_bounds__(kThreads)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         if (tid == 0) {
-            const int64_t cn = c + static_cast<int64_t>(kFwdRing) * gridDim.x;
+            const int64_t cn = c + static_cast<int64_t>(kRing) * gridDim.x;
             if (cn < a.n_chunks) issue(s, cn);
         }
 #pragma unroll
@@ -123,47 +117,6 @@ __global__ void __launch_bounds__(kThreads)
             if (idx < nv) st_stream16(a.dst + c * kChunk + idx * 16, v[k]);
         }
     }
-}
-
-__global__ void __launch_bounds__(kThreads)
-    relayout_tma_inv_kernel(const __grid_constant__ CUtensorMap map, const TmaRelayoutArgs a) {
-    pdl_launch_dependents();
-    pdl_wait();  // before any global memory access
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const int tid = threadIdx.x;
-    uint4 v[kVecs];
-    auto load = [&](int64_t c) {
-        const int nv = chunk_vecs(a, c);
-#pragma unroll
-        for (int k = 0; k < kVecs; ++k) {
-            const int idx = k * kThreads + tid;
-            if (idx < nv) v[k] = ld_stream16(a.src + c * kChunk + idx * 16);
-        }
-    };
-    int64_t c = blockIdx.x;
-    if (c < a.n_chunks) load(c);
-    for (int64_t it = 0; c < a.n_chunks; ++it, c += gridDim.x) {
-        const int s = static_cast<int>(it % kInvRing);
-        // the store issued from buffer s kInvRing chunks ago has read it
-        if (tid == 0 && it >= kInvRing) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kInvRing - 1) : "memory");
-        __syncthreads();
-        const int nv = chunk_vecs(a, c);
-#pragma unroll
-        for (int k = 0; k < kVecs; ++k) {
-            const int idx = k * kThreads + tid;
-            if (idx < nv) sts16(base + s * kChunk + idx * 16, v[k]);
-        }
-        if (c + gridDim.x < a.n_chunks) load(c + gridDim.x);  // the next chunk's loads overlap this store
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // these writes before the tensor store
-        __syncthreads();
-        if (tid == 0) {
-            // rows past the end of the buffer are dropped
-            tma_store_2d(&map, 0, static_cast<int>(c * a.rows_per_chunk), base + s * kChunk);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-    }
-    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 }  // namespace
@@ -192,8 +145,8 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(span)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(span), static_cast<cuuint32_t>(kChunk / span)};
     const cuuint32_t estride[2] = {1, 1};
-    void *tensor_side = direction == 0 ? const_cast<void *>(src) : dst;
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, tensor_side, gdim, gstride, box, estride,
+    (void)direction;  // every hardware mode is its own inverse: both directions are the same copy
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(src), gdim, gstride, box, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, modes[B], CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SWZ_ERR_CUDA;
@@ -206,12 +159,10 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     a.rows_per_chunk = static_cast<int>(kChunk / span);
     a.wait_ns = kWaitLimitNs;
     a.status = status;
-    int64_t grid = static_cast<int64_t>(sm_count()) * (direction == 0 ? kFwdCtasPerSm : kInvCtasPerSm);
+    int64_t grid = static_cast<int64_t>(sm_count()) * kCtasPerSm;
     if (a.n_chunks < grid) grid = a.n_chunks;
     const dim3 g(static_cast<unsigned>(grid));
-    if (direction == 0)
-        return launched(launch_pdl(relayout_tma_fwd_kernel, g, dim3(kThreads), kFwdRing * kChunk + 1024, st, map, a));
-    return launched(launch_pdl(relayout_tma_inv_kernel, g, dim3(kThreads), kInvRing * kChunk + 1024, st, map, a));
+    return launched(launch_pdl(relayout_tma_kernel, g, dim3(kThreads), kRing * kChunk + 1024, st, map, a));
 }
 
 }  // namespace swz
