@@ -97,20 +97,37 @@ swz_status swz_relayout(void *dst, const void *src, int64_t n_tiles, int64_t row
  * Sw<3,3,3>" (Sw<3,4,3> is the 128-byte pattern the TMA descriptor carries)
  * and "H100 TMA + Swizzle".  The TMA 32-, 64- and 128-byte swizzle modes are
  * the byte-address Swizzle<1,4,3>, <2,4,3> and <3,4,3>, i.e. element
- * Swizzle<B, 4 - log2(esize), 3> for B = 1, 2, 3.
+ * Swizzle<B, 4 - log2(esize), 3> for B = 1, 2, 3; the 128-byte mode with
+ * 32-byte atoms is the byte-address Swizzle<2,5,2>, element
+ * Swizzle<2, 5 - log2(esize), 2>.
  *
  * Same arguments, rules, errors and result as swz_relayout.  The swizzled side
  * of the copy runs on the TMA (a swizzled tensor load into shared memory, then
  * 16-byte stores of it in order; each mode is its own inverse, so both
- * directions are this copy) when S = 3, M + log2(esize) = 4,
- * 1 <= B <= 3, each tile holds a multiple of 2^(B+7) bytes and dst and src are
- * 16-byte aligned; any other request runs swz_relayout's kernels.  The TMA
+ * directions are this copy) when (B, M + log2(esize), S) is one of the four
+ * modes above, each tile holds a whole number of the mode's periods
+ * (2^(B + M + log2(esize) + S) bytes) and dst and src are 16-byte aligned;
+ * any other request runs swz_relayout's kernels (swz_relayout_tma_path tells
+ * which).  The TMA
  * path's bounded waits report to swz_device_status() (its status word is the
  * one SWZ_T_TMA allocates on first use).
  */
 swz_status swz_relayout_tma(void *dst, const void *src, int64_t n_tiles, int64_t rows,
                             int64_t cols, int esize, int B, int M, int S, int direction,
                             void *stream);
+
+/*
+ * The path swz_relayout_tma takes for these arguments, without running it:
+ *   0  swz_relayout's register kernels;
+ *   1  the TMA 32-byte mode (byte-address Swizzle<1,4,3>);
+ *   2  the 64-byte mode (Swizzle<2,4,3>);
+ *   3  the 128-byte mode (Swizzle<3,4,3>);
+ *   4  the 128-byte mode with 32-byte atoms (Swizzle<2,5,2>);
+ *  -s  the swz_status s that swz_relayout_tma would return for bad arguments.
+ * An empty request returns 0.  Host function; pointers are not dereferenced.
+ */
+int swz_relayout_tma_path(const void *dst, const void *src, int64_t n_tiles, int64_t rows,
+                          int64_t cols, int esize, int B, int M, int S, int direction);
 
 /*
  * Matrix transpose HBM -> shared memory -> HBM.

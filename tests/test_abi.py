@@ -136,3 +136,13 @@ def test_layout_text_matches_oracle_dump(swz, orc):
     buf = ctypes.create_string_buffer(10)
     assert swz.lib().swz_layout_text(buf, 10, 4, 4, 4, 2, 0, 2) == len(full)
     assert buf.value.decode() == full[:9]
+
+
+def test_relayout_tma_path_reports_argument_errors(swz):
+    """The path query validates like swz_relayout_tma and returns -status."""
+    a, b = 1 << 20, 1 << 21   # never dereferenced
+    assert swz.swz_relayout_tma_path(a, b, 4, 64, 64, 2, 3, 3, 0, 0) == -swz.SWZ_ERR_PARAM     # S = 0
+    assert swz.swz_relayout_tma_path(a, b, 4, 1, 60, 2, 3, 3, 3, 0) == -swz.SWZ_ERR_SHAPE     # tile not closed
+    assert swz.swz_relayout_tma_path(a, a, 4, 64, 64, 2, 3, 3, 3, 0) == -swz.SWZ_ERR_ALIAS
+    assert swz.swz_relayout_tma_path(a, b, 0, 64, 64, 2, 3, 3, 3, 0) == 0                     # empty
+    assert swz.swz_relayout_tma_path(a + 2, b, 4, 64, 64, 2, 3, 3, 3, 0) == 0                 # misaligned

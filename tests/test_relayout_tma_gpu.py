@@ -1,10 +1,12 @@
 """swz_relayout_tma against the CPU oracle, bit-exact.
 
-Where it applies, the relayout runs on the TMA's hardware swizzle modes, so
-these tests also pin the hardware: the 32-, 64- and 128-byte modes must
-produce exactly the oracle's element Swizzle<B, 4 - log2(esize), 3>, B = 1, 2, 3,
-in both directions (each mode is its own inverse: both run as a swizzled
-tensor load)."""
+Where it applies, the relayout runs on the TMA's hardware swizzle modes
+(swz_relayout_tma_path says which; the tests check it), so these tests also
+pin the hardware: the 32-, 64- and 128-byte modes must produce exactly the
+oracle's element Swizzle<B, 4 - log2(esize), 3>, B = 1, 2, 3, and the 128-byte
+mode with 32-byte atoms the oracle's element Swizzle<2, 5 - log2(esize), 2>, in
+both directions (each mode is its own inverse: both run as a swizzled tensor
+load)."""
 import numpy as np
 import pytest
 
@@ -24,10 +26,12 @@ def swz():
     return m
 
 
-def run(swz, host, n_tiles, rows, cols, esize, B, M, S, direction, src_off=0, dst_off=0):
+def run(swz, host, n_tiles, rows, cols, esize, B, M, S, direction, src_off=0, dst_off=0, path=None):
     nbytes = host.nbytes
     _, src = to_device(host, src_off)
     full, dst = empty_device(nbytes, dst_off)
+    if path is not None:
+        assert swz.swz_relayout_tma_path(dst, src, n_tiles, rows, cols, esize, B, M, S, direction) == path
     swz.swz_relayout_tma(dst, src, n_tiles, rows, cols, esize, B, M, S, direction)
     torch.cuda.synchronize()
     assert guards_intact(full, dst_off, nbytes)
@@ -47,7 +51,25 @@ def test_hardware_modes(swz, orc, esize, B, tile_bytes, n_tiles):
     rows = tile // cols
     host = inputs.random_bytes(n_tiles * tile_bytes, seed=11).view(void_dtype(esize))
     for direction in (0, 1):
-        got = run(swz, host, n_tiles, rows, cols, esize, B, M, S, direction)
+        got = run(swz, host, n_tiles, rows, cols, esize, B, M, S, direction, path=B)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), direction
+    assert swz.swz_device_status() == swz.SWZ_OK
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("tile_bytes,n_tiles", [(512, 37), (8192, 9), (1536, 11), (65536, 5)])
+def test_atom32_mode(swz, orc, esize, tile_bytes, n_tiles):
+    """The 128-byte mode with 32-byte atoms is element Swizzle<2, 5 - log2 e, 2>
+    for every element size: 32-byte chunks XOR-ed with the 128-byte row mod 4."""
+    from xor_swizzle_movement_gb300 import inputs
+    B, M, S = 2, 5 - LOG2[esize], 2
+    tile = tile_bytes // esize
+    cols = max(1, 128 // esize)
+    rows = tile // cols
+    host = inputs.random_bytes(n_tiles * tile_bytes, seed=14).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run(swz, host, n_tiles, rows, cols, esize, B, M, S, direction, path=4)
         want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
         assert got.tobytes() == want.tobytes(), direction
     assert swz.swz_device_status() == swz.SWZ_OK
@@ -64,7 +86,7 @@ def test_buffer_smaller_than_one_chunk(swz, orc, B, n_tiles):
     rows = tile_bytes // 2 // cols
     host = inputs.uint16_bits(n_tiles * tile_bytes // 2, seed=12)
     for direction in (0, 1):
-        got = run(swz, host, n_tiles, rows, cols, 2, B, 3, 3, direction)
+        got = run(swz, host, n_tiles, rows, cols, 2, B, 3, 3, direction, path=B)
         want = orc.relayout(host, tile_elems=tile_bytes // 2, B=B, M=3, S=3, direction=direction)
         assert np.array_equal(got, want), direction
     assert swz.swz_device_status() == swz.SWZ_OK
@@ -105,6 +127,8 @@ def test_fp16_1gib_sw333(swz, orc):
     dict(esize=2, rows=64, cols=64, B=3, M=3, S=2, n_tiles=4),     # not a hardware mode (S)
     dict(esize=2, rows=8, cols=32, B=3, M=3, S=3, n_tiles=7),      # 512-byte tiles < 1024-byte period
     dict(esize=4, rows=32, cols=32, B=5, M=0, S=5, n_tiles=3),     # B beyond the modes
+    dict(esize=2, rows=2, cols=64, B=2, M=4, S=2, n_tiles=5),      # 256-byte tiles < the 32-byte-atom period
+    dict(esize=2, rows=64, cols=64, B=1, M=5, S=1, n_tiles=3),     # 64-byte atoms: not routed
 ])
 def test_fallback_matches_oracle(swz, orc, case):
     """Requests the TMA modes cannot express run the register kernels."""
@@ -113,7 +137,8 @@ def test_fallback_matches_oracle(swz, orc, case):
     tile = c["rows"] * c["cols"]
     host = inputs.random_bytes(c["n_tiles"] * tile * c["esize"], seed=12).view(void_dtype(c["esize"]))
     for direction in (0, 1):
-        got = run(swz, host, c["n_tiles"], c["rows"], c["cols"], c["esize"], c["B"], c["M"], c["S"], direction)
+        got = run(swz, host, c["n_tiles"], c["rows"], c["cols"], c["esize"], c["B"], c["M"], c["S"], direction,
+                  path=0)
         want = orc.relayout(host, tile_elems=tile, B=c["B"], M=c["M"], S=c["S"], direction=direction)
         assert got.tobytes() == want.tobytes()
 
@@ -121,5 +146,5 @@ def test_fallback_matches_oracle(swz, orc, case):
 def test_misaligned_falls_back(swz, orc):
     from xor_swizzle_movement_gb300 import inputs
     host = inputs.uint16_bits(16 * 64 * 64, seed=13)
-    got = run(swz, host, 16, 64, 64, 2, 3, 3, 3, 0, src_off=2, dst_off=6)
+    got = run(swz, host, 16, 64, 64, 2, 3, 3, 3, 0, src_off=2, dst_off=6, path=0)
     assert np.array_equal(got, orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=0))

@@ -17,7 +17,7 @@ import os
 
 __all__ = [
     "SwzError", "lib", "library_path",
-    "swz_relayout", "swz_relayout_tma", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
+    "swz_relayout", "swz_relayout_tma", "swz_relayout_tma_path", "swz_transpose", "swz_transpose_relayout", "swz_bank_profile", "swz_slice_collision",
     "swz_slice_collision_batch", "swz_slice_layout", "swz_layout_text", "swz_apply", "swz_device_status", "swz_selftest_tma_timeout",
     "swz_transpose_tma_noalloc", "swz_selftest_noalloc_timeout", "swz_staging_probe",
     "swz_status_string", "swz_version",
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.swz_device_status.restype = i32
         L.swz_selftest_tma_timeout.argtypes = [vp, vp, i64, i64, u64, vp]
         L.swz_selftest_tma_timeout.restype = i32
+        L.swz_relayout_tma_path.argtypes = [vp, vp, i64, i64, i64, i32, i32, i32, i32, i32]
+        L.swz_relayout_tma_path.restype = i32
         L.swz_transpose_tma_noalloc.argtypes = [vp, vp, i64, i64, ctypes.POINTER(ctypes.c_uint32), vp]
         L.swz_transpose_tma_noalloc.restype = i32
         L.swz_selftest_noalloc_timeout.argtypes = [vp, vp, i64, i64, u64, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -145,6 +147,13 @@ def swz_relayout_tma(dst, src, n_tiles: int, rows: int, cols: int, esize: int, B
     (S = 3, M + log2 esize = 4, 1 <= B <= 3); otherwise the same as swz_relayout."""
     _check(lib().swz_relayout_tma(_ptr(dst), _ptr(src), n_tiles, rows, cols, esize, B, M, S, direction,
                                   _stream(stream)), "swz_relayout_tma")
+
+
+def swz_relayout_tma_path(dst, src, n_tiles: int, rows: int, cols: int, esize: int, B: int, M: int, S: int,
+                          direction: int) -> int:
+    """0: swz_relayout_tma would run the register kernels; 1..4: the TMA mode
+    (32-, 64-, 128-byte, 128-byte with 32-byte atoms); -status for bad arguments."""
+    return int(lib().swz_relayout_tma_path(_ptr(dst), _ptr(src), n_tiles, rows, cols, esize, B, M, S, direction))
 
 
 def swz_transpose(dst, src, rows: int, cols: int, esize: int, variant: int = SWZ_T_SWIZZLED,

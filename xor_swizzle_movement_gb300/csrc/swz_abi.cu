@@ -11,6 +11,8 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
                            int B, int M, int S, int direction, cudaStream_t st);
 swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize,
                                int B, int M, int S, int direction, cudaStream_t st);
+int relayout_tma_path(const void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize, int B,
+                      int M, int S);
 swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
                             cudaStream_t st);
 swz_status transpose_relayout_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int64_t te,
@@ -133,6 +135,18 @@ swz_status swz_relayout_tma(void *dst, const void *src, int64_t n_tiles, int64_t
     if (v != SWZ_OK || !launch) return v;
     return relayout_tma_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction,
                                static_cast<cudaStream_t>(stream));
+}
+
+int swz_relayout_tma_path(const void *dst, const void *src, int64_t n_tiles, int64_t rows, int64_t cols, int esize,
+                          int B, int M, int S, int direction) {
+    using namespace swz;
+    int64_t tile_elems = 0;
+    bool launch = false;
+    const swz_status v = check_relayout(const_cast<void *>(dst), src, n_tiles, rows, cols, esize, B, M, S, direction,
+                                        &tile_elems, &launch);
+    if (v != SWZ_OK) return -static_cast<int>(v);
+    if (!launch) return 0;
+    return relayout_tma_path(dst, src, n_tiles, tile_elems, esize, B, M, S);
 }
 
 swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols, int esize, int variant,

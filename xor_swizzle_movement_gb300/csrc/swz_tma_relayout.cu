@@ -5,8 +5,10 @@
 // [4, 4 + B) of the shared-memory byte address with bits [7, 7 + B), B = 1, 2,
 // 3: the byte-address Swizzle<B,4,3>, i.e. element Swizzle<B, 4 - log2 e, 3> on
 // e-byte elements ("CuTe Swizzle 学习手册", sections "Sw<3,4,3> vs Sw<3,3,3>"
-// and "H100 TMA + Swizzle").  The buffer is viewed as rows of 2^(B+4) bytes
-// (the swizzle span) and moved in 8 KiB chunks: a swizzled tensor load puts
+// and "H100 TMA + Swizzle").  The 128-byte mode with 32-byte atoms XORs bits
+// [5, 7) with bits [7, 9): the byte-address Swizzle<2,5,2>.  The buffer is
+// viewed as rows of the swizzle span (32, 64 or 128 bytes) and moved in 8 KiB
+// chunks: a swizzled tensor load puts
 // the logical byte at offset i of a chunk at shared offset sw(i), then every
 // thread copies its 16-byte vectors out to dst in order, so dst[sw(i)] =
 // src[i].  Every hardware mode is its own inverse (the field it reads sits
@@ -15,7 +17,7 @@
 // memory with 16-byte stores and left by a swizzled tensor store ran at 6.73
 // against 6.9 TB/s, and its shared stores collided with the tensor store's
 // shared reads on 11% of their wavefronts.)
-// Each chunk covers whole swizzle periods (2^(B+7) bytes) of whole tiles, so
+// Each chunk covers whole swizzle periods (at most 1 KiB) of whole tiles, so
 // the tile-local swizzle equals the swizzle of the chunk-local offset.  The
 // kernel waits on its loads with bounded mbarrier waits (kWaitLimitNs) and
 // records an expiry in the per-device status word.
@@ -119,27 +121,62 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// The hardware swizzle modes as byte-address Swizzle<B, Mb, S> (measured on
+// GB300 with tensor loads of every element size): 16-byte chunks within 32-,
+// 64- and 128-byte spans XOR-ed with the row (bits 7..), and 32-byte chunks
+// within a 128-byte span XOR-ed with the row mod 4.
+struct HwMode {
+    int B, Mb, S;
+    int span;  // bytes per tensor row: the swizzle span
+    CUtensorMapSwizzle mode;
+};
+constexpr int kHwModes = 4;
+const HwMode kModes[kHwModes] = {
+    {1, 4, 3, 32, CU_TENSOR_MAP_SWIZZLE_32B},
+    {2, 4, 3, 64, CU_TENSOR_MAP_SWIZZLE_64B},
+    {3, 4, 3, 128, CU_TENSOR_MAP_SWIZZLE_128B},
+    {2, 5, 2, 128, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B},
+};
+
+// Index into kModes of the hardware mode that runs this request, or -1 when
+// the register kernels run it.
+int tma_plan(const void *dst, const void *src, int64_t bytes, int64_t tile_bytes, int esize, int B, int M, int S) {
+    int k = 0;
+    while ((1 << k) < esize) ++k;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    if (!aligned || !encode_fn()) return -1;
+    for (int i = 0; i < kHwModes; ++i) {
+        const HwMode &h = kModes[i];
+        if (B != h.B || S != h.S || M + k != h.Mb) continue;
+        const int64_t period = int64_t(1) << (h.B + h.Mb + h.S);  // bytes
+        if (tile_bytes % period != 0 || bytes / h.span >= (int64_t(1) << 31)) return -1;
+        return i;
+    }
+    return -1;
+}
+
 }  // namespace
+
+// Which path swz_relayout_tma takes (arguments validated by the caller):
+// 0 for the register kernels, else 1 + the index of the hardware mode.
+int relayout_tma_path(const void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize, int B,
+                      int M, int S) {
+    return 1 + tma_plan(dst, src, n_tiles * tile_elems * esize, tile_elems * esize, esize, B, M, S);
+}
 
 // Arguments are validated by the caller (swz_relayout_tma in swz_abi.cu).
 swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize, int B,
                                int M, int S, int direction, cudaStream_t st) {
-    int k = 0;
-    while ((1 << k) < esize) ++k;
-    const int64_t span = int64_t(16) << B;       // swizzle span: 32, 64 or 128 bytes
-    const int64_t period = span * 8;             // 2^(B+7) bytes
     const int64_t tile_bytes = tile_elems * esize;
     const int64_t bytes = n_tiles * tile_bytes;
-    const bool aligned = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    const int plan = tma_plan(dst, src, bytes, tile_bytes, esize, B, M, S);
+    if (plan < 0) return relayout_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction, st);
+    const HwMode &h = kModes[plan];
     EncodeTiledFn encode = encode_fn();
-    const bool hw_mode = B >= 1 && B <= 3 && S == 3 && M + k == 4;
-    if (!hw_mode || !aligned || !encode || tile_bytes % period != 0 || bytes / span >= (int64_t(1) << 31))
-        return relayout_launch(dst, src, n_tiles, tile_elems, esize, B, M, S, direction, st);
     uint32_t *status = device_status_word(true);
     if (!status) return SWZ_ERR_CUDA;
 
-    static const CUtensorMapSwizzle modes[4] = {CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
-                                                CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_SWIZZLE_128B};
+    const int64_t span = h.span;
     CUtensorMap map;
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(span), static_cast<cuuint64_t>(bytes / span)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(span)};
@@ -147,7 +184,7 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     const cuuint32_t estride[2] = {1, 1};
     (void)direction;  // every hardware mode is its own inverse: both directions are the same copy
     if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(src), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, modes[B], CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, h.mode, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return SWZ_ERR_CUDA;
 
