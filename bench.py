@@ -452,6 +452,14 @@ def measure_rows(torch, swz, dev, flush, peak):
             ms = back_to_back_ms(torch, lambda: fn(dst, src, nt, 64, 64, 2, 3, 3, 3, d))
             r[f"{name}_{'forward' if d == 0 else 'inverse'}"] = summary(ms, 2 << 30)
     out["relayout_fp16_64x64_sw333_1GiB"] = r
+    # Swizzle<2,4,2> on the same buffer: the TMA 128-byte mode with 32-byte atoms
+    r = {}
+    for name, fn in (("register", swz.swz_relayout), ("tma_128B_atom32B", swz.swz_relayout_tma)):
+        for d in (0, 1):
+            ms = back_to_back_ms(torch, lambda: fn(dst, src, nt, 64, 64, 2, 2, 4, 2, d))
+            r[f"{name}_{'forward' if d == 0 else 'inverse'}"] = summary(ms, 2 << 30)
+    r["tma_path"] = swz.swz_relayout_tma_path(dst, src, nt, 64, 64, 2, 2, 4, 2, 0)
+    out["relayout_fp16_64x64_sw242_1GiB"] = r
     del src, dst
 
     src = rand_bytes(1 << 30, 4)
