@@ -902,7 +902,7 @@ def run_case(args):
         shapes = [(iters, torch.cuda.get_device_properties(dev).multi_processor_count * 4), (1, 16384)]
         gbytes = 256 << 20                 # larger than L2: the streamed data comes from DRAM
         gsrc, gdst = rand_bytes(gbytes), torch.empty(gbytes, dtype=torch.uint8, device=dev)
-        stagings = [(4, 0), (4, 1), (4, 2), (2, 0), (2, 1), (2, 2), (8, 0), (8, 1), (8, 2), (1, 0)]
+        stagings = [(4, 0), (4, 1), (4, 2), (2, 0), (2, 1), (2, 2), (2, 3), (8, 0), (8, 1), (8, 2), (1, 0)]
         for it_, ctas in shapes:
             for mode in ("shared_only", "with_global"):
                 for esize, v in stagings:

@@ -52,7 +52,9 @@ enum {
     SWZ_T_UNSWIZZLED = 1, /* plain [T][T] tile: column access is bank-conflicted */
     SWZ_T_PADDED = 2,     /* [T][T + pad] tile: conflict-free, wastes shared memory */
     SWZ_T_TMA = 3         /* 16-bit data only: tile loaded by a TMA tensor copy
-                             with the hardware 128-byte swizzle */
+                             with the hardware 128-byte swizzle (and stored by
+                             one when the output rows are whole 16-byte
+                             vectors) */
 };
 
 /*
@@ -226,8 +228,12 @@ swz_status swz_bank_profile(const uint32_t *byte_addrs, const uint32_t *active, 
  * one shared tile `iters` times with exactly the shared-memory instructions
  * and addresses of the swz_transpose staging of that element size and
  * variant (esize 4 / 8 / 2: SWZ_T_SWIZZLED, SWZ_T_UNSWIZZLED, SWZ_T_PADDED;
- * esize 1: SWZ_T_SWIZZLED, the 128 x 128-byte tile), on values held in
- * registers.
+ * esize 2 also SWZ_T_TMA: the swizzled tile, whose transposing reads are
+ * written with stmatrix into a second tile under the same swizzle, as the
+ * TMA transpose does before its tensor store; esize 1: SWZ_T_SWIZZLED, the
+ * 128 x 128-byte tile), on values held in registers.  The SWZ_T_TMA replay
+ * fills the input tile with 16-byte stores where the transpose uses a tensor
+ * load, so it shows the LSU side of that kernel without any tensor copy.
  *
  * gsrc, gdst, gbytes: optional device buffers of gbytes bytes (a multiple of
  * 16, 16-byte aligned, not overlapping).  NULL: the kernel makes no global
@@ -320,14 +326,13 @@ swz_status swz_selftest_tma_timeout(void *dst, const void *src, int64_t rows, in
  * allocating routine.
  *
  * Computes the same result as swz_transpose(dst, src, rows, cols, 2,
- * SWZ_T_TMA, stream): out[c][r] = in[r][c] for 16-bit elements (raw bits).
- * It always runs the TMA-loaded kernel that stores with 16-byte stores
- * (tensor loads under the hardware 128-byte swizzle, conflict-free
- * transposing matrix reads); SWZ_T_TMA runs that kernel too, except when dst
- * is 16-byte aligned and rows is a multiple of 8, where it also stores
- * through a tensor map.  The two calls can differ in speed, never in result.
- * Both fall back to the shared-memory-staged swizzled kernel when src is not
- * 16-byte aligned or cols is not a multiple of 8.
+ * SWZ_T_TMA, stream): out[c][r] = in[r][c] for 16-bit elements (raw bits),
+ * with the same kernel (one tile per CTA: a tensor load under the hardware
+ * 128-byte swizzle, conflict-free transposing matrix reads, and a tensor
+ * store when dst is 16-byte aligned and rows is a multiple of 8, element
+ * stores otherwise); only the place of its status word differs.  Both fall
+ * back to the shared-memory-staged swizzled kernel when src is not 16-byte
+ * aligned or cols is not a multiple of 8.
  *
  * dst, src  : device buffers of rows x cols 2-byte elements (caller-owned).
  * rows, cols: 0 <= rows, cols < 2^31 (the TMA coordinate range); larger

@@ -44,8 +44,11 @@ def test_layouts_read_back_the_same(swz, esize, with_global):
         gen.manual_seed(7)
         src = torch.randint(0, 256, (1 << 20,), dtype=torch.uint8, device="cuda", generator=gen)
         g = (src, torch.empty_like(src))
-    sums = [_sums(swz, esize, v, ctas, iters, g) for v in (swz.SWZ_T_SWIZZLED, swz.SWZ_T_UNSWIZZLED, swz.SWZ_T_PADDED)]
-    assert np.array_equal(sums[0], sums[1]) and np.array_equal(sums[0], sums[2])
+    variants = [swz.SWZ_T_SWIZZLED, swz.SWZ_T_UNSWIZZLED, swz.SWZ_T_PADDED]
+    if esize == 2:
+        variants.append(swz.SWZ_T_TMA)   # the TMA kernel's staging: an stmatrix output tile as well
+    sums = [_sums(swz, esize, v, ctas, iters, g) for v in variants]
+    assert all(np.array_equal(sums[0], s) for s in sums[1:])
     # the CTAs differ only through the streamed data
     assert (len(set(sums[0].tolist())) > 1) == with_global
     if with_global:
@@ -58,6 +61,9 @@ def test_byte_staging_runs_and_rejects(swz):
     assert s.shape == (16,)
     with pytest.raises(swz.SwzError) as e:
         swz.swz_staging_probe(1, swz.SWZ_T_UNSWIZZLED, 1, 1)
+    assert e.value.status == swz.SWZ_ERR_PARAM
+    with pytest.raises(swz.SwzError) as e:
+        swz.swz_staging_probe(4, swz.SWZ_T_TMA, 1, 1)
     assert e.value.status == swz.SWZ_ERR_PARAM
     with pytest.raises(swz.SwzError) as e:
         swz.swz_staging_probe(16, swz.SWZ_T_SWIZZLED, 1, 1)

@@ -12,6 +12,10 @@
 //   2 bytes:     64 x 64 with 16-byte chunk c of row r at c ^ (r mod 8)
 //                (byte-address Swizzle<3,4,3>), plain, or rows of 72
 //                elements; the drain reads with ldmatrix .x4 .trans;
+//                SWZ_T_TMA adds the TMA kernel's second tile: each drained
+//                8 x 8 block is written with stmatrix .x4 into an output
+//                tile under the same swizzle (which the tensor store reads
+//                in the transpose; here nothing reads it);
 //   1 byte:      128 x 128 bytes, 16-byte chunk c of row r at
 //                c ^ ((r / 16) mod 8) (byte-address Swizzle<3,4,7>).
 // A tile is filled and drained `iters` times.  With no global buffer given the
@@ -120,9 +124,13 @@ template <int VARIANT>
 __global__ void __launch_bounds__(128) probe_16_kernel(const ProbeArgs a) {
     constexpr int THREADS = 128;
     constexpr int PITCH = (VARIANT == SWZ_T_PADDED) ? 72 : 64;
+    constexpr bool OUT_TILE = VARIANT == SWZ_T_TMA;
     __shared__ __align__(1024) uint16_t sm[64 * PITCH];
+    __shared__ __align__(1024) uint16_t out_sm[OUT_TILE ? 64 * 64 : 8];
     const int tid = threadIdx.x;
-    auto chunk = [](int row, int ch) -> int { return VARIANT == SWZ_T_SWIZZLED ? (ch ^ (row & 7)) : ch; };
+    auto chunk = [](int row, int ch) -> int {
+        return (VARIANT == SWZ_T_SWIZZLED || VARIANT == SWZ_T_TMA) ? (ch ^ (row & 7)) : ch;
+    };
     uint32_t acc = tid;
     for (int it = 0; it < a.iters; ++it) {
         uint4 v[4];
@@ -149,6 +157,14 @@ __global__ void __launch_bounds__(128) probe_16_kernel(const ProbeArgs a) {
             const int row = (rbg + m) * 8 + i;
             uint32_t a0, a1, a2, a3;
             probe_ldmatrix_x4_trans(smem_u32(sm + row * PITCH + chunk(row, cb) * 8), a0, a1, a2, a3);
+            if constexpr (OUT_TILE) {
+                // block (rbg + m, cb) transposed goes to output block (cb, rbg + m)
+                const int orow = cb * 8 + i;
+                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(
+                                 smem_u32(out_sm + orow * 64 + (((rbg + m) ^ (orow & 7)) << 3))),
+                             "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+                             : "memory");
+            }
             const uint4 o = make_uint4(a0, a1, a2, a3);
             acc ^= fold(o);
             if (a.gdst) st_stream16(a.gdst + probe_gvec(a, it, k, 4), o);
@@ -207,7 +223,9 @@ extern "C" swz_status swz_staging_probe(int esize, int variant, int iters, const
                                         int64_t gbytes, uint32_t *sink, int64_t ctas, void *stream) {
     using namespace swz;
     if (iters < 0 || ctas < 0 || ctas > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    if (variant != SWZ_T_SWIZZLED && variant != SWZ_T_UNSWIZZLED && variant != SWZ_T_PADDED) return SWZ_ERR_PARAM;
+    if (variant != SWZ_T_SWIZZLED && variant != SWZ_T_UNSWIZZLED && variant != SWZ_T_PADDED &&
+        !(variant == SWZ_T_TMA && esize == 2))
+        return SWZ_ERR_PARAM;
     if (esize != 1 && esize != 2 && esize != 4 && esize != 8) return SWZ_ERR_PARAM;
     if (esize == 1 && variant != SWZ_T_SWIZZLED) return SWZ_ERR_PARAM;
     if ((gsrc || gdst) && (gbytes < 16 || gbytes % 16 != 0)) return SWZ_ERR_SHAPE;
@@ -227,6 +245,7 @@ extern "C" swz_status swz_staging_probe(int esize, int variant, int iters, const
         case 2:
             if (variant == SWZ_T_SWIZZLED) probe_16_kernel<SWZ_T_SWIZZLED><<<g, 128, 0, st>>>(a);
             else if (variant == SWZ_T_UNSWIZZLED) probe_16_kernel<SWZ_T_UNSWIZZLED><<<g, 128, 0, st>>>(a);
+            else if (variant == SWZ_T_TMA) probe_16_kernel<SWZ_T_TMA><<<g, 128, 0, st>>>(a);
             else probe_16_kernel<SWZ_T_PADDED><<<g, 128, 0, st>>>(a);
             break;
         case 4:

@@ -8,26 +8,28 @@
 // rows it is exactly the layout of the SWZ_T_SWIZZLED 16-bit kernel, so the
 // same conflict-free transposing matrix loads drain it.
 //
-// When the output rows are whole 16-byte vectors the output leaves by TMA
-// too (transpose16_tma_ls_kernel): ldmatrix .trans, then stmatrix into an
-// output tile under the same 128-byte swizzle, then one tensor store per tile.
-// Otherwise the drained rows leave by 16-byte stores (transpose16_tma_kernel).
+// One 64 x 64 tile per CTA (a grid of one CTA per tile, up to 12 resident per
+// SM): one thread issues the tile's tensor load, every thread waits on the
+// tile's mbarrier, and the drain reads 8 x 8 blocks with ldmatrix .trans.
+// When the output rows are whole 16-byte vectors (TSTORE) the blocks go out
+// through stmatrix into an output tile under the same 128-byte swizzle and
+// one tensor store; otherwise element by element from the shared tile.
+// The hardware block scheduler hands out tiles in order, so the tiles in
+// flight stay a compact band of the matrix; a persistent grid that walked
+// tiles blockIdx.x, +gridDim.x, ... with a ring of stages drifted apart and
+// ran 5-10% slower on the 16384^2 matrix.
 //
-// Persistent kernels: each CTA walks tiles blockIdx.x, +gridDim.x, ...; a
-// ring of kStages shared buffers keeps kStages tile loads in flight while the
-// current tile is drained.  One elected thread issues the copies; each buffer
-// has an mbarrier that the copy completes.  Every wait on an mbarrier is
-// bounded by a time limit; on expiry the kernel records SWZ_ERR_TIMEOUT in a
-// per-device status word, waits (again bounded) for its own copies still in
-// flight, and returns; swz_device_status() reports it to the host.
+// Every wait on the mbarrier is bounded by a time limit; on expiry the kernel
+// records SWZ_ERR_TIMEOUT in a status word, waits (again bounded) for its own
+// copy still in flight, and returns; swz_device_status() reports it.
 #include "swz_tma_common.cuh"
 
+#include <climits>
 #include <mutex>
 
 namespace swz {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTile = 64;                        // 64 x 64 elements
 constexpr int kTileBytes = kTile * kTile * 2;    // 8 KiB
 constexpr int kThreads = 128;
@@ -39,209 +41,98 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &d0, u
                  : "r"(addr));
 }
 
-__device__ __forceinline__ uint32_t pick4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, int i) {
-    const uint32_t lo = (i & 1) ? a1 : a0;
-    const uint32_t hi = (i & 1) ? a3 : a2;
-    return (i & 2) ? hi : lo;
-}
-
-struct TmaArgs {
-    uint16_t *dst;
-    int64_t R, C, tiles_c, n_tiles;
-    int vec_store_ok;
-    int issue_copies;   // 0 only in the timeout self-test: no copy is issued, every wait expires
-    uint64_t wait_ns;
-    uint32_t *status;   // per-device status word
-};
-
-__global__ void __launch_bounds__(kThreads)
-    transpose16_tma_kernel(const __grid_constant__ CUtensorMap map, const TmaArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kStages];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
-    uint8_t *const gbase = smem_raw + (base - raw);
-    const int tid = threadIdx.x;
-    const uint32_t bar0 = smem_u32(&bars[0]);
-
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
-
-    auto issue = [&](int s, int64_t t) {
-        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
-        mbar_expect_tx(bar0 + 8u * s, kTileBytes);
-        tma_load_2d(base + s * kTileBytes, &map, static_cast<int>(tc * kTile), static_cast<int>(tr * kTile),
-                    bar0 + 8u * s);
-    };
-    if (tid == 0 && a.issue_copies) {
-        for (int s = 0; s < kStages; ++s) {
-            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-            if (t < a.n_tiles) issue(s, t);
-        }
-    }
-
-    const int lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, kk = lane & 3, m = lane >> 3, i8 = lane & 7;
-    int64_t it = 0;
-    for (;; ++it) {
-        const int64_t t = blockIdx.x + it * gridDim.x;
-        if (t >= a.n_tiles) break;
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t parity = static_cast<uint32_t>((it / kStages) & 1);
-        const bool ok = mbar_wait_bounded(bar0 + 8u * s, parity, a.wait_ns);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
-            // let this CTA's copies still in flight land before the CTA exits
-            if (a.issue_copies) {
-                for (int64_t j = it; j < it + kStages; ++j) {
-                    const int64_t tj = blockIdx.x + j * gridDim.x;
-                    if (tj >= a.n_tiles) break;
-                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kStages),
-                                      static_cast<uint32_t>((j / kStages) & 1), a.wait_ns);
-                }
-            }
-            return;
-        }
-        const uint16_t *sm = reinterpret_cast<const uint16_t *>(gbase + s * kTileBytes);
-        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
-        const int64_t r0 = tr * kTile, c0 = tc * kTile;
-        if (a.vec_store_ok && r0 + kTile <= a.R && c0 + kTile <= a.C) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int xi = warp * 4 + k;
-                const int cb = xi & 7, rbg = (xi >> 3) * 4;
-                const int row = (rbg + m) * 8 + i8;
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(base + s * kTileBytes + row * 128 + ((cb ^ (row & 7)) << 4), a0, a1, a2, a3);
-                uint32_t b0 = 0, b1 = 0, b2 = 0, b3 = 0;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int from = kk ^ r;
-                    const uint32_t send = pick4(a0, a1, a2, a3, from);
-                    const uint32_t got = r ? __shfl_xor_sync(kFullMask, send, r) : send;
-                    b0 = (from == 0) ? got : b0;
-                    b1 = (from == 1) ? got : b1;
-                    b2 = (from == 2) ? got : b2;
-                    b3 = (from == 3) ? got : b3;
-                }
-                st_stream16(a.dst + (c0 + cb * 8 + g) * a.R + r0 + (rbg + kk) * 8, make_uint4(b0, b1, b2, b3));
-            }
-        } else {
-            for (int idx = tid; idx < kTile * kTile; idx += kThreads) {
-                const int ocl = idx / kTile, orow = idx % kTile;
-                if (c0 + ocl < a.C && r0 + orow < a.R)
-                    a.dst[(c0 + ocl) * a.R + r0 + orow] = sm[orow * 64 + (((ocl >> 3) ^ (orow & 7)) << 3) + (ocl & 7)];
-            }
-        }
-        // every thread orders its reads of buffer s before the tensor copy
-        // that refills it (the copy writes through the async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        if (tid == 0 && a.issue_copies) {
-            const int64_t tn = t + static_cast<int64_t>(kStages) * gridDim.x;
-            if (tn < a.n_tiles) issue(s, tn);
-        }
-    }
-}
-
 __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3) {
     asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(d0), "r"(d1),
                  "r"(d2), "r"(d3)
                  : "memory");
 }
 
-constexpr int kOutBufs = 2;
+struct TmaArgs {
+    uint16_t *dst;
+    int64_t R, C, tiles_c, n_tiles;
+    int issue_copies;   // 0 only in the timeout self-tests: no copy is issued, every wait expires
+    uint64_t wait_ns;
+    uint32_t *status;   // status word that an expired wait reports to
+};
 
-// Both directions through the tensor-memory accelerator: the input tile
-// arrives under the 128-byte swizzle, each warp transposes its 8 x 8 blocks
-// with ldmatrix .trans and writes them with stmatrix into an output tile laid
-// out under the same swizzle, and one thread stores that tile with a tensor
-// copy.  Edge tiles need no special case: the load fills out-of-range
-// elements with zeros and the store drops them.  Output buffers are double
-// buffered; a buffer is rewritten only after the store issued from it two
-// tiles earlier has finished reading it.
+// Dynamic shared memory of the kernel: the input tile, the output tile when
+// TSTORE, and up to 1 KiB of slack to align them to the swizzle's 1024 bytes.
+constexpr int tma_smem_bytes(bool tstore) { return (tstore ? 2 : 1) * kTileBytes + 1024; }
+
+template <bool TSTORE>
 __global__ void __launch_bounds__(kThreads)
-    transpose16_tma_ls_kernel(const __grid_constant__ CUtensorMap map_in, const __grid_constant__ CUtensorMap map_out,
-                              const TmaArgs a) {
+    transpose16_tma_kernel(const __grid_constant__ CUtensorMap map_in, const __grid_constant__ CUtensorMap map_out,
+                           const TmaArgs a) {
     pdl_launch_dependents();
     pdl_wait();  // before the first tensor copy
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[kStages];
+    __shared__ __align__(8) uint64_t bar;
     const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t out_base = base + kStages * kTileBytes;
+    const uint32_t ib = (raw + 1023u) & ~1023u;  // the 128-byte swizzle repeats every 1024 bytes
+    const uint32_t ob = ib + kTileBytes;
+    const uint16_t *sm = reinterpret_cast<const uint16_t *>(smem_raw + (ib - raw));
     const int tid = threadIdx.x;
-    const uint32_t bar0 = smem_u32(&bars[0]);
+    const uint32_t b = smem_u32(&bar);
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8u * s, 1);
+        mbar_init(b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
 
-    auto issue = [&](int s, int64_t t) {
-        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
-        mbar_expect_tx(bar0 + 8u * s, kTileBytes);
-        tma_load_2d(base + s * kTileBytes, &map_in, static_cast<int>(tc * kTile), static_cast<int>(tr * kTile),
-                    bar0 + 8u * s);
-    };
-    if (tid == 0 && a.issue_copies) {
-        for (int s = 0; s < kStages; ++s) {
-            const int64_t t = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-            if (t < a.n_tiles) issue(s, t);
-        }
-    }
-
     const int lane = tid & 31, warp = tid >> 5;
     const int m = lane >> 3, i8 = lane & 7;  // matrix addressed by this lane, its row
-    for (int64_t it = 0;; ++it) {
-        const int64_t t = blockIdx.x + it * gridDim.x;
-        if (t >= a.n_tiles) break;
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t ob = out_base + static_cast<uint32_t>(it & 1) * kTileBytes;
-        const bool ok = mbar_wait_bounded(bar0 + 8u * s, static_cast<uint32_t>((it / kStages) & 1), a.wait_ns);
-        if (tid == 0 && it >= kOutBufs) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    uint32_t it = 0;                         // tiles done by this CTA (the barrier's phase)
+    for (int64_t t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++it) {
+        const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
+        if (tid == 0 && a.issue_copies) {
+            mbar_expect_tx(b, kTileBytes);
+            tma_load_2d(ib, &map_in, static_cast<int>(tc * kTile), static_cast<int>(tr * kTile), b);
+        }
+        const bool ok = mbar_wait_bounded(b, it & 1u, a.wait_ns);
         if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
-            if (a.issue_copies) {
-                for (int64_t j = it; j < it + kStages; ++j) {
-                    const int64_t tj = blockIdx.x + j * gridDim.x;
-                    if (tj >= a.n_tiles) break;
-                    mbar_wait_bounded(bar0 + 8u * static_cast<uint32_t>(j % kStages),
-                                      static_cast<uint32_t>((j / kStages) & 1), a.wait_ns);
-                }
+            if (tid == 0) {
+                atomicOr(a.status, 1u << SWZ_ERR_TIMEOUT);
+                // let this CTA's copy still in flight land before the CTA exits
+                if (a.issue_copies) mbar_wait_bounded(b, it & 1u, a.wait_ns);
+                if (TSTORE) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             }
-            if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
             return;
         }
-        const uint32_t ib = base + s * kTileBytes;
+        if constexpr (TSTORE) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int xi = warp * 4 + k;
-            const int cb = xi & 7, rbg = (xi >> 3) * 4;
-            const int row = (rbg + m) * 8 + i8;   // input tile row this lane addresses
-            uint32_t d0, d1, d2, d3;
-            ldmatrix_x4_trans(ib + row * 128 + ((cb ^ (row & 7)) << 4), d0, d1, d2, d3);
-            // block (rbg + m, cb) transposed lands at output block (cb, rbg + m)
-            const int orow = cb * 8 + i8;
-            stmatrix_x4(ob + orow * 128 + (((rbg + m) ^ (orow & 7)) << 4), d0, d1, d2, d3);
+            for (int k = 0; k < 4; ++k) {
+                const int xi = warp * 4 + k;
+                const int cb = xi & 7, rbg = (xi >> 3) * 4;
+                const int row = (rbg + m) * 8 + i8;   // input tile row this lane addresses
+                uint32_t d0, d1, d2, d3;
+                ldmatrix_x4_trans(ib + row * 128 + ((cb ^ (row & 7)) << 4), d0, d1, d2, d3);
+                // block (rbg + m, cb) transposed lands at output block (cb, rbg + m)
+                const int orow = cb * 8 + i8;
+                stmatrix_x4(ob + orow * 128 + (((rbg + m) ^ (orow & 7)) << 4), d0, d1, d2, d3);
+            }
+            // the shared writes are ordered before the tensor store that reads them,
+            // and the shared reads before the next tensor load into the input tile
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (tid == 0) {
+                tma_store_2d(&map_out, static_cast<int>(tr * kTile), static_cast<int>(tc * kTile), ob);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                // the output tile is read before this CTA rewrites it or exits
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            }
+        } else {
+            const int64_t r0 = tr * kTile, c0 = tc * kTile;
+            for (int idx = tid; idx < kTile * kTile; idx += kThreads) {
+                const int ocl = idx / kTile, orow = idx % kTile;
+                if (c0 + ocl < a.C && r0 + orow < a.R)
+                    a.dst[(c0 + ocl) * a.R + r0 + orow] = sm[orow * 64 + (((ocl >> 3) ^ (orow & 7)) << 3) + (ocl & 7)];
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();  // output tile complete, input buffer s consumed
-        if (tid == 0) {
-            const int64_t tr = t / a.tiles_c, tc = t - tr * a.tiles_c;
-            tma_store_2d(&map_out, static_cast<int>(tr * kTile), static_cast<int>(tc * kTile), ob);
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            const int64_t tn = t + static_cast<int64_t>(kStages) * gridDim.x;
-            if (a.issue_copies && tn < a.n_tiles) issue(s, tn);
-        }
+        __syncthreads();  // the tiles are free for the next tile of this CTA
     }
-    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---- host side ---------------------------------------------------------
@@ -266,23 +157,6 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// The load+store kernel needs more than the default 48 KiB of dynamic shared
-// memory; the attribute is set once per device.
-bool ls_smem_attribute_set(int smem) {
-    static std::mutex mu;
-    static bool done[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
-        if (cudaFuncSetAttribute(transpose16_tma_ls_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return false;
-        done[dev] = true;
-    }
-    return true;
-}
-
 // The per-device status word (allocated once per device, on first use).
 uint32_t *device_status_word(bool create) {
     int dev = 0;
@@ -300,6 +174,52 @@ uint32_t *device_status_word(bool create) {
 swz_status transpose_launch(void *dst, const void *src, int64_t R, int64_t C, int esize, int variant,
                             cudaStream_t st);
 
+// Encodes the tensor maps and launches transpose16_tma_kernel: the output
+// leaves by tensor store when its rows are whole 16-byte vectors (dst 16-byte
+// aligned, rows a multiple of 8), element by element otherwise.  Expired waits
+// report to `status`.  The caller has checked that TMA applies (src 16-byte
+// aligned, cols a multiple of 8, rows and cols below 2^31).
+swz_status tma_transpose_enqueue(EncodeTiledFn encode, void *dst, const void *src, int64_t R, int64_t C,
+                                 cudaStream_t st, int issue_copies, uint64_t wait_ns, uint32_t *status) {
+    CUtensorMap map_in, map_out;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(C) * 2};
+    const cuuint32_t box[2] = {kTile, kTile};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&map_in, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(src), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SWZ_ERR_CUDA;
+    const bool tstore = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (R % 8 == 0);
+    if (tstore) {
+        // the output (C x R, rows of R elements) goes out through its own tensor map
+        const cuuint64_t odim[2] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(C)};
+        const cuuint64_t ostride[1] = {static_cast<cuuint64_t>(R) * 2};
+        if (encode(&map_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dst, odim, ostride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return SWZ_ERR_CUDA;
+    } else {
+        map_out = map_in;  // not read by the element-wise drain
+    }
+    TmaArgs a;
+    a.dst = static_cast<uint16_t *>(dst);
+    a.R = R;
+    a.C = C;
+    a.tiles_c = (C + kTile - 1) / kTile;
+    a.n_tiles = ((R + kTile - 1) / kTile) * a.tiles_c;
+    a.issue_copies = issue_copies;
+    a.wait_ns = wait_ns;
+    a.status = status;
+    // one CTA per tile; past the grid limit each CTA takes every gridDim.x-th tile
+    const unsigned grid = static_cast<unsigned>(a.n_tiles < INT_MAX ? a.n_tiles : INT_MAX);
+    if (tstore)
+        return launched(launch_pdl(transpose16_tma_kernel<true>, dim3(grid), dim3(kThreads), tma_smem_bytes(true),
+                                   st, map_in, map_out, a));
+    return launched(launch_pdl(transpose16_tma_kernel<false>, dim3(grid), dim3(kThreads), tma_smem_bytes(false), st,
+                               map_in, map_out, a));
+}
+
 swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st,
                              int issue_copies, uint64_t wait_ns) {
     // TMA needs 16-byte aligned source rows and int32 coordinates; otherwise
@@ -310,44 +230,7 @@ swz_status transpose_tma_run(void *dst, const void *src, int64_t R, int64_t C, c
     if (!tma_ok || !encode) return transpose_launch(dst, src, R, C, 2, SWZ_T_SWIZZLED, st);
     uint32_t *status = device_status_word(true);
     if (!status) return SWZ_ERR_CUDA;
-
-    CUtensorMap map;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(C) * 2};
-    const cuuint32_t box[2] = {kTile, kTile};
-    const cuuint32_t estride[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(src), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return SWZ_ERR_CUDA;
-
-    TmaArgs a;
-    a.dst = static_cast<uint16_t *>(dst);
-    a.R = R;
-    a.C = C;
-    a.tiles_c = (C + kTile - 1) / kTile;
-    a.n_tiles = ((R + kTile - 1) / kTile) * a.tiles_c;
-    a.vec_store_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (R % 8 == 0);
-    a.issue_copies = issue_copies;
-    a.wait_ns = wait_ns;
-    a.status = status;
-    int grid = sm_count() * 4;
-    if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
-    if (a.vec_store_ok) {
-        // the output (C x R, rows of R elements) also goes out through a tensor map
-        CUtensorMap map_out;
-        const cuuint64_t odim[2] = {static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(C)};
-        const cuuint64_t ostride[1] = {static_cast<cuuint64_t>(R) * 2};
-        if (encode(&map_out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dst, odim, ostride, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return SWZ_ERR_CUDA;
-        const int smem = (kStages + kOutBufs) * kTileBytes + 1024;
-        if (!ls_smem_attribute_set(smem)) return SWZ_ERR_CUDA;
-        return launched(launch_pdl(transpose16_tma_ls_kernel, dim3(grid), dim3(kThreads), smem, st, map, map_out, a));
-    }
-    transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
-    return launch_status();
+    return tma_transpose_enqueue(encode, dst, src, R, C, st, issue_copies, wait_ns, status);
 }
 
 swz_status transpose_tma_launch(void *dst, const void *src, int64_t R, int64_t C, cudaStream_t st) {
@@ -454,29 +337,7 @@ swz_status noalloc_run(void *dst, const void *src, int64_t rows, int64_t cols, u
     if (cudaMemsetAsync(scratch, 0, kNoAllocWordsNeeded * sizeof(uint32_t), st) != cudaSuccess)
         return SWZ_ERR_CUDA;
 
-    CUtensorMap map;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {kTile, kTile};
-    const cuuint32_t estride[2] = {1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(src), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return SWZ_ERR_CUDA;
-    TmaArgs a;
-    a.dst = static_cast<uint16_t *>(dst);
-    a.R = rows;
-    a.C = cols;
-    a.tiles_c = (cols + kTile - 1) / kTile;
-    a.n_tiles = ((rows + kTile - 1) / kTile) * a.tiles_c;
-    a.vec_store_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (rows % 8 == 0);
-    a.issue_copies = issue_copies;
-    a.wait_ns = wait_ns;
-    a.status = scratch;
-    int grid = sm_count() * 4;
-    if (a.n_tiles < grid) grid = static_cast<int>(a.n_tiles);
-    transpose16_tma_kernel<<<grid, kThreads, kStages * kTileBytes + 1024, st>>>(map, a);
-    const swz_status s = launch_status();
+    const swz_status s = tma_transpose_enqueue(encode, dst, src, rows, cols, st, issue_copies, wait_ns, scratch);
     if (s != SWZ_OK || !timed_out) return s;
     uint32_t v = 0;
     if (cudaStreamSynchronize(st) != cudaSuccess ||

@@ -8,7 +8,7 @@
 // and "H100 TMA + Swizzle").  The 128-byte mode with 32-byte atoms XORs bits
 // [5, 7) with bits [7, 9): the byte-address Swizzle<2,5,2>.  The buffer is
 // viewed as rows of the swizzle span (32, 64 or 128 bytes) and moved in 8 KiB
-// chunks: a swizzled tensor load puts
+// chunks, one per CTA: a swizzled tensor load puts
 // the logical byte at offset i of a chunk at shared offset sw(i), then every
 // thread copies its 16-byte vectors out to dst in order, so dst[sw(i)] =
 // src[i].  Every hardware mode is its own inverse (the field it reads sits
@@ -23,6 +23,8 @@
 // records an expiry in the per-device status word.
 #include "swz_tma_common.cuh"
 
+#include <climits>
+
 namespace swz {
 
 swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems, int esize, int B,
@@ -33,7 +35,12 @@ namespace {
 constexpr int kChunk = 8192;                         // bytes per tensor copy
 constexpr int kThreads = 256;
 constexpr int kVecs = kChunk / 16 / kThreads;        // 16-byte vectors per thread per chunk
-constexpr int kRing = 3, kCtasPerSm = 2;           // 3 chunks in flight per CTA
+// One chunk per CTA: a grid of one CTA per chunk (8 resident per SM) keeps the
+// chunks in flight a compact band of the buffer.  A persistent grid of 2 CTAs
+// per SM with 3 chunks in flight each ran at 6.84 against 7.06 TB/s (1 GiB,
+// 128-byte mode); past the grid limit a CTA takes every gridDim.x-th chunk and
+// loads the next while it stores the current one.
+constexpr int kRing = 1;
 
 struct TmaRelayoutArgs {
     uint8_t *dst;
@@ -196,8 +203,7 @@ swz_status relayout_tma_launch(void *dst, const void *src, int64_t n_tiles, int6
     a.rows_per_chunk = static_cast<int>(kChunk / span);
     a.wait_ns = kWaitLimitNs;
     a.status = status;
-    int64_t grid = static_cast<int64_t>(sm_count()) * kCtasPerSm;
-    if (a.n_chunks < grid) grid = a.n_chunks;
+    const int64_t grid = a.n_chunks < INT_MAX ? a.n_chunks : INT_MAX;
     const dim3 g(static_cast<unsigned>(grid));
     return launched(launch_pdl(relayout_tma_kernel, g, dim3(kThreads), kRing * kChunk + 1024, st, map, a));
 }
