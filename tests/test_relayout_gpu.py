@@ -252,3 +252,30 @@ def test_host_buffers_through_the_device_address_space(swz, orc):
     want = orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=0)
     assert np.array_equal(phys.cpu().numpy().view(np.uint16), want)
     assert np.array_equal(h_back.numpy().view(np.uint16), host)
+
+
+@pytest.mark.parametrize("esize,rows,cols,bms", [
+    (1, 64, 128, (5, 2, 5)),    # the int8 tiles, lanes XOR-ed
+    (2, 64, 64, (3, 3, 3)),     # 16-bit, lanes fixed
+    (2, 3, 8, (2, 1, 3)),       # 48-byte tiles, period 64 elements: tile-local offsets
+    (4, 5, 8, (2, 1, 1)),       # S < B, 160-byte tiles: tile-local offsets, general lane map
+])
+def test_host_buffers_larger_than_the_link_grid(swz, orc, esize, rows, cols, bms):
+    """On host buffers the library caps the grid at 4 CTAs per SM and strides
+    over the buffer; 64 MiB takes several strides.  Forward reads a pinned
+    host buffer, inverse writes one; both match the oracle."""
+    from xor_swizzle_movement_gb300 import inputs
+    tile_bytes = rows * cols * esize
+    n_tiles = (64 << 20) // tile_bytes
+    host = inputs.random_bytes(n_tiles * tile_bytes, seed=8)
+    h_src = torch.from_numpy(host.copy()).pin_memory()
+    h_back = torch.zeros_like(h_src).pin_memory()
+    phys = torch.empty(h_src.numel(), dtype=torch.uint8, device="cuda")
+    B, M, S = bms
+    swz.swz_relayout(phys, h_src.data_ptr(), n_tiles, rows, cols, esize, B, M, S, 0)
+    swz.swz_relayout(h_back.data_ptr(), phys, n_tiles, rows, cols, esize, B, M, S, 1)
+    torch.cuda.synchronize()
+    view = {1: np.uint8, 2: np.uint16, 4: np.uint32}[esize]
+    want = orc.relayout(host.view(view), tile_elems=rows * cols, B=B, M=M, S=S, direction=0)
+    assert np.array_equal(phys.cpu().numpy().view(view), want)
+    assert np.array_equal(h_back.numpy(), host)

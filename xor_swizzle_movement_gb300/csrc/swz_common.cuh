@@ -153,10 +153,11 @@ inline void lane_map_selectors(const int *src_lane, int esize, uint32_t sel[12])
 }
 }  // namespace swz
 
-// Launch `kernel` with programmatic dependent launch allowed (see pdl_wait).
+// Launch `kernel` with programmatic dependent launch allowed (see pdl_wait),
+// or, with pdl false, as a plain launch (its pdl_wait is then a no-op).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args &&...args) {
+cudaError_t launch_pdl_if(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -166,8 +167,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    return launch_pdl_if(true, kernel, grid, block, smem, st, std::forward<Args>(args)...);
 }
 
 // Host-side helpers shared by the launchers (defined in swz_abi.cu).
@@ -176,4 +183,5 @@ swz_status launch_status();
 swz_status launched(cudaError_t launch_result);  // status of a launch_pdl call
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes);
 int sm_count();  // SMs of the current device (cached per device)
+bool host_resident(const void *p);  // p is host memory (pinned or pageable), not device or managed memory
 }  // namespace swz

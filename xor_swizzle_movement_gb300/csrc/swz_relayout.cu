@@ -62,41 +62,50 @@ struct RelayoutArgs {
 constexpr int kMaxPerThread = 4;
 
 
-template <int E, int MODE, bool LOCAL>
+// LINK: the variant for host-resident buffers, whose grid is sized for the
+// host link: the grid walks the buffer in strides of itself, and loads carry
+// no L2 eviction hint (with the evict-first hint a host-reading launch beside
+// a host-writing one moved 12% less over the link).  Otherwise one CTA covers
+// one stretch of blockDim.x * per_thread vectors, loads marked evict-first.
+template <int E, int MODE, bool LOCAL, bool LINK>
 __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a) {
     constexpr int LV = VecTraits<E>::LV;
     constexpr uint64_t VM = (1u << LV) - 1u;
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
-    uint4 r[kMaxPerThread];
-    uint32_t lx[kMaxPerThread];
-    const uint64_t policy = l2_evict_first_policy();
-    // all loads first, so that each thread keeps up to kMaxPerThread 16-byte loads in flight
+    const int64_t step = LINK ? static_cast<int64_t>(gridDim.x) * blockDim.x * a.per_thread : a.nvec;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x; base < a.nvec;
+         base += step) {
+        uint4 r[kMaxPerThread];
+        uint32_t lx[kMaxPerThread];
+        const uint64_t policy = l2_evict_first_policy();
+        // all loads first, so that each thread keeps up to kMaxPerThread 16-byte loads in flight
 #pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
-        if (k < a.per_thread && u < a.nvec) {
-            int64_t local = u, tile0 = 0;
-            if constexpr (LOCAL) {
-                local = u % a.tile_vecs;
-                tile0 = u - local;
+        for (int k = 0; k < kMaxPerThread; ++k) {
+            const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+            if (k < a.per_thread && u < a.nvec) {
+                int64_t local = u, tile0 = 0;
+                if constexpr (LOCAL) {
+                    local = u % a.tile_vecs;
+                    tile0 = u - local;
+                }
+                const uint64_t y = static_cast<uint64_t>(local) << LV;
+                const uint64_t x = sw_inv(y, a.B, a.M, a.S, a.steps);
+                const uint4 *p = a.src + tile0 + static_cast<int64_t>(x >> LV);
+                r[k] = LINK ? ld_stream16(p) : ld_stream16_hint(p, policy);
+                lx[k] = static_cast<uint32_t>(x & VM);
             }
-            const uint64_t y = static_cast<uint64_t>(local) << LV;
-            const uint64_t x = sw_inv(y, a.B, a.M, a.S, a.steps);
-            r[k] = ld_stream16_hint(a.src + tile0 + static_cast<int64_t>(x >> LV), policy);
-            lx[k] = static_cast<uint32_t>(x & VM);
         }
-    }
 #pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
-        if (k < a.per_thread && u < a.nvec) {
-            uint4 out;
-            if constexpr (MODE == kLanesFixed) out = r[k];
-            else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
-            else out = bytes_permute(lanes_xor<E>(r[k], lx[k]), a.perm_sel);
-            st_stream16(a.dst + u, out);
+        for (int k = 0; k < kMaxPerThread; ++k) {
+            const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+            if (k < a.per_thread && u < a.nvec) {
+                uint4 out;
+                if constexpr (MODE == kLanesFixed) out = r[k];
+                else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
+                else out = bytes_permute(lanes_xor<E>(r[k], lx[k]), a.perm_sel);
+                st_stream16(a.dst + u, out);
+            }
         }
     }
 }
@@ -148,24 +157,34 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// link_grid: a buffer lives in host memory.  The host link, not the SMs,
+// bounds such a copy (about 0.2 TB/s each way, reached with a few dozen
+// CTAs), so the grid is capped at 4 CTAs per SM and strides over the buffer:
+// a relayout writing host memory on one stream then runs beside one reading
+// it on another, and both directions of the link carry data at once.  A grid
+// of one CTA per stretch would fill every SM until its last wave and
+// serialise the two.  Such launches also go without programmatic dependent
+// launch: the next kernel's CTAs would otherwise sit resident, waiting, in
+// the slots the other stream's kernel needs.
 template <int E>
-swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, cudaStream_t st) {
+swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, bool link_grid, cudaStream_t st) {
     const int threads = 256;
     const int64_t per_cta = static_cast<int64_t>(threads) * a.per_thread;
-    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+    if (link_grid && grid > cap) grid = cap;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     const dim3 g(static_cast<unsigned>(grid));
-#define SWZ_LAUNCH(MODE, LOCAL) launch_pdl(relayout_vec_kernel<E, MODE, LOCAL>, g, dim3(threads), 0, st, a)
+#define SWZ_LAUNCH(MODE, LOCAL, LINK) \
+    launch_pdl_if(!LINK, relayout_vec_kernel<E, MODE, LOCAL, LINK>, g, dim3(threads), 0, st, a)
+#define SWZ_LAUNCH_MODES(LOCAL, LINK)                                         \
+    (mode == kLanesFixed ? SWZ_LAUNCH(kLanesFixed, LOCAL, LINK)               \
+     : mode == kLanesXor ? SWZ_LAUNCH(kLanesXor, LOCAL, LINK)                 \
+                         : SWZ_LAUNCH(kLanesGeneral, LOCAL, LINK))
     cudaError_t e;
-    if (local) {
-        if (mode == kLanesFixed) e = SWZ_LAUNCH(kLanesFixed, true);
-        else if (mode == kLanesXor) e = SWZ_LAUNCH(kLanesXor, true);
-        else e = SWZ_LAUNCH(kLanesGeneral, true);
-    } else {
-        if (mode == kLanesFixed) e = SWZ_LAUNCH(kLanesFixed, false);
-        else if (mode == kLanesXor) e = SWZ_LAUNCH(kLanesXor, false);
-        else e = SWZ_LAUNCH(kLanesGeneral, false);
-    }
+    if (local) e = link_grid ? SWZ_LAUNCH_MODES(true, true) : SWZ_LAUNCH_MODES(true, false);
+    else e = link_grid ? SWZ_LAUNCH_MODES(false, true) : SWZ_LAUNCH_MODES(false, false);
+#undef SWZ_LAUNCH_MODES
 #undef SWZ_LAUNCH
     return launched(e);
 }
@@ -291,6 +310,7 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
     const int steps = (direction == 0 && B > 0 && S < B) ? (B + S - 1) / S : 1;
     const int64_t tile_bytes = tile_elems * esize;
     const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
+    const bool link_grid = host_resident(dst) || host_resident(src);
     if (tile_bytes < 16 && 16 % tile_bytes == 0 && aligned16 && (n_elems * esize) % 16 == 0) {
         // Every 16-byte vector holds whole tiles, so each vector stays where it
         // is and its lanes move by one fixed permutation: the vector kernel
@@ -311,10 +331,10 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
         lane_map_selectors(src_lane, esize, a.perm_sel);
         switch (esize) {
-            case 1: return launch_vec<1>(a, kLanesGeneral, false, st);
-            case 2: return launch_vec<2>(a, kLanesGeneral, false, st);
-            case 4: return launch_vec<4>(a, kLanesGeneral, false, st);
-            default: return launch_vec<8>(a, kLanesGeneral, false, st);
+            case 1: return launch_vec<1>(a, kLanesGeneral, false, link_grid, st);
+            case 2: return launch_vec<2>(a, kLanesGeneral, false, link_grid, st);
+            case 4: return launch_vec<4>(a, kLanesGeneral, false, link_grid, st);
+            default: return launch_vec<8>(a, kLanesGeneral, false, link_grid, st);
         }
     }
     if (tile_bytes % 16 != 0 && aligned16) {
@@ -361,11 +381,11 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         const int period = B + M + S;
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
         switch (esize) {
-            case 1: return launch_vec<1>(a, mode, local, st);
-            case 2: return launch_vec<2>(a, mode, local, st);
-            case 4: return launch_vec<4>(a, mode, local, st);
-            case 8: return launch_vec<8>(a, mode, local, st);
-            case 16: return launch_vec<16>(a, mode, local, st);
+            case 1: return launch_vec<1>(a, mode, local, link_grid, st);
+            case 2: return launch_vec<2>(a, mode, local, link_grid, st);
+            case 4: return launch_vec<4>(a, mode, local, link_grid, st);
+            case 8: return launch_vec<8>(a, mode, local, link_grid, st);
+            case 16: return launch_vec<16>(a, mode, local, link_grid, st);
             default: return SWZ_ERR_PARAM;
         }
     }
