@@ -19,7 +19,10 @@
  *        example), "什么是 Bank Conflict".
  *
  * Parity status per function (what pins it is listed in the test suite):
- *   orc_swizzle            pinned (worked example, 2-D closed forms, bit diagrams)
+ *   orc_swizzle            pinned (worked example, 2-D closed forms, bit diagrams);
+ *                          negative shifts pinned to the positive ones by the
+ *                          bit-reversal mirror identity (the reading of the
+ *                          negative case itself is argued, not printed)
  *   orc_relayout           pinned (reduces to orc_swizzle + byte copies)
  *   orc_transpose          pinned (textbook transpose, explicit small cases)
  *   orc_transpose_relayout the two pinned steps above, in that order
@@ -56,14 +59,25 @@ static int orc_bit(uint64_t v, int p)
  * becomes (bit i of Z) xor (bit i of Y), and every bit outside Z is the
  * input's.  The output is built one bit at a time from the input, so no
  * written bit feeds a later read.
+ *
+ * Negative shift.  [P1]'s bit-diagram comment makes SShift the distance the
+ * YYY mask is moved to land on ZZZ, rightward when positive and leftward when
+ * negative, and keeps the lowest MBase bits constant.  So for a negative
+ * shift YYY is the lower of the two fields, and both fields stay above the
+ * `base` constant bits: Y starts at bit `base` and Z starts -shift bits
+ * above it.  (The pages print no example of a negative shift; this is the
+ * reading that keeps the lowest `base` bits out of the map, as for a
+ * positive shift.)
  */
 uint64_t orc_swizzle(uint64_t offset, int base, int bits, int shift)
 {
     uint64_t out = offset;
+    int zlo = shift >= 0 ? base : base - shift;   /* the field that is written */
+    int ylo = shift >= 0 ? base + shift : base;   /* the field that is read */
     int i;
     for (i = 0; i < bits; ++i) {
-        int zpos = base + i;
-        int ypos = base + shift + i;
+        int zpos = zlo + i;
+        int ypos = ylo + i;
         int v;
         if (zpos >= 64)
             break;

@@ -106,7 +106,9 @@ def test_bit_diagrams(orc):
         assert len(zs) == len(ys) > 0
         assert zs == list(range(zs[0], zs[0] + len(zs)))
         assert ys == list(range(ys[0], ys[0] + len(ys)))
-        B, M, S = len(zs), zs[0], ys[0] - zs[0]
+        # MBase is where the lower field starts; SShift is Y's distance from Z
+        # (negative when Y is the lower field)
+        B, M, S = len(zs), min(zs[0], ys[0]), ys[0] - zs[0]
         expected_params[name] = (B, M, S)
         for x in itertools.chain(rng.integers(0, 2**32, 2000, dtype=np.uint64).tolist(),
                                  [0, 2**32 - 1]):
@@ -119,7 +121,7 @@ def test_bit_diagrams(orc):
             assert orc.swizzle(int(x), B=B, M=M, S=S) == want
     # counting the characters gives these parameters
     assert expected_params == {"p1_diagram": (3, 4, 10), "p1_example": (2, 3, 11),
-                               "p3_tokens": (4, 4, 11)}
+                               "p3_tokens": (4, 4, 11), "p1_diagram_negative_shift": (3, 4, -10)}
 
 
 @pytest.mark.parametrize("B,M,S", SWEEP + CONFIG_SWIZZLES)
@@ -138,6 +140,46 @@ def test_swizzle_invariants(orc, B, M, S):
     assert np.array_equal(sw & np.uint64(low), x & np.uint64(low))
     # bits at and above M+B are only read, never written
     assert np.array_equal(sw >> np.uint64(M + B), x >> np.uint64(M + B))
+
+
+NEGATIVE = [(B, M, -s) for B in range(1, 6) for M in range(0, 5) for s in range(1, 8)]
+
+
+def _bit_reverse(x: int, width: int) -> int:
+    return int(format(x, f"0{width}b")[::-1], 2)
+
+
+@pytest.mark.parametrize("B,M,s,Mr", [(3, 4, 10, 4), (2, 3, 11, 0), (1, 0, 1, 0), (3, 0, 1, 2),
+                                      (3, 0, 3, 0), (5, 2, 5, 1), (4, 1, 2, 3), (2, 2, 7, 5)])
+def test_negative_shift_mirrors_positive(orc, B, M, s, Mr):
+    """A negative shift is the positive one seen in a mirror.  Reverse the bit
+    order of a W-bit offset: the written field of Sw<B, M, s> (bits M .. M+B-1)
+    lands on bits Mr+s .. Mr+s+B-1 and its read field (bits M+s ..) on
+    Mr .. Mr+B-1, with W = M + Mr + s + B, and the pairing of the bits is kept.
+    So Sw<B, Mr, -s> = reverse . Sw<B, M, s> . reverse on every W-bit offset:
+    the positive swizzle, pinned by the pages' examples, fixes the negative
+    one (YYY at MBase, ZZZ |SShift| above it, "NVIDIA CuTe Swizzle")."""
+    W = M + Mr + s + B
+    for x in range(1 << W) if W <= 14 else np.random.default_rng(W).integers(0, 1 << W, 20000).tolist():
+        pos = orc.swizzle(_bit_reverse(int(x), W), B=B, M=M, S=s)
+        assert orc.swizzle(int(x), B=B, M=Mr, S=-s) == _bit_reverse(pos, W)
+
+
+@pytest.mark.parametrize("B,M,S", NEGATIVE)
+def test_negative_shift_invariants(orc, B, M, S):
+    """Negative shifts over offsets 0..65535: a bijection; its own inverse
+    when the fields do not overlap (|S| >= B); the low M bits (and groups of
+    2^M elements) kept; only the field |S| bits above MBase is written."""
+    x = np.arange(1 << 16, dtype=np.uint64)
+    sw = np.array([orc.swizzle(int(v), B=B, M=M, S=S) for v in x], dtype=np.uint64)
+    assert np.array_equal(np.sort(sw), x)
+    if -S >= B:
+        back = np.array([orc.swizzle(int(v), B=B, M=M, S=S) for v in sw], dtype=np.uint64)
+        assert np.array_equal(back, x)
+    zlo = M - S
+    keep = ~np.uint64(((1 << B) - 1) << zlo)
+    assert np.array_equal(sw & keep, x & keep)
+    assert np.array_equal(sw & np.uint64((1 << M) - 1), x & np.uint64((1 << M) - 1))
 
 
 def test_swizzle_degenerate(orc):

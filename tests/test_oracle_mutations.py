@@ -12,9 +12,15 @@ import oracle
 import test_oracle as pins
 
 MUTATIONS = [
-    ("y field one bit too high", "int ypos = base + shift + i;", "int ypos = base + shift + 1 + i;"),
-    ("y field one bit too low", "int ypos = base + shift + i;", "int ypos = base + shift - 1 + i;"),
-    ("z field one bit too high", "int zpos = base + i;", "int zpos = base + 1 + i;"),
+    ("y field one bit too high", "int ypos = ylo + i;", "int ypos = ylo + 1 + i;"),
+    ("y field one bit too low", "int ypos = ylo + i;", "int ypos = ylo - 1 + i;"),
+    ("z field one bit too high", "int zpos = zlo + i;", "int zpos = zlo + 1 + i;"),
+    ("negative shift read below MBase (the formula taken literally)",
+     "int zlo = shift >= 0 ? base : base - shift;   /* the field that is written */\n    int ylo = shift >= 0 ? base + shift : base;",
+     "int zlo = base;   /* the field that is written */\n    int ylo = base + shift;"),
+    ("negative shift taken as its magnitude",
+     "int zlo = shift >= 0 ? base : base - shift;   /* the field that is written */\n    int ylo = shift >= 0 ? base + shift : base;",
+     "int zlo = base;   /* the field that is written */\n    int ylo = shift >= 0 ? base + shift : base - shift;"),
     ("field one bit short", "for (i = 0; i < bits; ++i) {", "for (i = 0; i < bits - 1; ++i) {"),
     ("OR instead of XOR", "v = orc_bit(offset, zpos) ^ orc_bit(offset, ypos);",
      "v = orc_bit(offset, zpos) | orc_bit(offset, ypos);"),
@@ -63,6 +69,9 @@ def battery(orc):
         ("invariants_333", lambda: pins.test_swizzle_invariants(orc, 3, 3, 3)),
         ("invariants_525", lambda: pins.test_swizzle_invariants(orc, 5, 2, 5)),
         ("degenerate", lambda: pins.test_swizzle_degenerate(orc)),
+        ("negative_mirror", lambda: pins.test_negative_shift_mirrors_positive(orc, 3, 4, 10, 4)),
+        ("negative_mirror_overlap", lambda: pins.test_negative_shift_mirrors_positive(orc, 3, 0, 1, 2)),
+        ("negative_invariants", lambda: pins.test_negative_shift_invariants(orc, 3, 2, -4)),
         ("relayout_roundtrip", lambda: pins.test_relayout_roundtrip_and_closed(orc)),
         ("relayout_tile_local", lambda: pins.test_relayout_tile_local(orc, 48)),
         ("relayout_usage_loop", lambda: pins.test_relayout_usage_loop(orc)),
