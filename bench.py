@@ -486,6 +486,17 @@ def measure_rows(torch, swz, dev, flush, peak):
         "median_GB/s": round(statistics.median(vals), 1),
         "max": {"GB/s": round(vals[-1], 1), "BMS": res[-1][1]},
         "min_frac_of_hbm": round(vals[0] / peak, 3)}
+
+    # negative SShift on the same buffer, forward: one parameter set per relayout path
+    neg = {}
+    for label, (Bq, Mq, Sq) in (("whole_vectors_sw33m3", (3, 3, -3)), ("lane_map_sw20m1", (2, 0, -1)),
+                                ("staged_sw30m4", (3, 0, -4)), ("staged_4KiB_sw31m7", (3, 1, -7)),
+                                ("element_wise_sw42m9", (4, 2, -9))):
+        ms = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0),
+                             reps=3, groups=2, warm=1)
+        neg[label] = summary(ms, 2 << 30)
+    neg["note"] = "1 GiB uint16 as one tile, forward; the path each set takes is in its label"
+    out["relayout_uint16_1GiB_negative_shift"] = neg
     del src, dst
 
     # transposes, with the bank model's prediction for each staging's warp accesses

@@ -12,6 +12,14 @@
  * contiguous) and every other bit are kept.  All B, M, S arguments below are
  * in ELEMENT-offset units.
  *
+ * A negative S moves the read field (YYY) leftward onto the written one
+ * (ZZZ): the B bits that start at bit M are XOR-ed into the B bits that start
+ * at bit M + |S|, i.e. sw(x) = x ^ (((x >> M) & ((1 << B) - 1)) << (M - S)).
+ * ("NVIDIA CuTe Swizzle", the bit-diagram comment: the sign of SShift gives
+ * the direction the YYY mask moves, and the low MBase bits stay constant.  The
+ * pages give no formula for this case; this placement is the one that keeps
+ * the low M bits out of the map, as for S > 0.)
+ *
  * Conventions shared by every entry point:
  *   - Pointers named dst/src/out are DEVICE pointers owned by the caller (the
  *     relayout also accepts host memory the device can address); the library
@@ -71,9 +79,10 @@ enum {
  *            at the host link's rate.
  * esize    : 1, 2, 4, 8 or 16 bytes.  Elements are copied as raw bits.
  * B, M, S  : swizzle parameters in element units; 0 <= B <= 16,
- *            0 <= M <= 32, and when B > 0: 1 <= S <= 32, B + M + S <= 48.
- *            S = 0 is rejected (it is not a bijection); 1 <= S < B is
- *            accepted (a bijection, but not its own inverse).
+ *            0 <= M <= 32, -32 <= S <= 32, and when B > 0: S != 0 and
+ *            B + M + |S| <= 48.  S = 0 is rejected (it is not a bijection);
+ *            1 <= |S| < B is accepted (a bijection, but not its own
+ *            inverse).  B = 0 is the identity.
  * direction: 0 = forward, logical row-major to swizzled physical order:
  *                dst[t][sw(i)] = src[t][i];
  *            1 = inverse, swizzled physical to logical:
@@ -82,8 +91,9 @@ enum {
  *
  * Errors: SWZ_ERR_NULL (dst or src NULL with a non-empty request),
  * SWZ_ERR_PARAM, SWZ_ERR_SHAPE (negative sizes, byte size overflowing
- * int64, or rows * cols not a multiple of 2^(M + B), so that a tile would not
- * be closed under sw), SWZ_ERR_ALIGN (dst or src not aligned to esize),
+ * int64, or rows * cols not a multiple of 2^h, h the bit above the written
+ * field: M + B for S > 0, M + |S| + B for S < 0, so that a tile would not be
+ * closed under sw), SWZ_ERR_ALIGN (dst or src not aligned to esize),
  * SWZ_ERR_ALIAS (the two byte ranges overlap), SWZ_ERR_CUDA.
  * An empty request (no element) returns SWZ_OK and launches nothing.
  */
@@ -179,7 +189,11 @@ swz_status swz_transpose(void *dst, const void *src, int64_t rows, int64_t cols,
  * SWZ_T_SWIZZLED's.
  *
  * rows, cols >= 0; tile_elems > 0 divides rows * cols and is a multiple of
- * 2^(M + B); B, M, S as in swz_relayout; esize 1, 2, 4, 8 or 16.
+ * 2^h (h as in swz_relayout: M + B, or M + |S| + B for S < 0); B, M, S as
+ * in swz_relayout; esize 1, 2, 4, 8 or 16.  With S < 0 and M below the lane
+ * bits of a 16-byte vector (2^M < 16 / esize) the transposed elements are
+ * stored one by one (the swizzle then moves elements of one vector to
+ * several), which is slower than the vector stores of every other case.
  * Errors: as swz_transpose, SWZ_ERR_PARAM for B, M, S, and SWZ_ERR_SHAPE
  * when tile_elems breaks the rules above.
  */
@@ -259,7 +273,7 @@ swz_status swz_staging_probe(int esize, int variant, int iters, const void *gsrc
  *
  * Host function, synchronous, no GPU involved.  C_out: host pointer.
  * Errors: SWZ_ERR_NULL (C_out NULL), SWZ_ERR_PARAM (B, M, S out of the range
- * of swz_relayout, or B + M + S > 64).
+ * of swz_relayout, or B + M + |S| > 64).
  */
 swz_status swz_slice_collision(uint64_t A, int B, int M, int S, uint64_t *C_out);
 

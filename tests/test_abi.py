@@ -36,13 +36,14 @@ def test_exports_every_declared_function(swz):
 
 
 def test_apply_matches_oracle(swz, orc):
-    for (B, M, S) in [(5, 0, 6), (3, 3, 3), (3, 4, 3), (2, 0, 1), (4, 4, 11), (0, 3, 3)]:
+    for (B, M, S) in [(5, 0, 6), (3, 3, 3), (3, 4, 3), (2, 0, 1), (4, 4, 11), (0, 3, 3),
+                      (3, 4, -10), (2, 0, -1), (3, 1, -2), (5, 2, -5), (4, 0, -7)]:
         for x in list(range(0, 5000, 7)) + [673, 2**40 + 12345]:
             assert swz.swz_apply(x, B, M, S) == orc.swizzle(x, B=B, M=M, S=S)
 
 
 def test_slice_collision_host(swz, orc):
-    for (B, M, S) in [(3, 2, 4), (2, 0, 1), (3, 1, 2), (5, 0, 5)]:
+    for (B, M, S) in [(3, 2, 4), (2, 0, 1), (3, 1, 2), (5, 0, 5), (3, 2, -4), (2, 0, -1), (3, 1, -2)]:
         for A in range(1 << (B + M + S + 1)):
             assert swz.swz_slice_collision(A, B, M, S) == orc.slice_collision(A, B=B, M=M, S=S)
     with pytest.raises(swz.SwzError) as e:
@@ -60,6 +61,9 @@ FAKE_A, FAKE_B = 1 << 40, 1 << 41  # never dereferenced: every case below fails 
     ((FAKE_B, FAKE_A, 1, 8, 8, 2, 17, 0, 1, 0), "SWZ_ERR_PARAM"),     # B > 16
     ((FAKE_B, FAKE_A, 1, 8, 8, 2, 3, 0, 3, 2), "SWZ_ERR_PARAM"),      # direction
     ((FAKE_B, FAKE_A, 1, 8, 8, 2, 16, 16, 17, 0), "SWZ_ERR_PARAM"),   # B + M + S > 48
+    ((FAKE_B, FAKE_A, 1, 8, 8, 2, 3, 0, -33, 0), "SWZ_ERR_PARAM"),    # |S| > 32
+    ((FAKE_B, FAKE_A, 1, 8, 8, 2, 16, 16, -17, 0), "SWZ_ERR_PARAM"),  # B + M + |S| > 48
+    ((FAKE_B, FAKE_A, 1, 8, 8, 2, 3, 0, -4, 0), "SWZ_ERR_SHAPE"),     # 64 % 2^(0 + 4 + 3) != 0
     ((FAKE_B, FAKE_A, -1, 8, 8, 2, 3, 0, 3, 0), "SWZ_ERR_SHAPE"),
     ((FAKE_B, FAKE_A, 1, 3, 4, 2, 2, 2, 2, 0), "SWZ_ERR_SHAPE"),      # tile not closed
     ((FAKE_B, FAKE_A, 2**40, 2**20, 2**20, 2, 3, 0, 3, 0), "SWZ_ERR_SHAPE"),  # overflow
@@ -108,13 +112,13 @@ def test_status_strings(swz):
     assert swz.swz_version() >= 100
 
 
-@pytest.mark.parametrize("B,M,S", [(2, 0, 2), (3, 1, 2), (2, 1, 3), (3, 0, 1)])
+@pytest.mark.parametrize("B,M,S", [(2, 0, 2), (3, 1, 2), (2, 1, 3), (3, 0, 1), (2, 0, -2), (3, 1, -2), (3, 0, -1)])
 def test_slice_layout(swz, orc, B, M, S):
     """Slices whose collision mask is 0 come back as per-bit strides that
     reproduce the swizzle on every subset (the oracle's brute force agrees);
     the others are refused."""
     import itertools
-    for A in range(1 << (B + M + S + 1)):
+    for A in range(1 << (B + M + abs(S) + 1)):
         strides = swz.swz_slice_layout(A, B, M, S)
         assert (strides is not None) == orc.slice_is_layout(A, B=B, M=M, S=S), A
         if strides is None:

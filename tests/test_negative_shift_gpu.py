@@ -1,0 +1,139 @@
+"""Negative SShift on the GPU, bit for bit against the oracle.
+
+A negative shift reads the field at MBase and writes the field |S| bits above
+it (the reading of "NVIDIA CuTe Swizzle"'s bit-diagram comment that the oracle
+pins).  The read field can then sit below a 16-byte vector's lane bits while
+the written one sits above them, so the relayout takes other paths than for a
+positive shift: whole vectors (M >= log2 V), a fixed lane map when the map
+stays inside a vector, staged periods in shared memory, element by element.
+The parameter grid below reaches each of them for every element size."""
+import numpy as np
+import pytest
+
+from gpu_util import empty_device, guards_intact, to_device, to_host, torch, void_dtype
+
+pytestmark = pytest.mark.gpu
+
+NEGATIVE = [(B, M, -s) for B in range(1, 6) for M in range(0, 5) for s in range(1, 8)]
+
+
+@pytest.fixture(scope="module")
+def swz():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import xor_swizzle_movement_gb300 as m
+    m.lib()
+    return m
+
+
+def _wtop(B, M, S):
+    """Offsets close under the swizzle in aligned blocks of 2^wtop elements."""
+    return M - S + B
+
+
+def _run(swz, orc, host, n_tiles, rows, cols, esize, B, M, S, direction, src_off=0, dst_off=0, tma=False):
+    _, src = to_device(host, src_off)
+    full, dst = empty_device(host.nbytes, dst_off)
+    fn = swz.swz_relayout_tma if tma else swz.swz_relayout
+    fn(dst, src, n_tiles, rows, cols, esize, B, M, S, direction)
+    torch.cuda.synchronize()
+    want = orc.relayout(host, tile_elems=rows * cols, B=B, M=M, S=S, direction=direction)
+    got = to_host(dst, host.dtype)
+    assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), (esize, B, M, S, direction)
+    assert guards_intact(full, dst_off, host.nbytes)
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("B,M,S", NEGATIVE)
+def test_relayout_negative_shift(swz, orc, esize, B, M, S):
+    """Three tiles of two closure blocks each, both directions."""
+    from xor_swizzle_movement_gb300 import inputs
+    period = 1 << _wtop(B, M, S)
+    rows, cols, n_tiles = 2, period, 3
+    host = inputs.random_bytes(n_tiles * rows * cols * esize, seed=40 + B * 100 + M * 10 - S).view(void_dtype(esize))
+    for direction in (0, 1):
+        _run(swz, orc, host, n_tiles, rows, cols, esize, B, M, S, direction)
+
+
+@pytest.mark.parametrize("esize,mult,B,M,S,src_off,dst_off", [
+    (1, 3, 1, 0, -1, 0, 0),     # 12-byte tiles: staged ragged tiles
+    (1, 3, 2, 0, -1, 0, 0),     # 24-byte tiles
+    (2, 5, 1, 0, -1, 0, 0),     # 40-byte tiles
+    (1, 1, 1, 1, -1, 0, 0),     # 8-byte tiles: two per vector, fixed lane map
+    (2, 2, 2, 0, -2, 2, 0),     # unaligned source: element by element
+    (4, 3, 3, 1, -3, 0, 4),     # unaligned destination
+    (8, 1, 2, 0, -5, 8, 8),
+    (1, 2, 5, 0, -7, 1, 3),
+])
+def test_relayout_negative_shift_ragged_and_unaligned(swz, orc, esize, mult, B, M, S, src_off, dst_off):
+    from xor_swizzle_movement_gb300 import inputs
+    tile = mult << _wtop(B, M, S)
+    n_tiles = 7
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=77 + mult).view(void_dtype(esize))
+    for direction in (0, 1):
+        _run(swz, orc, host, n_tiles, 1, tile, esize, B, M, S, direction, src_off, dst_off)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B,M,S", [(3, 3, -3),    # whole vectors move (M >= log2 8)
+                                   (3, 0, -4),    # staged blocks of 128 elements
+                                   (3, 1, -7),    # staged blocks of 2048 elements (4 KiB)
+                                   (4, 2, -9),    # blocks of 2^15 elements: element by element
+                                   (2, 0, -1)])   # the whole map inside one vector: fixed lane map
+def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
+    """A 64 MiB uint16 buffer as one tile, every position, both directions,
+    and forward then inverse gives the input back."""
+    from xor_swizzle_movement_gb300 import inputs
+    n = 1 << 25
+    host = inputs.uint16_bits(n, seed=9)
+    src = torch.from_numpy(host.view(np.int16).copy()).cuda()
+    fwd, back = torch.empty_like(src), torch.empty_like(src)
+    swz.swz_relayout(fwd, src, 1, 1, n, 2, B, M, S, 0)
+    swz.swz_relayout(back, fwd, 1, 1, n, 2, B, M, S, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    want = orc.relayout(host, tile_elems=n, B=B, M=M, S=S, direction=0)
+    assert np.array_equal(fwd.cpu().numpy().view(np.uint16), want)
+
+
+@pytest.mark.parametrize("esize,rows,cols,te,B,M,S", [
+    (2, 64, 4096, 8192, 3, 3, -4),    # M >= log2 8: 16-byte vectors land whole
+    (2, 64, 4096, 8192, 2, 1, -3),    # M < log2 8: element by element
+    (4, 96, 520, 1040, 1, 0, -2),     # ragged matrix, fp32
+    (1, 256, 384, 4096, 3, 0, -5),    # bytes
+    (8, 48, 80, 64, 2, 1, -1),        # fp64, overlapping fields
+])
+def test_transpose_relayout_negative_shift(swz, orc, esize, rows, cols, te, B, M, S):
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.random_bytes(rows * cols * esize, seed=3 + esize).view(void_dtype(esize)).reshape(rows, cols)
+    _, src = to_device(host)
+    full, dst = empty_device(host.nbytes)
+    swz.swz_transpose_relayout(dst, src, rows, cols, esize, te, B, M, S)
+    torch.cuda.synchronize()
+    want = orc.transpose_relayout(host, tile_elems=te, B=B, M=M, S=S)
+    assert np.array_equal(to_host(dst, host.dtype).view(np.uint8), want.view(np.uint8))
+    assert guards_intact(full, 0, host.nbytes)
+
+
+def test_relayout_tma_negative_shift_runs_register_kernels(swz, orc):
+    """No tensor-map swizzle mode has a negative shift: the TMA entry point
+    reports path 0 and runs the register kernels, with the oracle's result."""
+    from xor_swizzle_movement_gb300 import inputs
+    host = inputs.random_bytes(64 * 64 * 2 * 16, seed=5).view(np.uint16)
+    _, src = to_device(host)
+    _, dst = empty_device(host.nbytes)
+    assert swz.swz_relayout_tma_path(dst, src, 16, 64, 64, 2, 3, 3, -3, 0) == 0
+    _run(swz, orc, host, 16, 64, 64, 2, 3, 3, -3, 0, tma=True)
+
+
+def test_slice_collision_batch_negative_shift(swz, orc):
+    rng = np.random.default_rng(11)
+    A = rng.integers(0, 1 << 40, 4096, dtype=np.int64)
+    dA = torch.from_numpy(A).cuda()
+    for B, M, S in [(3, 2, -4), (2, 0, -1), (5, 1, -9)]:
+        C = torch.empty_like(dA)
+        swz.swz_slice_collision_batch(dA, A.size, B, M, S, C)
+        torch.cuda.synchronize()
+        got = C.cpu().numpy().view(np.uint64)
+        want = np.array([orc.slice_collision(int(a), B=B, M=M, S=S) for a in A], dtype=np.uint64)
+        assert np.array_equal(got, want)

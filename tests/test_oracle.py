@@ -448,11 +448,12 @@ def test_collision_truth_table(orc):
 
 
 @pytest.mark.parametrize("B,M,S", [(1, 0, 1), (2, 0, 2), (2, 1, 2), (2, 0, 3), (3, 0, 3),
-                                   (2, 0, 1), (3, 0, 1), (3, 1, 2)])
+                                   (2, 0, 1), (3, 0, 1), (3, 1, 2),
+                                   (2, 0, -2), (3, 0, -1), (3, 1, -2)])
 def test_collision_predicts_layout(orc, B, M, S):
     """Brute force: C == 0 exactly when the swizzle restricted to the slice is a
     plain layout (a sum of per-bit strides), on every mask A of the low bits."""
-    nbits = B + M + S + 1
+    nbits = B + M + abs(S) + 1
     for A in range(1 << nbits):
         C = orc.slice_collision(A, B=B, M=M, S=S)
         assert (C == 0) == orc.slice_is_layout(A, B=B, M=M, S=S), (A, C)

@@ -221,7 +221,8 @@ def test_empty_and_errors(swz):
         (dict(n_tiles=1, rows=3, cols=4, esize=2, B=2, M=2, S=2), swz.SWZ_ERR_SHAPE),  # 12 % 16 != 0
         (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=0), swz.SWZ_ERR_PARAM),  # S = 0
         (dict(n_tiles=1, rows=8, cols=8, esize=3, B=3, M=0, S=3), swz.SWZ_ERR_PARAM),  # esize
-        (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=-1), swz.SWZ_ERR_PARAM),
+        (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=-6), swz.SWZ_ERR_SHAPE),  # 64 % 2^9 != 0
+        (dict(n_tiles=1, rows=8, cols=8, esize=2, B=3, M=0, S=-33), swz.SWZ_ERR_PARAM),
         (dict(n_tiles=-1, rows=8, cols=8, esize=2, B=3, M=0, S=3), swz.SWZ_ERR_SHAPE),
     ]
     for kw, status in cases:

@@ -78,11 +78,12 @@ namespace {
 bool valid_esize(int e) { return e == 1 || e == 2 || e == 4 || e == 8 || e == 16; }
 
 // B, M, S in element units.  S = 0 makes the map non-injective; negative S
-// (the YYY field moved below ZZZ) has no formula on the pages.
+// puts the read field at M and the written one |S| bits above it (sw_fwd).
 bool valid_bms(int B, int M, int S, int max_total) {
-    if (B < 0 || B > 16 || M < 0 || M > 32) return false;
-    if (B == 0) return S >= 0 && S <= 32;
-    return S >= 1 && S <= 32 && B + M + S <= max_total;
+    if (B < 0 || B > 16 || M < 0 || M > 32 || S < -32 || S > 32) return false;
+    if (B == 0) return true;  // the identity
+    const int a = S < 0 ? -S : S;
+    return a >= 1 && B + M + a <= max_total;
 }
 
 // a * b without int64 overflow (a, b >= 0)
@@ -112,7 +113,7 @@ swz_status check_relayout(void *dst, const void *src, int64_t n_tiles, int64_t r
         !mul_ok(n_elems, esize, &n_bytes))
         return SWZ_ERR_SHAPE;
     if (n_elems == 0) return SWZ_OK;
-    if (*tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
+    if (*tile_elems % (int64_t(1) << (B ? sw_write_hi(B, M, S) : M)) != 0) return SWZ_ERR_SHAPE;
     if (!dst || !src) return SWZ_ERR_NULL;
     if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;
     if (ranges_overlap(dst, n_bytes, src, n_bytes)) return SWZ_ERR_ALIAS;
@@ -180,7 +181,8 @@ swz_status swz_transpose_relayout(void *dst, const void *src, int64_t rows, int6
     if (rows < 0 || cols < 0 || tile_elems <= 0) return SWZ_ERR_SHAPE;
     int64_t n_elems, n_bytes;
     if (!mul_ok(rows, cols, &n_elems) || !mul_ok(n_elems, esize, &n_bytes)) return SWZ_ERR_SHAPE;
-    if (n_elems % tile_elems != 0 || tile_elems % (int64_t(1) << (M + B)) != 0) return SWZ_ERR_SHAPE;
+    if (n_elems % tile_elems != 0 || tile_elems % (int64_t(1) << (B ? sw_write_hi(B, M, S) : M)) != 0)
+        return SWZ_ERR_SHAPE;
     if (n_elems == 0) return SWZ_OK;
     if (!dst || !src) return SWZ_ERR_NULL;
     if (!aligned_to(dst, esize) || !aligned_to(src, esize)) return SWZ_ERR_ALIGN;

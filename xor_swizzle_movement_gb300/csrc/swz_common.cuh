@@ -11,22 +11,40 @@ namespace swz {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
-// Swizzle<B,M,S> on an element offset: one shift, one mask, one XOR.
-// ("CuTe Swizzle 学习手册", section "Swizzle 数学公式".)
-__host__ __device__ __forceinline__ uint64_t sw_fwd(uint64_t x, int B, int M, int S) {
-    const uint64_t mask = (B >= 64) ? ~0ull : ((1ull << B) - 1ull);
-    return x ^ (((x >> (M + S)) & mask) << M);
+// The two B-bit fields of Swizzle<B,M,S>.  S > 0: the written field (ZZZ)
+// starts at bit M and the read field (YYY) S bits above it ("CuTe Swizzle
+// 学习手册", section "Swizzle 数学公式").  S < 0: YYY is moved leftward onto
+// ZZZ ("NVIDIA CuTe Swizzle", the bit-diagram comment), so the read field
+// starts at M and the written one |S| bits above it; the lowest M bits stay
+// out of the map either way.
+__host__ __device__ __forceinline__ int sw_read_lo(int M, int S) { return S > 0 ? M + S : M; }
+__host__ __device__ __forceinline__ int sw_write_lo(int M, int S) { return S > 0 ? M : M - S; }
+// Bit above the written field: offsets close under the swizzle in aligned
+// blocks of 2^sw_write_hi elements.
+__host__ __device__ __forceinline__ int sw_write_hi(int B, int M, int S) { return sw_write_lo(M, S) + B; }
+// Steps of sw_inv that reach the exact inverse (see there).
+__host__ __device__ __forceinline__ int sw_inv_steps(int B, int S) {
+    const int a = S < 0 ? -S : S;
+    return (B > 0 && a < B) ? (B + a - 1) / a : 1;
 }
 
-// Inverse of sw_fwd.  For S >= B the function is an involution and one step
-// suffices.  For 1 <= S < B the read field overlaps the written one; writing
-// y = x ^ f(x), the iteration x <- y ^ f(x) started at x = y fixes S more bits
-// of x per step from the top of the written field downwards, so ceil(B / S)
-// steps reach the exact inverse.
+// Swizzle<B,M,S> on an element offset: one shift, one mask, one XOR.
+__host__ __device__ __forceinline__ uint64_t sw_fwd(uint64_t x, int B, int M, int S) {
+    const uint64_t mask = (B >= 64) ? ~0ull : ((1ull << B) - 1ull);
+    return x ^ (((x >> sw_read_lo(M, S)) & mask) << sw_write_lo(M, S));
+}
+
+// Inverse of sw_fwd.  For |S| >= B the function is an involution and one
+// step suffices.  For 1 <= |S| < B the read field overlaps the written one;
+// writing y = x ^ f(x), the iteration x <- y ^ f(x) started at x = y fixes
+// |S| more bits of x per step (from the top of the written field downwards
+// for S > 0, from its bottom upwards for S < 0), so ceil(B / |S|) steps reach
+// the exact inverse.
 __host__ __device__ __forceinline__ uint64_t sw_inv(uint64_t y, int B, int M, int S, int steps) {
     const uint64_t mask = (B >= 64) ? ~0ull : ((1ull << B) - 1ull);
+    const int r = sw_read_lo(M, S), w = sw_write_lo(M, S);
     uint64_t x = y;
-    for (int i = 0; i < steps; ++i) x = y ^ (((x >> (M + S)) & mask) << M);
+    for (int i = 0; i < steps; ++i) x = y ^ (((x >> r) & mask) << w);
     return x;
 }
 

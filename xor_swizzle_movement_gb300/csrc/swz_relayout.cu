@@ -205,8 +205,9 @@ constexpr int kStageBytes = 8192;
 // identity on every offset of a staged block).
 __device__ __forceinline__ uint32_t sw_inv32(uint32_t y, int B, int M, int S, int steps) {
     const uint32_t mask = (1u << B) - 1u;
+    const int r = sw_read_lo(M, S), w = sw_write_lo(M, S);
     uint32_t x = y;
-    for (int i = 0; i < steps; ++i) x = y ^ (((x >> (M + S)) & mask) << M);
+    for (int i = 0; i < steps; ++i) x = y ^ (((x >> r) & mask) << w);
     return x;
 }
 
@@ -273,7 +274,7 @@ swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_by
     const uint32_t recip = te == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / te + 1);
     // staged offsets are below kStageBytes <= 2^16: a read field at or above
     // bit 16 is all zero there, and the swizzle is the identity
-    if (M + S >= 16) { B = 0; M = 0; S = 1; steps = 1; }
+    if (sw_read_lo(M, S) >= 16) { B = 0; M = 0; S = 1; steps = 1; }
     // the source pattern of output vectors repeats every lcm(tile bytes, 16) bytes
     int64_t g = te * E, h = 16;
     while (h) { const int64_t r = g % h; g = h; h = r; }
@@ -291,7 +292,7 @@ swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, in
     int64_t grid = (n + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 32;
     if (grid > cap) grid = cap;
-    const int period = B + M + S;
+    const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
     const bool local = B > 0 && (period >= 62 || (tile & ((int64_t(1) << period) - 1)) != 0);
     const dim3 g(static_cast<unsigned>(grid));
     if (local)
@@ -301,66 +302,108 @@ swz_status launch_scalar(void *dst, const void *src, int64_t n, int64_t tile, in
                                S, steps));
 }
 
+// Every 16-byte vector holds whole blocks of `te` elements that the swizzle
+// maps onto themselves (te divides 16 / esize): each vector stays where it is
+// and its lanes move by one fixed permutation.  The vector kernel runs with
+// the identity at vector level (B = 0) and that permutation as its lane map.
+swz_status launch_lane_map(void *dst, const void *src, int64_t n_elems, int esize, int te, int B, int M, int S,
+                           int steps, bool link_grid, cudaStream_t st) {
+    const int lanes = 16 / esize;
+    int src_lane[16];
+    for (int l = 0; l < lanes; ++l)
+        src_lane[l] = (l - l % te) + static_cast<int>(sw_inv(static_cast<uint64_t>(l % te), B, M, S, steps));
+    RelayoutArgs a;
+    a.dst = static_cast<uint4 *>(dst);
+    a.src = static_cast<const uint4 *>(src);
+    a.nvec = n_elems * esize / 16;
+    a.tile_vecs = 1;
+    a.B = 0; a.M = 0; a.S = 1;
+    a.steps = 1;
+    const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
+    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+    lane_map_selectors(src_lane, esize, a.perm_sel);
+    switch (esize) {
+        case 1: return launch_vec<1>(a, kLanesGeneral, false, link_grid, st);
+        case 2: return launch_vec<2>(a, kLanesGeneral, false, link_grid, st);
+        case 4: return launch_vec<4>(a, kLanesGeneral, false, link_grid, st);
+        default: return launch_vec<8>(a, kLanesGeneral, false, link_grid, st);
+    }
+}
+
+// The staged kernel over blocks of whole `te`-element tiles (te * esize need
+// not be a multiple of 16), with 16-byte aligned pointers.  Returns
+// SWZ_ERR_UNSUPPORTED, launching nothing, when lcm(te * esize, 16) exceeds
+// the staging buffer.
+swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int64_t te, int esize, int B, int M,
+                               int S, int steps, cudaStream_t st) {
+    const int64_t tile_bytes = te * esize;
+    int64_t g = tile_bytes, h = 16;
+    while (h) { const int64_t r = g % h; g = h; h = r; }
+    const int64_t l = tile_bytes / g * 16;  // lcm(tile bytes, 16)
+    if (l > kStageBytes) return SWZ_ERR_UNSUPPORTED;
+    const int block = static_cast<int>(l * (kStageBytes / l));
+    const int64_t bytes = n_elems * esize;
+    // groups of 2^M elements move intact: gather units of 2^k elements,
+    // k = min(M, log2(16 / esize)), under Swizzle<B, M - k, S> on unit
+    // offsets (tiles hold a multiple of 2^M elements)
+    int k = 0;
+    while (k < M && (esize << (k + 1)) <= 8) ++k;
+    const int64_t te_u = te >> k;
+    switch (esize << k) {
+        case 1: return launch_staged<1>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+        case 2: return launch_staged<2>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+        case 4: return launch_staged<4>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+        default: return launch_staged<8>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+    }
+}
+
+swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
+                             int M, int S, int steps, cudaStream_t st) {
+    switch (esize) {
+        case 1: return launch_scalar<1>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 2: return launch_scalar<2>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 4: return launch_scalar<4>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 8: return launch_scalar<8>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        case 16: return launch_scalar<16>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
+        default: return SWZ_ERR_PARAM;
+    }
+}
+
 }  // namespace
 
 // Arguments are validated by the caller (swz_relayout in swz_abi.cu).
 swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t tile_elems,
                            int esize, int B, int M, int S, int direction, cudaStream_t st) {
     const int64_t n_elems = n_tiles * tile_elems;
-    const int steps = (direction == 0 && B > 0 && S < B) ? (B + S - 1) / S : 1;
+    const int steps = direction == 0 ? sw_inv_steps(B, S) : 1;
     const int64_t tile_bytes = tile_elems * esize;
     const bool aligned16 = ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0;
     const bool link_grid = host_resident(dst) || host_resident(src);
-    if (tile_bytes < 16 && 16 % tile_bytes == 0 && aligned16 && (n_elems * esize) % 16 == 0) {
-        // Every 16-byte vector holds whole tiles, so each vector stays where it
-        // is and its lanes move by one fixed permutation: the vector kernel
-        // with the identity at vector level (B = 0) and that permutation as
-        // its lane map.
-        const int lanes = 16 / esize, te = static_cast<int>(tile_elems);
-        int src_lane[16];
-        for (int l = 0; l < lanes; ++l)
-            src_lane[l] = (l - l % te) + static_cast<int>(sw_inv(static_cast<uint64_t>(l % te), B, M, S, steps));
-        RelayoutArgs a;
-        a.dst = static_cast<uint4 *>(dst);
-        a.src = static_cast<const uint4 *>(src);
-        a.nvec = n_elems * esize / 16;
-        a.tile_vecs = 1;
-        a.B = 0; a.M = 0; a.S = 1;
-        a.steps = 1;
-        const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
-        a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
-        lane_map_selectors(src_lane, esize, a.perm_sel);
-        switch (esize) {
-            case 1: return launch_vec<1>(a, kLanesGeneral, false, link_grid, st);
-            case 2: return launch_vec<2>(a, kLanesGeneral, false, link_grid, st);
-            case 4: return launch_vec<4>(a, kLanesGeneral, false, link_grid, st);
-            default: return launch_vec<8>(a, kLanesGeneral, false, link_grid, st);
-        }
-    }
+    int lv = 0;
+    while ((1 << lv) < 16 / esize) ++lv;
+    if (tile_bytes < 16 && 16 % tile_bytes == 0 && aligned16 && (n_elems * esize) % 16 == 0)
+        return launch_lane_map(dst, src, n_elems, esize, static_cast<int>(tile_elems), B, M, S, steps, link_grid,
+                               st);
     if (tile_bytes % 16 != 0 && aligned16) {
-        int64_t g = tile_bytes, h = 16;
-        while (h) { const int64_t r = g % h; g = h; h = r; }
-        const int64_t l = tile_bytes / g * 16;  // lcm(tile bytes, 16)
-        if (l <= kStageBytes) {
-            const int block = static_cast<int>(l * (kStageBytes / l));
-            const int64_t bytes = n_elems * esize;
-            // groups of 2^M elements move intact: gather units of 2^k elements,
-            // k = min(M, log2(16 / esize)), under Swizzle<B, M - k, S> on unit
-            // offsets (tiles hold a multiple of 2^M elements)
-            int k = 0;
-            while (k < M && (esize << (k + 1)) <= 8) ++k;
-            const int64_t te_u = tile_elems >> k;
-            switch (esize << k) {
-                case 1: return launch_staged<1>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-                case 2: return launch_staged<2>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-                case 4: return launch_staged<4>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-                default: return launch_staged<8>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-            }
-        }
+        const swz_status s = launch_staged_tiles(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
+        if (s != SWZ_ERR_UNSUPPORTED) return s;
+    }
+    if (B > 0 && S < 0 && M < lv && tile_bytes % 16 == 0 && aligned16) {
+        // A negative shift reads the field at M, below the lane bits of a
+        // vector, and writes |S| bits higher.  The offsets close under the
+        // swizzle in aligned blocks of 2^wtop elements (tiles are multiples
+        // of such blocks).  Blocks inside one vector: a fixed lane map.
+        // Otherwise the lanes of one destination vector come from several
+        // source vectors: blocks of up to the staging size are gathered in
+        // shared memory, larger ones element by element.
+        const int wtop = sw_write_hi(B, M, S);
+        if (wtop <= lv)
+            return launch_lane_map(dst, src, n_elems, esize, 1 << wtop, B, M, S, steps, link_grid, st);
+        const swz_status s = launch_staged_tiles(dst, src, n_elems, int64_t(1) << wtop, esize, B, M, S, steps, st);
+        if (s != SWZ_ERR_UNSUPPORTED) return s;
+        return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
     }
     if (tile_bytes % 16 == 0 && aligned16) {
-        int lv = 0;
-        while ((1 << lv) < 16 / esize) ++lv;
         RelayoutArgs a;
         a.dst = static_cast<uint4 *>(dst);
         a.src = static_cast<const uint4 *>(src);
@@ -377,8 +420,9 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         for (int l = 0; l < 16 / esize; ++l)
             src_lane[l] = static_cast<int>(sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & ((16 / esize) - 1));
         lane_map_selectors(src_lane, esize, a.perm_sel);
+        // (a negative shift reaches here only with M >= log2 V: whole vectors move)
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
-        const int period = B + M + S;
+        const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
         switch (esize) {
             case 1: return launch_vec<1>(a, mode, local, link_grid, st);
@@ -389,14 +433,7 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
             default: return SWZ_ERR_PARAM;
         }
     }
-    switch (esize) {
-        case 1: return launch_scalar<1>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
-        case 2: return launch_scalar<2>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
-        case 4: return launch_scalar<4>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
-        case 8: return launch_scalar<8>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
-        case 16: return launch_scalar<16>(dst, src, n_elems, tile_elems, B, M, S, steps, st);
-        default: return SWZ_ERR_PARAM;
-    }
+    return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
 }
 
 }  // namespace swz

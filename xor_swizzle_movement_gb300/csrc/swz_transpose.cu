@@ -57,14 +57,18 @@ namespace swz {
 // A transpose can hand its output straight to a forward relayout: the
 // transposed matrix, cut into tiles of `te` consecutive elements, each tile
 // stored in Swizzle<B,M,S> order.  Transposed element y then lands at
-// fused_pos(y); a 16-byte vector of it lands in one 16-byte vector (the
-// swizzle only reads bits above the bits it writes), with its lanes moved by
-// the inverse lane map L^-1 (fixed, `sel`) and then XOR-ed by the vector's k.
+// fused_pos(y).  For S > 0 a 16-byte vector of it lands in one 16-byte vector
+// (the swizzle only reads bits above the bits it writes), with its lanes moved
+// by the inverse lane map L^-1 (fixed, `sel`) and then XOR-ed by the vector's
+// k.  A negative shift reads below the bits it writes: vectors stay whole only
+// when M >= log2 V; otherwise (vec_whole = 0) every element is stored on its
+// own through the kernels' element path.
 struct FuseArgs {
     int64_t te;         // relayout tile, elements
     int B, M, S;
-    int global;         // te is a multiple of 2^(B+M+S): the whole-matrix offset may be swizzled directly
+    int global;         // te is a multiple of 2^(B+M+|S|): the whole-matrix offset may be swizzled directly
     int lanes;          // 0: lanes stay (M >= log2 V); 1: lanes XOR-ed by k only (M + S >= log2 V); 2: general
+    int vec_whole;      // 16-byte vectors of the transposed matrix land whole
     uint32_t sel[12];   // bytes_permute selectors of L^-1, L(l) = sw(l) mod V
 };
 
@@ -398,7 +402,7 @@ swz_status launch_unit(void *dst, const void *src, int64_t R, int64_t C, int var
     const int64_t tiles_c = (C + TC - 1) / TC, tiles = ((R + TR - 1) / TR) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     // a fused relayout needs its tiles to hold whole 16-byte vectors
-    const int vec_ok = aligned16 && (C % VPE == 0) && (R % VPE == 0) && (!fuse || fuse->te % VPE == 0);
+    const int vec_ok = aligned16 && (C % VPE == 0) && (R % VPE == 0) && (!fuse || (fuse->te % VPE == 0 && fuse->vec_whole));
     T *d = static_cast<T *>(dst);
     const T *s = static_cast<const T *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
@@ -419,7 +423,7 @@ swz_status launch_16(void *dst, const void *src, int64_t R, int64_t C, int varia
                      const FuseArgs *fuse, cudaStream_t st) {
     const int64_t tiles_c = (C + 63) / 64, tiles = ((R + 63) / 64) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    const int vec_ok = aligned16 && (C % 8 == 0) && (R % 8 == 0) && (!fuse || fuse->te % 8 == 0);
+    const int vec_ok = aligned16 && (C % 8 == 0) && (R % 8 == 0) && (!fuse || (fuse->te % 8 == 0 && fuse->vec_whole));
     uint16_t *d = static_cast<uint16_t *>(dst);
     const uint16_t *s = static_cast<const uint16_t *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
@@ -440,7 +444,7 @@ swz_status launch_8(void *dst, const void *src, int64_t R, int64_t C, bool align
                     cudaStream_t st) {
     const int64_t tiles_c = (C + 127) / 128, tiles = ((R + 127) / 128) * tiles_c;
     if (tiles > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    const int vec_ok = aligned16 && (C % 16 == 0) && (R % 16 == 0) && (!fuse || fuse->te % 16 == 0);
+    const int vec_ok = aligned16 && (C % 16 == 0) && (R % 16 == 0) && (!fuse || (fuse->te % 16 == 0 && fuse->vec_whole));
     uint8_t *d = static_cast<uint8_t *>(dst);
     const uint8_t *s = static_cast<const uint8_t *>(src);
     const unsigned g = static_cast<unsigned>(tiles);
@@ -512,7 +516,7 @@ swz_status transpose_relayout_launch(void *dst, const void *src, int64_t R, int6
     f.B = B;
     f.M = M;
     f.S = S;
-    const int period = B + M + S;
+    const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
     f.global = (B == 0) || (period < 62 && te % (int64_t(1) << period) == 0);
     // L(l) = sw(l) mod V on the lanes of a 16-byte vector; bytes_permute needs L^-1
     const int lanes = 16 / esize;
@@ -523,6 +527,7 @@ swz_status transpose_relayout_launch(void *dst, const void *src, int64_t R, int6
     int lv = 0;
     while ((1 << lv) < lanes) ++lv;
     f.lanes = (B == 0 || M >= lv) ? 0 : (M + S >= lv) ? 1 : 2;
+    f.vec_whole = (B == 0 || S > 0 || M >= lv) ? 1 : 0;
     return dispatch(dst, src, R, C, esize, SWZ_T_SWIZZLED, &f, st);
 }
 
