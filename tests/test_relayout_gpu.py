@@ -280,3 +280,57 @@ def test_host_buffers_larger_than_the_link_grid(swz, orc, esize, rows, cols, bms
     want = orc.relayout(host.view(view), tile_elems=rows * cols, B=B, M=M, S=S, direction=0)
     assert np.array_equal(phys.cpu().numpy().view(view), want)
     assert np.array_equal(h_back.numpy(), host)
+
+
+@pytest.mark.parametrize("esize,src_off,dst_off", [
+    (1, 1, 0), (1, 0, 7), (1, 3, 13), (2, 2, 0), (2, 0, 6), (2, 10, 14), (4, 4, 0), (4, 8, 12), (8, 8, 0), (8, 0, 8),
+])
+@pytest.mark.parametrize("rows,cols,bms,n_tiles", [
+    (64, 64, (3, 3, 3), 9),     # the 16-bit config tile: tiles of whole vectors
+    (64, 128, (5, 2, 5), 5),    # the int8 config tile
+    (24, 64, (3, 3, 3), 3),     # period 512 does not divide 1536: tile-local offsets
+    (8, 8, (2, 0, 1), 5),       # general lane map for 1- and 2-byte elements
+    (1, 16, (1, 0, 1), 1),      # one or a few vectors: the buffer's first and last vectors coincide
+    (1, 1 << 16, (5, 0, 11), 1),  # one large tile
+    (3, 4, (2, 0, 1), 1001),    # ragged tiles: the staged kernel
+    (1, 2, (1, 0, 1), 513),     # tiny tiles: the staged kernel
+    (8, 16, (3, 0, -4), 33),    # a negative shift that splits vectors: staged blocks of 128 elements
+    (2, 8, (0, 0, 1), 100),     # B = 0: a plain copy
+    (6, 464, (0, 3, 2), 34),    # B = 0 with M = 3
+])
+def test_relayout_unaligned_pointers(swz, orc, esize, src_off, dst_off, rows, cols, bms, n_tiles):
+    """Pointers aligned to the element size but not to 16 bytes.  Tiles of
+    whole 16-byte vectors run the vector kernel on two aligned source chunks
+    per vector and aligned destination chunks assembled across lanes; other
+    tiles run the staged kernel at the pointers' offsets within their 16-byte
+    chunks.  Both directions against the oracle; the guard bytes around the
+    destination stay untouched."""
+    from xor_swizzle_movement_gb300 import inputs
+    B, M, S = bms
+    host = inputs.random_bytes(n_tiles * rows * cols * esize, seed=21 + esize).view(void_dtype(esize))
+    _, src = to_device(host, src_off)
+    for direction in (0, 1):
+        full, dst = empty_device(host.nbytes, dst_off)
+        swz.swz_relayout(dst, src, n_tiles, rows, cols, esize, B, M, S, direction)
+        torch.cuda.synchronize()
+        want = orc.relayout(host, tile_elems=rows * cols, B=B, M=M, S=S, direction=direction)
+        assert np.array_equal(to_host(dst, host.dtype).view(np.uint8), want.view(np.uint8)), direction
+        assert guards_intact(full, dst_off, host.nbytes)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("src_off,dst_off", [(2, 0), (0, 6), (10, 4)])
+def test_relayout_unaligned_64mib(swz, orc, src_off, dst_off):
+    """64 MiB of 16-bit 64 x 64 tiles under Swizzle<3,3,3> with pointers off
+    16-byte alignment (four vectors per thread, many warps), both directions."""
+    from xor_swizzle_movement_gb300 import inputs
+    n_tiles = (64 << 20) // 8192
+    host = inputs.uint16_bits(n_tiles * 4096, seed=31)
+    _, src = to_device(host, src_off)
+    for direction in (0, 1):
+        full, dst = empty_device(host.nbytes, dst_off)
+        swz.swz_relayout(dst, src, n_tiles, 64, 64, 2, 3, 3, 3, direction)
+        torch.cuda.synchronize()
+        want = orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=direction)
+        assert np.array_equal(to_host(dst, np.uint16), want), direction
+        assert guards_intact(full, dst_off, host.nbytes)

@@ -110,6 +110,114 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
     }
 }
 
+// Bytes n .. n + 15 of the 32 bytes lo:hi (0 <= n < 16, n uniform over the
+// launch): word selects and funnel shifts, no local memory.
+__device__ __forceinline__ uint4 bytes_from_pair(uint4 lo, uint4 hi, int n) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const int q = n >> 2, r = (n & 3) * 8;
+    uint32_t sel[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+        const uint32_t a0 = w[j], a1 = w[j + 1], a2 = w[j + 2], a3 = w[j + 3 < 8 ? j + 3 : 7];
+        sel[j] = q == 0 ? a0 : q == 1 ? a1 : q == 2 ? a2 : a3;
+    }
+    return make_uint4(__funnelshift_r(sel[0], sel[1], r), __funnelshift_r(sel[1], sel[2], r),
+                      __funnelshift_r(sel[2], sel[3], r), __funnelshift_r(sel[3], sel[4], r));
+}
+
+__device__ __forceinline__ uint8_t byte_of(const uint4 &v, int i) {
+    const uint32_t w = i < 4 ? v.x : i < 8 ? v.y : i < 12 ? v.z : v.w;
+    return static_cast<uint8_t>(w >> ((i & 3) * 8));
+}
+
+// The vector kernel for buffers whose pointers are aligned to the element
+// size but not to 16 bytes (a_src, a_dst: their offsets within a 16-byte
+// chunk, uniform).  Source: the two aligned chunks that cover a source vector,
+// shifted by a_src bytes (the buffer's first and last vectors are read byte by
+// byte, so no chunk outside the buffer is touched).  Destination: vector u
+// straddles aligned chunks u and u + 1 (counted from dst - a_dst).  The lanes
+// of a warp hold 32 consecutive vectors: each lane but the first takes its
+// left neighbour's vector with a shuffle and stores aligned chunk u whole, and
+// the last lane also computes the next vector (loaded with the others) and
+// stores chunk u + 1 whole.  So every aligned chunk is written once, by one
+// 16-byte store; only the buffer's first and last vectors write their outer
+// part byte by byte.
+template <int E, int MODE, bool LOCAL, bool DMIS>
+__global__ void __launch_bounds__(256, 4) relayout_vec_mis_kernel(const RelayoutArgs a, int a_src, int a_dst) {
+    constexpr int LV = VecTraits<E>::LV;
+    constexpr uint64_t VM = (1u << LV) - 1u;
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    const uint8_t *srcb = reinterpret_cast<const uint8_t *>(a.src);
+    uint8_t *dstb = reinterpret_cast<uint8_t *>(a.dst);
+    const uint4 *sal = reinterpret_cast<const uint4 *>(srcb - a_src);
+    uint4 *dal = reinterpret_cast<uint4 *>(dstb - a_dst);
+    const int lane = threadIdx.x & 31;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
+    // the source vector of destination vector u, its lanes not yet moved
+    auto load_vec = [&](int64_t u, uint32_t &lxo) -> uint4 {
+        int64_t local = u, tile0 = 0;
+        if constexpr (LOCAL) {
+            local = u % a.tile_vecs;
+            tile0 = u - local;
+        }
+        const uint64_t y = static_cast<uint64_t>(local) << LV;
+        const uint64_t x = sw_inv(y, a.B, a.M, a.S, a.steps);
+        const int64_t sv = tile0 + static_cast<int64_t>(x >> LV);
+        lxo = static_cast<uint32_t>(x & VM);
+        if (a_src == 0) return ld_stream16(sal + sv);
+        if (sv == 0 || sv == a.nvec - 1) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int i = 0; i < 16; ++i) w[i >> 2] |= static_cast<uint32_t>(srcb[16 * sv + i]) << ((i & 3) * 8);
+            return make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        return bytes_from_pair(ld_stream16(sal + sv), ld_stream16(sal + sv + 1), a_src);
+    };
+    auto permute = [&](uint4 v, uint32_t lxv) -> uint4 {
+        if constexpr (MODE == kLanesFixed) return v;
+        else if constexpr (MODE == kLanesXor) return lanes_xor<E>(v, lxv);
+        else return bytes_permute(lanes_xor<E>(v, lxv), a.perm_sel);
+    };
+    // DMIS: a_dst != 0 (the halo vectors and the shuffles exist only then)
+    uint4 r[kMaxPerThread], rh[DMIS ? kMaxPerThread : 1];
+    uint32_t lx[kMaxPerThread], lxh[DMIS ? kMaxPerThread : 1];
+    const bool halo_lane = DMIS && lane == 31;
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if (k < a.per_thread && u < a.nvec) r[k] = load_vec(u, lx[k]);
+        if constexpr (DMIS)
+            if (halo_lane && k < a.per_thread && u + 1 < a.nvec) rh[k] = load_vec(u + 1, lxh[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        if (k >= a.per_thread) break;  // uniform
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        const bool act = u < a.nvec;
+        const uint4 out = act ? permute(r[k], lx[k]) : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (!DMIS) {
+            if (act) st_stream16(dal + u, out);
+            continue;
+        }
+        uint4 prev;
+        prev.x = __shfl_up_sync(kFullMask, out.x, 1);
+        prev.y = __shfl_up_sync(kFullMask, out.y, 1);
+        prev.z = __shfl_up_sync(kFullMask, out.z, 1);
+        prev.w = __shfl_up_sync(kFullMask, out.w, 1);
+        if (!act) continue;
+        const int head = 16 - a_dst;  // bytes of vector u in aligned chunk u
+        if (lane > 0) st_stream16(dal + u, bytes_from_pair(prev, out, head));
+        else if (u == 0)
+            for (int i = 0; i < head; ++i) dstb[i] = byte_of(out, i);
+        // (lane 0 with u > 0: the last lane of the warp that holds vector u - 1 stores chunk u)
+        if (u == a.nvec - 1) {
+            for (int i = head; i < 16; ++i) dstb[16 * u + i] = byte_of(out, i);
+        } else if (lane == 31) {
+            st_stream16(dal + u + 1, bytes_from_pair(out, permute(rh[DMIS ? k : 0], lxh[DMIS ? k : 0]), head));
+        }
+    }
+}
+
 template <int E>
 struct ElemType;
 template <> struct ElemType<1> { using T = uint8_t; };
@@ -189,6 +297,27 @@ swz_status launch_vec(const RelayoutArgs &a, int mode, bool local, bool link_gri
     return launched(e);
 }
 
+// Tiles of whole 16-byte vectors on pointers aligned to the element size but
+// not to 16 bytes: relayout_vec_mis_kernel, one CTA per stretch of vectors.
+template <int E>
+swz_status launch_vec_mis(const RelayoutArgs &a, int mode, bool local, int a_src, int a_dst, cudaStream_t st) {
+    const int threads = 256;
+    const int64_t per_cta = static_cast<int64_t>(threads) * a.per_thread;
+    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const dim3 g(static_cast<unsigned>(grid));
+#define SWZ_LAUNCH(MODE, LOCAL)                                                                        \
+    (a_dst ? launch_pdl(relayout_vec_mis_kernel<E, MODE, LOCAL, true>, g, dim3(threads), 0, st, a, a_src, a_dst) \
+           : launch_pdl(relayout_vec_mis_kernel<E, MODE, LOCAL, false>, g, dim3(threads), 0, st, a, a_src, a_dst))
+    cudaError_t e;
+    if (local) e = mode == kLanesFixed ? SWZ_LAUNCH(kLanesFixed, true)
+                   : mode == kLanesXor ? SWZ_LAUNCH(kLanesXor, true) : SWZ_LAUNCH(kLanesGeneral, true);
+    else e = mode == kLanesFixed ? SWZ_LAUNCH(kLanesFixed, false)
+             : mode == kLanesXor ? SWZ_LAUNCH(kLanesXor, false) : SWZ_LAUNCH(kLanesGeneral, false);
+#undef SWZ_LAUNCH
+    return launched(e);
+}
+
 // Tiles whose byte size is not a multiple of 16, with 16-byte aligned
 // pointers: a CTA stages a block of whole tiles (a multiple of
 // lcm(tile bytes, 16), at most kStageBytes) in shared memory with 16-byte
@@ -211,21 +340,31 @@ __device__ __forceinline__ uint32_t sw_inv32(uint32_t y, int B, int M, int S, in
     return x;
 }
 
-template <int E>
+// MIS: dst or src is not 16-byte aligned (both are aligned to the element
+// size).  The block is staged at its source's offset within a 16-byte chunk
+// (a_src) by 16-byte loads of the aligned chunks that cover it, gathered into
+// a second shared buffer at the destination's offset (a_dst), and written out
+// by 16-byte stores of every aligned destination chunk the block owns whole.
+// The chunk shared with the neighbouring block at each end goes out byte by
+// byte (only this block's bytes), and chunks that reach past either end of
+// the buffer are read byte by byte too.
+template <int E, bool MIS>
 __global__ void __launch_bounds__(256)
     relayout_staged_kernel(uint8_t *dst, const uint8_t *src, int64_t bytes, int block_bytes, uint32_t te,
                            uint32_t te_recip, uint32_t pat, uint32_t pat_recip, int B, int M, int S,
-                           int steps) {
+                           int steps, int a_src, int a_dst) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     using T = typename ElemType<E>::T;
     constexpr int V = 16 / E;  // elements per output vector
-    __shared__ __align__(16) uint8_t a_s[kStageBytes];
+    __shared__ __align__(16) uint8_t a_s[kStageBytes + (MIS ? 16 : 0)];
+    __shared__ __align__(16) uint8_t b_s[MIS ? kStageBytes + 16 : 16];
     // Source of each element of an output vector, relative to the vector's
     // first element.  Blocks start on multiples of lcm(tile bytes, 16), so the
     // pattern repeats every `pat` vectors; it is computed once per CTA.
     __shared__ __align__(16) int16_t rel_s[kStageBytes / E];
     const int tid = threadIdx.x;
+    if (!MIS) a_src = a_dst = 0;
     auto local_of = [&](uint32_t e) -> uint32_t { return te == 1 ? 0u : e - __umulhi(e, te_recip) * te; };
     for (uint32_t i = tid; i < pat * V; i += 256) {
         const uint32_t local = local_of(i);
@@ -233,40 +372,87 @@ __global__ void __launch_bounds__(256)
                                         static_cast<int>(i));
     }
     __syncthreads();
+    const uint8_t *sa = a_s + a_src;  // element-space byte j of the block is sa[j]
     for (int64_t b0 = static_cast<int64_t>(blockIdx.x) * block_bytes; b0 < bytes;
          b0 += static_cast<int64_t>(gridDim.x) * block_bytes) {
         const int nb = static_cast<int>(bytes - b0 < block_bytes ? bytes - b0 : block_bytes);
         const int nv = nb / 16;
-        for (int v = tid; v < nv; v += 256)
-            *reinterpret_cast<uint4 *>(a_s + 16 * v) = ld_stream16(src + b0 + 16 * v);
-        for (int t = 16 * nv + tid; t < nb; t += 256) a_s[t] = src[b0 + t];
-        __syncthreads();
-        for (int v = tid; v < nv; v += 256) {
-            const uint32_t e = static_cast<uint32_t>(v) * V;
-            const uint32_t p = pat == 1 ? 0u : static_cast<uint32_t>(v) - __umulhi(static_cast<uint32_t>(v), pat_recip) * pat;
-            int16_t rel[V];
-            memcpy(rel, rel_s + p * V, sizeof rel);
-            T lanes[V];
-#pragma unroll
-            for (int k = 0; k < V; ++k)
-                lanes[k] = *reinterpret_cast<const T *>(a_s + (static_cast<int>(e + k) + rel[k]) * E);
-            uint4 o;
-            memcpy(&o, lanes, 16);
-            st_stream16(dst + b0 + 16 * v, o);
+        if constexpr (MIS) {
+            // chunk q of a_s holds the element-space bytes b0 - a_src + 16q .. + 15
+            const int nq = (a_src + nb + 15) / 16;
+            for (int q = tid; q < nq; q += 256) {
+                const int64_t g0 = b0 - a_src + 16 * q;
+                if (g0 >= 0 && g0 + 16 <= bytes) {
+                    *reinterpret_cast<uint4 *>(a_s + 16 * q) = ld_stream16(src + g0);
+                } else {
+                    for (int t = 0; t < 16; ++t)
+                        if (g0 + t >= 0 && g0 + t < bytes) a_s[16 * q + t] = src[g0 + t];
+                }
+            }
+        } else {
+            for (int v = tid; v < nv; v += 256)
+                *reinterpret_cast<uint4 *>(a_s + 16 * v) = ld_stream16(src + b0 + 16 * v);
+            for (int t = 16 * nv + tid; t < nb; t += 256) a_s[t] = src[b0 + t];
         }
+        __syncthreads();
         const uint32_t ne = static_cast<uint32_t>(nb / E);
+        if constexpr (MIS) {
+            // one unit per thread, consecutive units on consecutive lanes, so
+            // that both the staged reads and the shared writes stay free of
+            // bank conflicts (a vector per thread would put the lanes 16
+            // bytes apart); the table repeats every pat * V units
+            const uint32_t pv = pat * V;
+            const uint32_t pv_recip = pv == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / pv + 1);
+            for (uint32_t e = tid; e < static_cast<uint32_t>(nv) * V; e += 256) {
+                const uint32_t i = pv == 1 ? 0u : e - __umulhi(e, pv_recip) * pv;
+                *reinterpret_cast<T *>(b_s + a_dst + e * E) =
+                    *reinterpret_cast<const T *>(sa + (static_cast<int>(e) + rel_s[i]) * E);
+            }
+        } else {
+            for (int v = tid; v < nv; v += 256) {
+                const uint32_t e = static_cast<uint32_t>(v) * V;
+                const uint32_t p = pat == 1 ? 0u : static_cast<uint32_t>(v) - __umulhi(static_cast<uint32_t>(v), pat_recip) * pat;
+                int16_t rel[V];
+                memcpy(rel, rel_s + p * V, sizeof rel);
+                T lanes[V];
+#pragma unroll
+                for (int k = 0; k < V; ++k)
+                    lanes[k] = *reinterpret_cast<const T *>(sa + (static_cast<int>(e + k) + rel[k]) * E);
+                uint4 o;
+                memcpy(&o, lanes, 16);
+                st_stream16(dst + b0 + 16 * v, o);
+            }
+        }
         for (uint32_t e = static_cast<uint32_t>(nv) * V + tid; e < ne; e += 256) {
             const uint32_t local = local_of(e);
             const uint32_t x = sw_inv32(local, B, M, S, steps);
-            *reinterpret_cast<T *>(dst + b0 + e * E) = *reinterpret_cast<const T *>(a_s + (e - local + x) * E);
+            const T val = *reinterpret_cast<const T *>(sa + (e - local + x) * E);
+            if constexpr (MIS) *reinterpret_cast<T *>(b_s + a_dst + e * E) = val;
+            else *reinterpret_cast<T *>(dst + b0 + e * E) = val;
         }
-        __syncthreads();  // the buffer is refilled for the next block
+        if constexpr (MIS) {
+            __syncthreads();
+            // chunk q of b_s is the 16-byte aligned destination chunk at dst + b0 - a_dst + 16q;
+            // this block owns its bytes a_dst .. a_dst + nb - 1
+            const int nq = (a_dst + nb + 15) / 16;
+            for (int q = tid; q < nq; q += 256) {
+                const int t0 = 16 * q;
+                if (t0 >= a_dst && t0 + 16 <= a_dst + nb) {
+                    st_stream16(dst + b0 - a_dst + t0, *reinterpret_cast<const uint4 *>(b_s + t0));
+                } else {
+                    for (int t = t0; t < t0 + 16; ++t)
+                        if (t >= a_dst && t < a_dst + nb) dst[b0 - a_dst + t] = b_s[t];
+                }
+            }
+        }
+        __syncthreads();  // the buffers are refilled for the next block
     }
 }
 
-template <int E>
+template <int E, bool MIS>
 swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_bytes, int64_t tile_elems, int B,
-                         int M, int S, int steps, cudaStream_t st) {
+                         int M, int S, int steps, int a_src, int a_dst, cudaStream_t st) {
+    if (tile_elems <= 0 || block_bytes <= 0) return SWZ_ERR_PARAM;
     int64_t grid = (bytes + block_bytes - 1) / block_bytes;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
     if (grid > cap) grid = cap;
@@ -280,9 +466,9 @@ swz_status launch_staged(void *dst, const void *src, int64_t bytes, int block_by
     while (h) { const int64_t r = g % h; g = h; h = r; }
     const uint32_t pat = static_cast<uint32_t>(te * E / g);  // lcm / 16 vectors
     const uint32_t pat_recip = pat == 1 ? 0u : static_cast<uint32_t>((uint64_t(1) << 32) / pat + 1);
-    return launched(launch_pdl(relayout_staged_kernel<E>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
+    return launched(launch_pdl(relayout_staged_kernel<E, MIS>, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
                                static_cast<uint8_t *>(dst), static_cast<const uint8_t *>(src), bytes, block_bytes,
-                               te, recip, pat, pat_recip, B, M, S, steps));
+                               te, recip, pat, pat_recip, B, M, S, steps, a_src, a_dst));
 }
 
 template <int E>
@@ -331,9 +517,9 @@ swz_status launch_lane_map(void *dst, const void *src, int64_t n_elems, int esiz
 }
 
 // The staged kernel over blocks of whole `te`-element tiles (te * esize need
-// not be a multiple of 16), with 16-byte aligned pointers.  Returns
-// SWZ_ERR_UNSUPPORTED, launching nothing, when lcm(te * esize, 16) exceeds
-// the staging buffer.
+// not be a multiple of 16).  Pointers that are not 16-byte aligned take the
+// kernel's MIS form.  Returns SWZ_ERR_UNSUPPORTED, launching nothing, when
+// lcm(te * esize, 16) exceeds the staging buffer.
 swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int64_t te, int esize, int B, int M,
                                int S, int steps, cudaStream_t st) {
     const int64_t tile_bytes = te * esize;
@@ -343,18 +529,26 @@ swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int6
     if (l > kStageBytes) return SWZ_ERR_UNSUPPORTED;
     const int block = static_cast<int>(l * (kStageBytes / l));
     const int64_t bytes = n_elems * esize;
+    const int a_src = static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15u);
+    const int a_dst = static_cast<int>(reinterpret_cast<uintptr_t>(dst) & 15u);
+    const bool mis = (a_src | a_dst) != 0;
     // groups of 2^M elements move intact: gather units of 2^k elements,
     // k = min(M, log2(16 / esize)), under Swizzle<B, M - k, S> on unit
-    // offsets (tiles hold a multiple of 2^M elements)
+    // offsets (tiles hold a multiple of 2^M elements); a unit also has to
+    // keep the alignment of both pointers within their 16-byte chunks
     int k = 0;
-    while (k < M && (esize << (k + 1)) <= 8) ++k;
+    while (k < M && (esize << (k + 1)) <= 8 && ((a_src | a_dst) % (esize << (k + 1))) == 0) ++k;
+    if (te <= 0 || te % (int64_t(1) << k) != 0) return SWZ_ERR_UNSUPPORTED;  // blocks of whole units only
     const int64_t te_u = te >> k;
+#define SWZ_STAGED(U) (mis ? launch_staged<U, true>(dst, src, bytes, block, te_u, B, M - k, S, steps, a_src, a_dst, st) \
+                           : launch_staged<U, false>(dst, src, bytes, block, te_u, B, M - k, S, steps, 0, 0, st))
     switch (esize << k) {
-        case 1: return launch_staged<1>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-        case 2: return launch_staged<2>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-        case 4: return launch_staged<4>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
-        default: return launch_staged<8>(dst, src, bytes, block, te_u, B, M - k, S, steps, st);
+        case 1: return SWZ_STAGED(1);
+        case 2: return SWZ_STAGED(2);
+        case 4: return SWZ_STAGED(4);
+        default: return SWZ_STAGED(8);
     }
+#undef SWZ_STAGED
 }
 
 swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
@@ -403,7 +597,8 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         if (s != SWZ_ERR_UNSUPPORTED) return s;
         return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
     }
-    if (tile_bytes % 16 == 0 && aligned16) {
+    // (a negative shift with M < log2 V splits vectors: not for this kernel)
+    if (tile_bytes % 16 == 0 && (aligned16 || esize < 16) && !(B > 0 && S < 0 && M < lv)) {
         RelayoutArgs a;
         a.dst = static_cast<uint4 *>(dst);
         a.src = static_cast<const uint4 *>(src);
@@ -424,6 +619,16 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
         const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
+        if (!aligned16) {
+            const int a_src = static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15u);
+            const int a_dst = static_cast<int>(reinterpret_cast<uintptr_t>(dst) & 15u);
+            switch (esize) {
+                case 1: return launch_vec_mis<1>(a, mode, local, a_src, a_dst, st);
+                case 2: return launch_vec_mis<2>(a, mode, local, a_src, a_dst, st);
+                case 4: return launch_vec_mis<4>(a, mode, local, a_src, a_dst, st);
+                default: return launch_vec_mis<8>(a, mode, local, a_src, a_dst, st);
+            }
+        }
         switch (esize) {
             case 1: return launch_vec<1>(a, mode, local, link_grid, st);
             case 2: return launch_vec<2>(a, mode, local, link_grid, st);
@@ -432,6 +637,20 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
             case 16: return launch_vec<16>(a, mode, local, link_grid, st);
             default: return SWZ_ERR_PARAM;
         }
+    }
+    if (!aligned16 && esize < 16) {
+        // Pointers not 16-byte aligned: the staged kernel in its MIS form over
+        // the smallest blocks the swizzle maps onto themselves (a swizzle
+        // period when the tiles hold whole periods, else a tile); blocks
+        // larger than the staging buffer go element by element.
+        const int period = B + M + (S < 0 ? -S : S);
+        // (blocks are whole groups of 2^M elements: the gather moves units of
+        // up to 2^M elements, and every tile holds whole groups)
+        int64_t te_c = tile_elems;
+        if (B == 0) te_c = int64_t(1) << M;
+        else if (period < 62 && tile_elems % (int64_t(1) << period) == 0) te_c = int64_t(1) << period;
+        const swz_status s = launch_staged_tiles(dst, src, n_elems, te_c, esize, B, M, S, steps, st);
+        if (s != SWZ_ERR_UNSUPPORTED) return s;
     }
     return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
 }
