@@ -7,9 +7,10 @@
 //   forward  dst[sw(i)] = src[i]            -> source of y is sw^-1(y)
 // (sw^-1 == sw when S >= B; otherwise the unitriangular inverse, see sw_inv.)
 //
-// Why a 16-byte vector always maps to ONE source vector: bit p of sw(x) (and
-// of sw^-1(x)) depends only on bits p and above of x, because the field that
-// is read (starting at M + S, S >= 1) sits above the field that is written.
+// Why a 16-byte vector always maps to ONE source vector (S > 0, or S < 0 with
+// M >= log2 V): bit p of sw(x) (and of sw^-1(x)) depends only on bits p and
+// above of x, because the field that is read (starting at M + S, S >= 1) sits
+// above the field that is written.
 // So the bits of the source offset at and above log2(16 / esize) depend only
 // on the same bits of the destination offset: all lanes of a destination
 // vector come from one source vector, permuted inside it.  The kernel is one
@@ -38,7 +39,13 @@
 //   other tiles that are not whole 16-byte vectors, aligned pointers: the
 //     staged kernel (blocks of whole tiles in shared memory, 16-byte output
 //     vectors gathered through a per-CTA table of their sources);
-//   pointers that are not 16-byte aligned: element by element.
+//   negative shifts whose read field lies below the lane bits (they split
+//     vectors): a fixed lane map, the staged kernel over closure blocks, or
+//     element by element;
+//   pointers aligned to the element size but not to 16 bytes: the vector
+//     kernel on shifted pairs of aligned chunks (relayout_vec_mis_kernel) for
+//     tiles of whole vectors, else the staged kernel staged at the pointers'
+//     offsets, else element by element.
 #include "swz_common.cuh"
 
 #include <cstring>
