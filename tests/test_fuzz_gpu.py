@@ -1,8 +1,9 @@
 """Seeded random parity sweep: many small relayout, transpose and fused
-requests with random parameters, shapes and pointer offsets, each compared
-bit for bit with the CPU oracle.  Every request is valid; together they reach
-every kernel path (vector, fixed lane map, staged, element by element, TMA
-modes, each transpose staging)."""
+requests with random parameters (negative shifts included), shapes and
+pointer offsets, each compared bit for bit with the CPU oracle.  Every
+request is valid; together they reach every kernel path (vector, misaligned
+vector, fixed lane map, staged, element by element, TMA modes, each
+transpose staging)."""
 import math
 
 import numpy as np
@@ -29,8 +30,9 @@ def random_relayout(rng):
     esize = int(rng.choice(ESIZES))
     B = int(rng.integers(0, 5))
     M = int(rng.integers(0, 5))
-    S = int(rng.integers(1, 8))
-    unit = 1 << (M + B)
+    S = int(rng.integers(1, 8)) * (-1 if rng.random() < 0.3 else 1)
+    # tiles close under the swizzle in blocks of 2^(bit above the written field)
+    unit = 1 << (M + B + (-S if S < 0 else 0))
     # tile: a multiple of 2^(M+B) elements, up to ~4096
     mult = int(rng.integers(1, max(2, 4096 // unit) + 1))
     tile = unit * mult
@@ -128,7 +130,9 @@ def test_transpose_relayout_fuzz(swz, orc, block):
     while done < 30:
         esize = int(rng.choice(ESIZES))
         B, M, S = int(rng.integers(0, 4)), int(rng.integers(0, 4)), int(rng.integers(1, 6))
-        unit = 1 << (M + B)
+        if rng.random() < 0.3:
+            S = -S
+        unit = 1 << (M + B + (-S if S < 0 and B > 0 else 0))
         rows = int(rng.integers(1, 300))
         cols = int(rng.integers(1, 300))
         n = rows * cols
