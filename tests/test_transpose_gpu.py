@@ -88,7 +88,7 @@ def test_fp16_16384(swz, orc):
     host = inputs.f16_bits_no_nan(n * n, seed=3).reshape(n, n)
     want = orc.transpose(host)
     _, src = to_device(host)
-    for variant in (0, 3):
+    for variant in (0, 3, 1, 2):   # swizzled, TMA, unswizzled, padded: every staging at full size
         full, dst = empty_device(host.nbytes)
         swz.swz_transpose(dst, src, n, n, 2, variant)
         torch.cuda.synchronize()
@@ -102,8 +102,11 @@ def test_fp64_8192(swz, orc):
     from xor_swizzle_movement_gb300 import inputs
     n = 8192
     host = inputs.random_bytes(n * n * 8, seed=4).view(np.uint64).reshape(n, n)
-    got = run_transpose(swz, host, 8, 0)
-    assert np.array_equal(got, orc.transpose(host))
+    want = orc.transpose(host)
+    for variant in (0, 1, 2):      # swizzled, unswizzled, padded: every staging at full size
+        got = run_transpose(swz, host, 8, variant)
+        assert np.array_equal(got, want), variant
+        del got
 
 
 def test_errors(swz):
