@@ -875,6 +875,7 @@ def run_case(args):
         for _ in range(args.reps):
             swz.swz_relayout(dst, src, nbytes // 24, 3, 4, 2, 2, 0, 1, 0)     # uint16 3 x 4, Sw<2,0,1>
             swz.swz_relayout(dst, src, nbytes // 24, 1, 24, 1, 1, 2, 3, 0)    # int8 24, Sw<1,2,3>
+            swz.swz_relayout(dst, src, nbytes // 24, 1, 24, 1, 2, 0, 1, 0)    # int8 24, Sw<2,0,1>: 1-byte units
         done.append(f"relayout staged bytes={nbytes}")
     elif args.case == "transposes":        # every staging of the fp32 / fp16 / fp64 transposes
         for esize, n, variants in ((4, args.n or 8192, (0, 1, 2)), (2, args.n or 8192, (0, 3, 1, 2)),
