@@ -334,3 +334,22 @@ def test_relayout_unaligned_64mib(swz, orc, src_off, dst_off):
         want = orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=direction)
         assert np.array_equal(to_host(dst, np.uint16), want), direction
         assert guards_intact(full, dst_off, host.nbytes)
+
+
+@pytest.mark.parametrize("src_off,dst_off", [(2, 6), (0, 10), (14, 0)])
+def test_relayout_unaligned_tile_local_two_per_thread(swz, orc, src_off, dst_off):
+    """About 700 000 vectors (two per thread on this GPU's grid), tiles of
+    24 x 64 16-bit elements under Swizzle<3,4,3> (period 1024 elements does not
+    divide the 1536-element tile: tile-local offsets), a last warp that is only
+    partly used, pointers off 16-byte alignment; both directions."""
+    from xor_swizzle_movement_gb300 import inputs
+    n_tiles, rows, cols = 3647, 24, 64
+    host = inputs.uint16_bits(n_tiles * rows * cols, seed=33)
+    _, src = to_device(host, src_off)
+    for direction in (0, 1):
+        full, dst = empty_device(host.nbytes, dst_off)
+        swz.swz_relayout(dst, src, n_tiles, rows, cols, 2, 3, 4, 3, direction)
+        torch.cuda.synchronize()
+        want = orc.relayout(host, tile_elems=rows * cols, B=3, M=4, S=3, direction=direction)
+        assert np.array_equal(to_host(dst, np.uint16), want), direction
+        assert guards_intact(full, dst_off, host.nbytes)
