@@ -558,12 +558,13 @@ def measure_rows(torch, swz, dev, flush, peak):
                         ("u32_tile30_sw105", (nb // 120, 1, 30, 4, 1, 0, 5))):
         ms = back_to_back_ms(torch, lambda: swz.swz_relayout(d_, s_[:nb], *args_, 0))
         rag[name] = summary(ms, 2 * nb)
-    # 16-bit 64 x 64 tiles, Swizzle<3,3,3>, 64 MiB, with pointers off 16-byte alignment
+    # 16-bit 64 x 64 tiles, Swizzle<3,3,3>, 240 MiB (larger than L2), with pointers off 16-byte alignment
+    nu = 240 * MiB
     for name, so, do in (("u16_64x64_sw333_source_plus_2B", 2, 0), ("u16_64x64_sw333_destination_plus_2B", 0, 2),
                          ("u16_64x64_sw333_source_plus_6B_destination_plus_10B", 6, 10)):
-        s_off, d_off = s_[so:so + 64 * MiB], d_[do:do + 64 * MiB]
-        ms = back_to_back_ms(torch, lambda: swz.swz_relayout(d_off, s_off, 64 * MiB // 8192, 64, 64, 2, 3, 3, 3, 0))
-        rag[name] = summary(ms, 2 * 64 * MiB)
+        s_off, d_off = s_[so:so + nu], d_[do:do + nu]
+        ms = back_to_back_ms(torch, lambda: swz.swz_relayout(d_off, s_off, nu // 8192, 64, 64, 2, 3, 3, 3, 0))
+        rag[name] = summary(ms, 2 * nu)
     out["relayout_ragged_or_unaligned"] = rag
     del s_, d_, s_off, d_off
 
