@@ -78,7 +78,8 @@ def test_relayout_negative_shift_ragged_and_unaligned(swz, orc, esize, mult, B, 
 @pytest.mark.parametrize("B,M,S", [(3, 3, -3),    # whole vectors move (M >= log2 8)
                                    (3, 0, -4),    # staged blocks of 128 elements
                                    (3, 1, -7),    # staged blocks of 2048 elements (4 KiB)
-                                   (4, 2, -9),    # blocks of 2^15 elements: element by element
+                                   (4, 2, -9),    # blocks of 2^15 elements: whole-vector loads in 2 lane groups
+                                   (4, 0, -9),    # blocks of 2^13 elements, 8 lane groups: element by element
                                    (2, 0, -1)])   # the whole map inside one vector: fixed lane map
 def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     """A 64 MiB uint16 buffer as one tile, every position, both directions,

@@ -223,6 +223,64 @@ __global__ void __launch_bounds__(256) relayout_vec_mis_kernel(const RelayoutArg
     }
 }
 
+// Negative shifts whose read field starts below a vector's lane bits (M <
+// log2 V) but whose written field lies at or above them (M + |S| >= log2 V):
+// the written bits are above the lanes, so lane l of a destination vector
+// comes from lane l of a source vector, and which source vector depends only
+// on the read-field bits of l, the lane bits at M and above.  The V lanes
+// fall into NG = 2^(min(log2 V, M + B) - M) groups; the kernel loads the NG
+// whole source vectors and keeps each group's lanes with a byte mask (the
+// host computes the masks, 4 words per group).  Each source vector is read NG
+// times in all, by NG destination vectors of the same closure block; DRAM
+// serves it once while the block stays in L2.  Tiles hold whole closure
+// blocks (2^(M + |S| + B) elements, checked by the caller), so global offsets
+// equal tile-local ones.
+struct GroupArgs {
+    uint4 *dst;
+    const uint4 *src;
+    int64_t nvec;
+    int B, M, S, steps, per_thread;
+    uint32_t mask[4][4];  // byte masks of the lane groups (group g, word w)
+};
+
+template <int E, int NG>
+__global__ void __launch_bounds__(256) relayout_vec_groups_kernel(const GroupArgs a) {
+    constexpr int LV = VecTraits<E>::LV;
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
+    uint4 r[kMaxPerThread][NG];
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if (k < a.per_thread && u < a.nvec) {
+            const uint64_t y = static_cast<uint64_t>(u) << LV;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                // lane g << M of the vector stands for group g
+                const uint64_t x = sw_inv(y + (static_cast<uint64_t>(g) << a.M), a.B, a.M, a.S, a.steps);
+                // no evict-first hint: every source line is read NG times
+                r[k][g] = ld_stream16(a.src + static_cast<int64_t>(x >> LV));
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if (k < a.per_thread && u < a.nvec) {
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                o.x |= r[k][g].x & a.mask[g][0];
+                o.y |= r[k][g].y & a.mask[g][1];
+                o.z |= r[k][g].z & a.mask[g][2];
+                o.w |= r[k][g].w & a.mask[g][3];
+            }
+            st_stream16(a.dst + u, o);
+        }
+    }
+}
+
 template <int E>
 struct ElemType;
 template <> struct ElemType<1> { using T = uint8_t; };
@@ -577,6 +635,43 @@ swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int6
 #undef SWZ_STAGED
 }
 
+// relayout_vec_groups_kernel for a negative shift with M < log2 V <= M + |S|
+// and at most 4 lane groups; SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.
+swz_status launch_groups(void *dst, const void *src, int64_t n_elems, int esize, int B, int M, int S, int steps,
+                         cudaStream_t st) {
+    int lv = 0;
+    while ((1 << lv) < 16 / esize) ++lv;
+    if (S >= 0 || M >= lv || M - S < lv) return SWZ_ERR_UNSUPPORTED;
+    const int gbits = ((M + B < lv) ? M + B : lv) - M;
+    if (gbits > 2) return SWZ_ERR_UNSUPPORTED;
+    const int ng = 1 << gbits;
+    GroupArgs a{};
+    a.dst = static_cast<uint4 *>(dst);
+    a.src = static_cast<const uint4 *>(src);
+    a.nvec = n_elems * esize / 16;
+    a.B = B; a.M = M; a.S = S;
+    a.steps = steps;
+    const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
+    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+    for (int byte = 0; byte < 16; ++byte) {
+        const int lane = byte / esize;
+        const int g = (lane >> M) & (ng - 1);
+        a.mask[g][byte >> 2] |= 0xffu << ((byte & 3) * 8);
+    }
+    const int64_t per_cta = int64_t(256) * a.per_thread;
+    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    const dim3 g(static_cast<unsigned>(grid));
+#define SWZ_G(EE, NGG) launched(launch_pdl(relayout_vec_groups_kernel<EE, NGG>, g, dim3(256), 0, st, a))
+    switch (esize) {
+        case 1: return ng == 2 ? SWZ_G(1, 2) : SWZ_G(1, 4);
+        case 2: return ng == 2 ? SWZ_G(2, 2) : SWZ_G(2, 4);
+        case 4: return ng == 2 ? SWZ_G(4, 2) : SWZ_G(4, 4);
+        default: return SWZ_G(8, 2);
+    }
+#undef SWZ_G
+}
+
 swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
                              int M, int S, int steps, cudaStream_t st) {
     switch (esize) {
@@ -615,12 +710,16 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // of such blocks).  Blocks inside one vector: a fixed lane map.
         // Otherwise the lanes of one destination vector come from several
         // source vectors: blocks of up to the staging size are gathered in
-        // shared memory, larger ones element by element.
+        // shared memory; larger ones, when the written field lies above the
+        // lane bits and the lanes form at most 4 groups, by whole-vector
+        // loads and byte masks; the rest element by element.
         const int wtop = sw_write_hi(B, M, S);
         if (wtop <= lv)
             return launch_lane_map(dst, src, n_elems, esize, 1 << wtop, B, M, S, steps, link_grid, st);
         const swz_status s = launch_staged_tiles(dst, src, n_elems, int64_t(1) << wtop, esize, B, M, S, steps, st);
         if (s != SWZ_ERR_UNSUPPORTED) return s;
+        const swz_status sg = launch_groups(dst, src, n_elems, esize, B, M, S, steps, st);
+        if (sg != SWZ_ERR_UNSUPPORTED) return sg;
         return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
     }
     // (a negative shift with M < log2 V splits vectors: not for this kernel)
