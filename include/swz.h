@@ -76,7 +76,13 @@ enum {
  *            tile stored contiguously, row-major (offset o = r * cols + c).
  *            Normally device memory; host memory the device can address
  *            (pinned, or any on systems with address translation) also works,
- *            at the host link's rate.
+ *            at the host link's rate.  A call with a host-resident buffer
+ *            runs a grid sized for the link (4 CTAs per SM), so a relayout
+ *            that reads host memory and one that writes it, on two streams,
+ *            run at the same time and use both directions of the link.
+ *            Pointers need only be aligned to esize; pointers off 16-byte
+ *            alignment keep 16-byte global accesses (aligned chunks shifted
+ *            in registers or staged in shared memory) at some cost in speed.
  * esize    : 1, 2, 4, 8 or 16 bytes.  Elements are copied as raw bits.
  * B, M, S  : swizzle parameters in element units; 0 <= B <= 16,
  *            0 <= M <= 32, -32 <= S <= 32, and when B > 0: S != 0 and

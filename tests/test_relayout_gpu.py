@@ -353,3 +353,24 @@ def test_relayout_unaligned_tile_local_two_per_thread(swz, orc, src_off, dst_off
         want = orc.relayout(host, tile_elems=rows * cols, B=3, M=4, S=3, direction=direction)
         assert np.array_equal(to_host(dst, np.uint16), want), direction
         assert guards_intact(full, dst_off, host.nbytes)
+
+
+@pytest.mark.parametrize("src_off,dst_off", [(2, 0), (0, 6)])
+def test_host_buffers_off_16_byte_alignment(swz, orc, src_off, dst_off):
+    """Pinned host buffers whose pointers are off 16-byte alignment: the
+    forward relayout reads the host buffer, the inverse writes one."""
+    from xor_swizzle_movement_gb300 import inputs
+    n_tiles = 512
+    host = inputs.uint16_bits(n_tiles * 4096, seed=34)
+    h_src = torch.zeros(host.nbytes + 16, dtype=torch.uint8).pin_memory()
+    h_src[src_off:src_off + host.nbytes].copy_(torch.from_numpy(host.view(np.uint8)))
+    h_back = torch.zeros(host.nbytes + 16, dtype=torch.uint8).pin_memory()
+    phys = torch.empty(host.nbytes, dtype=torch.uint8, device="cuda")
+    swz.swz_relayout(phys, h_src.data_ptr() + src_off, n_tiles, 64, 64, 2, 3, 3, 3, 0)
+    swz.swz_relayout(h_back.data_ptr() + dst_off, phys, n_tiles, 64, 64, 2, 3, 3, 3, 1)
+    torch.cuda.synchronize()
+    want = orc.relayout(host, tile_elems=4096, B=3, M=3, S=3, direction=0)
+    assert np.array_equal(phys.cpu().numpy().view(np.uint16), want)
+    back = h_back.numpy()
+    assert np.array_equal(back[dst_off:dst_off + host.nbytes].view(np.uint16), host)
+    assert not back[:dst_off].any() and not back[dst_off + host.nbytes:].any()
