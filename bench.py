@@ -607,6 +607,15 @@ def measure_rows(torch, swz, dev, flush, peak):
     ms = back_to_back_ms(torch, lambda: swz.swz_bank_profile(pats, None, npat, 4, ways, wf))
     out["bank_profile_4M_patterns_w4"] = {"ms": round(ms, 4), "Gpatterns/s": round(npat / (ms * 1e-3) / 1e9, 3),
                                           "GB/s": round(npat * 136 / (ms * 1e-3) / GB, 1)}
+
+    # batched slice collision: 2^27 64-bit masks (1 GiB in, 1 GiB out), Swizzle<3,4,3>
+    nm = 1 << 27
+    gen.manual_seed(6)
+    masks = torch.randint(0, 1 << 62, (nm,), dtype=torch.int64, device=dev, generator=gen)
+    coll = torch.empty_like(masks)
+    ms = back_to_back_ms(torch, lambda: swz.swz_slice_collision_batch(masks, nm, 3, 4, 3, coll))
+    out["slice_collision_128M_masks"] = {**summary(ms, 16 * nm), "Gmasks/s": round(nm / (ms * 1e-3) / 1e9, 2)}
+    del masks, coll
     return out
 
 

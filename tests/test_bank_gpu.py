@@ -99,5 +99,31 @@ def test_slice_collision_batch(swz, orc, B, M, S):
     swz.swz_slice_collision_batch(dA, masks.size, B, M, S, dC)
     torch.cuda.synchronize()
     got = dC.cpu().numpy().view(np.uint64)
-    for i in range(0, masks.size, 13):
-        assert int(got[i]) == orc.slice_collision(int(masks[i]), B=B, M=M, S=S)
+    want = np.array([orc.slice_collision(int(a), B=B, M=M, S=S) for a in masks], dtype=np.uint64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n,a_off,c_off,in_place", [
+    (1001, 0, 0, False),   # odd count: pairs by 16-byte accesses, the last mask on its own
+    (1000, 8, 0, False),   # masks off 16-byte alignment: element by element
+    (999, 0, 8, False),
+    (4097, 0, 0, True),    # in place (A == C)
+    (1, 0, 0, False),
+])
+def test_slice_collision_batch_shapes(swz, orc, n, a_off, c_off, in_place):
+    B, M, S = 3, 1, 2
+    masks = np.random.default_rng(n).integers(0, 2**63, n, dtype=np.uint64)
+    bufA = torch.zeros(n + 2, dtype=torch.int64, device="cuda")
+    bufA.view(torch.uint8)[a_off:a_off + 8 * n].copy_(torch.from_numpy(masks.view(np.uint8)).cuda())
+    pa = bufA.data_ptr() + a_off
+    bufC = bufA if in_place else torch.full((n + 2,), -1, dtype=torch.int64, device="cuda")
+    pc = pa if in_place else bufC.data_ptr() + c_off
+    swz.swz_slice_collision_batch(pa, n, B, M, S, pc)
+    torch.cuda.synchronize()
+    raw = bufC.view(torch.uint8).cpu().numpy()
+    off = a_off if in_place else c_off
+    got = raw[off:off + 8 * n].view(np.uint64)
+    want = np.array([orc.slice_collision(int(a), B=B, M=M, S=S) for a in masks], dtype=np.uint64)
+    assert np.array_equal(got, want)
+    if not in_place:  # nothing written outside the n masks
+        assert (raw[:off] == 0xFF).all() and (raw[off + 8 * n:] == 0xFF).all()

@@ -125,14 +125,41 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, 8)  // 8 CTAs (64 warps) pe
     }
 }
 
-__global__ void slice_collision_kernel(const uint64_t *__restrict__ A, int64_t n, int B, int M,
-                                       int S, uint64_t *__restrict__ C) {
+// Element by element (A or C not 16-byte aligned, and the odd last mask).
+__global__ void slice_collision_kernel(const uint64_t *A, int64_t i0, int64_t n, int B, int M, int S,
+                                       uint64_t *C) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    for (int64_t i = i0 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint64_t a = A[i];
         C[i] = a & ~sw_fwd(a, B, M, S);
+    }
+}
+
+// Two masks per 16-byte access, four accesses in flight per thread, one CTA
+// per 1024 accesses.  Plain loads (not the read-only path): A and C may be the
+// same array.
+__global__ void __launch_bounds__(256) slice_collision_vec_kernel(const ulonglong2 *A, int64_t npairs, int B,
+                                                                  int M, int S, ulonglong2 *C) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * 4 + threadIdx.x;
+    ulonglong2 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = base + static_cast<int64_t>(k) * blockDim.x;
+        if (i < npairs) v[k] = A[i];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t i = base + static_cast<int64_t>(k) * blockDim.x;
+        if (i < npairs) {
+            ulonglong2 c;
+            c.x = v[k].x & ~sw_fwd(v[k].x, B, M, S);
+            c.y = v[k].y & ~sw_fwd(v[k].y, B, M, S);
+            C[i] = c;
+        }
     }
 }
 
@@ -158,11 +185,24 @@ swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, in
 
 swz_status slice_collision_launch(const uint64_t *A, int64_t n, int B, int M, int S, uint64_t *C,
                                   cudaStream_t st) {
-    int64_t grid = (n + 255) / 256;
+    const bool aligned16 = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(C)) & 15u) == 0;
+    int64_t done = 0;  // masks handled by the vector kernel
+    if (aligned16 && n >= 2) {
+        const int64_t npairs = n / 2;
+        const int64_t grid = (npairs + 1023) / 1024;
+        if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+        const swz_status s = launched(launch_pdl(slice_collision_vec_kernel, dim3(static_cast<unsigned>(grid)),
+                                                 dim3(256), 0, st, reinterpret_cast<const ulonglong2 *>(A), npairs,
+                                                 B, M, S, reinterpret_cast<ulonglong2 *>(C)));
+        if (s != SWZ_OK) return s;
+        done = 2 * npairs;
+    }
+    if (done == n) return SWZ_OK;
+    int64_t grid = (n - done + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
     if (grid > cap) grid = cap;
-    return launched(launch_pdl(slice_collision_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, A, n, B, M,
-                               S, C));
+    return launched(launch_pdl(slice_collision_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, A, done,
+                               n, B, M, S, C));
 }
 
 }  // namespace swz
