@@ -5,8 +5,10 @@ it (the reading of "NVIDIA CuTe Swizzle"'s bit-diagram comment that the oracle
 pins).  The read field can then sit below a 16-byte vector's lane bits while
 the written one sits above them, so the relayout takes other paths than for a
 positive shift: whole vectors (M >= log2 V), a fixed lane map when the map
-stays inside a vector, staged periods in shared memory, element by element.
-The parameter grid below reaches each of them for every element size."""
+stays inside a vector, cosets of whole vectors in registers when the written
+field lies at or above the lane bits, staged periods in shared memory, element
+by element.  The parameter grid below reaches each of them for every element
+size."""
 import numpy as np
 import pytest
 
@@ -76,10 +78,12 @@ def test_relayout_negative_shift_ragged_and_unaligned(swz, orc, esize, mult, B, 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("B,M,S", [(3, 3, -3),    # whole vectors move (M >= log2 8)
-                                   (3, 0, -4),    # staged blocks of 128 elements
-                                   (3, 1, -7),    # staged blocks of 2048 elements (4 KiB)
-                                   (4, 2, -9),    # blocks of 2^15 elements: whole-vector loads in 2 lane groups
-                                   (4, 0, -9),    # blocks of 2^13 elements, 8 lane groups: element by element
+                                   (3, 0, -4),    # cosets of 8 vectors, 2 adjacent vectors per 256 bytes
+                                   (3, 1, -7),    # cosets of 4 vectors
+                                   (4, 2, -9),    # cosets of 2 vectors
+                                   (4, 0, -9),    # cosets of 8 vectors, one more read bit above the lanes
+                                   (3, 0, -2),    # written field inside the lanes: staged blocks of 32 elements
+                                   (16, 0, -2),   # blocks of 2^18 elements: element by element
                                    (2, 0, -1)])   # the whole map inside one vector: fixed lane map
 def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     """A 64 MiB uint16 buffer as one tile, every position, both directions,
@@ -95,6 +99,41 @@ def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     assert torch.equal(back, src)
     want = orc.relayout(host, tile_elems=n, B=B, M=M, S=S, direction=0)
     assert np.array_equal(fwd.cpu().numpy().view(np.uint16), want)
+
+
+# One parameter set per instantiation of the coset kernel (U = esize * 2^M
+# bytes move together, g read-field bits lie in the lanes), several with
+# overlapping fields (|S| < B).  Buffers of a few MiB: many CTAs, and an odd
+# number of closure blocks so that the last CTA is partly idle.
+COSETS = [
+    # esize, B, M, S          U, g
+    (1, 1, 0, -4),          # 1, 1
+    (1, 2, 0, -5),          # 1, 2
+    (1, 3, 0, -6),          # 1, 3
+    (1, 5, 0, -4),          # 1, 4 (overlap)
+    (1, 4, 0, -9),          # 1, 4
+    (1, 3, 1, -3),          # 2, 3
+    (2, 2, 0, -3),          # 2, 2
+    (2, 1, 0, -5),          # 2, 1
+    (2, 4, 1, -2),          # 4, 2 (overlap)
+    (4, 1, 0, -2),          # 4, 1
+    (4, 3, 0, -2),          # 4, 2 (overlap)
+    (8, 2, 0, -1),          # 8, 1 (overlap)
+    (1, 1, 3, -1),          # 8, 1
+    (2, 6, 0, -5),          # 2, 3 (overlap), read bits above the lanes
+]
+
+
+@pytest.mark.parametrize("esize,B,M,S", COSETS)
+def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
+    from xor_swizzle_movement_gb300 import inputs
+    block = 1 << _wtop(B, M, S)
+    n_blocks = max(1, (6 << 20) // (block * esize)) | 1
+    tile = block * (n_blocks if n_blocks < 8 else 1)
+    n_tiles = (block * n_blocks) // tile
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=500 + esize * 37 + B * 5 - S).view(void_dtype(esize))
+    for direction in (0, 1):
+        _run(swz, orc, host, n_tiles, 1, tile, esize, B, M, S, direction)
 
 
 @pytest.mark.parametrize("esize,rows,cols,te,B,M,S", [

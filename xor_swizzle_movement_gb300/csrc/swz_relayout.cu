@@ -40,7 +40,8 @@
 //     staged kernel (blocks of whole tiles in shared memory, 16-byte output
 //     vectors gathered through a per-CTA table of their sources);
 //   negative shifts whose read field lies below the lane bits (they split
-//     vectors): a fixed lane map, the staged kernel over closure blocks, or
+//     vectors): a fixed lane map, cosets of whole vectors in registers
+//     (relayout_coset_kernel), the staged kernel over closure blocks, or
 //     element by element;
 //   pointers aligned to the element size but not to 16 bytes: the vector
 //     kernel on shifted pairs of aligned chunks (relayout_vec_mis_kernel) for
@@ -48,6 +49,7 @@
 //     offsets, else element by element.
 #include "swz_common.cuh"
 
+#include <algorithm>
 #include <cstring>
 
 namespace swz {
@@ -224,59 +226,104 @@ __global__ void __launch_bounds__(256) relayout_vec_mis_kernel(const RelayoutArg
 }
 
 // Negative shifts whose read field starts below a vector's lane bits (M <
-// log2 V) but whose written field lies at or above them (M + |S| >= log2 V):
-// the written bits are above the lanes, so lane l of a destination vector
-// comes from lane l of a source vector, and which source vector depends only
-// on the read-field bits of l, the lane bits at M and above.  The V lanes
-// fall into NG = 2^(min(log2 V, M + B) - M) groups; the kernel loads the NG
-// whole source vectors and keeps each group's lanes with a byte mask (the
-// host computes the masks, 4 words per group).  Each source vector is read NG
-// times in all, by NG destination vectors of the same closure block; DRAM
-// serves it once while the block stays in L2.  Tiles hold whole closure
+// log2 V) but whose written field lies at or above them (M + |S| >= log2 V).
+// The gather map G (sw^-1 forward, sw inverse) then never changes a lane bit,
+// and on the bits of an offset it is linear over GF(2).  For destination
+// vector d and lane l the source element is G(dV) ^ G(l): lane l of vector
+// Gv(d) ^ Gv(l), Gv(.) the vector part.  Gv(l) only depends on the g read-
+// field bits inside the lanes (g = min(M + B, log2 V) - M); their images w_i
+// = Gv(2^(M+i)) span a g-dimensional space W.  The destination vectors whose
+// sources lie in one coset s0 ^ W form one coset d0 ^ W' (W' = Gv^-1(W), basis
+// w'_i = Gv^-1(w_i), s0 = Gv(d0)), so a thread owns such a pair: it loads the
+// 2^g vectors V_k = s0 ^ w(k) once and stores the 2^g vectors D_j = d0 ^ w'(j),
+// lane l of D_j being lane l of V_{j ^ phi(l)}, phi(l) = (l >> M) mod 2^g.
+// Each source and each destination vector is touched once.  Lanes move in
+// units of U = esize * 2^M bytes, so the kernel is instantiated on (U, g).
+// Threads enumerate the cosets by their representative with zeros at the
+// pivot bits of W' (reduced echelon form): consecutive threads take
+// consecutive vectors below the lowest pivot.  Tiles hold whole closure
 // blocks (2^(M + |S| + B) elements, checked by the caller), so global offsets
 // equal tile-local ones.
-struct GroupArgs {
+struct CosetArgs {
     uint4 *dst;
     const uint4 *src;
-    int64_t nvec;
-    int B, M, S, steps, per_thread;
-    uint32_t mask[4][4];  // byte masks of the lane groups (group g, word w)
+    int64_t n_cosets;   // 16-byte vectors / 2^g
+    int B, M, S, steps, lv;
+    int pivot[4];       // ascending bit positions left zero in a coset's representative
+    uint64_t w[4];      // source side: w_i (vector offsets)
+    uint64_t wd[4];     // destination side: w'_i
 };
 
-template <int E, int NG>
-__global__ void __launch_bounds__(256) relayout_vec_groups_kernel(const GroupArgs a) {
-    constexpr int LV = VecTraits<E>::LV;
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
+    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+// Word q of D_j (j, q compile-time after unrolling): its bytes come from
+// lanes of the same word in V_{j ^ phi}, one unit of U bytes at a time.
+template <int U, int G>
+__device__ __forceinline__ uint32_t coset_word(const uint4 (&v)[1 << G], int j, int q) {
+    constexpr int m = (1 << G) - 1;
+    if constexpr (U >= 4) {
+        return word_of(v[j ^ (((4 * q) / U) & m)], q);
+    } else if constexpr (U == 2) {
+        return __byte_perm(word_of(v[j ^ ((2 * q) & m)], q), word_of(v[j ^ ((2 * q + 1) & m)], q), 0x7610);
+    } else {
+        const uint32_t ab = __byte_perm(word_of(v[j ^ ((4 * q) & m)], q), word_of(v[j ^ ((4 * q + 1) & m)], q), 0x3250);
+        const uint32_t cd = __byte_perm(word_of(v[j ^ ((4 * q + 2) & m)], q), word_of(v[j ^ ((4 * q + 3) & m)], q), 0x7210);
+        return __byte_perm(ab, cd, 0x7610);
+    }
+}
+
+template <int U, int G>
+__global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) {
+    constexpr int NV = 1 << G;
+    constexpr int NC = (G >= 3) ? 1 : (8 >> G);  // cosets per thread: 8 or 16 vectors in flight
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
-    uint4 r[kMaxPerThread][NG];
+    const uint64_t pol = l2_evict_first_policy();  // every source vector is read once
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * NC + threadIdx.x;
+    uint4 v[NC][NV];
+    uint64_t d0[NC];
+    // every load first, then every store (a store is a compiler barrier)
 #pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
-        if (k < a.per_thread && u < a.nvec) {
-            const uint64_t y = static_cast<uint64_t>(u) << LV;
+    for (int c = 0; c < NC; ++c) {
+        const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
+        if (t < a.n_cosets) {
+            uint64_t d = static_cast<uint64_t>(t);
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                // lane g << M of the vector stands for group g
-                const uint64_t x = sw_inv(y + (static_cast<uint64_t>(g) << a.M), a.B, a.M, a.S, a.steps);
-                // no evict-first hint: every source line is read NG times
-                r[k][g] = ld_stream16(a.src + static_cast<int64_t>(x >> LV));
+            for (int i = 0; i < G; ++i) {
+                const int p = a.pivot[i];
+                d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
+            }
+            d0[c] = d;
+            const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                uint64_t s = s0;
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if ((k >> i) & 1) s ^= a.w[i];
+                v[c][k] = ld_stream16_hint(a.src + s, pol);
             }
         }
     }
 #pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
-        if (k < a.per_thread && u < a.nvec) {
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < NC; ++c) {
+        const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
+        if (t < a.n_cosets) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                o.x |= r[k][g].x & a.mask[g][0];
-                o.y |= r[k][g].y & a.mask[g][1];
-                o.z |= r[k][g].z & a.mask[g][2];
-                o.w |= r[k][g].w & a.mask[g][3];
+            for (int j = 0; j < NV; ++j) {
+                uint64_t d = d0[c];
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if ((j >> i) & 1) d ^= a.wd[i];
+                uint4 o;
+                o.x = coset_word<U, G>(v[c], j, 0);
+                o.y = coset_word<U, G>(v[c], j, 1);
+                o.z = coset_word<U, G>(v[c], j, 2);
+                o.w = coset_word<U, G>(v[c], j, 3);
+                st_stream16(a.dst + d, o);
             }
-            st_stream16(a.dst + u, o);
         }
     }
 }
@@ -635,41 +682,65 @@ swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int6
 #undef SWZ_STAGED
 }
 
-// relayout_vec_groups_kernel for a negative shift with M < log2 V <= M + |S|
-// and at most 4 lane groups; SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.
-swz_status launch_groups(void *dst, const void *src, int64_t n_elems, int esize, int B, int M, int S, int steps,
-                         cudaStream_t st) {
+// relayout_coset_kernel for a negative shift with M < log2 V <= M + |S|;
+// SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.  The bases of W and W'
+// and the pivots of W' are computed here, once per launch.
+swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, int B, int M, int S, int steps,
+                        cudaStream_t st) {
     int lv = 0;
     while ((1 << lv) < 16 / esize) ++lv;
-    if (S >= 0 || M >= lv || M - S < lv) return SWZ_ERR_UNSUPPORTED;
-    const int gbits = ((M + B < lv) ? M + B : lv) - M;
-    if (gbits > 2) return SWZ_ERR_UNSUPPORTED;
-    const int ng = 1 << gbits;
-    GroupArgs a{};
+    if (B <= 0 || S >= 0 || M >= lv || M - S < lv) return SWZ_ERR_UNSUPPORTED;
+    const int g = ((M + B < lv) ? M + B : lv) - M;  // 1..4
+    const int U = esize << M;                       // 1, 2, 4 or 8 bytes
+    const int other = (steps == 1) ? sw_inv_steps(B, S) : 1;  // steps of G^-1
+    CosetArgs a{};
     a.dst = static_cast<uint4 *>(dst);
     a.src = static_cast<const uint4 *>(src);
-    a.nvec = n_elems * esize / 16;
+    const int64_t nvec = n_elems * esize / 16;
+    a.n_cosets = nvec >> g;
     a.B = B; a.M = M; a.S = S;
     a.steps = steps;
-    const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
-    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
-    for (int byte = 0; byte < 16; ++byte) {
-        const int lane = byte / esize;
-        const int g = (lane >> M) & (ng - 1);
-        a.mask[g][byte >> 2] |= 0xffu << ((byte & 3) * 8);
+    a.lv = lv;
+    uint64_t r[4];
+    for (int i = 0; i < g; ++i) {
+        a.w[i] = sw_inv(1ull << (M + i), B, M, S, steps) >> lv;
+        a.wd[i] = sw_inv(a.w[i] << lv, B, M, S, other) >> lv;
+        r[i] = a.wd[i];
     }
-    const int64_t per_cta = int64_t(256) * a.per_thread;
-    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    // reduced echelon form of W': pivot i is the top bit of row i, cleared
+    // from every other row
+    for (int i = 0; i < g; ++i) {
+        for (int k = 0; k < i; ++k)
+            if ((r[i] >> a.pivot[k]) & 1u) r[i] ^= r[k];
+        if (r[i] == 0) return SWZ_ERR_UNSUPPORTED;  // (W' has dimension g for every valid swizzle)
+        int p = 63;
+        while (!((r[i] >> p) & 1u)) --p;
+        a.pivot[i] = p;
+        for (int k = 0; k < i; ++k)
+            if ((r[k] >> p) & 1u) r[k] ^= r[i];
+    }
+    std::sort(a.pivot, a.pivot + g);
+    const int nc = (g >= 3) ? 1 : (8 >> g);
+    const int64_t per_cta = int64_t(256) * nc;
+    const int64_t grid = (a.n_cosets + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
-    const dim3 g(static_cast<unsigned>(grid));
-#define SWZ_G(EE, NGG) launched(launch_pdl(relayout_vec_groups_kernel<EE, NGG>, g, dim3(256), 0, st, a))
-    switch (esize) {
-        case 1: return ng == 2 ? SWZ_G(1, 2) : SWZ_G(1, 4);
-        case 2: return ng == 2 ? SWZ_G(2, 2) : SWZ_G(2, 4);
-        case 4: return ng == 2 ? SWZ_G(4, 2) : SWZ_G(4, 4);
-        default: return SWZ_G(8, 2);
+    if (grid == 0) return SWZ_OK;
+    const dim3 gr(static_cast<unsigned>(grid));
+#define SWZ_C(UU, GG) launched(launch_pdl(relayout_coset_kernel<UU, GG>, gr, dim3(256), 0, st, a))
+    switch (U * 8 + g) {
+        case 1 * 8 + 1: return SWZ_C(1, 1);
+        case 1 * 8 + 2: return SWZ_C(1, 2);
+        case 1 * 8 + 3: return SWZ_C(1, 3);
+        case 1 * 8 + 4: return SWZ_C(1, 4);
+        case 2 * 8 + 1: return SWZ_C(2, 1);
+        case 2 * 8 + 2: return SWZ_C(2, 2);
+        case 2 * 8 + 3: return SWZ_C(2, 3);
+        case 4 * 8 + 1: return SWZ_C(4, 1);
+        case 4 * 8 + 2: return SWZ_C(4, 2);
+        case 8 * 8 + 1: return SWZ_C(8, 1);
+        default: return SWZ_ERR_UNSUPPORTED;
     }
-#undef SWZ_G
+#undef SWZ_C
 }
 
 swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
@@ -709,17 +780,17 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // swizzle in aligned blocks of 2^wtop elements (tiles are multiples
         // of such blocks).  Blocks inside one vector: a fixed lane map.
         // Otherwise the lanes of one destination vector come from several
-        // source vectors: blocks of up to the staging size are gathered in
-        // shared memory; larger ones, when the written field lies above the
-        // lane bits and the lanes form at most 4 groups, by whole-vector
-        // loads and byte masks; the rest element by element.
+        // source vectors: when the written field lies at or above the lane
+        // bits, by cosets of whole vectors in registers; else blocks of up to
+        // the staging size are gathered in shared memory, and the rest
+        // element by element.
         const int wtop = sw_write_hi(B, M, S);
         if (wtop <= lv)
             return launch_lane_map(dst, src, n_elems, esize, 1 << wtop, B, M, S, steps, link_grid, st);
+        const swz_status sc = launch_coset(dst, src, n_elems, esize, B, M, S, steps, st);
+        if (sc != SWZ_ERR_UNSUPPORTED) return sc;
         const swz_status s = launch_staged_tiles(dst, src, n_elems, int64_t(1) << wtop, esize, B, M, S, steps, st);
         if (s != SWZ_ERR_UNSUPPORTED) return s;
-        const swz_status sg = launch_groups(dst, src, n_elems, esize, B, M, S, steps, st);
-        if (sg != SWZ_ERR_UNSUPPORTED) return sg;
         return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
     }
     // (a negative shift with M < log2 V splits vectors: not for this kernel)
