@@ -81,7 +81,7 @@ def parse():
                    help="run one kernel case for a profiler and exit: relayout, relayout_bf16, relayout_bms, staging_probe, "
                         "relayout_staged, relayout_tma, transposes, transpose_u8, transpose_relayout, bank_profile")
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
-    p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S")
+    p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S (several sets separated by ';')")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
     p.add_argument("--launcher-check", action="store_true",
                    help="check the multi-rank launch on CPU (gloo): each rank reports a fixed time, rank 0 "
@@ -871,14 +871,15 @@ def run_case(args):
             swz.swz_relayout(a, src, nt, nr, nc, ne, *BF16["bms"], 0)
             swz.swz_relayout(b, a, nt, nr, nc, ne, *BF16["bms"], 1)
         done.append("relayout bf16 64 MiB Sw<3,4,3> fwd+inv")
-    elif args.case == "relayout_bms":      # one uint16 buffer as one tile, forward
+    elif args.case == "relayout_bms":      # one uint16 buffer as one tile, forward, per parameter set
         n = args.n or (1 << 27)
-        Bq, Mq, Sq = (int(v) for v in args.bms.split(","))
         src = rand_bytes(2 * n)
         dst = torch.empty_like(src)
-        for _ in range(args.reps):
-            swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0)
-        done.append(f"relayout uint16 n={n} Sw<{Bq},{Mq},{Sq}>")
+        for bms in args.bms.split(";"):
+            Bq, Mq, Sq = (int(v) for v in bms.split(","))
+            for _ in range(args.reps):
+                swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0)
+            done.append(f"relayout uint16 n={n} Sw<{Bq},{Mq},{Sq}>")
     elif args.case == "relayout_staged":   # ragged 24-byte tiles staged in shared memory
         nbytes = (args.n or (256 << 20)) // 24 * 24
         src = rand_bytes(nbytes)

@@ -102,8 +102,8 @@ def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
 
 
 # One parameter set per instantiation of the coset kernel (U = esize * 2^M
-# bytes move together, g read-field bits lie in the lanes), several with
-# overlapping fields (|S| < B).  Buffers of a few MiB: many CTAs, and an odd
+# bytes move together, g read-field bits lie in the lanes, 2^SB cosets per
+# thread), several with overlapping fields (|S| < B).  Buffers of a few MiB: many CTAs, and an odd
 # number of closure blocks so that the last CTA is partly idle.
 COSETS = [
     # esize, B, M, S          U, g
@@ -121,6 +121,13 @@ COSETS = [
     (8, 2, 0, -1),          # 8, 1 (overlap)
     (1, 1, 3, -1),          # 8, 1
     (2, 6, 0, -5),          # 2, 3 (overlap), read bits above the lanes
+    # disjoint fields, r >= 2 read-field bits above the lanes: 2^SB cosets per thread
+    (2, 3, 2, -3),          # 8, 1, SB 2
+    (1, 4, 3, -4),          # 8, 1, SB 3
+    (2, 4, 1, -4),          # 4, 2, SB 2
+    (1, 4, 2, -5),          # 4, 2, SB 2
+    (2, 5, 0, -5),          # 2, 3, SB 1
+    (1, 5, 1, -6),          # 2, 3, SB 1
 ]
 
 

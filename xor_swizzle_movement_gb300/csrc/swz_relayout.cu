@@ -250,6 +250,7 @@ struct CosetArgs {
     int64_t n_cosets;   // 16-byte vectors / 2^g
     int B, M, S, steps, lv;
     int pivot[4];       // ascending bit positions left zero in a coset's representative
+    int sbase;          // SB > 0: first of the g + SB bits a thread's cosets leave to its slots
     uint64_t w[4];      // source side: w_i (vector offsets)
     uint64_t wd[4];     // destination side: w'_i
 };
@@ -274,56 +275,104 @@ __device__ __forceinline__ uint32_t coset_word(const uint4 (&v)[1 << G], int j, 
     }
 }
 
-template <int U, int G>
+// SB > 0 (fields disjoint, |S| >= B, with r = B - g >= 2 read-field bits
+// above the lanes): those bits sit at the bottom of the vector index and Gv
+// copies them into the region bits just above the pivots, so a warp whose
+// lanes take consecutive destination vectors reads 2^r regions, 16 bytes from
+// each sector.  A thread then owns 2^SB cosets, d0 = base | (c << |S|) for the
+// SB region bits c, base's low SB (read) bits being tau.  Load slot c fetches
+// coset c ^ tau, whose sources are base's run of vectors in one region, so
+// each load instruction reads whole sectors; SB stages of conditional swaps
+// (by the bits of tau) then put coset c in slot c, and each store
+// instruction writes whole sectors too.
+template <int U, int G, int SB>
 __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) {
     constexpr int NV = 1 << G;
-    constexpr int NC = (G >= 3) ? 1 : (8 >> G);  // cosets per thread: 8 or 16 vectors in flight
+    constexpr int NC = SB > 0 ? (1 << SB) : (G >= 3) ? 1 : (8 >> G);  // cosets per thread
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     const uint64_t pol = l2_evict_first_policy();  // every source vector is read once
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * NC + threadIdx.x;
     uint4 v[NC][NV];
     uint64_t d0[NC];
-    // every load first, then every store (a store is a compiler barrier)
+    if constexpr (SB > 0) {
+        const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (t >= a.n_cosets) return;  // (counts threads here: 2^SB cosets each)
+        const int sb = a.sbase, s = -a.S;
+        const uint64_t base = (static_cast<uint64_t>(t) & ((1ull << sb) - 1ull)) |
+                              ((static_cast<uint64_t>(t) >> sb) << (s + SB));
+        const uint32_t tau = static_cast<uint32_t>(base) & (NC - 1);
+        // every load first, then every store (a store is a compiler barrier)
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
-        if (t < a.n_cosets) {
-            uint64_t d = static_cast<uint64_t>(t);
-#pragma unroll
-            for (int i = 0; i < G; ++i) {
-                const int p = a.pivot[i];
-                d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
-            }
-            d0[c] = d;
-            const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
+        for (int c = 0; c < NC; ++c) {
+            d0[c] = base | (static_cast<uint64_t>(c) << s);
+            const uint64_t cl = base | (static_cast<uint64_t>(c ^ tau) << s);
+            const uint64_t s0 = sw_inv(cl << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
 #pragma unroll
             for (int k = 0; k < NV; ++k) {
-                uint64_t s = s0;
+                uint64_t x = s0;
 #pragma unroll
                 for (int i = 0; i < G; ++i)
-                    if ((k >> i) & 1) s ^= a.w[i];
-                v[c][k] = ld_stream16_hint(a.src + s, pol);
+                    if ((k >> i) & 1) x ^= a.w[i];
+                v[c][k] = ld_stream16_hint(a.src + x, pol);
+            }
+        }
+        // slot c <- slot c ^ tau
+#pragma unroll
+        for (int i = 0; i < SB; ++i) {
+            const bool f = (tau >> i) & 1u;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if (c & (1 << i)) continue;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    const uint4 x = v[c][k], y = v[c | (1 << i)][k];
+                    v[c][k] = f ? y : x;
+                    v[c | (1 << i)][k] = f ? x : y;
+                }
+            }
+        }
+    } else {
+        const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * NC + threadIdx.x;
+        // every load first, then every store (a store is a compiler barrier)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
+            if (t < a.n_cosets) {
+                uint64_t d = static_cast<uint64_t>(t);
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    const int p = a.pivot[i];
+                    d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
+                }
+                d0[c] = d;
+                const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    uint64_t x = s0;
+#pragma unroll
+                    for (int i = 0; i < G; ++i)
+                        if ((k >> i) & 1) x ^= a.w[i];
+                    v[c][k] = ld_stream16_hint(a.src + x, pol);
+                }
             }
         }
     }
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * (SB > 0 ? 1 : NC) + threadIdx.x;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
-        if (t < a.n_cosets) {
+        if (SB == 0 && base + static_cast<int64_t>(c) * blockDim.x >= a.n_cosets) continue;
 #pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                uint64_t d = d0[c];
+        for (int j = 0; j < NV; ++j) {
+            uint64_t d = d0[c];
 #pragma unroll
-                for (int i = 0; i < G; ++i)
-                    if ((j >> i) & 1) d ^= a.wd[i];
-                uint4 o;
-                o.x = coset_word<U, G>(v[c], j, 0);
-                o.y = coset_word<U, G>(v[c], j, 1);
-                o.z = coset_word<U, G>(v[c], j, 2);
-                o.w = coset_word<U, G>(v[c], j, 3);
-                st_stream16(a.dst + d, o);
-            }
+            for (int i = 0; i < G; ++i)
+                if ((j >> i) & 1) d ^= a.wd[i];
+            uint4 o;
+            o.x = coset_word<U, G>(v[c], j, 0);
+            o.y = coset_word<U, G>(v[c], j, 1);
+            o.z = coset_word<U, G>(v[c], j, 2);
+            o.w = coset_word<U, G>(v[c], j, 3);
+            st_stream16(a.dst + d, o);
         }
     }
 }
@@ -720,24 +769,37 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
             if ((r[k] >> p) & 1u) r[k] ^= r[i];
     }
     std::sort(a.pivot, a.pivot + g);
-    const int nc = (g >= 3) ? 1 : (8 >> g);
+    // disjoint fields with r >= 2 read-field bits above the lanes: 2^SB cosets
+    // per thread over the region bits (then W = W' is the g bits below bit |S|)
+    const int r_above = B - g;
+    const int sbits = (-S >= B && r_above >= 2) ? std::min(std::min(r_above, 3), 4 - g) : 0;
+    if (sbits > 0) {
+        a.sbase = -S - g;
+        a.n_cosets = nvec >> (g + sbits);  // threads
+    }
+    const int nc = sbits > 0 ? 1 : (g >= 3) ? 1 : (8 >> g);
     const int64_t per_cta = int64_t(256) * nc;
     const int64_t grid = (a.n_cosets + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_C(UU, GG) launched(launch_pdl(relayout_coset_kernel<UU, GG>, gr, dim3(256), 0, st, a))
-    switch (U * 8 + g) {
-        case 1 * 8 + 1: return SWZ_C(1, 1);
-        case 1 * 8 + 2: return SWZ_C(1, 2);
-        case 1 * 8 + 3: return SWZ_C(1, 3);
-        case 1 * 8 + 4: return SWZ_C(1, 4);
-        case 2 * 8 + 1: return SWZ_C(2, 1);
-        case 2 * 8 + 2: return SWZ_C(2, 2);
-        case 2 * 8 + 3: return SWZ_C(2, 3);
-        case 4 * 8 + 1: return SWZ_C(4, 1);
-        case 4 * 8 + 2: return SWZ_C(4, 2);
-        case 8 * 8 + 1: return SWZ_C(8, 1);
+#define SWZ_C(UU, GG, SS) launched(launch_pdl(relayout_coset_kernel<UU, GG, SS>, gr, dim3(256), 0, st, a))
+    switch ((U * 8 + g) * 4 + sbits) {
+        case (1 * 8 + 1) * 4: return SWZ_C(1, 1, 0);
+        case (1 * 8 + 2) * 4: return SWZ_C(1, 2, 0);
+        case (1 * 8 + 3) * 4: return SWZ_C(1, 3, 0);
+        case (1 * 8 + 4) * 4: return SWZ_C(1, 4, 0);
+        case (2 * 8 + 1) * 4: return SWZ_C(2, 1, 0);
+        case (2 * 8 + 2) * 4: return SWZ_C(2, 2, 0);
+        case (2 * 8 + 3) * 4: return SWZ_C(2, 3, 0);
+        case (4 * 8 + 1) * 4: return SWZ_C(4, 1, 0);
+        case (4 * 8 + 2) * 4: return SWZ_C(4, 2, 0);
+        case (8 * 8 + 1) * 4: return SWZ_C(8, 1, 0);
+        // (r >= 2 means g = log2 V - M, so U = 16 >> g)
+        case (8 * 8 + 1) * 4 + 2: return SWZ_C(8, 1, 2);
+        case (8 * 8 + 1) * 4 + 3: return SWZ_C(8, 1, 3);
+        case (4 * 8 + 2) * 4 + 2: return SWZ_C(4, 2, 2);
+        case (2 * 8 + 3) * 4 + 1: return SWZ_C(2, 3, 1);
         default: return SWZ_ERR_UNSUPPORTED;
     }
 #undef SWZ_C
