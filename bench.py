@@ -497,6 +497,25 @@ def measure_rows(torch, swz, dev, flush, peak):
                              reps=3, groups=2, warm=1)
         neg[label] = summary(ms, 2 << 30)
     neg["note"] = "1 GiB uint16 as one tile, forward; the path each set takes is in its label"
+    # every negative set of the sweep's ranges with the read field in the lanes
+    # (B 1..5, M below log2 V, S -1..-5), uint16 and int8, forward
+    sweep = []
+    for esize, lv in ((2, 3), (1, 4)):
+        ne = (1 << 30) // esize
+        for Bq in range(1, 6):
+            for Mq in range(lv):
+                for Sq in range(-1, -6, -1):
+                    ms = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, 1, 1, ne, esize, Bq, Mq, Sq, 0),
+                                         reps=3, groups=2, warm=1)
+                    sweep.append(((2 << 30) / (ms * 1e-3) / GB, (esize, Bq, Mq, Sq)))
+    sweep.sort()
+    sv = [v for v, _ in sweep]
+    neg["sweep_175"] = {
+        "min": {"GB/s": round(sv[0], 1), "esize_BMS": sweep[0][1]},
+        "median_GB/s": round(statistics.median(sv), 1),
+        "max": {"GB/s": round(sv[-1], 1), "esize_BMS": sweep[-1][1]},
+        "below_0.96_of_hbm": sum(1 for v in sv if v < 0.96 * peak),
+        "lowest_5": [[round(v / peak, 3), list(k)] for v, k in sweep[:5]]}
     out["relayout_uint16_1GiB_negative_shift"] = neg
     del src, dst
 

@@ -5,9 +5,9 @@ it (the reading of "NVIDIA CuTe Swizzle"'s bit-diagram comment that the oracle
 pins).  The read field can then sit below a 16-byte vector's lane bits while
 the written one sits above them, so the relayout takes other paths than for a
 positive shift: whole vectors (M >= log2 V), a fixed lane map when the map
-stays inside a vector, cosets of whole vectors in registers when the written
-field lies at or above the lane bits, staged periods in shared memory, element
-by element.  The parameter grid below reaches each of them for every element
+stays inside a vector, cosets of whole vectors in registers (with a fixed lane
+map when the written field starts inside the lanes), staged periods in shared
+memory for ragged tiles, element by element.  The parameter grid below reaches each of them for every element
 size."""
 import numpy as np
 import pytest
@@ -82,8 +82,8 @@ def test_relayout_negative_shift_ragged_and_unaligned(swz, orc, esize, mult, B, 
                                    (3, 1, -7),    # cosets of 4 vectors
                                    (4, 2, -9),    # cosets of 2 vectors
                                    (4, 0, -9),    # cosets of 8 vectors, one more read bit above the lanes
-                                   (3, 0, -2),    # written field inside the lanes: staged blocks of 32 elements
-                                   (16, 0, -2),   # blocks of 2^18 elements: element by element
+                                   (3, 0, -2),    # written field inside the lanes: cosets with a lane map
+                                   (16, 0, -2),   # the same, blocks of 2^18 elements, 8 inverse steps
                                    (2, 0, -1)])   # the whole map inside one vector: fixed lane map
 def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     """A 64 MiB uint16 buffer as one tile, every position, both directions,
@@ -128,10 +128,34 @@ COSETS = [
     (1, 4, 2, -5),          # 4, 2, SB 2
     (2, 5, 0, -5),          # 2, 3, SB 1
     (1, 5, 1, -6),          # 2, 3, SB 1
+    # M + |S| = log2 V, fields disjoint: a coset is an aligned block of 2^g
+    # vectors, moved with 32-byte accesses (with (1,1,0,-4), (1,3,1,-3),
+    # (2,2,0,-3), (4,1,0,-2) and (1,1,3,-1) above)
+    (1, 2, 0, -4),          # 1, 2, block
+    (1, 3, 0, -4),          # 1, 3, block
+    (1, 4, 0, -4),          # 1, 4, block
+    (2, 1, 0, -3),          # 2, 1, block
+    (4, 2, 0, -2),          # 4, 2, block
 ]
 
 
-@pytest.mark.parametrize("esize,B,M,S", COSETS)
+# Written field starting inside the lanes (M + |S| < log2 V < M + |S| + B):
+# cosets with a fixed lane map, one set per g and several per element size.
+COSETS_MAP = [
+    # esize, B, M, S          g
+    (1, 2, 0, -3),          # 1
+    (1, 3, 0, -3),          # 2
+    (1, 4, 0, -3),          # 3
+    (1, 9, 0, -3),          # 3, 3 inverse steps
+    (2, 2, 1, -1),          # 1
+    (2, 3, 0, -2),          # 2
+    (2, 12, 0, -1),         # 1, 12 inverse steps
+    (4, 2, 0, -1),          # 1
+    (4, 7, 0, -1),          # 1
+]
+
+
+@pytest.mark.parametrize("esize,B,M,S", COSETS + COSETS_MAP)
 def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
     from xor_swizzle_movement_gb300 import inputs
     block = 1 << _wtop(B, M, S)
@@ -141,6 +165,19 @@ def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
     host = inputs.random_bytes(n_tiles * tile * esize, seed=500 + esize * 37 + B * 5 - S).view(void_dtype(esize))
     for direction in (0, 1):
         _run(swz, orc, host, n_tiles, 1, tile, esize, B, M, S, direction)
+
+
+@pytest.mark.parametrize("esize,B,M,S", [(1, 3, 0, -4), (2, 2, 0, -3), (4, 2, 0, -2)])
+@pytest.mark.parametrize("src_off,dst_off", [(16, 48), (0, 16), (16, 0)])
+def test_relayout_cosets_block_16_byte_aligned(swz, orc, esize, B, M, S, src_off, dst_off):
+    """Cosets that are aligned blocks, on pointers 16- but not 32-byte aligned:
+    the kernel keeps 16-byte accesses."""
+    from xor_swizzle_movement_gb300 import inputs
+    block = 1 << _wtop(B, M, S)
+    n_tiles = 1001
+    host = inputs.random_bytes(n_tiles * block * esize, seed=900 + esize).view(void_dtype(esize))
+    for direction in (0, 1):
+        _run(swz, orc, host, n_tiles, 1, block, esize, B, M, S, direction, src_off, dst_off)
 
 
 @pytest.mark.parametrize("esize,rows,cols,te,B,M,S", [

@@ -41,8 +41,8 @@
 //     vectors gathered through a per-CTA table of their sources);
 //   negative shifts whose read field lies below the lane bits (they split
 //     vectors): a fixed lane map, cosets of whole vectors in registers
-//     (relayout_coset_kernel), the staged kernel over closure blocks, or
-//     element by element;
+//     (relayout_coset_kernel, relayout_coset_map_kernel), the staged kernel
+//     over closure blocks, or element by element;
 //   pointers aligned to the element size but not to 16 bytes: the vector
 //     kernel on shifted pairs of aligned chunks (relayout_vec_mis_kernel) for
 //     tiles of whole vectors, else the staged kernel staged at the pointers'
@@ -259,6 +259,19 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
+// 32-byte global access (two 16-byte vectors; the address is 32-byte aligned)
+__device__ __forceinline__ void ld_stream32_hint(const void *p, uint64_t policy, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p), "l"(policy));
+}
+
+__device__ __forceinline__ void st_stream32(void *p, const uint4 &a, const uint4 &b) {
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
 // Word q of D_j (j, q compile-time after unrolling): its bytes come from
 // lanes of the same word in V_{j ^ phi}, one unit of U bytes at a time.
 template <int U, int G>
@@ -285,7 +298,12 @@ __device__ __forceinline__ uint32_t coset_word(const uint4 (&v)[1 << G], int j, 
 // each load instruction reads whole sectors; SB stages of conditional swaps
 // (by the bits of tau) then put coset c in slot c, and each store
 // instruction writes whole sectors too.
-template <int U, int G, int SB>
+// BLK (SB = 0, fields disjoint, M + |S| = log2 V): Gv is the identity and W =
+// W' is spanned by the lowest g vector bits, so a coset is one aligned block
+// of 2^g vectors on both sides, moved with 32-byte accesses (both pointers
+// 32-byte aligned): a warp instruction then reads or writes whole sectors,
+// where 16-byte accesses at a 2^g-vector stride used half of each.
+template <int U, int G, int SB, bool BLK>
 __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) {
     constexpr int NV = 1 << G;
     constexpr int NC = SB > 0 ? (1 << SB) : (G >= 3) ? 1 : (8 >> G);  // cosets per thread
@@ -338,21 +356,28 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
         for (int c = 0; c < NC; ++c) {
             const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
             if (t < a.n_cosets) {
-                uint64_t d = static_cast<uint64_t>(t);
+                if constexpr (BLK) {
+                    const uint64_t d = static_cast<uint64_t>(t) << G;
+                    d0[c] = d;
 #pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    const int p = a.pivot[i];
-                    d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
-                }
-                d0[c] = d;
-                const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
+                    for (int k = 0; k < NV; k += 2) ld_stream32_hint(a.src + d + k, pol, v[c][k], v[c][k + 1]);
+                } else {
+                    uint64_t d = static_cast<uint64_t>(t);
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    uint64_t x = s0;
+                    for (int i = 0; i < G; ++i) {
+                        const int p = a.pivot[i];
+                        d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
+                    }
+                    d0[c] = d;
+                    const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
 #pragma unroll
-                    for (int i = 0; i < G; ++i)
-                        if ((k >> i) & 1) x ^= a.w[i];
-                    v[c][k] = ld_stream16_hint(a.src + x, pol);
+                    for (int k = 0; k < NV; ++k) {
+                        uint64_t x = s0;
+#pragma unroll
+                        for (int i = 0; i < G; ++i)
+                            if ((k >> i) & 1) x ^= a.w[i];
+                        v[c][k] = ld_stream16_hint(a.src + x, pol);
+                    }
                 }
             }
         }
@@ -361,18 +386,109 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         if (SB == 0 && base + static_cast<int64_t>(c) * blockDim.x >= a.n_cosets) continue;
+        if constexpr (BLK) {
+#pragma unroll
+            for (int j = 0; j < NV; j += 2) {
+                uint4 o0, o1;
+                o0.x = coset_word<U, G>(v[c], j, 0);
+                o0.y = coset_word<U, G>(v[c], j, 1);
+                o0.z = coset_word<U, G>(v[c], j, 2);
+                o0.w = coset_word<U, G>(v[c], j, 3);
+                o1.x = coset_word<U, G>(v[c], j + 1, 0);
+                o1.y = coset_word<U, G>(v[c], j + 1, 1);
+                o1.z = coset_word<U, G>(v[c], j + 1, 2);
+                o1.w = coset_word<U, G>(v[c], j + 1, 3);
+                st_stream32(a.dst + d0[c] + j, o0, o1);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                uint64_t d = d0[c];
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if ((j >> i) & 1) d ^= a.wd[i];
+                uint4 o;
+                o.x = coset_word<U, G>(v[c], j, 0);
+                o.y = coset_word<U, G>(v[c], j, 1);
+                o.z = coset_word<U, G>(v[c], j, 2);
+                o.w = coset_word<U, G>(v[c], j, 3);
+                st_stream16(a.dst + d, o);
+            }
+        }
+    }
+}
+
+// Negative shifts whose written field starts inside the lanes (M + |S| <
+// log2 V < M + |S| + B).  The lane bits of G(y) still depend only on the lane
+// bits of y, so G(dV) has no lane part and lane l of destination vector d
+// comes from lane Lam(l) of vector Gv(d) ^ Gv(l): Lam, the lane part of G on
+// a lane index, is a fixed permutation, and Gv(l) lies in the span W of the
+// vector images of the lane bits (dimension g).  With phi(l) the coordinates
+// of Gv(l) in a basis of W, destination D_j of a coset is the blend
+// OR_m (Lam(V_(j ^ m)) & mask_m), mask_m the bytes of the lanes with phi = m
+// (host-computed).  Cosets are enumerated as in relayout_coset_kernel.
+struct CosetMapArgs {
+    CosetArgs c;
+    uint32_t perm_sel[12];  // byte-permutation selectors of Lam (3 per word)
+    uint32_t mask[8][4];    // byte masks of the lanes with phi == m (m < 2^g)
+};
+
+template <int G>
+__global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapArgs a) {
+    constexpr int NV = 1 << G;
+    constexpr int NC = (G >= 3) ? 1 : (8 >> G);  // cosets per thread: 8 vectors in flight
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    const uint64_t pol = l2_evict_first_policy();  // every source vector is read once
+    const CosetArgs &c = a.c;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * NC + threadIdx.x;
+    uint4 v[NC][NV];
+    uint64_t d0[NC];
+    // every load first, then every store (a store is a compiler barrier)
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+        const int64_t t = base + static_cast<int64_t>(q) * blockDim.x;
+        if (t < c.n_cosets) {
+            uint64_t d = static_cast<uint64_t>(t);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                const int p = c.pivot[i];
+                d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
+            }
+            d0[q] = d;
+            const uint64_t s0 = sw_inv(d << c.lv, c.B, c.M, c.S, c.steps) >> c.lv;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                uint64_t x = s0;
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if ((k >> i) & 1) x ^= c.w[i];
+                v[q][k] = ld_stream16_hint(c.src + x, pol);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NC; ++q) {
+        if (base + static_cast<int64_t>(q) * blockDim.x >= c.n_cosets) continue;
+        // (a written bit lies inside the lanes, so Lam is never the identity)
+#pragma unroll
+        for (int k = 0; k < NV; ++k) v[q][k] = bytes_permute(v[q][k], a.perm_sel);
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            uint64_t d = d0[c];
+            uint64_t d = d0[q];
 #pragma unroll
             for (int i = 0; i < G; ++i)
-                if ((j >> i) & 1) d ^= a.wd[i];
-            uint4 o;
-            o.x = coset_word<U, G>(v[c], j, 0);
-            o.y = coset_word<U, G>(v[c], j, 1);
-            o.z = coset_word<U, G>(v[c], j, 2);
-            o.w = coset_word<U, G>(v[c], j, 3);
-            st_stream16(a.dst + d, o);
+                if ((j >> i) & 1) d ^= c.wd[i];
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int m = 0; m < NV; ++m) {
+                const uint4 x = v[q][j ^ m];
+                o.x |= x.x & a.mask[m][0];
+                o.y |= x.y & a.mask[m][1];
+                o.z |= x.z & a.mask[m][2];
+                o.w |= x.w & a.mask[m][3];
+            }
+            st_stream16(c.dst + d, o);
         }
     }
 }
@@ -777,13 +893,20 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
         a.sbase = -S - g;
         a.n_cosets = nvec >> (g + sbits);  // threads
     }
+    // BLK: Gv the identity on every vector bit of a closure block, w_i = e_i,
+    // both pointers 32-byte aligned
+    bool blk = sbits == 0 && ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 31u) == 0;
+    for (int i = 0; blk && i < g; ++i) blk = a.w[i] == (1ull << i);
+    for (int b = 0; blk && b < sw_write_hi(B, M, S) - lv; ++b)
+        blk = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
     const int nc = sbits > 0 ? 1 : (g >= 3) ? 1 : (8 >> g);
     const int64_t per_cta = int64_t(256) * nc;
     const int64_t grid = (a.n_cosets + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_C(UU, GG, SS) launched(launch_pdl(relayout_coset_kernel<UU, GG, SS>, gr, dim3(256), 0, st, a))
+#define SWZ_C(UU, GG, SS) launched(blk ? launch_pdl(relayout_coset_kernel<UU, GG, 0, true>, gr, dim3(256), 0, st, a) \
+                                       : launch_pdl(relayout_coset_kernel<UU, GG, SS, false>, gr, dim3(256), 0, st, a))
     switch ((U * 8 + g) * 4 + sbits) {
         case (1 * 8 + 1) * 4: return SWZ_C(1, 1, 0);
         case (1 * 8 + 2) * 4: return SWZ_C(1, 2, 0);
@@ -803,6 +926,99 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
         default: return SWZ_ERR_UNSUPPORTED;
     }
 #undef SWZ_C
+}
+
+// relayout_coset_map_kernel for a negative shift with M + |S| < log2 V <
+// M + |S| + B and g <= 3; SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.
+swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esize, int B, int M, int S,
+                            int steps, cudaStream_t st) {
+    int lv = 0;
+    while ((1 << lv) < 16 / esize) ++lv;
+    if (B <= 0 || S >= 0 || M >= lv || M - S >= lv || M - S + B <= lv) return SWZ_ERR_UNSUPPORTED;
+    const int V = 1 << lv;
+    const int other = (steps == 1) ? sw_inv_steps(B, S) : 1;  // steps of G^-1
+    CosetMapArgs a{};
+    CosetArgs &c = a.c;
+    c.dst = static_cast<uint4 *>(dst);
+    c.src = static_cast<const uint4 *>(src);
+    c.B = B; c.M = M; c.S = S;
+    c.steps = steps;
+    c.lv = lv;
+    // images of the lane bits: lane part lam[i], vector part u[i]; a basis of
+    // W from them in lane order, and the coordinates phi_bit[i] of each u[i]
+    int lam[4] = {0, 0, 0, 0};
+    uint32_t phi_bit[4] = {0, 0, 0, 0};
+    uint64_t red[4];
+    uint32_t combo[4];
+    int rpiv[4];
+    int g = 0;
+    for (int i = 0; i < lv; ++i) {
+        const uint64_t img = sw_inv(1ull << i, B, M, S, steps);
+        lam[i] = static_cast<int>(img & (V - 1));
+        const uint64_t u = img >> lv;
+        uint64_t x = u;
+        uint32_t cm = 0;
+        for (int t = 0; t < g; ++t)
+            if ((x >> rpiv[t]) & 1u) { x ^= red[t]; cm ^= combo[t]; }
+        if (x == 0) { phi_bit[i] = cm; continue; }
+        if (g == 3) return SWZ_ERR_UNSUPPORTED;  // (g = 4 does not occur in the parameter ranges)
+        int p = 63;
+        while (!((x >> p) & 1u)) --p;
+        const uint32_t cx = cm ^ (1u << g);  // x as a combination of basis elements
+        for (int k = 0; k < g; ++k)
+            if ((red[k] >> p) & 1u) { red[k] ^= x; combo[k] ^= cx; }
+        c.w[g] = u;
+        red[g] = x; rpiv[g] = p; combo[g] = cx;
+        phi_bit[i] = 1u << g;
+        ++g;
+    }
+    if (g == 0) return SWZ_ERR_UNSUPPORTED;
+    // Lam and phi on every lane; the byte permutation and the masks
+    int src_lane[16];
+    uint32_t phi[16];
+    for (int l = 0; l < V; ++l) {
+        int lm = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < lv; ++i)
+            if ((l >> i) & 1) { lm ^= lam[i]; ph ^= phi_bit[i]; }
+        src_lane[l] = lm;
+        phi[l] = ph;
+    }
+    lane_map_selectors(src_lane, esize, a.perm_sel);
+    for (int byte = 0; byte < 16; ++byte)
+        a.mask[phi[byte / esize]][byte >> 2] |= 0xffu << ((byte & 3) * 8);
+    // W' and its pivots
+    uint64_t r[4];
+    for (int i = 0; i < g; ++i) {
+        const uint64_t y = sw_inv(c.w[i] << lv, B, M, S, other);
+        if (y & (V - 1)) return SWZ_ERR_UNSUPPORTED;  // (G^-1 keeps lane bits of a vector offset at 0)
+        c.wd[i] = y >> lv;
+        r[i] = c.wd[i];
+    }
+    for (int i = 0; i < g; ++i) {
+        for (int k = 0; k < i; ++k)
+            if ((r[i] >> c.pivot[k]) & 1u) r[i] ^= r[k];
+        if (r[i] == 0) return SWZ_ERR_UNSUPPORTED;
+        int p = 63;
+        while (!((r[i] >> p) & 1u)) --p;
+        c.pivot[i] = p;
+        for (int k = 0; k < i; ++k)
+            if ((r[k] >> p) & 1u) r[k] ^= r[i];
+    }
+    std::sort(c.pivot, c.pivot + g);
+    const int64_t nvec = n_elems * esize / 16;
+    c.n_cosets = nvec >> g;
+    const int nc = (g >= 3) ? 1 : (8 >> g);
+    const int64_t per_cta = int64_t(256) * nc;
+    const int64_t grid = (c.n_cosets + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    if (grid == 0) return SWZ_OK;
+    const dim3 gr(static_cast<unsigned>(grid));
+    switch (g) {
+        case 1: return launched(launch_pdl(relayout_coset_map_kernel<1>, gr, dim3(256), 0, st, a));
+        case 2: return launched(launch_pdl(relayout_coset_map_kernel<2>, gr, dim3(256), 0, st, a));
+        default: return launched(launch_pdl(relayout_coset_map_kernel<3>, gr, dim3(256), 0, st, a));
+    }
 }
 
 swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
@@ -842,15 +1058,17 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // swizzle in aligned blocks of 2^wtop elements (tiles are multiples
         // of such blocks).  Blocks inside one vector: a fixed lane map.
         // Otherwise the lanes of one destination vector come from several
-        // source vectors: when the written field lies at or above the lane
-        // bits, by cosets of whole vectors in registers; else blocks of up to
-        // the staging size are gathered in shared memory, and the rest
-        // element by element.
+        // source vectors, and they are gathered by cosets of whole vectors in
+        // registers (with a fixed lane map when the written field starts
+        // inside the lanes); what neither covers goes through blocks of up to
+        // the staging size in shared memory, else element by element.
         const int wtop = sw_write_hi(B, M, S);
         if (wtop <= lv)
             return launch_lane_map(dst, src, n_elems, esize, 1 << wtop, B, M, S, steps, link_grid, st);
         const swz_status sc = launch_coset(dst, src, n_elems, esize, B, M, S, steps, st);
         if (sc != SWZ_ERR_UNSUPPORTED) return sc;
+        const swz_status sm = launch_coset_map(dst, src, n_elems, esize, B, M, S, steps, st);
+        if (sm != SWZ_ERR_UNSUPPORTED) return sm;
         const swz_status s = launch_staged_tiles(dst, src, n_elems, int64_t(1) << wtop, esize, B, M, S, steps, st);
         if (s != SWZ_ERR_UNSUPPORTED) return s;
         return launch_scalar_any(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
