@@ -200,6 +200,28 @@ def test_ragged_tiles_staged(swz, orc, esize, tile, B, M, S, n_tiles):
         assert got.tobytes() == want.tobytes(), direction
 
 
+@pytest.mark.parametrize("esize,tile,B,M,S", [
+    (1, 24, 2, 0, 1),     # 8-byte periods in 24-byte tiles
+    (1, 40, 1, 1, 1),     # 8-element periods, groups of 2 bytes
+    (2, 12, 1, 0, 1),     # 4-element periods in 24-byte tiles
+    (1, 24, 1, 0, -2),    # negative shift: 8-byte closure blocks, cosets with a lane map
+    (2, 12, 1, 0, -1),    # negative shift inside one vector
+    (8, 3, 0, 0, 1)])     # B = 0: a copy
+@pytest.mark.parametrize("n_tiles", [1 << 18, (1 << 18) + 2])
+def test_ragged_tiles_of_whole_periods(swz, orc, esize, tile, B, M, S, n_tiles):
+    """Tiles that are not whole 16-byte vectors but hold whole swizzle periods:
+    the swizzle is the same on whole-buffer offsets, and a buffer of whole
+    vectors runs as one tile (several MiB, many CTAs)."""
+    from xor_swizzle_movement_gb300 import inputs
+    if (n_tiles * tile * esize) % 16:
+        n_tiles += 1
+    host = inputs.random_bytes(n_tiles * tile * esize, seed=12).view(void_dtype(esize))
+    for direction in (0, 1):
+        got = run_relayout(swz, host, n_tiles, 1, tile, esize, B, M, S, direction)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), direction
+
+
 @pytest.mark.parametrize("esize", [1, 2, 4, 8])
 def test_misaligned_pointers(swz, orc, esize):
     """Pointers aligned to the element size but not to 16 bytes."""

@@ -1048,6 +1048,13 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
     if (tile_bytes < 16 && 16 % tile_bytes == 0 && aligned16 && (n_elems * esize) % 16 == 0)
         return launch_lane_map(dst, src, n_elems, esize, static_cast<int>(tile_elems), B, M, S, steps, link_grid,
                                st);
+    // Tiles holding whole swizzle periods (2^(B+M+|S|) elements) see the same
+    // swizzle on whole-buffer offsets, so a buffer of whole 16-byte vectors runs
+    // as one tile whatever the tile's own size.
+    const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
+    if (n_tiles > 1 && tile_bytes % 16 != 0 && aligned16 && (n_elems * esize) % 16 == 0 &&
+        (B == 0 || (period < 62 && tile_elems % (int64_t(1) << period) == 0)))
+        return relayout_launch(dst, src, 1, n_elems, esize, B, M, S, direction, st);
     if (tile_bytes % 16 != 0 && aligned16) {
         const swz_status s = launch_staged_tiles(dst, src, n_elems, tile_elems, esize, B, M, S, steps, st);
         if (s != SWZ_ERR_UNSUPPORTED) return s;
@@ -1093,7 +1100,6 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         lane_map_selectors(src_lane, esize, a.perm_sel);
         // (a negative shift reaches here only with M >= log2 V: whole vectors move)
         const int mode = (B == 0 || M >= lv) ? kLanesFixed : (M + S >= lv) ? kLanesXor : kLanesGeneral;
-        const int period = B + M + (S < 0 ? -S : S);  // the offset bits the swizzle touches
         const bool local = B > 0 && (period >= 62 || (tile_elems & ((1LL << period) - 1)) != 0);
         if (!aligned16) {
             const int a_src = static_cast<int>(reinterpret_cast<uintptr_t>(src) & 15u);
@@ -1119,7 +1125,6 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // the smallest blocks the swizzle maps onto themselves (a swizzle
         // period when the tiles hold whole periods, else a tile); blocks
         // larger than the staging buffer go element by element.
-        const int period = B + M + (S < 0 ? -S : S);
         // (blocks are whole groups of 2^M elements: the gather moves units of
         // up to 2^M elements, and every tile holds whole groups)
         int64_t te_c = tile_elems;
