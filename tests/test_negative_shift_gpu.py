@@ -136,6 +136,11 @@ COSETS = [
     (1, 4, 0, -4),          # 1, 4, block
     (2, 1, 0, -3),          # 2, 1, block
     (4, 2, 0, -2),          # 4, 2, block
+    # overlapping fields with M + |S| = log2 V: W' is still the lowest g bits,
+    # so destination blocks are stored with 32-byte accesses
+    (2, 4, 0, -3),          # 2, 3, block stores
+    (1, 5, 1, -3),          # 2, 3, block stores
+    (1, 3, 2, -2),          # 4, 2, block stores
 ]
 
 
@@ -152,6 +157,8 @@ COSETS_MAP = [
     (2, 12, 0, -1),         # 1, 12 inverse steps
     (4, 2, 0, -1),          # 1
     (4, 7, 0, -1),          # 1
+    (2, 4, 0, -2),          # 2, forward with block stores
+    (1, 5, 0, -3),          # 3, forward with block stores
 ]
 
 

@@ -298,12 +298,14 @@ __device__ __forceinline__ uint32_t coset_word(const uint4 (&v)[1 << G], int j, 
 // each load instruction reads whole sectors; SB stages of conditional swaps
 // (by the bits of tau) then put coset c in slot c, and each store
 // instruction writes whole sectors too.
-// BLK (SB = 0, fields disjoint, M + |S| = log2 V): Gv is the identity and W =
-// W' is spanned by the lowest g vector bits, so a coset is one aligned block
-// of 2^g vectors on both sides, moved with 32-byte accesses (both pointers
-// 32-byte aligned): a warp instruction then reads or writes whole sectors,
-// where 16-byte accesses at a 2^g-vector stride used half of each.
-template <int U, int G, int SB, bool BLK>
+// BLK (SB = 0), bit 1: W' is spanned by the lowest g vector bits with w'_i =
+// e_i, so a coset's destination vectors are one aligned block of 2^g vectors,
+// stored with 32-byte accesses (destination 32-byte aligned); bit 0 as well:
+// Gv is the identity (M + |S| = log2 V with disjoint fields), so the sources
+// are the same block, loaded with 32-byte accesses (source 32-byte aligned).
+// A warp instruction then reads or writes whole sectors, where 16-byte
+// accesses at a 2^g-vector stride used half of each.
+template <int U, int G, int SB, int BLK>
 __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) {
     constexpr int NV = 1 << G;
     constexpr int NC = SB > 0 ? (1 << SB) : (G >= 3) ? 1 : (8 >> G);  // cosets per thread
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
         for (int c = 0; c < NC; ++c) {
             const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
             if (t < a.n_cosets) {
-                if constexpr (BLK) {
+                if constexpr ((BLK & 1) != 0) {
                     const uint64_t d = static_cast<uint64_t>(t) << G;
                     d0[c] = d;
 #pragma unroll
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         if (SB == 0 && base + static_cast<int64_t>(c) * blockDim.x >= a.n_cosets) continue;
-        if constexpr (BLK) {
+        if constexpr ((BLK & 2) != 0) {
 #pragma unroll
             for (int j = 0; j < NV; j += 2) {
                 uint4 o0, o1;
@@ -433,7 +435,11 @@ struct CosetMapArgs {
     uint32_t mask[8][4];    // byte masks of the lanes with phi == m (m < 2^g)
 };
 
-template <int G>
+// BLK as for relayout_coset_kernel: bit 1, 32-byte stores of the aligned
+// destination block (the host picks the basis w'_i = e_i when W' is spanned by
+// the lowest g vector bits); bit 0, 32-byte loads of the same block when Gv is
+// the identity.
+template <int G, int BLK>
 __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapArgs a) {
     constexpr int NV = 1 << G;
     constexpr int NC = (G >= 3) ? 1 : (8 >> G);  // cosets per thread: 8 vectors in flight
@@ -456,14 +462,19 @@ __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapA
                 d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
             }
             d0[q] = d;
-            const uint64_t s0 = sw_inv(d << c.lv, c.B, c.M, c.S, c.steps) >> c.lv;
+            if constexpr ((BLK & 1) != 0) {
 #pragma unroll
-            for (int k = 0; k < NV; ++k) {
-                uint64_t x = s0;
+                for (int k = 0; k < NV; k += 2) ld_stream32_hint(c.src + d + k, pol, v[q][k], v[q][k + 1]);
+            } else {
+                const uint64_t s0 = sw_inv(d << c.lv, c.B, c.M, c.S, c.steps) >> c.lv;
 #pragma unroll
-                for (int i = 0; i < G; ++i)
-                    if ((k >> i) & 1) x ^= c.w[i];
-                v[q][k] = ld_stream16_hint(c.src + x, pol);
+                for (int k = 0; k < NV; ++k) {
+                    uint64_t x = s0;
+#pragma unroll
+                    for (int i = 0; i < G; ++i)
+                        if ((k >> i) & 1) x ^= c.w[i];
+                    v[q][k] = ld_stream16_hint(c.src + x, pol);
+                }
             }
         }
     }
@@ -473,22 +484,31 @@ __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapA
         // (a written bit lies inside the lanes, so Lam is never the identity)
 #pragma unroll
         for (int k = 0; k < NV; ++k) v[q][k] = bytes_permute(v[q][k], a.perm_sel);
+        uint4 o[NV];
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            uint64_t d = d0[q];
-#pragma unroll
-            for (int i = 0; i < G; ++i)
-                if ((j >> i) & 1) d ^= c.wd[i];
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            o[j] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int m = 0; m < NV; ++m) {
                 const uint4 x = v[q][j ^ m];
-                o.x |= x.x & a.mask[m][0];
-                o.y |= x.y & a.mask[m][1];
-                o.z |= x.z & a.mask[m][2];
-                o.w |= x.w & a.mask[m][3];
+                o[j].x |= x.x & a.mask[m][0];
+                o[j].y |= x.y & a.mask[m][1];
+                o[j].z |= x.z & a.mask[m][2];
+                o[j].w |= x.w & a.mask[m][3];
             }
-            st_stream16(c.dst + d, o);
+        }
+        if constexpr ((BLK & 2) != 0) {
+#pragma unroll
+            for (int j = 0; j < NV; j += 2) st_stream32(c.dst + d0[q] + j, o[j], o[j + 1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                uint64_t d = d0[q];
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if ((j >> i) & 1) d ^= c.wd[i];
+                st_stream16(c.dst + d, o[j]);
+            }
         }
     }
 }
@@ -895,18 +915,24 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
     }
     // BLK: Gv the identity on every vector bit of a closure block, w_i = e_i,
     // both pointers 32-byte aligned
-    bool blk = sbits == 0 && ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 31u) == 0;
-    for (int i = 0; blk && i < g; ++i) blk = a.w[i] == (1ull << i);
-    for (int b = 0; blk && b < sw_write_hi(B, M, S) - lv; ++b)
-        blk = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
+    // (block stores: w'_i = e_i, destination 32-byte aligned; block loads as well:
+    // Gv the identity on every vector bit of a closure block, source aligned too)
+    bool st32 = sbits == 0 && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
+    for (int i = 0; st32 && i < g; ++i) st32 = a.wd[i] == (1ull << i);
+    bool ld32 = st32 && (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
+    for (int b = 0; ld32 && b < sw_write_hi(B, M, S) - lv; ++b)
+        ld32 = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
+    const int blk = (st32 ? 2 : 0) | (ld32 ? 1 : 0);
     const int nc = sbits > 0 ? 1 : (g >= 3) ? 1 : (8 >> g);
     const int64_t per_cta = int64_t(256) * nc;
     const int64_t grid = (a.n_cosets + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_C(UU, GG, SS) launched(blk ? launch_pdl(relayout_coset_kernel<UU, GG, 0, true>, gr, dim3(256), 0, st, a) \
-                                       : launch_pdl(relayout_coset_kernel<UU, GG, SS, false>, gr, dim3(256), 0, st, a))
+#define SWZ_C(UU, GG, SS)                                                                              \
+    launched(blk == 3   ? launch_pdl(relayout_coset_kernel<UU, GG, 0, 3>, gr, dim3(256), 0, st, a)        \
+             : blk == 2 ? launch_pdl(relayout_coset_kernel<UU, GG, 0, 2>, gr, dim3(256), 0, st, a)        \
+                        : launch_pdl(relayout_coset_kernel<UU, GG, SS, 0>, gr, dim3(256), 0, st, a))
     switch ((U * 8 + g) * 4 + sbits) {
         case (1 * 8 + 1) * 4: return SWZ_C(1, 1, 0);
         case (1 * 8 + 2) * 4: return SWZ_C(1, 2, 0);
@@ -989,11 +1015,62 @@ swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esi
         a.mask[phi[byte / esize]][byte >> 2] |= 0xffu << ((byte & 3) * 8);
     // W' and its pivots
     uint64_t r[4];
+    bool wd_low = true;  // W' spanned by the lowest g vector bits
     for (int i = 0; i < g; ++i) {
         const uint64_t y = sw_inv(c.w[i] << lv, B, M, S, other);
         if (y & (V - 1)) return SWZ_ERR_UNSUPPORTED;  // (G^-1 keeps lane bits of a vector offset at 0)
         c.wd[i] = y >> lv;
         r[i] = c.wd[i];
+        wd_low = wd_low && c.wd[i] < (1ull << g);
+    }
+    int blk = 0;
+    if (wd_low) {
+        // change of basis: w'_i = e_i, w_i = Gv(e_i); phi again, as coordinates
+        // of each lane bit's vector image in the new w basis
+        for (int i = 0; i < g; ++i) {
+            c.wd[i] = 1ull << i;
+            const uint64_t y = sw_inv((1ull << i) << lv, B, M, S, steps);
+            if (y & (V - 1)) return SWZ_ERR_UNSUPPORTED;
+            c.w[i] = y >> lv;
+            r[i] = c.wd[i];
+        }
+        uint64_t nred[4];
+        uint32_t ncombo[4];
+        int npiv[4];
+        for (int i = 0; i < g; ++i) {  // reduced echelon form of the new w basis
+            uint64_t x = c.w[i];
+            uint32_t cx = 1u << i;
+            for (int t = 0; t < i; ++t)
+                if ((x >> npiv[t]) & 1u) { x ^= nred[t]; cx ^= ncombo[t]; }
+            if (x == 0) return SWZ_ERR_UNSUPPORTED;
+            int p = 63;
+            while (!((x >> p) & 1u)) --p;
+            for (int t = 0; t < i; ++t)
+                if ((nred[t] >> p) & 1u) { nred[t] ^= x; ncombo[t] ^= cx; }
+            nred[i] = x; ncombo[i] = cx; npiv[i] = p;
+        }
+        for (int i = 0; i < lv; ++i) {
+            uint64_t x = sw_inv(1ull << i, B, M, S, steps) >> lv;
+            uint32_t cx = 0;
+            for (int t = 0; t < g; ++t)
+                if ((x >> npiv[t]) & 1u) { x ^= nred[t]; cx ^= ncombo[t]; }
+            if (x != 0) return SWZ_ERR_UNSUPPORTED;  // (the images span W)
+            phi_bit[i] = cx;
+        }
+        for (int l = 0; l < V; ++l) {
+            uint32_t ph = 0;
+            for (int i = 0; i < lv; ++i)
+                if ((l >> i) & 1) ph ^= phi_bit[i];
+            phi[l] = ph;
+        }
+        for (int m = 0; m < 8; ++m)
+            for (int w = 0; w < 4; ++w) a.mask[m][w] = 0;
+        for (int byte = 0; byte < 16; ++byte)
+            a.mask[phi[byte / esize]][byte >> 2] |= 0xffu << ((byte & 3) * 8);
+        bool ld32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
+        for (int b = 0; ld32 && b < sw_write_hi(B, M, S) - lv; ++b)
+            ld32 = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
+        if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) blk = ld32 ? 3 : 2;
     }
     for (int i = 0; i < g; ++i) {
         for (int k = 0; k < i; ++k)
@@ -1014,11 +1091,16 @@ swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esi
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
+#define SWZ_M(GG)                                                                                   \
+    launched(blk == 3   ? launch_pdl(relayout_coset_map_kernel<GG, 3>, gr, dim3(256), 0, st, a)      \
+             : blk == 2 ? launch_pdl(relayout_coset_map_kernel<GG, 2>, gr, dim3(256), 0, st, a)      \
+                        : launch_pdl(relayout_coset_map_kernel<GG, 0>, gr, dim3(256), 0, st, a))
     switch (g) {
-        case 1: return launched(launch_pdl(relayout_coset_map_kernel<1>, gr, dim3(256), 0, st, a));
-        case 2: return launched(launch_pdl(relayout_coset_map_kernel<2>, gr, dim3(256), 0, st, a));
-        default: return launched(launch_pdl(relayout_coset_map_kernel<3>, gr, dim3(256), 0, st, a));
+        case 1: return SWZ_M(1);
+        case 2: return SWZ_M(2);
+        default: return SWZ_M(3);
     }
+#undef SWZ_M
 }
 
 swz_status launch_scalar_any(void *dst, const void *src, int64_t n_elems, int64_t tile_elems, int esize, int B,
