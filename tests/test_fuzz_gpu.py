@@ -68,6 +68,35 @@ def test_relayout_fuzz(swz, orc, block):
         assert got.tobytes() == want.tobytes(), (esize, n_tiles, rows, cols, B, M, S, direction, so, do, tma)
 
 
+@pytest.mark.parametrize("block", range(4))
+def test_relayout_fuzz_16_byte_offsets(swz, orc, block):
+    """Requests on pointers 16-byte aligned but, at random, not 32-byte aligned
+    (offsets 0, 16, 32 or 48 bytes from a 512-byte boundary), half of them with
+    negative shifts: the kernels that move 32 bytes per access must fall back
+    when either pointer is off 32-byte alignment."""
+    from xor_swizzle_movement_gb300 import inputs
+    rng = np.random.default_rng(5000 + block)
+    for case in range(40):
+        esize, n_tiles, rows, cols, B, M, S, direction, _, _ = random_relayout(rng)
+        if rng.random() < 0.5 and S > 0:
+            S = -S
+            unit = 1 << (M + B - S)
+            tile = rows * cols
+            if tile % unit:
+                rows, cols = 1, unit * max(1, tile // unit)
+        tile = rows * cols
+        so, do = (int(x) for x in rng.choice([0, 16, 32, 48], size=2))
+        host = inputs.random_bytes(n_tiles * tile * esize, seed=7000 + block * 100 + case).view(void_dtype(esize))
+        _, src = to_device(host, so)
+        full, dst = empty_device(host.nbytes, do)
+        swz.swz_relayout(dst, src, n_tiles, rows, cols, esize, B, M, S, direction)
+        torch.cuda.synchronize()
+        assert guards_intact(full, do, host.nbytes)
+        got = to_host(dst, host.dtype)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), (esize, n_tiles, rows, cols, B, M, S, direction, so, do)
+
+
 def test_relayout_tma_modes_fuzz(swz, orc):
     """Requests inside the TMA's hardware modes (Sw<B, 4 - log2 e, 3>, tiles of
     whole 2^(B+7)-byte periods) with random tile and buffer sizes."""
