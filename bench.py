@@ -402,11 +402,29 @@ def measure_rows(torch, swz, dev, flush, peak):
         swz.swz_relayout_tma(a, src, 256, 64, 64, 2, 3, 3, 3, 0)
         swz.swz_relayout_tma(b, a, 256, 64, 64, 2, 3, 3, 3, 1)
     cold_tma = statistics.mean(timed_launches(torch, small_step_tma, 100, flush))
+    # the floor for a step this small: the same two dependent 2 MiB moves as
+    # plain device-to-device copies (cudaMemcpyAsync), timed the same two ways
+    def copy_step():
+        a.copy_(src)
+        b.copy_(a)
+    copy_cold = statistics.mean(timed_launches(torch, copy_step, 100, flush))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            copy_step()
+    torch.cuda.current_stream().wait_stream(side)
+    cgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cgraph):
+        for _ in range(20):
+            copy_step()
+    copy_warm = back_to_back_ms(torch, cgraph.replay, reps=10) / 20
     out["relayout_fp16_64x64_sw333_2MiB"] = {
         "cold_l2": summary(cold, 8 * src.numel()), "warm_l2_graph": summary(warm, 8 * src.numel()),
         "tma_cold_l2": summary(cold_tma, 8 * src.numel()),
-        "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound"}
-    del src, a, b, graph
+        "copy_floor_cold_l2": summary(copy_cold, 8 * src.numel()),
+        "copy_floor_warm_l2_graph": summary(copy_warm, 8 * src.numel()),
+        "note": "one step = forward + inverse, 8 MiB moved; too small for HBM: launch- and L2-bound. "
+                "copy_floor: the same two dependent 2 MiB moves by cudaMemcpyAsync"}
+    del src, a, b, graph, cgraph
 
     # the 64 MiB bf16 workload: Swizzle<3,4,3> relayout of 4096 tiles of 128 x 64
     # (N(0,1) from seed 1), forward then inverse, L2 flushed before every step
