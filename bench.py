@@ -508,9 +508,10 @@ def measure_rows(torch, swz, dev, flush, peak):
     # negative SShift on the same buffer, forward: one parameter set per relayout path
     neg = {}
     for label, (Bq, Mq, Sq) in (("whole_vectors_sw33m3", (3, 3, -3)), ("lane_map_sw20m1", (2, 0, -1)),
-                                ("cosets_of_8_sw30m4", (3, 0, -4)), ("cosets_of_4_sw31m7", (3, 1, -7)),
+                                ("warp_shuffles_sw30m4", (3, 0, -4)), ("cosets_of_4_sw31m7", (3, 1, -7)),
                                 ("cosets_of_2_sw42m9", (4, 2, -9)), ("cosets_of_8_sw40m9", (4, 0, -9)),
-                                ("cosets_lane_map_sw30m2", (3, 0, -2)), ("cosets_lane_map_sw160m2", (16, 0, -2))):
+                                ("warp_shuffles_lane_map_sw30m2", (3, 0, -2)),
+                                ("cosets_lane_map_sw160m2", (16, 0, -2))):
         ms = back_to_back_ms(torch, lambda: swz.swz_relayout(dst, src, 1, 1, n, 2, Bq, Mq, Sq, 0),
                              reps=3, groups=2, warm=1)
         neg[label] = summary(ms, 2 << 30)

@@ -78,12 +78,12 @@ def test_relayout_negative_shift_ragged_and_unaligned(swz, orc, esize, mult, B, 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("B,M,S", [(3, 3, -3),    # whole vectors move (M >= log2 8)
-                                   (3, 0, -4),    # cosets of 8 vectors, 2 adjacent vectors per 256 bytes
-                                   (3, 1, -7),    # cosets of 4 vectors
-                                   (4, 2, -9),    # cosets of 2 vectors
-                                   (4, 0, -9),    # cosets of 8 vectors, one more read bit above the lanes
-                                   (3, 0, -2),    # written field inside the lanes: cosets with a lane map
-                                   (16, 0, -2),   # the same, blocks of 2^18 elements, 8 inverse steps
+                                   (3, 0, -4),    # warp shuffles (cosets of 8 inside blocks of 32 vectors)
+                                   (3, 1, -7),    # register cosets of 4 vectors
+                                   (4, 2, -9),    # register cosets of 2 vectors, 8 per thread
+                                   (4, 0, -9),    # register cosets of 8 vectors, one more read bit above the lanes
+                                   (3, 0, -2),    # written field inside the lanes: warp shuffles after a lane map
+                                   (16, 0, -2),   # register cosets with a lane map, 2^18-element blocks, 8 inverse steps
                                    (2, 0, -1)])   # the whole map inside one vector: fixed lane map
 def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     """A 64 MiB uint16 buffer as one tile, every position, both directions,
@@ -101,68 +101,88 @@ def test_relayout_negative_shift_64mib(swz, orc, B, M, S):
     assert np.array_equal(fwd.cpu().numpy().view(np.uint16), want)
 
 
-# One parameter set per instantiation of the coset kernel (U = esize * 2^M
-# bytes move together, g read-field bits lie in the lanes, 2^SB cosets per
-# thread), several with overlapping fields (|S| < B).  Buffers of a few MiB: many CTAs, and an odd
-# number of closure blocks so that the last CTA is partly idle.
+# Negative shifts that split vectors, at a few MiB (many CTAs, and an odd
+# number of closure blocks so that the last CTA or warp is partly idle): sets
+# that reach every path, with the path each direction takes (several with
+# overlapping fields, |S| < B).
 COSETS = [
-    # esize, B, M, S          U, g
-    (1, 1, 0, -4),          # 1, 1
-    (1, 2, 0, -5),          # 1, 2
-    (1, 3, 0, -6),          # 1, 3
-    (1, 5, 0, -4),          # 1, 4 (overlap)
-    (1, 4, 0, -9),          # 1, 4
-    (1, 3, 1, -3),          # 2, 3
-    (2, 2, 0, -3),          # 2, 2
-    (2, 1, 0, -5),          # 2, 1
-    (2, 4, 1, -2),          # 4, 2 (overlap)
-    (4, 1, 0, -2),          # 4, 1
-    (4, 3, 0, -2),          # 4, 2 (overlap)
-    (8, 2, 0, -1),          # 8, 1 (overlap)
-    (1, 1, 3, -1),          # 8, 1
-    (2, 6, 0, -5),          # 2, 3 (overlap), read bits above the lanes
-    # disjoint fields, r >= 2 read-field bits above the lanes: 2^SB cosets per thread
-    (2, 3, 2, -3),          # 8, 1, SB 2
-    (1, 4, 3, -4),          # 8, 1, SB 3
-    (2, 4, 1, -4),          # 4, 2, SB 2
-    (1, 4, 2, -5),          # 4, 2, SB 2
-    (2, 5, 0, -5),          # 2, 3, SB 1
-    (1, 5, 1, -6),          # 2, 3, SB 1
-    # M + |S| = log2 V, fields disjoint: a coset is an aligned block of 2^g
-    # vectors, moved with 32-byte accesses (with (1,1,0,-4), (1,3,1,-3),
-    # (2,2,0,-3), (4,1,0,-2) and (1,1,3,-1) above)
-    (1, 2, 0, -4),          # 1, 2, block
-    (1, 3, 0, -4),          # 1, 3, block
-    (1, 4, 0, -4),          # 1, 4, block
-    (2, 1, 0, -3),          # 2, 1, block
-    (4, 2, 0, -2),          # 4, 2, block
-    # overlapping fields with M + |S| = log2 V: W' is still the lowest g bits,
-    # so destination blocks are stored with 32-byte accesses
-    (2, 4, 0, -3),          # 2, 3, block stores
-    (1, 5, 1, -3),          # 2, 3, block stores
-    (1, 3, 2, -2),          # 4, 2, block stores
+    # esize, B, M, S
+    (1, 1, 0, -4),          # warp shuffles
+    (1, 2, 0, -5),          # warp shuffles
+    (1, 3, 0, -6),          # warp shuffles
+    (1, 5, 0, -4),          # warp shuffles
+    (1, 4, 0, -9),          # register cosets U 1 g 4
+    (1, 3, 1, -3),          # warp shuffles
+    (2, 2, 0, -3),          # warp shuffles
+    (2, 1, 0, -5),          # warp shuffles
+    (2, 4, 1, -2),          # warp shuffles
+    (4, 1, 0, -2),          # warp shuffles
+    (4, 3, 0, -2),          # warp shuffles
+    (8, 2, 0, -1),          # warp shuffles
+    (1, 1, 3, -1),          # warp shuffles
+    (2, 6, 0, -5),          # register cosets U 2 g 3
+    (2, 3, 2, -3),          # warp shuffles
+    (1, 4, 3, -4),          # register cosets U 8 g 1 SB 3
+    (2, 4, 1, -4),          # register cosets U 4 g 2 SB 2
+    (1, 4, 2, -5),          # register cosets U 4 g 2 SB 2
+    (2, 5, 0, -5),          # register cosets U 2 g 3 SB 1
+    (1, 5, 1, -6),          # register cosets U 2 g 3 SB 1
+    (1, 2, 0, -4),          # warp shuffles
+    (1, 3, 0, -4),          # warp shuffles
+    (1, 4, 0, -4),          # warp shuffles
+    (2, 1, 0, -3),          # warp shuffles
+    (4, 2, 0, -2),          # warp shuffles
+    (2, 4, 0, -3),          # warp shuffles
+    (1, 5, 1, -3),          # warp shuffles
+    (1, 3, 2, -2),          # warp shuffles
+    (2, 3, 0, -4),          # warp shuffles
+    (4, 2, 0, -3),          # warp shuffles
+    (8, 1, 0, -2),          # warp shuffles
+    (4, 1, 0, -4),          # warp shuffles
+    (1, 1, 0, -5),          # warp shuffles
+    (2, 2, 0, -4),          # warp shuffles
+    (1, 2, 0, -3),          # warp shuffles after a lane map
+    (1, 3, 0, -3),          # warp shuffles after a lane map
+    (1, 4, 0, -3),          # warp shuffles after a lane map
+    (1, 9, 0, -3),          # lane-map cosets g 3 block stores; inverse: lane-map cosets g 3
+    (2, 2, 1, -1),          # warp shuffles after a lane map
+    (2, 3, 0, -2),          # warp shuffles after a lane map
+    (2, 12, 0, -1),         # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
+    (4, 2, 0, -1),          # warp shuffles after a lane map
+    (4, 7, 0, -1),          # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
+    (2, 4, 0, -2),          # warp shuffles after a lane map
+    (1, 5, 0, -3),          # warp shuffles after a lane map
+]
+
+# Sets that stay on the register coset kernels (their sources leave the
+# destination's block of 32 vectors): one per instantiation.
+COSETS_REG = [
+    # esize, B, M, S
+    (1, 1, 0, -9),          # register cosets U 1 g 1
+    (1, 2, 0, -8),          # register cosets U 1 g 2
+    (1, 3, 0, -7),          # register cosets U 1 g 3
+    (1, 4, 0, -6),          # register cosets U 1 g 4
+    (1, 6, 0, -4),          # register cosets U 1 g 4 block stores; inverse: register cosets U 1 g 4
+    (2, 1, 0, -8),          # register cosets U 2 g 1
+    (2, 2, 0, -7),          # register cosets U 2 g 2
+    (2, 3, 0, -6),          # register cosets U 2 g 3
+    (2, 6, 0, -3),          # register cosets U 2 g 3 block stores; inverse: register cosets U 2 g 3
+    (2, 5, 0, -5),          # register cosets U 2 g 3 SB 1
+    (4, 1, 0, -7),          # register cosets U 4 g 1
+    (4, 2, 0, -6),          # register cosets U 4 g 2
+    (4, 6, 0, -2),          # register cosets U 4 g 2 block stores; inverse: register cosets U 4 g 2
+    (4, 4, 0, -4),          # register cosets U 4 g 2 SB 2
+    (8, 1, 0, -6),          # register cosets U 8 g 1
+    (8, 6, 0, -1),          # register cosets U 8 g 1 block stores; inverse: register cosets U 8 g 1
+    (8, 3, 0, -4),          # register cosets U 8 g 1 SB 2
+    (8, 4, 0, -4),          # register cosets U 8 g 1 SB 3
+    (4, 7, 0, -1),          # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
+    (2, 7, 0, -2),          # lane-map cosets g 2 block stores; inverse: lane-map cosets g 2
+    (1, 7, 0, -3),          # lane-map cosets g 3 block stores; inverse: lane-map cosets g 3
 ]
 
 
-# Written field starting inside the lanes (M + |S| < log2 V < M + |S| + B):
-# cosets with a fixed lane map, one set per g and several per element size.
-COSETS_MAP = [
-    # esize, B, M, S          g
-    (1, 2, 0, -3),          # 1
-    (1, 3, 0, -3),          # 2
-    (1, 4, 0, -3),          # 3
-    (1, 9, 0, -3),          # 3, 3 inverse steps
-    (2, 2, 1, -1),          # 1
-    (2, 3, 0, -2),          # 2
-    (2, 12, 0, -1),         # 1, 12 inverse steps
-    (4, 2, 0, -1),          # 1
-    (4, 7, 0, -1),          # 1
-    (2, 4, 0, -2),          # 2, forward with block stores
-    (1, 5, 0, -3),          # 3, forward with block stores
-]
-
-
-@pytest.mark.parametrize("esize,B,M,S", COSETS + COSETS_MAP)
+@pytest.mark.parametrize("esize,B,M,S", COSETS + COSETS_REG)
 def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
     from xor_swizzle_movement_gb300 import inputs
     block = 1 << _wtop(B, M, S)
@@ -174,11 +194,12 @@ def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
         _run(swz, orc, host, n_tiles, 1, tile, esize, B, M, S, direction)
 
 
-@pytest.mark.parametrize("esize,B,M,S", [(1, 3, 0, -4), (2, 2, 0, -3), (4, 2, 0, -2)])
+@pytest.mark.parametrize("esize,B,M,S", [(1, 6, 0, -4), (2, 6, 0, -3), (4, 6, 0, -2), (8, 6, 0, -1), (4, 7, 0, -1)])
 @pytest.mark.parametrize("src_off,dst_off", [(16, 48), (0, 16), (16, 0)])
 def test_relayout_cosets_block_16_byte_aligned(swz, orc, esize, B, M, S, src_off, dst_off):
-    """Cosets that are aligned blocks, on pointers 16- but not 32-byte aligned:
-    the kernel keeps 16-byte accesses."""
+    """Cosets whose destination side is an aligned block (stored with 32-byte
+    accesses on a 32-byte aligned destination), on pointers 16- but not 32-byte
+    aligned: the kernels keep 16-byte stores."""
     from xor_swizzle_movement_gb300 import inputs
     block = 1 << _wtop(B, M, S)
     n_tiles = 1001

@@ -40,7 +40,8 @@
 //     staged kernel (blocks of whole tiles in shared memory, 16-byte output
 //     vectors gathered through a per-CTA table of their sources);
 //   negative shifts whose read field lies below the lane bits (they split
-//     vectors): a fixed lane map, cosets of whole vectors in registers
+//     vectors): a fixed lane map, warp shuffles within blocks of 32 vectors
+//     (relayout_warp_coset_kernel), cosets of whole vectors in registers
 //     (relayout_coset_kernel, relayout_coset_map_kernel), the staged kernel
 //     over closure blocks, or element by element;
 //   pointers aligned to the element size but not to 16 bytes: the vector
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(256) relayout_vec_mis_kernel(const RelayoutArg
 struct CosetArgs {
     uint4 *dst;
     const uint4 *src;
-    int64_t n_cosets;   // 16-byte vectors / 2^g
+    int64_t n_cosets;   // cosets (16-byte vectors / 2^g); with SB > 0, threads (vectors / 2^(g + SB))
     int B, M, S, steps, lv;
     int pivot[4];       // ascending bit positions left zero in a coset's representative
     int sbase;          // SB > 0: first of the g + SB bits a thread's cosets leave to its slots
@@ -272,13 +273,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int q) {
     return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-// 32-byte global access (two 16-byte vectors; the address is 32-byte aligned)
-__device__ __forceinline__ void ld_stream32_hint(const void *p, uint64_t policy, uint4 &a, uint4 &b) {
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
-                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                 : "l"(p), "l"(policy));
-}
-
+// 32-byte global store (two 16-byte vectors; the address is 32-byte aligned)
 __device__ __forceinline__ void st_stream32(void *p, const uint4 &a, const uint4 &b) {
     asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
                  "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
@@ -311,14 +306,13 @@ __device__ __forceinline__ uint32_t coset_word(const uint4 (&v)[1 << G], int j, 
 // each load instruction reads whole sectors; SB stages of conditional swaps
 // (by the bits of tau) then put coset c in slot c, and each store
 // instruction writes whole sectors too.
-// BLK (SB = 0), bit 1: W' is spanned by the lowest g vector bits with w'_i =
-// e_i, so a coset's destination vectors are one aligned block of 2^g vectors,
-// stored with 32-byte accesses (destination 32-byte aligned); bit 0 as well:
-// Gv is the identity (M + |S| = log2 V with disjoint fields), so the sources
-// are the same block, loaded with 32-byte accesses (source 32-byte aligned).
-// A warp instruction then reads or writes whole sectors, where 16-byte
-// accesses at a 2^g-vector stride used half of each.
-template <int U, int G, int SB, int BLK>
+// ST32 (SB = 0): W' is spanned by the lowest g vector bits with w'_i = e_i,
+// so a coset's destination vectors are one aligned block of 2^g vectors,
+// stored with 32-byte accesses (destination 32-byte aligned): a warp
+// instruction then writes whole sectors, where 16-byte stores at a 2^g-vector
+// stride wrote half of each.  (Such cosets whose sources stay in a block of 32
+// vectors go to relayout_warp_coset_kernel instead.)
+template <int U, int G, int SB, bool ST32>
 __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) {
     constexpr int NV = 1 << G;
     constexpr int NC = SB > 0 ? (1 << SB) : (G >= 3) ? 1 : (8 >> G);  // cosets per thread
@@ -371,28 +365,21 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
         for (int c = 0; c < NC; ++c) {
             const int64_t t = base + static_cast<int64_t>(c) * blockDim.x;
             if (t < a.n_cosets) {
-                if constexpr ((BLK & 1) != 0) {
-                    const uint64_t d = static_cast<uint64_t>(t) << G;
-                    d0[c] = d;
+                uint64_t d = static_cast<uint64_t>(t);
 #pragma unroll
-                    for (int k = 0; k < NV; k += 2) ld_stream32_hint(a.src + d + k, pol, v[c][k], v[c][k + 1]);
-                } else {
-                    uint64_t d = static_cast<uint64_t>(t);
+                for (int i = 0; i < G; ++i) {
+                    const int p = a.pivot[i];
+                    d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
+                }
+                d0[c] = d;
+                const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
 #pragma unroll
-                    for (int i = 0; i < G; ++i) {
-                        const int p = a.pivot[i];
-                        d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
-                    }
-                    d0[c] = d;
-                    const uint64_t s0 = sw_inv(d << a.lv, a.B, a.M, a.S, a.steps) >> a.lv;
+                for (int k = 0; k < NV; ++k) {
+                    uint64_t x = s0;
 #pragma unroll
-                    for (int k = 0; k < NV; ++k) {
-                        uint64_t x = s0;
-#pragma unroll
-                        for (int i = 0; i < G; ++i)
-                            if ((k >> i) & 1) x ^= a.w[i];
-                        v[c][k] = ld_stream16_hint(a.src + x, pol);
-                    }
+                    for (int i = 0; i < G; ++i)
+                        if ((k >> i) & 1) x ^= a.w[i];
+                    v[c][k] = ld_stream16_hint(a.src + x, pol);
                 }
             }
         }
@@ -401,7 +388,7 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         if (SB == 0 && base + static_cast<int64_t>(c) * blockDim.x >= a.n_cosets) continue;
-        if constexpr ((BLK & 2) != 0) {
+        if constexpr (ST32) {
 #pragma unroll
             for (int j = 0; j < NV; j += 2) {
                 uint4 o0, o1;
@@ -433,6 +420,78 @@ __global__ void __launch_bounds__(256) relayout_coset_kernel(const CosetArgs a) 
     }
 }
 
+// Negative shifts that split vectors, where the gather map G keeps every
+// destination vector's sources inside its own aligned block of 32 vectors:
+// Gv preserves the block index on every vector bit, and the offset
+// off(t) = Gv(unit t's first lane) of every unit of U = esize * 2^M bytes is
+// below 32.  The source of unit t of destination vector u is then unit t of
+// vector Gv(u) ^ off(t) after the fixed lane permutation Lam (the lane part of
+// G; the identity when the written field lies at or above the lanes).  A warp
+// loads its 32 destination positions' own vectors (one coalesced 512-byte load,
+// as the plain relayout), permutes each by Lam when needed, and builds every
+// output word from shuffles across the warp: lane Gv(u) ^ off(t) mod 32.
+// Every global access is a whole 512-byte warp access, where the register
+// coset kernels read a coset at a 2^p0-vector stride.  Lanes past the buffer's
+// end take part in the shuffles without touching memory; no lane inside the
+// buffer reads theirs (a source lies in its destination's closure block).
+struct WarpCosetArgs {
+    uint4 *dst;
+    const uint4 *src;
+    int64_t nvec;
+    int B, M, S, steps, lv;
+    int per_thread;
+    uint32_t off[16];       // per unit: the source's vector offset, XOR-ed onto Gv(u) (below 32)
+    uint32_t perm_sel[12];  // MAP: byte-permutation selectors of Lam (3 per word)
+};
+
+template <int U>
+__device__ __forceinline__ uint32_t warp_coset_word(const uint4 &v, int q, uint32_t gl, const uint32_t *off) {
+    const uint32_t w = word_of(v, q);
+    auto from = [&](int t) -> uint32_t { return __shfl_sync(kFullMask, w, static_cast<int>(gl ^ off[t])); };
+    if constexpr (U >= 4) {
+        return from((4 * q) / U);
+    } else if constexpr (U == 2) {
+        return __byte_perm(from(2 * q), from(2 * q + 1), 0x7610);
+    } else {
+        const uint32_t ab = __byte_perm(from(4 * q), from(4 * q + 1), 0x3250);
+        const uint32_t cd = __byte_perm(from(4 * q + 2), from(4 * q + 3), 0x7210);
+        return __byte_perm(ab, cd, 0x7610);
+    }
+}
+
+template <int U, bool MAP>
+__global__ void __launch_bounds__(256) relayout_warp_coset_kernel(const WarpCosetArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();  // before any global memory access
+    const uint64_t pol = l2_evict_first_policy();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
+    // Gv(u) mod 32: a negative shift writes each read bit higher up, so the
+    // bits of u from 5 up never reach the low 5 bits of Gv(u), and u mod 32 is
+    // the lane (warps start on multiples of 32 vectors): one value per thread
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t gl =
+        static_cast<uint32_t>(sw_inv(static_cast<uint64_t>(lane) << a.lv, a.B, a.M, a.S, a.steps) >> a.lv) & 31u;
+    uint4 v[kMaxPerThread];
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < a.per_thread && u < a.nvec) v[k] = ld_stream16_hint(a.src + u, pol);
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        if (k >= a.per_thread) break;  // uniform: every lane of the warp shuffles
+        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        if constexpr (MAP) v[k] = bytes_permute(v[k], a.perm_sel);
+        uint4 o;
+        o.x = warp_coset_word<U>(v[k], 0, gl, a.off);
+        o.y = warp_coset_word<U>(v[k], 1, gl, a.off);
+        o.z = warp_coset_word<U>(v[k], 2, gl, a.off);
+        o.w = warp_coset_word<U>(v[k], 3, gl, a.off);
+        if (u < a.nvec) st_stream16(a.dst + u, o);
+    }
+}
+
 // Negative shifts whose written field starts inside the lanes (M + |S| <
 // log2 V < M + |S| + B).  The lane bits of G(y) still depend only on the lane
 // bits of y, so G(dV) has no lane part and lane l of destination vector d
@@ -448,11 +507,10 @@ struct CosetMapArgs {
     uint32_t mask[8][4];    // byte masks of the lanes with phi == m (m < 2^g)
 };
 
-// BLK as for relayout_coset_kernel: bit 1, 32-byte stores of the aligned
+// ST32 as for relayout_coset_kernel: 32-byte stores of the aligned
 // destination block (the host picks the basis w'_i = e_i when W' is spanned by
-// the lowest g vector bits); bit 0, 32-byte loads of the same block when Gv is
-// the identity.
-template <int G, int BLK>
+// the lowest g vector bits).
+template <int G, bool ST32>
 __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapArgs a) {
     constexpr int NV = 1 << G;
     constexpr int NC = (G >= 3) ? 1 : (8 >> G);  // cosets per thread: 8 vectors in flight
@@ -475,19 +533,14 @@ __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapA
                 d = ((d >> p) << (p + 1)) | (d & ((1ull << p) - 1ull));
             }
             d0[q] = d;
-            if constexpr ((BLK & 1) != 0) {
+            const uint64_t s0 = sw_inv(d << c.lv, c.B, c.M, c.S, c.steps) >> c.lv;
 #pragma unroll
-                for (int k = 0; k < NV; k += 2) ld_stream32_hint(c.src + d + k, pol, v[q][k], v[q][k + 1]);
-            } else {
-                const uint64_t s0 = sw_inv(d << c.lv, c.B, c.M, c.S, c.steps) >> c.lv;
+            for (int k = 0; k < NV; ++k) {
+                uint64_t x = s0;
 #pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    uint64_t x = s0;
-#pragma unroll
-                    for (int i = 0; i < G; ++i)
-                        if ((k >> i) & 1) x ^= c.w[i];
-                    v[q][k] = ld_stream16_hint(c.src + x, pol);
-                }
+                for (int i = 0; i < G; ++i)
+                    if ((k >> i) & 1) x ^= c.w[i];
+                v[q][k] = ld_stream16_hint(c.src + x, pol);
             }
         }
     }
@@ -510,7 +563,7 @@ __global__ void __launch_bounds__(256) relayout_coset_map_kernel(const CosetMapA
                 o[j].w |= x.w & a.mask[m][3];
             }
         }
-        if constexpr ((BLK & 2) != 0) {
+        if constexpr (ST32) {
 #pragma unroll
             for (int j = 0; j < NV; j += 2) st_stream32(c.dst + d0[q] + j, o[j], o[j + 1]);
         } else {
@@ -880,6 +933,59 @@ swz_status launch_staged_tiles(void *dst, const void *src, int64_t n_elems, int6
 #undef SWZ_STAGED
 }
 
+// relayout_warp_coset_kernel for a negative shift whose map keeps each
+// destination vector's sources inside its aligned block of 32 vectors;
+// SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.
+swz_status launch_warp_coset(void *dst, const void *src, int64_t n_elems, int esize, int B, int M, int S, int steps,
+                             cudaStream_t st) {
+    int lv = 0;
+    while ((1 << lv) < 16 / esize) ++lv;
+    if (B <= 0 || S >= 0 || M >= lv || sw_write_hi(B, M, S) <= lv) return SWZ_ERR_UNSUPPORTED;
+    const uint64_t V = 1ull << lv;
+    // Gv keeps the block of 32 vectors of every vector bit of a closure block
+    for (int b = 0; b < sw_write_hi(B, M, S) - lv; ++b) {
+        const uint64_t y = sw_inv((1ull << b) << lv, B, M, S, steps);
+        if ((y & (V - 1)) != 0 || ((y >> lv) >> 5) != ((1ull << b) >> 5)) return SWZ_ERR_UNSUPPORTED;
+    }
+    WarpCosetArgs a{};
+    a.dst = static_cast<uint4 *>(dst);
+    a.src = static_cast<const uint4 *>(src);
+    a.nvec = n_elems * esize / 16;
+    a.B = B; a.M = M; a.S = S;
+    a.steps = steps;
+    a.lv = lv;
+    const int U = esize << M;
+    for (int t = 0; t < 16 / U; ++t) {
+        const uint64_t y = sw_inv(static_cast<uint64_t>(t) * (U / esize), B, M, S, steps);
+        a.off[t] = static_cast<uint32_t>(y >> lv);
+        if ((y >> lv) >= 32) return SWZ_ERR_UNSUPPORTED;
+    }
+    int src_lane[16];
+    bool map = false;
+    for (int l = 0; l < static_cast<int>(V); ++l) {
+        src_lane[l] = static_cast<int>(sw_inv(static_cast<uint64_t>(l), B, M, S, steps) & (V - 1));
+        map = map || src_lane[l] != l;
+    }
+    lane_map_selectors(src_lane, esize, a.perm_sel);
+    const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
+    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+    const int64_t per_cta = int64_t(256) * a.per_thread;
+    const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
+    if (grid == 0) return SWZ_OK;
+    const dim3 gr(static_cast<unsigned>(grid));
+#define SWZ_W(UU) (map ? launch_pdl(relayout_warp_coset_kernel<UU, true>, gr, dim3(256), 0, st, a) \
+                       : launch_pdl(relayout_warp_coset_kernel<UU, false>, gr, dim3(256), 0, st, a))
+    switch (U) {
+        case 1: return launched(SWZ_W(1));
+        case 2: return launched(SWZ_W(2));
+        case 4: return launched(SWZ_W(4));
+        // U = 8 puts the written field at or above the lanes: no lane map
+        default: return launched(launch_pdl(relayout_warp_coset_kernel<8, false>, gr, dim3(256), 0, st, a));
+    }
+#undef SWZ_W
+}
+
 // relayout_coset_kernel for a negative shift with M < log2 V <= M + |S|;
 // SWZ_ERR_UNSUPPORTED (nothing launched) otherwise.  The bases of W and W'
 // and the pivots of W' are computed here, once per launch.
@@ -926,37 +1032,31 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
         a.sbase = -S - g;
         a.n_cosets = nvec >> (g + sbits);  // threads
     }
-    // BLK: Gv the identity on every vector bit of a closure block, w_i = e_i,
-    // both pointers 32-byte aligned
-    // (block stores: w'_i = e_i, destination 32-byte aligned; block loads as well:
-    // Gv the identity on every vector bit of a closure block, source aligned too)
-    bool st32 = sbits == 0 && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
+    // block stores: w'_i = e_i, destination 32-byte aligned (instantiated where
+    // such cosets occur outside the warp kernel's reach: U * 2^g = 16)
+    bool st32 = sbits == 0 && (U << g) == 16 && (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
     for (int i = 0; st32 && i < g; ++i) st32 = a.wd[i] == (1ull << i);
-    bool ld32 = st32 && (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
-    for (int b = 0; ld32 && b < sw_write_hi(B, M, S) - lv; ++b)
-        ld32 = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
-    const int blk = (st32 ? 2 : 0) | (ld32 ? 1 : 0);
     const int nc = sbits > 0 ? 1 : (g >= 3) ? 1 : (8 >> g);
     const int64_t per_cta = int64_t(256) * nc;
     const int64_t grid = (a.n_cosets + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_C(UU, GG, SS)                                                                              \
-    launched(blk == 3   ? launch_pdl(relayout_coset_kernel<UU, GG, 0, 3>, gr, dim3(256), 0, st, a)        \
-             : blk == 2 ? launch_pdl(relayout_coset_kernel<UU, GG, 0, 2>, gr, dim3(256), 0, st, a)        \
-                        : launch_pdl(relayout_coset_kernel<UU, GG, SS, 0>, gr, dim3(256), 0, st, a))
+#define SWZ_C(UU, GG, SS) launched(launch_pdl(relayout_coset_kernel<UU, GG, SS, false>, gr, dim3(256), 0, st, a))
+#define SWZ_C32(UU, GG)                                                                                 \
+    launched(st32 ? launch_pdl(relayout_coset_kernel<UU, GG, 0, true>, gr, dim3(256), 0, st, a)          \
+                  : launch_pdl(relayout_coset_kernel<UU, GG, 0, false>, gr, dim3(256), 0, st, a))
     switch ((U * 8 + g) * 4 + sbits) {
         case (1 * 8 + 1) * 4: return SWZ_C(1, 1, 0);
         case (1 * 8 + 2) * 4: return SWZ_C(1, 2, 0);
         case (1 * 8 + 3) * 4: return SWZ_C(1, 3, 0);
-        case (1 * 8 + 4) * 4: return SWZ_C(1, 4, 0);
+        case (1 * 8 + 4) * 4: return SWZ_C32(1, 4);
         case (2 * 8 + 1) * 4: return SWZ_C(2, 1, 0);
         case (2 * 8 + 2) * 4: return SWZ_C(2, 2, 0);
-        case (2 * 8 + 3) * 4: return SWZ_C(2, 3, 0);
+        case (2 * 8 + 3) * 4: return SWZ_C32(2, 3);
         case (4 * 8 + 1) * 4: return SWZ_C(4, 1, 0);
-        case (4 * 8 + 2) * 4: return SWZ_C(4, 2, 0);
-        case (8 * 8 + 1) * 4: return SWZ_C(8, 1, 0);
+        case (4 * 8 + 2) * 4: return SWZ_C32(4, 2);
+        case (8 * 8 + 1) * 4: return SWZ_C32(8, 1);
         // (r >= 2 means g = log2 V - M, so U = 16 >> g)
         case (8 * 8 + 1) * 4 + 2: return SWZ_C(8, 1, 2);
         case (8 * 8 + 1) * 4 + 3: return SWZ_C(8, 1, 3);
@@ -964,6 +1064,7 @@ swz_status launch_coset(void *dst, const void *src, int64_t n_elems, int esize, 
         case (2 * 8 + 3) * 4 + 1: return SWZ_C(2, 3, 1);
         default: return SWZ_ERR_UNSUPPORTED;
     }
+#undef SWZ_C32
 #undef SWZ_C
 }
 
@@ -1036,7 +1137,7 @@ swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esi
         r[i] = c.wd[i];
         wd_low = wd_low && c.wd[i] < (1ull << g);
     }
-    int blk = 0;
+    bool st32 = false;
     if (wd_low) {
         // change of basis: w'_i = e_i, w_i = Gv(e_i); phi again, as coordinates
         // of each lane bit's vector image in the new w basis
@@ -1080,10 +1181,7 @@ swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esi
             for (int w = 0; w < 4; ++w) a.mask[m][w] = 0;
         for (int byte = 0; byte < 16; ++byte)
             a.mask[phi[byte / esize]][byte >> 2] |= 0xffu << ((byte & 3) * 8);
-        bool ld32 = (reinterpret_cast<uintptr_t>(src) & 31u) == 0;
-        for (int b = 0; ld32 && b < sw_write_hi(B, M, S) - lv; ++b)
-            ld32 = sw_inv((1ull << b) << lv, B, M, S, steps) == ((1ull << b) << lv);
-        if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) blk = ld32 ? 3 : 2;
+        st32 = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;
     }
     for (int i = 0; i < g; ++i) {
         for (int k = 0; k < i; ++k)
@@ -1104,10 +1202,9 @@ swz_status launch_coset_map(void *dst, const void *src, int64_t n_elems, int esi
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_M(GG)                                                                                   \
-    launched(blk == 3   ? launch_pdl(relayout_coset_map_kernel<GG, 3>, gr, dim3(256), 0, st, a)      \
-             : blk == 2 ? launch_pdl(relayout_coset_map_kernel<GG, 2>, gr, dim3(256), 0, st, a)      \
-                        : launch_pdl(relayout_coset_map_kernel<GG, 0>, gr, dim3(256), 0, st, a))
+#define SWZ_M(GG)                                                                              \
+    launched(st32 ? launch_pdl(relayout_coset_map_kernel<GG, true>, gr, dim3(256), 0, st, a)      \
+                  : launch_pdl(relayout_coset_map_kernel<GG, false>, gr, dim3(256), 0, st, a))
     switch (g) {
         case 1: return SWZ_M(1);
         case 2: return SWZ_M(2);
@@ -1160,13 +1257,16 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         // swizzle in aligned blocks of 2^wtop elements (tiles are multiples
         // of such blocks).  Blocks inside one vector: a fixed lane map.
         // Otherwise the lanes of one destination vector come from several
-        // source vectors, and they are gathered by cosets of whole vectors in
-        // registers (with a fixed lane map when the written field starts
-        // inside the lanes); what neither covers goes through blocks of up to
-        // the staging size in shared memory, else element by element.
+        // source vectors.  When they stay inside the destination's block of
+        // 32 vectors, warp shuffles gather them; otherwise cosets of whole
+        // vectors in registers (with a fixed lane map when the written field
+        // starts inside the lanes); what none covers goes through blocks of up
+        // to the staging size in shared memory, else element by element.
         const int wtop = sw_write_hi(B, M, S);
         if (wtop <= lv)
             return launch_lane_map(dst, src, n_elems, esize, 1 << wtop, B, M, S, steps, link_grid, st);
+        const swz_status sw = launch_warp_coset(dst, src, n_elems, esize, B, M, S, steps, st);
+        if (sw != SWZ_ERR_UNSUPPORTED) return sw;
         const swz_status sc = launch_coset(dst, src, n_elems, esize, B, M, S, steps, st);
         if (sc != SWZ_ERR_UNSUPPORTED) return sc;
         const swz_status sm = launch_coset_map(dst, src, n_elems, esize, B, M, S, steps, st);
