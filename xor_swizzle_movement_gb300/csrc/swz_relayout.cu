@@ -36,6 +36,9 @@
 // Other requests (relayout_launch picks the path):
 //   tiles of 1-8 bytes that divide 16: every vector holds whole tiles, so the
 //     same kernel runs with the identity at vector level and one fixed lane map;
+//   tiles that are not whole 16-byte vectors but hold whole swizzle periods,
+//     on a buffer of whole vectors and aligned pointers: one tile (the swizzle
+//     is the same on whole-buffer offsets);
 //   other tiles that are not whole 16-byte vectors, aligned pointers: the
 //     staged kernel (blocks of whole tiles in shared memory, 16-byte output
 //     vectors gathered through a per-CTA table of their sources);
