@@ -249,3 +249,54 @@ def test_slice_collision_batch_negative_shift(swz, orc):
         got = C.cpu().numpy().view(np.uint64)
         want = np.array([orc.slice_collision(int(a), B=B, M=M, S=S) for a in A], dtype=np.uint64)
         assert np.array_equal(got, want)
+
+
+NEG_SWEEP = [(esize, B, M, -s) for esize, lv in ((2, 3), (1, 4)) for B in range(1, 6) for M in range(lv)
+             for s in range(1, 6)]
+
+
+@pytest.fixture(scope="module")
+def gib_bytes():
+    """1 GiB of random bytes (seed 4), on the GPU: the bench's negative-shift sweep buffer."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    return torch.randint(0, 256, (1 << 30,), dtype=torch.uint8, device="cuda", generator=g)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("esize,B,M,S", NEG_SWEEP)
+def test_negative_sweep_1gib_every_position(swz, orc, gib_bytes, esize, B, M, S):
+    """Every negative set the bench's sweep times (uint16 and int8, B 1..5, M
+    below log2 V, S -1..-5), on its 1 GiB buffer as one tile and in its launch
+    configuration, compared at every position in both directions.  The map
+    reads and writes only offset bits below M + |S| + B <= 13, so the oracle's
+    map of the first 2^16 offsets, repeated on every 2^16-element block, is the
+    whole map; torch index operations apply it.  The oracle's map at 2^14
+    random global offsets checks the repetition, and forward then inverse must
+    give the input back."""
+    period = 1 << 16
+    n = (1 << 30) // esize
+    dt = torch.int16 if esize == 2 else torch.uint8
+    src = gib_bytes
+    fwd, back = torch.empty_like(src), torch.empty_like(src)
+    swz.swz_relayout(fwd, src, 1, 1, n, esize, B, M, S, 0)
+    swz.swz_relayout(back, fwd, 1, 1, n, esize, B, M, S, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    perm = orc.relayout_positions(np.arange(period, dtype=np.int64), tile_elems=n, B=B, M=M, S=S)
+    assert np.array_equal(np.sort(perm), np.arange(period))
+    tp = torch.from_numpy(perm).cuda()
+    s2 = src.view(dt).view(-1, period)
+    want_fwd = torch.empty_like(s2).index_copy_(1, tp, s2)       # dst[sw(i)] = src[i]
+    assert torch.equal(fwd.view(dt).view(-1, period), want_fwd)
+    del want_fwd
+    inv = torch.empty_like(src)
+    swz.swz_relayout(inv, src, 1, 1, n, esize, B, M, S, 1)
+    want_inv = s2.index_select(1, tp)                              # dst[i] = src[sw(i)]
+    assert torch.equal(inv.view(dt).view(-1, period), want_inv)
+    del want_inv, inv
+    rng = np.random.default_rng(esize * 1000 + B * 100 + M * 10 - S)
+    idx = np.sort(rng.choice(n, 1 << 14, replace=False)).astype(np.int64)
+    pos = orc.relayout_positions(idx, tile_elems=n, B=B, M=M, S=S)
+    ti = torch.from_numpy(idx).cuda()
+    assert torch.equal(fwd.view(dt)[torch.from_numpy(pos).cuda()], src.view(dt)[ti])
