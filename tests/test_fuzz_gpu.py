@@ -97,6 +97,39 @@ def test_relayout_fuzz_16_byte_offsets(swz, orc, block):
         assert got.tobytes() == want.tobytes(), (esize, n_tiles, rows, cols, B, M, S, direction, so, do)
 
 
+@pytest.mark.parametrize("block", range(3))
+def test_relayout_fuzz_wide_parameters(swz, orc, block):
+    """Wider swizzles than the sweep's ranges (B up to 8, M up to 5, |S| up to
+    12, mostly negative): closure blocks up to 2^17 elements, where the
+    negative shifts reach the register coset kernels' slot and block-store
+    forms, lane maps with larger g, and the warp kernel's bigger blocks."""
+    from xor_swizzle_movement_gb300 import inputs
+    rng = np.random.default_rng(9000 + block)
+    for case in range(30):
+        esize = int(rng.choice([1, 2, 4, 8]))
+        lv = {1: 4, 2: 3, 4: 2, 8: 1}[esize]
+        B = int(rng.integers(1, 9))
+        M = int(rng.integers(0, lv + 1))              # mostly below log2 V: vectors split
+        S = int(rng.integers(1, 4) if rng.random() < 0.5 else rng.integers(1, 13))
+        S = -S if rng.random() < 0.75 else S
+        hi = (M - S + B) if S < 0 else (M + B)       # tiles close under sw in blocks of 2^hi
+        if hi > 17:
+            continue
+        tile = (1 << hi) * int(rng.integers(1, 4))
+        n_tiles = max(1, min(64, (4 << 20) // (tile * esize)))
+        direction = int(rng.integers(0, 2))
+        so, do = (int(x) for x in rng.choice([0, 16, 32], size=2))
+        host = inputs.random_bytes(n_tiles * tile * esize, seed=9500 + block * 100 + case).view(void_dtype(esize))
+        _, src = to_device(host, so)
+        full, dst = empty_device(host.nbytes, do)
+        swz.swz_relayout(dst, src, n_tiles, 1, tile, esize, B, M, S, direction)
+        torch.cuda.synchronize()
+        assert guards_intact(full, do, host.nbytes)
+        got = to_host(dst, host.dtype)
+        want = orc.relayout(host, tile_elems=tile, B=B, M=M, S=S, direction=direction)
+        assert got.tobytes() == want.tobytes(), (esize, n_tiles, tile, B, M, S, direction, so, do)
+
+
 def test_relayout_tma_modes_fuzz(swz, orc):
     """Requests inside the TMA's hardware modes (Sw<B, 4 - log2 e, 3>, tiles of
     whole 2^(B+7)-byte periods) with random tile and buffer sizes."""
