@@ -123,7 +123,7 @@ COSETS = [
     (2, 6, 0, -5),          # register cosets U 2 g 3
     (2, 3, 2, -3),          # warp shuffles
     (1, 4, 3, -4),          # register cosets U 8 g 1 SB 3
-    (2, 4, 1, -4),          # register cosets U 4 g 2 SB 2
+    (2, 4, 1, -4),          # warp shuffles, 64-vector blocks
     (1, 4, 2, -5),          # register cosets U 4 g 2 SB 2
     (2, 5, 0, -5),          # register cosets U 2 g 3 SB 1
     (1, 5, 1, -6),          # register cosets U 2 g 3 SB 1
@@ -149,36 +149,45 @@ COSETS = [
     (2, 3, 0, -2),          # warp shuffles after a lane map
     (2, 12, 0, -1),         # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
     (4, 2, 0, -1),          # warp shuffles after a lane map
-    (4, 7, 0, -1),          # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
+    (4, 7, 0, -1),          # warp shuffles, 64-vector blocks after a lane map
     (2, 4, 0, -2),          # warp shuffles after a lane map
     (1, 5, 0, -3),          # warp shuffles after a lane map
+    (1, 5, 0, -5),          # register cosets U 1 g 4
+    (2, 5, 0, -4),          # warp shuffles, 64-vector blocks
+    (1, 5, 1, -4),          # warp shuffles, 64-vector blocks
+    (1, 1, 0, -9),          # register cosets U 1 g 1
+    (1, 7, 0, -3),          # lane-map cosets g 3 block stores; inverse: lane-map cosets g 3
+    (2, 1, 0, -8),          # warp shuffles, 64-vector blocks
+    (2, 7, 0, -2),          # warp shuffles, 64-vector blocks after a lane map
+    (4, 1, 0, -7),          # warp shuffles, 64-vector blocks
+    (8, 1, 0, -6),          # warp shuffles, 64-vector blocks
 ]
 
 # Sets that stay on the register coset kernels (their sources leave the
-# destination's block of 32 vectors): one per instantiation.
+# destination's block of 64 vectors): one per instantiation.
 COSETS_REG = [
     # esize, B, M, S
-    (1, 1, 0, -9),          # register cosets U 1 g 1
-    (1, 2, 0, -8),          # register cosets U 1 g 2
-    (1, 3, 0, -7),          # register cosets U 1 g 3
-    (1, 4, 0, -6),          # register cosets U 1 g 4
-    (1, 6, 0, -4),          # register cosets U 1 g 4 block stores; inverse: register cosets U 1 g 4
-    (2, 1, 0, -8),          # register cosets U 2 g 1
-    (2, 2, 0, -7),          # register cosets U 2 g 2
-    (2, 3, 0, -6),          # register cosets U 2 g 3
-    (2, 6, 0, -3),          # register cosets U 2 g 3 block stores; inverse: register cosets U 2 g 3
+    (1, 1, 0, -10),         # register cosets U 1 g 1
+    (1, 2, 0, -9),          # register cosets U 1 g 2
+    (1, 3, 0, -8),          # register cosets U 1 g 3
+    (1, 4, 0, -7),          # register cosets U 1 g 4
+    (1, 7, 0, -4),          # register cosets U 1 g 4 block stores; inverse: register cosets U 1 g 4
+    (2, 1, 0, -9),          # register cosets U 2 g 1
+    (2, 2, 0, -8),          # register cosets U 2 g 2
+    (2, 3, 0, -7),          # register cosets U 2 g 3
+    (2, 7, 0, -3),          # register cosets U 2 g 3 block stores; inverse: register cosets U 2 g 3
     (2, 5, 0, -5),          # register cosets U 2 g 3 SB 1
-    (4, 1, 0, -7),          # register cosets U 4 g 1
-    (4, 2, 0, -6),          # register cosets U 4 g 2
-    (4, 6, 0, -2),          # register cosets U 4 g 2 block stores; inverse: register cosets U 4 g 2
-    (4, 4, 0, -4),          # register cosets U 4 g 2 SB 2
-    (8, 1, 0, -6),          # register cosets U 8 g 1
-    (8, 6, 0, -1),          # register cosets U 8 g 1 block stores; inverse: register cosets U 8 g 1
-    (8, 3, 0, -4),          # register cosets U 8 g 1 SB 2
+    (4, 1, 0, -8),          # register cosets U 4 g 1
+    (4, 2, 0, -7),          # register cosets U 4 g 2
+    (4, 7, 0, -2),          # register cosets U 4 g 2 block stores; inverse: register cosets U 4 g 2
+    (4, 4, 0, -5),          # register cosets U 4 g 2 SB 2
+    (8, 1, 0, -7),          # register cosets U 8 g 1
+    (8, 7, 0, -1),          # register cosets U 8 g 1 block stores; inverse: register cosets U 8 g 1
+    (8, 3, 0, -5),          # register cosets U 8 g 1 SB 2
     (8, 4, 0, -4),          # register cosets U 8 g 1 SB 3
-    (4, 7, 0, -1),          # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
-    (2, 7, 0, -2),          # lane-map cosets g 2 block stores; inverse: lane-map cosets g 2
-    (1, 7, 0, -3),          # lane-map cosets g 3 block stores; inverse: lane-map cosets g 3
+    (4, 8, 0, -1),          # lane-map cosets g 1 block stores; inverse: lane-map cosets g 1
+    (2, 8, 0, -2),          # lane-map cosets g 2 block stores; inverse: lane-map cosets g 2
+    (1, 8, 0, -3),          # lane-map cosets g 3 block stores; inverse: lane-map cosets g 3
 ]
 
 
@@ -194,7 +203,7 @@ def test_relayout_cosets_ragged_grid(swz, orc, esize, B, M, S):
         _run(swz, orc, host, n_tiles, 1, tile, esize, B, M, S, direction)
 
 
-@pytest.mark.parametrize("esize,B,M,S", [(1, 6, 0, -4), (2, 6, 0, -3), (4, 6, 0, -2), (8, 6, 0, -1), (4, 7, 0, -1)])
+@pytest.mark.parametrize("esize,B,M,S", [(1, 7, 0, -4), (2, 7, 0, -3), (4, 7, 0, -2), (8, 7, 0, -1), (4, 8, 0, -1)])
 @pytest.mark.parametrize("src_off,dst_off", [(16, 48), (0, 16), (16, 0)])
 def test_relayout_cosets_block_16_byte_aligned(swz, orc, esize, B, M, S, src_off, dst_off):
     """Cosets whose destination side is an aligned block (stored with 32-byte

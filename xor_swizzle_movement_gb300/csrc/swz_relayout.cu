@@ -447,10 +447,25 @@ struct WarpCosetArgs {
     uint32_t perm_sel[12];  // MAP: byte-permutation selectors of Lam (3 per word)
 };
 
-template <int U>
-__device__ __forceinline__ uint32_t warp_coset_word(const uint4 &v, int q, uint32_t gl, const uint32_t *off) {
-    const uint32_t w = word_of(v, q);
-    auto from = [&](int t) -> uint32_t { return __shfl_sync(kFullMask, w, static_cast<int>(gl ^ off[t])); };
+// Word q of an output vector from the warp's vectors: NB = 1, the block is
+// the warp's 32 vectors (one register, v0); NB = 2, a block of 64 vectors,
+// the lane's vectors in its two halves in v0 and v1 (two shuffles, then a
+// select by bit 5 of the source position).
+template <int U, int NB>
+__device__ __forceinline__ uint32_t warp_coset_word(const uint4 &v0, const uint4 &v1, int q, uint32_t gl,
+                                                    const uint32_t *off) {
+    const uint32_t w0 = word_of(v0, q);
+    const uint32_t w1 = NB == 2 ? word_of(v1, q) : 0u;
+    auto from = [&](int t) -> uint32_t {
+        const uint32_t x = gl ^ off[t];
+        const uint32_t a0 = __shfl_sync(kFullMask, w0, static_cast<int>(x & 31u));
+        if constexpr (NB == 1) {
+            return a0;
+        } else {
+            const uint32_t a1 = __shfl_sync(kFullMask, w1, static_cast<int>(x & 31u));
+            return (x & 32u) ? a1 : a0;
+        }
+    };
     if constexpr (U >= 4) {
         return from((4 * q) / U);
     } else if constexpr (U == 2) {
@@ -462,35 +477,58 @@ __device__ __forceinline__ uint32_t warp_coset_word(const uint4 &v, int q, uint3
     }
 }
 
-template <int U, bool MAP>
+template <int U, bool MAP, int NB>
 __global__ void __launch_bounds__(256) relayout_warp_coset_kernel(const WarpCosetArgs a) {
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     const uint64_t pol = l2_evict_first_policy();
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x;
-    // Gv(u) mod 32: a negative shift writes each read bit higher up, so the
-    // bits of u from 5 up never reach the low 5 bits of Gv(u), and u mod 32 is
-    // the lane (warps start on multiples of 32 vectors): one value per thread
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t gl =
-        static_cast<uint32_t>(sw_inv(static_cast<uint64_t>(lane) << a.lv, a.B, a.M, a.S, a.steps) >> a.lv) & 31u;
+    // Gv(u) mod 32 NB: a negative shift writes each read bit higher up, so the
+    // bits of u above the block never reach Gv(u)'s position in the block, and
+    // u's position in the block is the lane (plus 32 in a block's second half):
+    // one value per half, per thread
+    uint32_t gl[NB];
+#pragma unroll
+    for (int h = 0; h < NB; ++h)
+        gl[h] = static_cast<uint32_t>(sw_inv(static_cast<uint64_t>(h * 32 + lane) << a.lv, a.B, a.M, a.S, a.steps) >>
+                                      a.lv) &
+                (32u * NB - 1u);
+    // vector k of the thread: NB = 1, a stride of the CTA; NB = 2, the halves of
+    // the warp's k / 2-th block of 64 (every load instruction covers 32
+    // consecutive vectors either way)
+    auto vec_index = [&](int k) -> int64_t {
+        if constexpr (NB == 1) {
+            return static_cast<int64_t>(blockIdx.x) * blockDim.x * a.per_thread + threadIdx.x +
+                   static_cast<int64_t>(k) * blockDim.x;
+        } else {
+            const int64_t warp = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+            return (warp * (a.per_thread >> 1) + (k >> 1)) * 64 + (k & 1) * 32 + lane;
+        }
+    };
     uint4 v[kMaxPerThread];
 #pragma unroll
     for (int k = 0; k < kMaxPerThread; ++k) {
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
+        const int64_t u = vec_index(k);
         v[k] = make_uint4(0u, 0u, 0u, 0u);
         if (k < a.per_thread && u < a.nvec) v[k] = ld_stream16_hint(a.src + u, pol);
     }
 #pragma unroll
     for (int k = 0; k < kMaxPerThread; ++k) {
         if (k >= a.per_thread) break;  // uniform: every lane of the warp shuffles
-        const int64_t u = base + static_cast<int64_t>(k) * blockDim.x;
         if constexpr (MAP) v[k] = bytes_permute(v[k], a.perm_sel);
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+        if (k >= a.per_thread) break;
+        const int64_t u = vec_index(k);
+        const uint4 &v0 = NB == 1 ? v[k] : v[k & ~1];
+        const uint4 &v1 = NB == 1 ? v[k] : v[k | 1];
+        const uint32_t g = gl[NB == 1 ? 0 : (k & 1)];
         uint4 o;
-        o.x = warp_coset_word<U>(v[k], 0, gl, a.off);
-        o.y = warp_coset_word<U>(v[k], 1, gl, a.off);
-        o.z = warp_coset_word<U>(v[k], 2, gl, a.off);
-        o.w = warp_coset_word<U>(v[k], 3, gl, a.off);
+        o.x = warp_coset_word<U, NB>(v0, v1, 0, g, a.off);
+        o.y = warp_coset_word<U, NB>(v0, v1, 1, g, a.off);
+        o.z = warp_coset_word<U, NB>(v0, v1, 2, g, a.off);
+        o.w = warp_coset_word<U, NB>(v0, v1, 3, g, a.off);
         if (u < a.nvec) st_stream16(a.dst + u, o);
     }
 }
@@ -945,11 +983,26 @@ swz_status launch_warp_coset(void *dst, const void *src, int64_t n_elems, int es
     while ((1 << lv) < 16 / esize) ++lv;
     if (B <= 0 || S >= 0 || M >= lv || sw_write_hi(B, M, S) <= lv) return SWZ_ERR_UNSUPPORTED;
     const uint64_t V = 1ull << lv;
-    // Gv keeps the block of 32 vectors of every vector bit of a closure block
-    for (int b = 0; b < sw_write_hi(B, M, S) - lv; ++b) {
-        const uint64_t y = sw_inv((1ull << b) << lv, B, M, S, steps);
-        if ((y & (V - 1)) != 0 || ((y >> lv) >> 5) != ((1ull << b) >> 5)) return SWZ_ERR_UNSUPPORTED;
+    // the smallest block (32 or 64 vectors) that Gv keeps for every vector bit
+    // of a closure block, and that holds every unit's offset
+    int nb = 0;
+    // (64-vector blocks take two shuffles per unit: for 1-byte units, 32 per
+    // vector, which ran at 0.67 of the copy bandwidth where the register
+    // kernel reaches 0.92, so those stay there)
+    const int max_nb = (esize << M) == 1 ? 1 : 2;
+    for (int cand = 1; cand <= max_nb && nb == 0; ++cand) {
+        const int shift = cand == 1 ? 5 : 6;
+        bool ok = true;
+        for (int b = 0; ok && b < sw_write_hi(B, M, S) - lv; ++b) {
+            const uint64_t y = sw_inv((1ull << b) << lv, B, M, S, steps);
+            ok = (y & (V - 1)) == 0 && ((y >> lv) >> shift) == ((1ull << b) >> shift);
+        }
+        const int U0 = esize << M;
+        for (int t = 0; ok && t < 16 / U0; ++t)
+            ok = (sw_inv(static_cast<uint64_t>(t) * (U0 / esize), B, M, S, steps) >> lv) < (32ull * cand);
+        if (ok) nb = cand;
     }
+    if (nb == 0) return SWZ_ERR_UNSUPPORTED;
     WarpCosetArgs a{};
     a.dst = static_cast<uint4 *>(dst);
     a.src = static_cast<const uint4 *>(src);
@@ -958,11 +1011,8 @@ swz_status launch_warp_coset(void *dst, const void *src, int64_t n_elems, int es
     a.steps = steps;
     a.lv = lv;
     const int U = esize << M;
-    for (int t = 0; t < 16 / U; ++t) {
-        const uint64_t y = sw_inv(static_cast<uint64_t>(t) * (U / esize), B, M, S, steps);
-        a.off[t] = static_cast<uint32_t>(y >> lv);
-        if ((y >> lv) >= 32) return SWZ_ERR_UNSUPPORTED;
-    }
+    for (int t = 0; t < 16 / U; ++t)
+        a.off[t] = static_cast<uint32_t>(sw_inv(static_cast<uint64_t>(t) * (U / esize), B, M, S, steps) >> lv);
     int src_lane[16];
     bool map = false;
     for (int l = 0; l < static_cast<int>(V); ++l) {
@@ -971,20 +1021,27 @@ swz_status launch_warp_coset(void *dst, const void *src, int64_t n_elems, int es
     }
     lane_map_selectors(src_lane, esize, a.perm_sel);
     const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
-    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
+    a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave || nb == 2) ? 2 : 1;  // (even for 64-blocks)
     const int64_t per_cta = int64_t(256) * a.per_thread;
     const int64_t grid = (a.nvec + per_cta - 1) / per_cta;
     if (grid > 0x7fffffffLL) return SWZ_ERR_SHAPE;
     if (grid == 0) return SWZ_OK;
     const dim3 gr(static_cast<unsigned>(grid));
-#define SWZ_W(UU) (map ? launch_pdl(relayout_warp_coset_kernel<UU, true>, gr, dim3(256), 0, st, a) \
-                       : launch_pdl(relayout_warp_coset_kernel<UU, false>, gr, dim3(256), 0, st, a))
+#define SWZ_W(UU, NB) (map ? launch_pdl(relayout_warp_coset_kernel<UU, true, NB>, gr, dim3(256), 0, st, a) \
+                           : launch_pdl(relayout_warp_coset_kernel<UU, false, NB>, gr, dim3(256), 0, st, a))
+    if (nb == 1) {
+        switch (U) {
+            case 1: return launched(SWZ_W(1, 1));
+            case 2: return launched(SWZ_W(2, 1));
+            case 4: return launched(SWZ_W(4, 1));
+            // U = 8 puts the written field at or above the lanes: no lane map
+            default: return launched(launch_pdl(relayout_warp_coset_kernel<8, false, 1>, gr, dim3(256), 0, st, a));
+        }
+    }
     switch (U) {
-        case 1: return launched(SWZ_W(1));
-        case 2: return launched(SWZ_W(2));
-        case 4: return launched(SWZ_W(4));
-        // U = 8 puts the written field at or above the lanes: no lane map
-        default: return launched(launch_pdl(relayout_warp_coset_kernel<8, false>, gr, dim3(256), 0, st, a));
+        case 2: return launched(SWZ_W(2, 2));
+        case 4: return launched(SWZ_W(4, 2));
+        default: return launched(launch_pdl(relayout_warp_coset_kernel<8, false, 2>, gr, dim3(256), 0, st, a));
     }
 #undef SWZ_W
 }
