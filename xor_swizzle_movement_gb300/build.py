@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "_build", "libswz.so")
-SOURCES = ["swz_abi.cu", "swz_relayout.cu", "swz_transpose.cu", "swz_bank.cu", "swz_tma.cu",
+SOURCES = ["swz_abi.cu", "swz_relayout.cu", "swz_relayout_neg.cu", "swz_transpose.cu", "swz_bank.cu", "swz_tma.cu",
            "swz_tma_relayout.cu", "swz_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
