@@ -1,0 +1,79 @@
+"""Relayouts of a 64 GiB buffer: vector indices beyond 2^32 (and element
+offsets beyond 2^35), where any 32-bit index arithmetic in a kernel or a
+launcher would wrap.  Each path is checked at 2^16 random positions spread
+over the whole buffer against the oracle's map, and forward then inverse must
+give the input back everywhere (the input is regenerated chunk by chunk from
+its seeds to compare)."""
+import numpy as np
+import pytest
+
+from gpu_util import torch
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+GIB = 1 << 30
+N_BYTES = 64 * GIB
+CHUNK = GIB
+
+
+@pytest.fixture(scope="module")
+def swz():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import xor_swizzle_movement_gb300 as m
+    m.lib()
+    return m
+
+
+def _fill(buf):
+    """Chunk i of the buffer: random bytes from seed 100 + i."""
+    g = torch.Generator(device="cuda")
+    for i in range(N_BYTES // CHUNK):
+        g.manual_seed(100 + i)
+        buf[i * CHUNK:(i + 1) * CHUNK].random_(0, 256, generator=g)
+
+
+def _equal_to_input(buf):
+    g = torch.Generator(device="cuda")
+    want = torch.empty(CHUNK, dtype=torch.uint8, device="cuda")
+    for i in range(N_BYTES // CHUNK):
+        g.manual_seed(100 + i)
+        want.random_(0, 256, generator=g)
+        if not torch.equal(buf[i * CHUNK:(i + 1) * CHUNK], want):
+            return False
+    return True
+
+
+@pytest.fixture(scope="module")
+def big():
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    if free < 140 * GIB:
+        pytest.skip("needs 128 GiB of free device memory")
+    src = torch.empty(N_BYTES, dtype=torch.uint8, device="cuda")
+    dst = torch.empty(N_BYTES, dtype=torch.uint8, device="cuda")
+    yield src, dst
+    del src, dst
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B,M,S", [(3, 3, 3),     # whole vectors, lanes XOR-ed in registers
+                                   (3, 0, -4),    # negative shift: warp shuffles
+                                   (4, 2, -9),    # negative shift: register cosets, 8 per thread
+                                   (3, 0, -2)])   # negative shift: warp shuffles after a lane map
+def test_relayout_64gib(swz, orc, big, B, M, S):
+    src, dst = big
+    n = N_BYTES // 2                              # uint16 elements, one tile
+    _fill(src)
+    rng = np.random.default_rng(B * 100 + M * 10 + S)
+    idx = np.sort(rng.choice(n, 1 << 16, replace=False)).astype(np.int64)
+    idx[-1] = n - 1                               # the last element
+    ti = torch.from_numpy(idx).cuda()
+    vals = src.view(torch.int16)[ti].clone()
+    swz.swz_relayout(dst, src, 1, 1, n, 2, B, M, S, 0)
+    torch.cuda.synchronize()
+    pos = orc.relayout_positions(idx, tile_elems=n, B=B, M=M, S=S)
+    assert torch.equal(dst.view(torch.int16)[torch.from_numpy(pos).cuda()], vals)
+    swz.swz_relayout(src, dst, 1, 1, n, 2, B, M, S, 1)
+    torch.cuda.synchronize()
+    assert _equal_to_input(src)
