@@ -77,3 +77,27 @@ def test_relayout_64gib(swz, orc, big, B, M, S):
     swz.swz_relayout(src, dst, 1, 1, n, 2, B, M, S, 1)
     torch.cuda.synchronize()
     assert _equal_to_input(src)
+
+
+@pytest.mark.parametrize("esize,variant", [(4, 0), (2, 0), (2, 3), (8, 0), (1, 0), (16, 0)])
+def test_transpose_64gib(swz, big, esize, variant):
+    """A 64 GiB matrix of 131072 rows (element offsets past 2^32; for the TMA
+    variant, tensor maps of 131072 x 262144 elements), transposed on each
+    element size's swizzled staging; 2^16 sampled elements checked, the last
+    one included."""
+    src, dst = big
+    R = 131072
+    C = N_BYTES // esize // R
+    dt = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64, 16: torch.int64}[esize]
+    w = esize // 8 if esize == 16 else 1          # 16-byte elements: two int64 words each
+    swz.swz_transpose(dst, src, R, C, esize, variant)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(esize * 10 + variant)
+    r = rng.integers(0, R, 1 << 16).astype(np.int64)
+    c = rng.integers(0, C, 1 << 16).astype(np.int64)
+    r[-1], c[-1] = R - 1, C - 1
+    sv, dv = src.view(dt), dst.view(dt)
+    for k in range(w):
+        si = torch.from_numpy((r * C + c) * w + k).cuda()
+        di = torch.from_numpy((c * R + r) * w + k).cuda()
+        assert torch.equal(dv[di], sv[si])
