@@ -151,3 +151,40 @@ def test_relayout_staged_and_unaligned_large(swz, orc, big):
     n_tiles = half // 8192 - 1
     nb = n_tiles * 8192
     _check_relayout(swz, orc, swz.swz_relayout, src[2:2 + nb], dst[6:6 + nb], n_tiles, 4096, 2, 3, 3, 3, seed=9)
+
+
+def test_bank_profile_and_slice_collision_large(swz, orc, big):
+    """The bank profiler over 2^27 patterns (16 GiB of addresses, pattern
+    words past 2^32) and the batched slice collision over 2^32 masks (32 GiB
+    in, 32 GiB out), each checked at sampled entries, the last included."""
+    src, dst = big
+    _fill(src)
+    # patterns: 32 byte addresses each, made 4-byte aligned below 228 KiB
+    n_pat = 1 << 27
+    addrs = src[:n_pat * 128].view(torch.int32)
+    addrs.bitwise_and_(0x3FFFC)
+    addrs.remainder_(228 * 1024)
+    ways = dst[:n_pat * 4].view(torch.int32)
+    wf = dst[n_pat * 4:n_pat * 8].view(torch.int32)
+    swz.swz_bank_profile(addrs, None, n_pat, 4, ways, wf)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    rows = np.sort(rng.choice(n_pat, 4096, replace=False)).astype(np.int64)
+    rows[-1] = n_pat - 1
+    tr = torch.from_numpy(rows).cuda()
+    host = addrs.view(-1, 32)[tr].cpu().numpy().view(np.uint32)
+    w_want, f_want = orc.bank_profile(host, 4)
+    assert np.array_equal(ways[tr].cpu().numpy(), w_want)
+    assert np.array_equal(wf[tr].cpu().numpy(), f_want)
+    # slice collision: C = A & ~sw(A) on 2^32 masks, Swizzle<3,4,3>
+    n_m = 1 << 32
+    A = src[:n_m * 8].view(torch.int64)
+    C = dst[:n_m * 8].view(torch.int64)
+    swz.swz_slice_collision_batch(A, n_m, 3, 4, 3, C)
+    torch.cuda.synchronize()
+    idx = np.sort(rng.choice(n_m, 4096, replace=False)).astype(np.int64)
+    idx[-1] = n_m - 1
+    ti = torch.from_numpy(idx).cuda()
+    a = A[ti].cpu().numpy().view(np.uint64)
+    want = np.array([orc.slice_collision(int(x), B=3, M=4, S=3) for x in a], dtype=np.uint64)
+    assert np.array_equal(C[ti].cpu().numpy().view(np.uint64), want)
