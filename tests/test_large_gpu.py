@@ -188,3 +188,23 @@ def test_bank_profile_and_slice_collision_large(swz, orc, big):
     a = A[ti].cpu().numpy().view(np.uint64)
     want = np.array([orc.slice_collision(int(x), B=3, M=4, S=3) for x in a], dtype=np.uint64)
     assert np.array_equal(C[ti].cpu().numpy().view(np.uint64), want)
+
+
+def test_transpose_relayout_32gib(swz, orc, big):
+    """The transpose fused with the Swizzle<3,4,3> relayout into 128 x 64 tiles,
+    on a 131072 x 131072 bf16 matrix (32 GiB): element (r, c) lands at the
+    forward relayout position of its transposed offset c * R + r; 2^16 sampled
+    elements checked, the last one included."""
+    src, dst = big
+    R = C = 131072
+    te = 128 * 64
+    s16 = src[:R * C * 2].view(torch.int16)
+    d16 = dst[:R * C * 2].view(torch.int16)
+    swz.swz_transpose_relayout(d16, s16, R, C, 2, te, 3, 4, 3)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(12)
+    r = rng.integers(0, R, 1 << 16).astype(np.int64)
+    c = rng.integers(0, C, 1 << 16).astype(np.int64)
+    r[-1], c[-1] = R - 1, C - 1
+    pos = orc.relayout_positions(c * R + r, tile_elems=te, B=3, M=4, S=3)
+    assert torch.equal(d16[torch.from_numpy(pos).cuda()], s16[torch.from_numpy(r * C + c).cuda()])
