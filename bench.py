@@ -83,6 +83,7 @@ def parse():
     p.add_argument("--n", type=int, default=0, help="--case size (matrix edge / elements / patterns)")
     p.add_argument("--bms", default="1,1,1", help="--case relayout_bms: B,M,S (several sets separated by ';')")
     p.add_argument("--reps", type=int, default=2, help="--case launches per kernel")
+    p.add_argument("--width", type=int, default=4, help="--case bank_profile: access bytes per lane")
     p.add_argument("--launcher-check", action="store_true",
                    help="check the multi-rank launch on CPU (gloo): each rank reports a fixed time, rank 0 "
                         "prints the world size and the slowest rank's time; no GPU, no bench line")
@@ -643,9 +644,21 @@ def measure_rows(torch, swz, dev, flush, peak):
     pats = (torch.randint(0, 228 * 1024 // 4, (npat, 32), dtype=torch.int32, device=dev, generator=gen) * 4)
     ways = torch.empty(npat, dtype=torch.int32, device=dev)
     wf = torch.empty(npat, dtype=torch.int32, device=dev)
-    ms = back_to_back_ms(torch, lambda: swz.swz_bank_profile(pats, None, npat, 4, ways, wf))
-    out["bank_profile_4M_patterns_w4"] = {"ms": round(ms, 4), "Gpatterns/s": round(npat / (ms * 1e-3) / 1e9, 3),
-                                          "GB/s": round(npat * 136 / (ms * 1e-3) / GB, 1)}
+    def profile_row(width, act):
+        # bytes per pattern: 128 of addresses and 4 of mask read, 8 of results written
+        per = 136 + (4 if act is not None else 0)
+        ms = back_to_back_ms(torch, lambda: swz.swz_bank_profile(pats, act, npat, width, ways, wf))
+        gbs = npat * per / (ms * 1e-3) / GB
+        return {"ms": round(ms, 4), "Gpatterns/s": round(npat / (ms * 1e-3) / 1e9, 3), "GB/s": round(gbs, 1),
+                "frac_of_hbm": round(gbs / peak, 3)}
+    out["bank_profile_4M_patterns_w4"] = profile_row(4, None)
+    masks = torch.randint(-(1 << 31), 1 << 31, (npat,), dtype=torch.int64, device=dev, generator=gen).to(torch.int32)
+    other = {"w4_masked": profile_row(4, masks)}
+    for width in (1, 2, 8, 16):
+        pats.bitwise_and_(~(width - 1))  # addresses aligned to the width (all are multiples of 4)
+        other[f"w{width}"] = profile_row(width, None)
+    out["bank_profile_4M_patterns_other_widths"] = other
+    del pats, masks, ways, wf
 
     # batched slice collision: 2^27 64-bit masks (1 GiB in, 1 GiB out), Swizzle<3,4,3>
     nm = 1 << 27
@@ -979,12 +992,13 @@ def run_case(args):
                     done.append(f"staging_probe esize={esize} variant={v} {mode} iters={it_} ctas={ctas}")
     elif args.case == "bank_profile":
         n = args.n or (1 << 20)
-        pats = torch.randint(0, 228 * 1024 // 4, (n, 32), dtype=torch.int32, device=dev, generator=gen) * 4
+        width = args.width
+        pats = torch.randint(0, 228 * 1024 // width, (n, 32), dtype=torch.int32, device=dev, generator=gen) * width
         w = torch.empty(n, dtype=torch.int32, device=dev)
         f = torch.empty(n, dtype=torch.int32, device=dev)
         for _ in range(args.reps):
-            swz.swz_bank_profile(pats, None, n, 4, w, f)
-        done.append(f"bank_profile n={n}")
+            swz.swz_bank_profile(pats, None, n, width, w, f)
+        done.append(f"bank_profile n={n} width={width}")
     else:
         raise SystemExit(f"unknown --case {args.case}")
     torch.cuda.synchronize()

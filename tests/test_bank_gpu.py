@@ -68,6 +68,81 @@ def test_random(swz, orc, width, aligned, masked):
     assert np.array_equal(gw, ow) and np.array_equal(gf, of)
 
 
+def gpu_profile_offset(swz, pats, width, active=None, word_offset=1):
+    """As gpu_profile, with the address and mask arrays starting word_offset
+    words into their buffers (off 16-byte alignment for odd offsets)."""
+    n = pats.shape[0]
+    flat = np.zeros(n * 32 + word_offset, dtype=np.uint32)
+    flat[word_offset:] = pats.reshape(-1)
+    dp = torch.from_numpy(flat.view(np.int32)).cuda()[word_offset:]
+    da = None
+    if active is not None:
+        fa = np.zeros(n + word_offset, dtype=np.uint32)
+        fa[word_offset:] = active
+        da = torch.from_numpy(fa.view(np.int32)).cuda()[word_offset:]
+    w = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    f = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    swz.swz_bank_profile(dp, da, n, width, w, f)
+    torch.cuda.synchronize()
+    return w.cpu().numpy(), f.cpu().numpy()
+
+
+def mixed_patterns(n, width, seed):
+    """Aligned random patterns, every third one with some lanes moved off
+    alignment, some squeezed into 512 bytes (shared words, deep conflicts) and
+    some near the top of the 32-bit address space."""
+    rng = np.random.default_rng(seed)
+    pats = (rng.integers(0, 228 * 1024 // width, (n, 32)) * width).astype(np.uint64)
+    pats[1::5] %= 512
+    pats[2::7] += (1 << 32) - 228 * 1024
+    bad = np.arange(n) % 3 == 0
+    shift = rng.integers(0, 2, (n, 32)) * rng.integers(1, 16, (n, 32))
+    pats[bad] += shift[bad].astype(np.uint64)
+    return (pats % (1 << 32)).astype(np.uint32)
+
+
+@pytest.mark.parametrize("width", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 31, 33, 97, 4099])
+@pytest.mark.parametrize("masked", [False, True])
+def test_ragged_mixed(swz, orc, width, n, masked):
+    """Pattern counts that leave a partial batch of 32, aligned and unaligned
+    patterns side by side in one batch (the unaligned ones take the exact
+    count), masks that switch off whole passes or only the unaligned lanes."""
+    pats = mixed_patterns(n, width, seed=n + width)
+    act = None
+    if masked:
+        act = inputs_masks(n, seed=n)
+        act[::4] = 0xFFFF0000
+        act[1::4] = 0x000000FF
+        act[2::9] = 0
+        # switch off exactly the unaligned lanes of some patterns: they count as aligned
+        for p in range(0, n, 6):
+            off = (pats[p] % max(width, 1)) != 0 if width > 4 else ((pats[p] & 3) + width > 4)
+            act[p] = np.uint32(sum(1 << l for l in range(32) if not off[l]))
+    gw, gf = gpu_profile(swz, pats, width, act)
+    ow, of = orc.bank_profile(pats, width, act)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
+@pytest.mark.parametrize("width", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("masked", [False, True])
+def test_address_array_off_16_bytes(swz, orc, width, masked):
+    """Address and mask arrays 4 and 12 bytes past a 16-byte boundary: the
+    patterns are staged word by word instead of in 16-byte chunks."""
+    n = 1000
+    pats = mixed_patterns(n, width, seed=40 + width)
+    act = inputs_masks(n, seed=41) if masked else None
+    ow, of = orc.bank_profile(pats, width, act)
+    for off in (1, 3):
+        gw, gf = gpu_profile_offset(swz, pats, width, act, word_offset=off)
+        assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
+def inputs_masks(n, seed):
+    from xor_swizzle_movement_gb300 import inputs
+    return inputs.active_masks(n, seed=seed)
+
+
 @pytest.mark.slow
 def test_bench_size(swz, orc):
     """2^22 aligned random 4-byte patterns: the benchmark's profiler batch."""

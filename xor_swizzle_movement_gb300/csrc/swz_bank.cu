@@ -1,128 +1,424 @@
 // swz_bank.cu -- shared-memory bank-conflict profiler for warp access
-// patterns, one warp per pattern (sm_103a).
+// patterns, and the batched slice collision (sm_103a).
 //
 // Model (see swz.h): 32 banks of 4 bytes; per pass, the cost is the largest
 // number of distinct 4-byte words that fall in one bank; same-word lanes are
 // served together.  Accesses of 8 bytes take two passes of 16 lanes, 16
 // bytes four passes of 8 lanes; up to 4 bytes one pass of 32 lanes.
 //
-// Lane l of the warp holds lane l's address, so the pattern is read with one
-// coalesced 128-byte load.  Aligned patterns (the only ones real hardware
-// accepts: a w-byte access on a multiple of w, or a sub-word access that does
-// not straddle a word) are counted in claim rounds through a 32-slot per-warp
-// table (one slot per pass and bank group): a round costs one shared store,
-// one shared load and a ballot, and a pass takes exactly as many rounds as
-// its cost.  (Two warp-wide match instructions per pattern, the obvious
-// alternative, cost about 50 SM cycles each here.)  Unaligned patterns, where
-// one lane may touch up to five words and neighbours may share some of them,
-// are counted exactly with a per-warp table of word candidates.
+// One lane profiles whole patterns, two at a time.  Each warp stages 64
+// consecutive patterns (8 KiB of addresses) in shared memory with cp.async,
+// two batches in flight; a pattern's 128 bytes form one row, stored with its
+// 16-byte chunks XOR-ed by the row index mod 8, so the copies into the row and
+// each lane's reads of its own row are both free of bank conflicts.
+//
+// Aligned patterns (every active access on a multiple of its width, or a
+// sub-word access inside one word): an access unit -- the word, or the
+// W-byte chunk -- shares no word with another unit, so a pass costs the
+// largest number of distinct units in one bank group.  The lane makes a key
+// of each unit with the bank-group bits on top and the unit's other address
+// bits below them.  Sorting a pass's keys (Batcher's odd-even merge network,
+// all in registers) puts each group's units together and equal units side by
+// side, and one scan counts the distinct keys of each group.  An inactive lane
+// takes the address of the pass's first active lane, which adds nothing.  For
+// addresses below 2^18 bytes (all of shared memory) a key fits in 16 bits and
+// a lane sorts its two patterns side by side, two keys per word with 16-bit
+// SIMD min and max; otherwise 32-bit keys, one pattern after the other.
+// Every lane does the same work, so the warp never diverges on the data.
+//
+// Patterns with an unaligned access, where one lane may touch up to five words
+// and neighbours may share some of them, are then counted exactly by the whole
+// warp, one pattern at a time, over per-lane word candidates.
 #include "swz_common.cuh"
 
 namespace swz {
 namespace {
 
-constexpr int kWarpsPerCta = 8;
+constexpr int kLaneWarps = 2;  // warps per CTA
 
-// W = access bytes per lane (1, 2, 4, 8, 16)
 template <int W>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, 8)  // 8 CTAs (64 warps) per SM: 32 registers
-    bank_profile_kernel(const uint32_t *__restrict__ addrs, const uint32_t *__restrict__ active,
-                        int64_t n, int32_t *__restrict__ ways, int32_t *__restrict__ wavefronts) {
-    constexpr int kPasses = W <= 4 ? 1 : W / 4;
-    constexpr int kLpp = 32 / kPasses;                       // lanes per pass
-    constexpr uint32_t kUnitShift = W <= 4 ? 2 : (W == 8 ? 3 : 4);  // log2 of the access unit (>= a word)
-    __shared__ uint32_t s_tab[kWarpsPerCta][32];
-    __shared__ uint32_t s_first[kWarpsPerCta][32];
-    __shared__ int s_nw[kWarpsPerCta][32];
-    __shared__ int s_cnt[kWarpsPerCta][4][32];
+struct Passes {
+    static constexpr int n = W <= 4 ? 1 : W / 4;  // passes per access
+    static constexpr int lanes = 32 / n;          // lanes per pass
+};
+
+// ---- exact count: the whole warp on one pattern ----------------------------
+
+struct ExactScratch {
+    uint32_t first[32];
+    int nw[32];
+    int cnt[4][32];
+};
+
+// Cost of this lane's pass, the same on every lane of the pass.  Lane l holds
+// lane l's address a and whether it is active.  Its candidate words are
+// first .. first + nw - 1; each word is counted once per pass, by the lowest
+// lane that touches it at its earliest candidate.
+template <int W>
+__device__ __forceinline__ int exact_pass_cost(uint32_t a, bool on, int lane, ExactScratch &s) {
+    constexpr int kPasses = Passes<W>::n, kLpp = Passes<W>::lanes;
+    const int pass = lane / kLpp;
+    const unsigned long long last = (static_cast<unsigned long long>(a) + W - 1) >> 2;
+    const uint32_t first = a >> 2;
+    const int nw = on ? static_cast<int>(last - first + 1) : 0;
+    s.first[lane] = first;
+    s.nw[lane] = nw;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s.cnt[q][lane] = 0;
+    __syncwarp();
+    for (int i = 0; i < 5; ++i) {
+        const bool valid = i < nw;
+        const unsigned long long wd = static_cast<unsigned long long>(first) + i;
+        const unsigned long long key = valid ? ((static_cast<unsigned long long>(pass) << 40) | wd)
+                                             : ((1ull << 63) | static_cast<unsigned long long>(lane));
+        const unsigned m = __match_any_sync(kFullMask, key);
+        bool fresh = valid && (__ffs(m) - 1 == lane);
+        if (fresh && i > 0) {
+            // did a lane of this pass touch the same word at an earlier candidate?
+            for (int l2 = pass * kLpp; l2 < (pass + 1) * kLpp; ++l2) {
+                const long long d = static_cast<long long>(wd) - static_cast<long long>(s.first[l2]);
+                if (d >= 0 && d < i && d < s.nw[l2]) fresh = false;
+            }
+        }
+        if (fresh) atomicAdd(&s.cnt[pass][static_cast<int>(wd & 31u)], 1);
+    }
+    __syncwarp();
+    int mine = 0;
+#pragma unroll
+    for (int q = 0; q < kPasses; ++q) {
+        const int c = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(s.cnt[q][lane])));
+        if (q == pass) mine = c;
+    }
+    __syncwarp();
+    return mine;
+}
+
+// worst pass and sum of passes from the per-lane pass costs of exact_pass_cost
+template <int W>
+__device__ __forceinline__ void exact_totals(int cost, int lane, int &worst, int &total) {
+    constexpr int kLpp = Passes<W>::lanes;
+    if constexpr (Passes<W>::n == 1) {
+        worst = total = cost;
+    } else {
+        const unsigned rep = (lane % kLpp == 0) ? static_cast<unsigned>(cost) : 0u;  // one lane per pass
+        worst = static_cast<int>(__reduce_max_sync(kFullMask, rep));
+        total = static_cast<int>(__reduce_add_sync(kFullMask, rep));
+    }
+}
+
+// ---- one lane, one aligned pattern --------------------------------------------
+
+__device__ __forceinline__ void order2(uint32_t &x, uint32_t &y) {
+    const uint32_t lo = min(x, y);
+    y = max(x, y);
+    x = lo;
+}
+
+// The same on two 16-bit keys per word, each half on its own.
+__device__ __forceinline__ void order2x(uint32_t &x, uint32_t &y) {
+    uint32_t lo, hi;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(lo) : "r"(x), "r"(y));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(hi) : "r"(x), "r"(y));
+    x = lo;
+    y = hi;
+}
+
+template <bool PK>
+__device__ __forceinline__ void order(uint32_t &x, uint32_t &y) {
+    if constexpr (PK) order2x(x, y);
+    else order2(x, y);
+}
+
+// Batcher's odd-even merge of k[LO .. LO+N), whose two halves are sorted,
+// restricted to the elements LO, LO + R, LO + 2R, ...: merge the even and the
+// odd subsequence (stride 2R), then order each odd element with the next one.
+template <bool PK, int LO, int N, int R>
+__device__ __forceinline__ void oe_merge(uint32_t (&k)[32]) {
+    if constexpr (2 * R < N) {
+        oe_merge<PK, LO, N, 2 * R>(k);
+        oe_merge<PK, LO + R, N, 2 * R>(k);
+#pragma unroll
+        for (int i = LO + R; i + R < LO + N; i += 2 * R) order<PK>(k[i], k[i + R]);
+    } else {
+        order<PK>(k[LO], k[LO + R]);
+    }
+}
+
+// Sorts k[LO .. LO+N), N a power of two (19 / 63 / 191 compare-exchanges
+// for 8 / 16 / 32 keys).  PK: two 16-bit keys per word, sorted side by side.
+template <bool PK, int LO, int N>
+__device__ __forceinline__ void oe_sort(uint32_t (&k)[32]) {
+    if constexpr (N > 1) {
+        oe_sort<PK, LO, N / 2>(k);
+        oe_sort<PK, LO + N / 2, N / 2>(k);
+        oe_merge<PK, LO, N, 1>(k);
+    }
+}
+
+// Sorts each pass's keys.
+template <int W, bool PK>
+__device__ __forceinline__ void sort_passes(uint32_t (&k)[32]) {
+    if constexpr (Passes<W>::n == 1) {
+        oe_sort<PK, 0, 32>(k);
+    } else if constexpr (Passes<W>::n == 2) {
+        oe_sort<PK, 0, 16>(k);
+        oe_sort<PK, 16, 16>(k);
+    } else {
+        oe_sort<PK, 0, 8>(k);
+        oe_sort<PK, 8, 8>(k);
+        oe_sort<PK, 16, 8>(k);
+        oe_sort<PK, 24, 8>(k);
+    }
+}
+
+// Cost of the pattern in this lane's row (chunk c at row[c ^ sw]), m its
+// active lanes.  bad: some active access is unaligned; the result is then
+// meaningless and the exact count must replace it.
+template <int W, bool MASKED>
+__device__ __forceinline__ void lane_pattern_cost(const uint4 *row, int sw, uint32_t m, int &worst, int &total,
+                                                  bool &bad) {
+    constexpr int kPasses = Passes<W>::n, kLpp = Passes<W>::lanes;
+    // keys of different bank groups differ in their top 5 / 4 / 3 bits
+    constexpr uint32_t kNextGroup = 1u << (kPasses == 1 ? 27 : (kPasses == 2 ? 28 : 29));
+    uint32_t k[32];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = row[c ^ sw];
+        k[4 * c] = v.x;
+        k[4 * c + 1] = v.y;
+        k[4 * c + 2] = v.z;
+        k[4 * c + 3] = v.w;
+    }
+    uint32_t mis = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        uint32_t u;
+        if constexpr (W == 1) u = 0u;
+        else if constexpr (W == 2) u = k[i] & (k[i] >> 1) & 1u;  // byte 3 of a word: the access straddles
+        else u = k[i] & static_cast<uint32_t>(W - 1);
+        if constexpr (MASKED) u = ((m >> i) & 1u) ? u : 0u;
+        mis |= u;
+        const uint32_t w = k[i] & ~3u;     // the unit's first byte (W >= 4 aligned: the address itself)
+        k[i] = __funnelshift_r(w, w, 7);  // rotate right by 7: bank group on top
+    }
+    bad = mis != 0u;
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int q = 0; q < kPasses; ++q) {
+            uint32_t kf = k[q * kLpp];
+#pragma unroll
+            for (int i = kLpp - 1; i >= 0; --i)
+                if ((m >> (q * kLpp + i)) & 1u) kf = k[q * kLpp + i];
+#pragma unroll
+            for (int i = 0; i < kLpp; ++i)
+                if (!((m >> (q * kLpp + i)) & 1u)) k[q * kLpp + i] = kf;
+        }
+    }
+    sort_passes<W, false>(k);
+    worst = 0;
+    total = 0;
+#pragma unroll
+    for (int q = 0; q < kPasses; ++q) {
+        int run = 1, mx = 1;  // distinct keys so far in the current group; the largest such count
+#pragma unroll
+        for (int i = 1; i < kLpp; ++i) {
+            const uint32_t x = k[q * kLpp + i] ^ k[q * kLpp + i - 1];
+            run = x >= kNextGroup ? 1 : run + (x != 0u ? 1 : 0);
+            mx = max(mx, run);
+        }
+        uint32_t pm = m;
+        if constexpr (kPasses > 1) pm = (m >> (q * kLpp)) & ((1u << kLpp) - 1u);
+        const int cost = pm ? mx : 0;
+        worst = max(worst, cost);
+        total += cost;
+    }
+}
+
+// Two patterns per lane on 16-bit keys: rows a and b (chunk c at a[c ^ sw]),
+// active masks ma and mb.  A key is the bank-group bits of the unit's address
+// (bits 2..6) over its bits 7..17, which holds every unit of an address below
+// 2^18 bytes; ok is false when some address of either row is not below that,
+// and the results are then not set.  Inactive lanes take the address of their
+// pass's first active lane (0 when the pass has none).  bad_a, bad_b: some
+// active access of that row is unaligned.
+template <int W, bool MASKED>
+__device__ __forceinline__ void lane_pair_cost16(const uint4 *a, const uint4 *b, int sw, uint32_t ma, uint32_t mb,
+                                                 int (&worst)[2], int (&total)[2], bool (&bad)[2], bool &ok) {
+    constexpr int kPasses = Passes<W>::n, kLpp = Passes<W>::lanes;
+    // 16-bit keys of different bank groups differ in their top 5 / 4 / 3 bits
+    constexpr uint32_t kGroupBits = (kPasses == 1 ? 0xF800u : (kPasses == 2 ? 0xF000u : 0xE000u)) * 0x10001u;
+    uint32_t fa[kPasses], fb[kPasses];  // first active address of each pass
+    if constexpr (MASKED) {
+#pragma unroll
+        for (int q = 0; q < kPasses; ++q) {
+            const uint32_t pa = kPasses == 1 ? ma : (ma >> (q * kLpp)) & ((1u << (kLpp & 31)) - 1u);
+            const uint32_t pb = kPasses == 1 ? mb : (mb >> (q * kLpp)) & ((1u << (kLpp & 31)) - 1u);
+            const int ia = q * kLpp + __ffs(pa) - 1, ib = q * kLpp + __ffs(pb) - 1;
+            fa[q] = pa ? reinterpret_cast<const uint32_t *>(a)[((ia >> 2) ^ sw) * 4 + (ia & 3)] : 0u;
+            fb[q] = pb ? reinterpret_cast<const uint32_t *>(b)[((ib >> 2) ^ sw) * 4 + (ib & 3)] : 0u;
+        }
+    }
+    uint32_t k[32];
+    uint32_t acc_a = 0, acc_b = 0;  // OR of the addresses (W = 2: of a & (a >> 1))
+    uint32_t hi = 0;                // OR of both rows' addresses, for the range
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 va = a[c ^ sw], vb = b[c ^ sw];
+        const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = 4 * c + j;
+            uint32_t ua = xa[j], ub = xb[j];
+            if constexpr (MASKED) {
+                ua = (ma & (1u << i)) ? ua : fa[i / kLpp];
+                ub = (mb & (1u << i)) ? ub : fb[i / kLpp];
+            }
+            if constexpr (W >= 4) {
+                acc_a |= ua;
+                acc_b |= ub;
+            } else {
+                hi |= ua | ub;
+                if constexpr (W == 2) {
+                    acc_a |= ua & (ua >> 1);
+                    acc_b |= ub & (ub >> 1);
+                }
+            }
+            // word indices of a (low half) and b (high half), each rotated left by
+            // 11 within its half: bank group (bits 2..6) over address bits 7..17
+            const uint32_t wp = __byte_perm(ua >> 2, ub >> 2, 0x5410);
+            k[i] = ((wp << 11) & 0xF800F800u) | ((wp >> 5) & 0x07FF07FFu);
+        }
+    }
+    if constexpr (W >= 4) hi = acc_a | acc_b;
+    constexpr uint32_t kMis = W == 1 ? 0u : (W == 2 ? 1u : static_cast<uint32_t>(W - 1));
+    bad[0] = (acc_a & kMis) != 0u;
+    bad[1] = (acc_b & kMis) != 0u;
+    ok = (hi >> 18) == 0u;
+    if (!__all_sync(kFullMask, ok)) return;  // some lane needs 32-bit keys: the warp takes them
+    sort_passes<W, true>(k);
+    worst[0] = worst[1] = total[0] = total[1] = 0;
+#pragma unroll
+    for (int q = 0; q < kPasses; ++q) {
+        // per half: distinct keys so far in the current group, and the largest such count
+        uint32_t run = 0x00010001u, mx = 0x00010001u;
+#pragma unroll
+        for (int i = 1; i < kLpp; ++i) {
+            const uint32_t x = k[q * kLpp + i] ^ k[q * kLpp + i - 1];
+            uint32_t d, g;
+            asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(0x00010001u));               // a new key
+            asm("min.u16x2 %0, %1, %2;" : "=r"(g) : "r"(x & kGroupBits), "r"(0x00010001u));  // a new group
+            const uint32_t msk = g * 0xFFFFu;  // 0xFFFF in the halves where a group starts
+            run = ((run + d) & ~msk) | (0x00010001u & msk);
+            asm("max.u16x2 %0, %1, %2;" : "=r"(mx) : "r"(mx), "r"(run));
+        }
+        const uint32_t pa = kPasses == 1 ? ma : (ma >> (q * kLpp)) & ((1u << (kLpp & 31)) - 1u);
+        const uint32_t pb = kPasses == 1 ? mb : (mb >> (q * kLpp)) & ((1u << (kLpp & 31)) - 1u);
+        const int ca = pa ? static_cast<int>(mx & 0xFFFFu) : 0, cb = pb ? static_cast<int>(mx >> 16) : 0;
+        worst[0] = max(worst[0], ca);
+        total[0] += ca;
+        worst[1] = max(worst[1], cb);
+        total[1] += cb;
+    }
+}
+
+// ---- kernel ---------------------------------------------------------------------
+
+constexpr int kRows = 64;  // patterns per warp and batch: two per lane
+
+struct __align__(16) LaneStage {
+    uint4 rows[2][kRows * 8];  // two batches of 64 rows of 8 chunks; chunk c of row r at r * 8 + (c ^ (r & 7))
+    uint32_t mask[2][kRows];
+    ExactScratch ex;
+};
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// W = access bytes per lane (1, 2, 4, 8, 16); MASKED: an active-lane mask per
+// pattern; VEC: the address array is 16-byte aligned and rows are copied in
+// 16-byte chunks (otherwise word by word).  Each warp takes batches of 64
+// patterns at a grid stride; lane l profiles rows l and l + 32 of a batch.
+template <int W, bool MASKED, bool VEC>
+__global__ void __launch_bounds__(kLaneWarps * 32, 6)  // 6 CTAs (12 warps, 207 KiB of stages) per SM
+    bank_profile_kernel(const uint32_t *__restrict__ addrs, const uint32_t *__restrict__ active, int64_t n,
+                        int32_t *__restrict__ ways, int32_t *__restrict__ wavefronts) {
+    __shared__ LaneStage s_stage[kLaneWarps];
     pdl_launch_dependents();
     pdl_wait();  // before any global memory access
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int pass = lane / kLpp;
-    const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
-    for (int64_t p = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + wid; p < n; p += warps_total) {
-        const uint32_t a = __ldcs(addrs + p * 32 + lane);
-        const uint32_t mask = active ? __ldcs(active + p) : kFullMask;
-        const bool on = (mask >> lane) & 1u;
-        const bool aligned = W <= 4 ? ((a & 3u) + static_cast<uint32_t>(W) <= 4u)
-                                    : ((a & static_cast<uint32_t>(W - 1)) == 0u);
-        int cost;  // cost of this lane's pass, valid on every lane of the pass
-        if (__all_sync(kFullMask, !on || aligned)) {
-            // An aligned access unit (a word, or a W-byte chunk) never shares a
-            // word with a different unit, so the pass cost is the largest
-            // number of distinct units in one bank group.  Count it by rounds:
-            // every lane still waiting writes its unit into its group's slot,
-            // one write per slot wins, and every lane whose unit is the one in
-            // its slot is served.  Each round serves exactly one distinct unit
-            // per slot, so a pass takes as many rounds as its worst group holds
-            // distinct units.
-            const uint32_t unit = a >> kUnitShift;
-            const int slot = pass * kLpp + static_cast<int>(unit & static_cast<uint32_t>(kLpp - 1));
-            const unsigned pass_lanes = (kLpp == 32) ? kFullMask : (((1u << (kLpp & 31)) - 1u) << (pass * kLpp));
-            volatile uint32_t *tab = s_tab[wid];
-            unsigned rem = __ballot_sync(kFullMask, on);
-            int rounds = 0;
-            while (rem) {  // warp-uniform; every round serves at least one lane
-                const bool waiting = (rem >> lane) & 1u;
-                if (waiting) tab[slot] = unit;
-                __syncwarp();
-                const bool served = waiting && tab[slot] == unit;
-                __syncwarp();
-                rounds += (rem & pass_lanes) != 0u;
-                rem &= ~__ballot_sync(kFullMask, served);
-            }
-            cost = rounds;
-        } else {
-            // exact count: candidate words first .. first + nw - 1 per lane
-            const unsigned long long last = (static_cast<unsigned long long>(a) + W - 1) >> 2;
-            const uint32_t first = a >> 2;
-            const int nw = on ? static_cast<int>(last - first + 1) : 0;
-            s_first[wid][lane] = first;
-            s_nw[wid][lane] = nw;
+    LaneStage &st = s_stage[wid];
+    const int64_t n_batches = (n + kRows - 1) / kRows;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kLaneWarps;
+    auto stage = [&](int64_t b, int buf) {
+        if (b < n_batches) {
+            const int64_t p0 = b * kRows;
+            if constexpr (VEC) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) s_cnt[wid][q][lane] = 0;
-            __syncwarp();
-            for (int i = 0; i < 5; ++i) {
-                const bool valid = i < nw;
-                const unsigned long long wd = static_cast<unsigned long long>(first) + i;
-                const unsigned long long key =
-                    valid ? ((static_cast<unsigned long long>(pass) << 40) | wd)
-                          : ((1ull << 63) | static_cast<unsigned long long>(lane));
-                const unsigned m = __match_any_sync(kFullMask, key);
-                bool fresh = valid && (__ffs(m) - 1 == lane);
-                if (fresh && i > 0) {
-                    // did a lane of this pass touch the same word in an earlier round?
-                    for (int l2 = pass * kLpp; l2 < (pass + 1) * kLpp; ++l2) {
-                        const long long d = static_cast<long long>(wd) - static_cast<long long>(s_first[wid][l2]);
-                        if (d >= 0 && d < i && d < s_nw[wid][l2]) fresh = false;
-                    }
+                for (int j = 0; j < kRows / 4; ++j) {
+                    const int r = 4 * j + (lane >> 3), c = lane & 7;
+                    if (p0 + r < n) cp_async16(&st.rows[buf][r * 8 + (c ^ (r & 7))], addrs + (p0 + r) * 32 + c * 4);
                 }
-                if (fresh) atomicAdd(&s_cnt[wid][pass][static_cast<int>(wd & 31u)], 1);
+            } else {
+                const int c = lane >> 2;
+                for (int r = 0; r < kRows && p0 + r < n; ++r)
+                    cp_async4(reinterpret_cast<uint32_t *>(&st.rows[buf][r * 8 + (c ^ (r & 7))]) + (lane & 3),
+                              addrs + (p0 + r) * 32 + lane);
             }
-            __syncwarp();
-            int mine = 0;
+            if constexpr (MASKED) {
+                if (p0 + lane < n) cp_async4(&st.mask[buf][lane], active + p0 + lane);
+                if (p0 + 32 + lane < n) cp_async4(&st.mask[buf][32 + lane], active + p0 + 32 + lane);
+            }
+        }
+        cp_async_commit();
+    };
+    int64_t b = static_cast<int64_t>(blockIdx.x) * kLaneWarps + wid;
+    stage(b, 0);
+    for (int buf = 0; b < n_batches; b += stride, buf ^= 1) {
+        stage(b + stride, buf ^ 1);
+        cp_async_wait_1();
+        __syncwarp();  // every lane's copies of this batch are visible to the warp
+        const int64_t p[2] = {b * kRows + lane, b * kRows + 32 + lane};
+        const uint32_t m[2] = {MASKED ? st.mask[buf][lane] : kFullMask, MASKED ? st.mask[buf][32 + lane] : kFullMask};
+        const uint4 *row[2] = {&st.rows[buf][lane * 8], &st.rows[buf][(32 + lane) * 8]};
+        int worst[2], total[2];
+        bool bad[2], ok;
+        lane_pair_cost16<W, MASKED>(row[0], row[1], lane & 7, m[0], m[1], worst, total, bad, ok);
+        if (!__all_sync(kFullMask, ok)) {  // an address at or above 2^18: 32-bit keys, one row at a time
+#pragma unroll 1  // one copy of the 32-bit path: fewer registers
+            for (int h = 0; h < 2; ++h) lane_pattern_cost<W, MASKED>(row[h], lane & 7, m[h], worst[h], total[h], bad[h]);
+        }
 #pragma unroll
-            for (int q = 0; q < kPasses; ++q) {
-                const int c = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(s_cnt[wid][q][lane])));
-                if (q == pass) mine = c;
+        for (int h = 0; h < 2; ++h) {
+            unsigned redo = __ballot_sync(kFullMask, bad[h] && p[h] < n);
+            while (redo) {  // warp-uniform
+                const int r = __ffs(redo) - 1, rr = 32 * h + r;
+                redo &= redo - 1u;
+                const int c = lane >> 2;
+                const uint32_t ad =
+                    reinterpret_cast<const uint32_t *>(&st.rows[buf][rr * 8 + (c ^ (rr & 7))])[lane & 3];
+                const uint32_t mr = __shfl_sync(kFullMask, m[h], r);
+                int w2, t2;
+                exact_totals<W>(exact_pass_cost<W>(ad, (mr >> lane) & 1u, lane, st.ex), lane, w2, t2);
+                if (lane == r) {
+                    worst[h] = w2;
+                    total[h] = t2;
+                }
             }
-            cost = mine;
-            __syncwarp();
+            if (p[h] < n) {
+                ways[p[h]] = worst[h];
+                wavefronts[p[h]] = total[h];
+            }
         }
-        unsigned worst, total;
-        if constexpr (kPasses == 1) {
-            worst = total = static_cast<unsigned>(cost);  // already uniform across the warp
-        } else {
-            // one representative lane per pass carries that pass's cost
-            const unsigned rep = (lane % kLpp == 0) ? static_cast<unsigned>(cost) : 0u;
-            worst = __reduce_max_sync(kFullMask, rep);
-            total = __reduce_add_sync(kFullMask, rep);
-        }
-        if (lane == 0) {
-            ways[p] = static_cast<int32_t>(worst);
-            wavefronts[p] = static_cast<int32_t>(total);
-        }
+        __syncwarp();  // the warp is done with this buffer before it is staged again
     }
+    cp_async_wait_all();
 }
 
 // Element by element (A or C not 16-byte aligned, and the odd last mask).
@@ -165,19 +461,36 @@ __global__ void __launch_bounds__(256) slice_collision_vec_kernel(const ulonglon
 
 }  // namespace
 
+template <int W, bool MASKED>
+static cudaError_t launch_profile(bool vec, unsigned grid, cudaStream_t st, const uint32_t *addrs,
+                                  const uint32_t *active, int64_t n, int32_t *ways, int32_t *wavefronts) {
+    const dim3 g(grid), blk(kLaneWarps * 32);
+    return vec ? launch_pdl(bank_profile_kernel<W, MASKED, true>, g, blk, 0, st, addrs, active, n, ways, wavefronts)
+               : launch_pdl(bank_profile_kernel<W, MASKED, false>, g, blk, 0, st, addrs, active, n, ways, wavefronts);
+}
+
+template <int W>
+static cudaError_t launch_profile(bool vec, unsigned grid, cudaStream_t st, const uint32_t *addrs,
+                                  const uint32_t *active, int64_t n, int32_t *ways, int32_t *wavefronts) {
+    return active ? launch_profile<W, true>(vec, grid, st, addrs, active, n, ways, wavefronts)
+                  : launch_profile<W, false>(vec, grid, st, addrs, active, n, ways, wavefronts);
+}
+
 swz_status bank_profile_launch(const uint32_t *addrs, const uint32_t *active, int64_t n, int width,
                                int32_t *ways, int32_t *wavefronts, cudaStream_t st) {
-    int64_t grid = (n + kWarpsPerCta - 1) / kWarpsPerCta;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * 64;  // grid-stride beyond 64 CTAs per SM
+    const int64_t batches = (n + kRows - 1) / kRows;  // 64 patterns per warp
+    int64_t grid = (batches + kLaneWarps - 1) / kLaneWarps;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 6;  // one wave of resident CTAs, then a grid stride
     if (grid > cap) grid = cap;
     const unsigned g = static_cast<unsigned>(grid);
+    const bool vec = (reinterpret_cast<uintptr_t>(addrs) & 15u) == 0;
     cudaError_t e;
     switch (width) {
-        case 1: e = launch_pdl(bank_profile_kernel<1>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
-        case 2: e = launch_pdl(bank_profile_kernel<2>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
-        case 4: e = launch_pdl(bank_profile_kernel<4>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
-        case 8: e = launch_pdl(bank_profile_kernel<8>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
-        case 16: e = launch_pdl(bank_profile_kernel<16>, dim3(g), dim3(kWarpsPerCta * 32), 0, st, addrs, active, n, ways, wavefronts); break;
+        case 1: e = launch_profile<1>(vec, g, st, addrs, active, n, ways, wavefronts); break;
+        case 2: e = launch_profile<2>(vec, g, st, addrs, active, n, ways, wavefronts); break;
+        case 4: e = launch_profile<4>(vec, g, st, addrs, active, n, ways, wavefronts); break;
+        case 8: e = launch_profile<8>(vec, g, st, addrs, active, n, ways, wavefronts); break;
+        case 16: e = launch_profile<16>(vec, g, st, addrs, active, n, ways, wavefronts); break;
         default: return SWZ_ERR_PARAM;
     }
     return launched(e);
