@@ -657,6 +657,8 @@ def measure_rows(torch, swz, dev, flush, peak):
     for width in (1, 2, 8, 16):
         pats.bitwise_and_(~(width - 1))  # addresses aligned to the width (all are multiples of 4)
         other[f"w{width}"] = profile_row(width, None)
+    pats.add_(2)  # every 4-byte access straddles two words: the word-key path
+    other["w4_all_unaligned"] = profile_row(4, None)
     out["bank_profile_4M_patterns_other_widths"] = other
     del pats, masks, ways, wf
 

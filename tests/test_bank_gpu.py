@@ -138,6 +138,34 @@ def test_address_array_off_16_bytes(swz, orc, width, masked):
         assert np.array_equal(gw, ow) and np.array_equal(gf, of)
 
 
+@pytest.mark.parametrize("width", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("masked", [False, True])
+def test_key_range_edges(swz, orc, width, masked):
+    """Addresses around 2^18 - 16 bytes (where 16-bit keys give way to 32-bit
+    ones) and at the top of the 32-bit space (an access's last word past
+    2^30 - 1), aligned and unaligned, each edge alone in its batches and
+    mixed with small addresses."""
+    rng = np.random.default_rng(60 + width)
+    n = 64 * 12
+    pats = rng.integers(0, 4096, (n, 32)).astype(np.int64) * 4
+    edges = [(1 << 18) - 40, (1 << 18) - 17, (1 << 18) - 16, (1 << 18) - 4, (1 << 32) - 64, (1 << 32) - 16]
+    for b, e in enumerate(edges):
+        blk = slice(64 * 2 * b, 64 * 2 * b + 64)      # the edge in a whole batch
+        pats[blk] = e + rng.integers(0, 40, (64, 32))
+        pats[64 * 2 * b + 64 + 5] = e + rng.integers(0, 40, 32)  # one row in a batch of small ones
+    pats = np.minimum(pats, (1 << 32) - 1)
+    aligned = rng.random(n) < 0.5
+    pats[aligned] = pats[aligned] // width * width
+    pats = pats.astype(np.uint32)
+    act = None
+    if masked:
+        act = inputs_masks(n, seed=61)
+        act[::5] = 0x80000001
+    gw, gf = gpu_profile(swz, pats, width, act)
+    ow, of = orc.bank_profile(pats, width, act)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
 def inputs_masks(n, seed):
     from xor_swizzle_movement_gb300 import inputs
     return inputs.active_masks(n, seed=seed)

@@ -26,9 +26,10 @@
 // SIMD min and max; otherwise 32-bit keys, one pattern after the other.
 // Every lane does the same work, so the warp never diverges on the data.
 //
-// Patterns with an unaligned access, where one lane may touch up to five words
-// and neighbours may share some of them, are then counted exactly by the whole
-// warp, one pattern at a time, over per-lane word candidates.
+// A batch holding an unaligned pattern (one lane may then touch up to five
+// words, and neighbours may share some of them) is counted on words instead:
+// every word an active lane touches becomes a key, and a pass's keys (up to
+// 64) are sorted and counted the same way.
 #include "swz_common.cuh"
 
 namespace swz {
@@ -41,70 +42,6 @@ struct Passes {
     static constexpr int n = W <= 4 ? 1 : W / 4;  // passes per access
     static constexpr int lanes = 32 / n;          // lanes per pass
 };
-
-// ---- exact count: the whole warp on one pattern ----------------------------
-
-struct ExactScratch {
-    uint32_t first[32];
-    int nw[32];
-    int cnt[4][32];
-};
-
-// Cost of this lane's pass, the same on every lane of the pass.  Lane l holds
-// lane l's address a and whether it is active.  Its candidate words are
-// first .. first + nw - 1; each word is counted once per pass, by the lowest
-// lane that touches it at its earliest candidate.
-template <int W>
-__device__ __forceinline__ int exact_pass_cost(uint32_t a, bool on, int lane, ExactScratch &s) {
-    constexpr int kPasses = Passes<W>::n, kLpp = Passes<W>::lanes;
-    const int pass = lane / kLpp;
-    const unsigned long long last = (static_cast<unsigned long long>(a) + W - 1) >> 2;
-    const uint32_t first = a >> 2;
-    const int nw = on ? static_cast<int>(last - first + 1) : 0;
-    s.first[lane] = first;
-    s.nw[lane] = nw;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) s.cnt[q][lane] = 0;
-    __syncwarp();
-    for (int i = 0; i < 5; ++i) {
-        const bool valid = i < nw;
-        const unsigned long long wd = static_cast<unsigned long long>(first) + i;
-        const unsigned long long key = valid ? ((static_cast<unsigned long long>(pass) << 40) | wd)
-                                             : ((1ull << 63) | static_cast<unsigned long long>(lane));
-        const unsigned m = __match_any_sync(kFullMask, key);
-        bool fresh = valid && (__ffs(m) - 1 == lane);
-        if (fresh && i > 0) {
-            // did a lane of this pass touch the same word at an earlier candidate?
-            for (int l2 = pass * kLpp; l2 < (pass + 1) * kLpp; ++l2) {
-                const long long d = static_cast<long long>(wd) - static_cast<long long>(s.first[l2]);
-                if (d >= 0 && d < i && d < s.nw[l2]) fresh = false;
-            }
-        }
-        if (fresh) atomicAdd(&s.cnt[pass][static_cast<int>(wd & 31u)], 1);
-    }
-    __syncwarp();
-    int mine = 0;
-#pragma unroll
-    for (int q = 0; q < kPasses; ++q) {
-        const int c = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(s.cnt[q][lane])));
-        if (q == pass) mine = c;
-    }
-    __syncwarp();
-    return mine;
-}
-
-// worst pass and sum of passes from the per-lane pass costs of exact_pass_cost
-template <int W>
-__device__ __forceinline__ void exact_totals(int cost, int lane, int &worst, int &total) {
-    constexpr int kLpp = Passes<W>::lanes;
-    if constexpr (Passes<W>::n == 1) {
-        worst = total = cost;
-    } else {
-        const unsigned rep = (lane % kLpp == 0) ? static_cast<unsigned>(cost) : 0u;  // one lane per pass
-        worst = static_cast<int>(__reduce_max_sync(kFullMask, rep));
-        total = static_cast<int>(__reduce_add_sync(kFullMask, rep));
-    }
-}
 
 // ---- one lane, one aligned pattern --------------------------------------------
 
@@ -132,8 +69,8 @@ __device__ __forceinline__ void order(uint32_t &x, uint32_t &y) {
 // Batcher's odd-even merge of k[LO .. LO+N), whose two halves are sorted,
 // restricted to the elements LO, LO + R, LO + 2R, ...: merge the even and the
 // odd subsequence (stride 2R), then order each odd element with the next one.
-template <bool PK, int LO, int N, int R>
-__device__ __forceinline__ void oe_merge(uint32_t (&k)[32]) {
+template <bool PK, int LO, int N, int R, int SZ>
+__device__ __forceinline__ void oe_merge(uint32_t (&k)[SZ]) {
     if constexpr (2 * R < N) {
         oe_merge<PK, LO, N, 2 * R>(k);
         oe_merge<PK, LO + R, N, 2 * R>(k);
@@ -144,10 +81,11 @@ __device__ __forceinline__ void oe_merge(uint32_t (&k)[32]) {
     }
 }
 
-// Sorts k[LO .. LO+N), N a power of two (19 / 63 / 191 compare-exchanges
-// for 8 / 16 / 32 keys).  PK: two 16-bit keys per word, sorted side by side.
-template <bool PK, int LO, int N>
-__device__ __forceinline__ void oe_sort(uint32_t (&k)[32]) {
+// Sorts k[LO .. LO+N), N a power of two (19 / 63 / 191 / 543 compare-
+// exchanges for 8 / 16 / 32 / 64 keys).  PK: two 16-bit keys per word,
+// sorted side by side.
+template <bool PK, int LO, int N, int SZ>
+__device__ __forceinline__ void oe_sort(uint32_t (&k)[SZ]) {
     if constexpr (N > 1) {
         oe_sort<PK, LO, N / 2>(k);
         oe_sort<PK, LO + N / 2, N / 2>(k);
@@ -321,6 +259,129 @@ __device__ __forceinline__ void lane_pair_cost16(const uint4 *a, const uint4 *b,
     }
 }
 
+// Any pattern, aligned or not: every word an active lane touches (first ..
+// last, the last repeated to fill J slots) becomes a key with its bank on top
+// and its other bits below, and a pass's keys (padded to 64 with copies of its
+// first key) are sorted and counted as above.  PK: rows a and b side by side
+// on 16-bit keys, which hold words below 2^16; returns false, setting nothing,
+// when some lane's row reaches 2^18 - 16 bytes (the warp then takes 32-bit
+// keys, one row at a time: PK false, row a only, results in worst[0] and
+// total[0]).  Inactive lanes take the address of their pass's first active lane.
+template <int W, bool MASKED, bool PK>
+__device__ __forceinline__ bool lane_words_cost(const uint4 *a, const uint4 *b, int sw, uint32_t ma, uint32_t mb,
+                                                int (&worst)[2], int (&total)[2]) {
+    constexpr int kPasses = Passes<W>::n, kLpp = Passes<W>::lanes;
+    constexpr int J = W <= 4 ? 2 : (W == 8 ? 3 : 5);  // most words one access touches
+    constexpr int kChunks = kLpp / 4;                  // 16-byte chunks of addresses per pass
+    const uint32_t m[2] = {ma, mb};
+    const uint4 *row[2] = {a, b};
+    constexpr int kRowsHere = PK ? 2 : 1;
+    if constexpr (PK) {
+        uint32_t hi = 0;  // every address below 2^18 - 16: no a + W - 1 wraps, no word + 4 leaves its half
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = row[h][c ^ sw];
+                const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t u = (!MASKED || (m[h] & (1u << (4 * c + j)))) ? x[j] : 0u;
+                    hi |= u | (u + 16u);
+                }
+            }
+        if (!__all_sync(kFullMask, (hi >> 18) == 0u)) return false;
+    }
+    worst[0] = worst[1] = total[0] = total[1] = 0;
+#pragma unroll 1
+    for (int q = 0; q < kPasses; ++q) {
+        uint32_t pm[2], f[2];  // the pass's active lanes and first active address per row
+#pragma unroll
+        for (int h = 0; h < kRowsHere; ++h) {
+            pm[h] = kPasses == 1 ? m[h] : (m[h] >> (q * kLpp)) & ((1u << (kLpp & 31)) - 1u);
+            f[h] = 0u;
+            if constexpr (MASKED) {
+                const int i = q * kLpp + __ffs(pm[h]) - 1;
+                if (pm[h]) f[h] = reinterpret_cast<const uint32_t *>(row[h])[((i >> 2) ^ sw) * 4 + (i & 3)];
+            }
+        }
+        uint32_t k[64];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+            uint32_t x[2][4];
+#pragma unroll
+            for (int h = 0; h < kRowsHere; ++h) {
+                const uint4 v = row[h][(q * kChunks + c) ^ sw];
+                x[h][0] = v.x;
+                x[h][1] = v.y;
+                x[h][2] = v.z;
+                x[h][3] = v.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = 4 * c + j;  // lane within the pass
+                if constexpr (PK) {
+                    uint32_t u[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) u[h] = (!MASKED || (pm[h] & (1u << i))) ? x[h][j] : f[h];
+                    const uint32_t w0 = __byte_perm(u[0] >> 2, u[1] >> 2, 0x5410);
+                    const uint32_t wl = __byte_perm((u[0] + (W - 1)) >> 2, (u[1] + (W - 1)) >> 2, 0x5410);
+#pragma unroll
+                    for (int t = 0; t < J; ++t) {
+                        uint32_t w;  // word t of the access, or its last word
+                        asm("min.u16x2 %0, %1, %2;" : "=r"(w) : "r"(w0 + t * 0x00010001u), "r"(wl));
+                        k[i * J + t] = ((w << 11) & 0xF800F800u) | ((w >> 5) & 0x07FF07FFu);
+                    }
+                } else {
+                    const uint32_t u = (!MASKED || (pm[0] & (1u << i))) ? x[0][j] : f[0];
+                    const uint32_t w0 = u >> 2;
+                    const uint32_t wl = static_cast<uint32_t>((static_cast<uint64_t>(u) + (W - 1)) >> 2);  // <= 2^30
+#pragma unroll
+                    for (int t = 0; t < J; ++t) {
+                        const uint32_t w = min(w0 + t, wl);
+                        k[i * J + t] = ((w & 31u) << 27) | (w >> 5);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = kLpp * J; i < 64; ++i) k[i] = k[0];
+        oe_sort<PK, 0, 64>(k);
+        int cost[2];
+        if constexpr (PK) {
+            uint32_t run = 0x00010001u, mx = 0x00010001u;
+#pragma unroll
+            for (int i = 1; i < 64; ++i) {
+                const uint32_t x = k[i] ^ k[i - 1];
+                uint32_t d, g;
+                asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(0x00010001u));
+                asm("min.u16x2 %0, %1, %2;" : "=r"(g) : "r"(x & 0xF800F800u), "r"(0x00010001u));
+                const uint32_t msk = g * 0xFFFFu;
+                run = ((run + d) & ~msk) | (0x00010001u & msk);
+                asm("max.u16x2 %0, %1, %2;" : "=r"(mx) : "r"(mx), "r"(run));
+            }
+            cost[0] = static_cast<int>(mx & 0xFFFFu);
+            cost[1] = static_cast<int>(mx >> 16);
+        } else {
+            int run = 1, mx = 1;
+#pragma unroll
+            for (int i = 1; i < 64; ++i) {
+                const uint32_t x = k[i] ^ k[i - 1];
+                run = x >= (1u << 27) ? 1 : run + (x != 0u ? 1 : 0);
+                mx = max(mx, run);
+            }
+            cost[0] = mx;
+        }
+#pragma unroll
+        for (int h = 0; h < kRowsHere; ++h) {
+            const int c = pm[h] ? cost[h] : 0;
+            worst[h] = max(worst[h], c);
+            total[h] += c;
+        }
+    }
+    return true;
+}
+
 // ---- kernel ---------------------------------------------------------------------
 
 constexpr int kRows = 64;  // patterns per warp and batch: two per lane
@@ -328,7 +389,6 @@ constexpr int kRows = 64;  // patterns per warp and batch: two per lane
 struct __align__(16) LaneStage {
     uint4 rows[2][kRows * 8];  // two batches of 64 rows of 8 chunks; chunk c of row r at r * 8 + (c ^ (r & 7))
     uint32_t mask[2][kRows];
-    ExactScratch ex;
 };
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
@@ -346,7 +406,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // 16-byte chunks (otherwise word by word).  Each warp takes batches of 64
 // patterns at a grid stride; lane l profiles rows l and l + 32 of a batch.
 template <int W, bool MASKED, bool VEC>
-__global__ void __launch_bounds__(kLaneWarps * 32, 6)  // 6 CTAs (12 warps, 207 KiB of stages) per SM
+__global__ void __launch_bounds__(kLaneWarps * 32, 6)  // 6 CTAs (12 warps, 198 KiB of stages) per SM
     bank_profile_kernel(const uint32_t *__restrict__ addrs, const uint32_t *__restrict__ active, int64_t n,
                         int32_t *__restrict__ ways, int32_t *__restrict__ wavefronts) {
     __shared__ LaneStage s_stage[kLaneWarps];
@@ -394,23 +454,22 @@ __global__ void __launch_bounds__(kLaneWarps * 32, 6)  // 6 CTAs (12 warps, 207 
 #pragma unroll 1  // one copy of the 32-bit path: fewer registers
             for (int h = 0; h < 2; ++h) lane_pattern_cost<W, MASKED>(row[h], lane & 7, m[h], worst[h], total[h], bad[h]);
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            unsigned redo = __ballot_sync(kFullMask, bad[h] && p[h] < n);
-            while (redo) {  // warp-uniform
-                const int r = __ffs(redo) - 1, rr = 32 * h + r;
-                redo &= redo - 1u;
-                const int c = lane >> 2;
-                const uint32_t ad =
-                    reinterpret_cast<const uint32_t *>(&st.rows[buf][rr * 8 + (c ^ (rr & 7))])[lane & 3];
-                const uint32_t mr = __shfl_sync(kFullMask, m[h], r);
-                int w2, t2;
-                exact_totals<W>(exact_pass_cost<W>(ad, (mr >> lane) & 1u, lane, st.ex), lane, w2, t2);
-                if (lane == r) {
-                    worst[h] = w2;
-                    total[h] = t2;
+        if constexpr (W > 1) {  // a 1-byte access never straddles a word
+            if (__any_sync(kFullMask, (bad[0] && p[0] < n) || (bad[1] && p[1] < n))) {
+                // an unaligned pattern in the batch: word keys for all of it
+                if (!lane_words_cost<W, MASKED, true>(row[0], row[1], lane & 7, m[0], m[1], worst, total)) {
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        int w1[2], t1[2];
+                        lane_words_cost<W, MASKED, false>(row[h], row[h], lane & 7, m[h], 0u, w1, t1);
+                        worst[h] = w1[0];
+                        total[h] = t1[0];
+                    }
                 }
             }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
             if (p[h] < n) {
                 ways[p[h]] = worst[h];
                 wavefronts[p[h]] = total[h];
