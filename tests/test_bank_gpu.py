@@ -182,6 +182,25 @@ def test_bench_size(swz, orc):
     assert np.array_equal(gw, ow) and np.array_equal(gf, of)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("width,masked,unaligned", [(1, False, False), (2, False, False), (8, False, False),
+                                                   (16, False, False), (4, True, False), (4, False, True),
+                                                   (16, True, True)])
+def test_bench_size_other_widths(swz, orc, width, masked, unaligned):
+    """2^22 random patterns, as the benchmark's other profiler rows: every
+    access width, lane masks, and patterns moved 2 bytes off alignment (the
+    word-key count)."""
+    from xor_swizzle_movement_gb300 import inputs
+    n = 1 << 22
+    pats = inputs.bank_patterns(n, width, seed=5)
+    if unaligned:
+        pats += 2
+    act = inputs.active_masks(n, seed=6) if masked else None
+    gw, gf = gpu_profile(swz, pats, width, act)
+    ow, of = orc.bank_profile(pats, width, act)
+    assert np.array_equal(gw, ow) and np.array_equal(gf, of)
+
+
 def test_errors(swz):
     w = torch.zeros(4, dtype=torch.int32, device="cuda")
     with pytest.raises(swz.SwzError) as e:
