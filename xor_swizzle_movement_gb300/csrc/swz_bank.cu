@@ -110,8 +110,9 @@ __device__ __forceinline__ void sort_passes(uint32_t (&k)[32]) {
 }
 
 // Cost of the pattern in this lane's row (chunk c at row[c ^ sw]), m its
-// active lanes.  bad: some active access is unaligned; the result is then
-// meaningless and the exact count must replace it.
+// active lanes, on 32-bit keys.  bad: some active access is unaligned; the
+// result is then meaningless and the count on words (lane_words_cost) must
+// replace it.
 template <int W, bool MASKED>
 __device__ __forceinline__ void lane_pattern_cost(const uint4 *row, int sw, uint32_t m, int &worst, int &total,
                                                   bool &bad) {
@@ -177,7 +178,7 @@ __device__ __forceinline__ void lane_pattern_cost(const uint4 *row, int sw, uint
 // (bits 2..6) over its bits 7..17, which holds every unit of an address below
 // 2^18 bytes; ok is false when some address of either row is not below that,
 // and the results are then not set.  Inactive lanes take the address of their
-// pass's first active lane (0 when the pass has none).  bad_a, bad_b: some
+// pass's first active lane (0 when the pass has none).  bad[0], bad[1]: some
 // active access of that row is unaligned.
 template <int W, bool MASKED>
 __device__ __forceinline__ void lane_pair_cost16(const uint4 *a, const uint4 *b, int sw, uint32_t ma, uint32_t mb,
