@@ -366,6 +366,25 @@ __device__ __forceinline__ uint32_t sw_inv32(uint32_t y, int B, int M, int S, in
     return x;
 }
 
+// x[w] := x[(w + g) & 3] (LEFT) or x[(w - g) & 3], g in 0..3 and different
+// across lanes: two conditional steps, so the words stay in registers.
+template <bool LEFT>
+__device__ __forceinline__ void rotate_words(uint32_t (&x)[4], int g) {
+    const uint32_t a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+    const bool one = g & 1;
+    uint32_t b0, b1, b2, b3;
+    if constexpr (LEFT) {
+        b0 = one ? a1 : a0; b1 = one ? a2 : a1; b2 = one ? a3 : a2; b3 = one ? a0 : a3;
+    } else {
+        b0 = one ? a3 : a0; b1 = one ? a0 : a1; b2 = one ? a1 : a2; b3 = one ? a2 : a3;
+    }
+    const bool two = g & 2;
+    x[0] = two ? b2 : b0;
+    x[1] = two ? b3 : b1;
+    x[2] = two ? b0 : b2;
+    x[3] = two ? b1 : b3;
+}
+
 // MIS: dst or src is not 16-byte aligned (both are aligned to the element
 // size).  The block is staged at its source's offset within a 16-byte chunk
 // (a_src) by 16-byte loads of the aligned chunks that cover it, gathered into
@@ -456,6 +475,33 @@ __global__ void __launch_bounds__(256)
                                       (static_cast<uint32_t>(sa[e + 2 + r2]) << 16) |
                                       (static_cast<uint32_t>(sa[e + 3 + r3]) << 24);
                 *reinterpret_cast<uint32_t *>(dst + b0 + 4 * w) = word;
+            }
+        } else if constexpr (E == 2) {
+            // A vector per thread puts the lanes 16 bytes apart, so lanes l,
+            // l + 8, l + 16 and l + 24 would read one bank in every 2-byte
+            // gather (4-way).  Each group of 8 lanes starts instead at another
+            // word of its vector (word g = lane / 8, then g + 1, ...): the four
+            // groups read four different banks, and the vector is rotated back
+            // before its store.  (For 4-byte units the same form measured about
+            // 1% slower than the plain order.)
+            const int g = (tid >> 3) & 3;
+            for (int v = tid; v < nv; v += 256) {
+                const int e = v * V;
+                const uint32_t p = pat == 1 ? 0u : static_cast<uint32_t>(v) - __umulhi(static_cast<uint32_t>(v), pat_recip) * pat;
+                const uint4 t = *reinterpret_cast<const uint4 *>(rel_s + p * 8);
+                uint32_t rw[4] = {t.x, t.y, t.z, t.w};  // the two table entries of word w's elements
+                rotate_words<true>(rw, g);              // rw[w] now belongs to word (w + g) & 3
+                uint32_t ow[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int s0 = e + 2 * ((w + g) & 3);  // the word's first element
+                    const int r0 = static_cast<int16_t>(rw[w] & 0xffffu), r1 = static_cast<int16_t>(rw[w] >> 16);
+                    const uint32_t lo = *reinterpret_cast<const uint16_t *>(sa + (s0 + r0) * 2);
+                    const uint32_t hi = *reinterpret_cast<const uint16_t *>(sa + (s0 + 1 + r1) * 2);
+                    ow[w] = lo | (hi << 16);
+                }
+                rotate_words<false>(ow, g);  // ow[w] is word w again
+                st_stream16(dst + b0 + 16 * v, make_uint4(ow[0], ow[1], ow[2], ow[3]));
             }
         } else {
             for (int v = tid; v < nv; v += 256) {
