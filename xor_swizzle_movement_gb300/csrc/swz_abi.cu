@@ -59,6 +59,29 @@ int sm_count() {
     return n;
 }
 
+// L2 cache size of the current device in bytes, queried once per device and
+// cached.  Returns 0 if the query fails (every buffer then counts as larger).
+int64_t l2_bytes() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int64_t> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int64_t c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 bool host_resident(const void *p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {

@@ -57,6 +57,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     return v;
 }
 
+// An L2 policy with the default eviction priority.
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // An L2 policy that marks lines as first to evict: for data read once.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
@@ -74,6 +81,23 @@ __device__ __forceinline__ uint4 ld_stream16_hint(const void *p, uint64_t policy
 
 __device__ __forceinline__ void st_stream16(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// A 16-byte store under an L2 policy (l2_evict_first_policy: for output that
+// nothing reads soon; l2_evict_normal_policy: as a plain store).
+__device__ __forceinline__ void st_hint16(void *p, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
+// The same store marked streaming (st.global.cs): its line leaves L2 first.
+// For output that nothing reads soon and that could not stay in L2 anyway;
+// output that a following launch reads from L2 keeps the plain store.
+__device__ __forceinline__ void st_once16(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
 }
@@ -201,5 +225,6 @@ swz_status launch_status();
 swz_status launched(cudaError_t launch_result);  // status of a launch_pdl call
 bool ranges_overlap(const void *a, int64_t a_bytes, const void *b, int64_t b_bytes);
 int sm_count();  // SMs of the current device (cached per device)
+int64_t l2_bytes();  // L2 cache bytes of the current device (cached per device)
 bool host_resident(const void *p);  // p is host memory (pinned or pageable), not device or managed memory
 }  // namespace swz

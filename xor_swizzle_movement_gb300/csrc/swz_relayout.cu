@@ -70,6 +70,7 @@ struct RelayoutArgs {
     int B, M, S;
     int steps;          // 1: source = sw(y); >1: source = sw^-1(y) by `steps` iterations
     int per_thread;     // vectors per thread, 1..kMaxPerThread
+    int once = 0;       // stores marked evict-first: the output is larger than L2
     uint32_t perm_sel[12];  // kLanesGeneral: prmt selectors of the fixed lane map L, 3 per word
 };
 
@@ -81,8 +82,10 @@ constexpr int kMaxPerThread = 4;
 // no L2 eviction hint (with the evict-first hint a host-reading launch beside
 // a host-writing one moved 12% less over the link).  Otherwise one CTA covers
 // one stretch of blockDim.x * per_thread vectors, loads marked evict-first.
+// At most 40 registers (6 CTAs per SM) with whole-buffer offsets; tile-local
+// offsets need a few more (5 CTAs per SM).
 template <int E, int MODE, bool LOCAL, bool LINK>
-__global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a) {
+__global__ void __launch_bounds__(256, LOCAL ? 5 : 6) relayout_vec_kernel(const RelayoutArgs a) {
     constexpr int LV = VecTraits<E>::LV;
     constexpr uint64_t VM = (1u << LV) - 1u;
     pdl_launch_dependents();
@@ -93,6 +96,7 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
         uint4 r[kMaxPerThread];
         uint32_t lx[kMaxPerThread];
         const uint64_t policy = l2_evict_first_policy();
+        const uint64_t store_policy = a.once ? policy : l2_evict_normal_policy();
         // all loads first, so that each thread keeps up to kMaxPerThread 16-byte loads in flight
 #pragma unroll
         for (int k = 0; k < kMaxPerThread; ++k) {
@@ -118,7 +122,7 @@ __global__ void __launch_bounds__(256) relayout_vec_kernel(const RelayoutArgs a)
                 if constexpr (MODE == kLanesFixed) out = r[k];
                 else if constexpr (MODE == kLanesXor) out = lanes_xor<E>(r[k], lx[k]);
                 else out = bytes_permute(lanes_xor<E>(r[k], lx[k]), a.perm_sel);
-                st_stream16(a.dst + u, out);
+                st_hint16(a.dst + u, out, store_policy);
             }
         }
     }
@@ -600,6 +604,7 @@ swz_status launch_lane_map(void *dst, const void *src, int64_t n_elems, int esiz
     a.tile_vecs = 1;
     a.B = 0; a.M = 0; a.S = 1;
     a.steps = 1;
+    a.once = !link_grid && n_elems * esize > l2_bytes();  // as in relayout_launch
     const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
     a.per_thread = (a.nvec >= 4 * wave) ? 4 : (a.nvec >= 2 * wave) ? 2 : 1;
     lane_map_selectors(src_lane, esize, a.perm_sel);
@@ -727,6 +732,12 @@ swz_status relayout_launch(void *dst, const void *src, int64_t n_tiles, int64_t 
         a.tile_vecs = tile_bytes / 16;
         a.B = B; a.M = M; a.S = S;
         a.steps = steps;
+        // An output larger than L2 cannot stay there for a following launch:
+        // stores marked evict-first (1 GiB: 1.042 -> 1.048 of the copy
+        // bandwidth).  A smaller one keeps the default priority, so the next
+        // launch finds it in L2 (evict-first stores took a 64 MiB forward +
+        // inverse from 37.5 to 47.7 us).  Host-resident buffers keep it too.
+        a.once = !link_grid && n_elems * esize > l2_bytes();
         // keep each SM fed: up to four vectors per thread once the grid is
         // several waves deep (every SM x 2048 threads per wave)
         const int64_t wave = static_cast<int64_t>(sm_count()) * 2048;
